@@ -1,0 +1,468 @@
+#!/usr/bin/env python
+"""Benchmark of the FP8 scaled-quantize + scaled-GEMM hot path on GB300.
+
+One step = one pass of the path over one batch of the blockwise workload
+(4096 x 4096 x 4096): cast-transpose X [4096, 4096] bf16 ~ N(0,1) with 1 % of
+columns x100 into row- and column-wise E4M3 with 1x128 scales, cast-transpose
+W [4096, 4096] ~ N(0, 0.02) with 128x128 scales, then Y = X W^T (FP8 GEMM,
+FP32 accumulation, BF16 out).  Inputs are resident in HBM; L2 is flushed
+(a 256 MiB write) between timed steps because the inputs fit in L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded slab of the same workload.  --sweep adds per-recipe kernel numbers.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+M = N = K = 4096
+WORKLOAD = "blockwise fprop 4096x4096x4096: X 1x128 E4M3 (row+col), W 128x128 E4M3 (row+col), Y=XW^T bf16"
+METRIC = "FP8 scaled-GEMM TFLOPS & quantize GB/s per recipe, % of GB300 roofline"
+UNIT = "TFLOP/s"
+FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+            if k in d:
+                p[k] = float(d[k])
+        p["source"] = "measured"
+    return p
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, out_path: str | None):
+        self.gpu = gpu_index
+        self.out_path = out_path
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if self.out_path:
+            with open(self.out_path, "w") as f:
+                f.write("\n".join(self.lines) + "\n")
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ our arm
+class Path:
+    """Buffers and launches of one step of the blockwise workload."""
+
+    def __init__(self, fq, x, w):
+        self.fq = fq
+        R, F = fq.Recipe, fq.Format
+        self.R, self.F = R, F
+        dev = x.device
+        self.x, self.w = x, w
+        self.qx = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        self.sx = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
+        self.qxt = torch.empty((K, M), dtype=torch.uint8, device=dev)
+        self.sxt = torch.empty((K, M // 128), dtype=torch.float32, device=dev)
+        self.qw = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        self.sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
+        self.qwt = torch.empty((K, N), dtype=torch.uint8, device=dev)
+        self.swt = torch.empty((K // 128, N // 128), dtype=torch.float32, device=dev)
+        self.y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.launches_per_step = 3
+
+    def cast_x(self):
+        self.fq.fp8_cast_transpose(self.x, self.R.BLOCK_1x128, self.F.E4M3, None, None, self.qx, self.sx, self.qxt,
+                                   self.sxt)
+
+    def cast_w(self):
+        self.fq.fp8_cast_transpose(self.w, self.R.BLOCK_128x128, self.F.E4M3, None, None, self.qw, self.sw, self.qwt,
+                                   self.swt)
+
+    def gemm(self):
+        self.fq.fp8_scaled_gemm(self.qx, self.F.E4M3, self.R.BLOCK_1x128, self.sx, self.qw, self.F.E4M3,
+                                self.R.BLOCK_128x128, self.sw, self.y)
+
+
+def bytes_cast_1x128(r, c):
+    return r * c * 4 + 2 * (r * c // 128) * 4
+
+
+def bytes_cast_128x128(r, c):
+    return r * c * 4 + 2 * (r * c // 16384) * 4
+
+
+def run_ours(args, rank, world):
+    import scaled_quantize_gemm_amax_gb300 as fq
+    from scaled_quantize_gemm_amax_gb300 import build as fqbuild
+    from scaled_quantize_gemm_amax_gb300 import workloads as wl
+
+    fqbuild.build()
+    fq.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x, w = wl.cfg2_blockwise(dev)
+    path = Path(fq, x, w)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        path.cast_x()
+        path.cast_w()
+        path.gemm()
+        flush.zero_()
+    torch.cuda.synchronize()
+    assert fq.fp8_get_device_status() == fq.Status.OK
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device(), os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    clocks.start()
+    time.sleep(0.2)
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        e = ev[i]
+        e[0].record(stream)
+        path.cast_x()
+        e[1].record(stream)
+        path.cast_w()
+        e[2].record(stream)
+        path.gemm()
+        e[3].record(stream)
+        flush.zero_()          # outside the step's events: L2 does not carry inputs across steps
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    st = fq.fp8_get_device_status()
+    assert st == fq.Status.OK, st
+
+    t_cx = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    t_cw = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    t_g = [ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps)]
+    step_ms_local = sum(ev[i][0].elapsed_time(ev[i][3]) for i in range(args.steps)) / args.steps
+    step_ms = max_over_ranks(step_ms_local, world)
+
+    flops = 2.0 * M * N * K
+    pk = peaks()
+    fp8_peak = 2.0 * pk["bf16_tflops"]           # FP8 dense = 2 x BF16 dense (nominal 4.5 / 2.25 PF)
+    g_ms = statistics.mean(t_g)
+    gemm_tflops = flops / (g_ms * 1e-3) / 1e12
+    cx_gbs = bytes_cast_1x128(M, K) / (statistics.mean(t_cx) * 1e-3) / 1e9
+    cw_gbs = bytes_cast_128x128(N, K) / (statistics.mean(t_cw) * 1e-3) / 1e9
+    value = world * flops / (step_ms * 1e-3) / 1e12
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8-e4m3 (fp32 accumulate, bf16 out)",
+        "data": "synthetic (seeded N(0,1) + 1% columns x100 / N(0,0.02))",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "recipe": "blockwise 1x128 x 128x128",
+                   "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
+        "kernels": {
+            "cast_transpose_x_1x128": {"us": round(statistics.mean(t_cx) * 1e3, 2), "GB/s": round(cx_gbs, 1),
+                                       "frac_hbm": round(cx_gbs / pk["hbm_gbs"], 4)},
+            "cast_transpose_w_128x128": {"us": round(statistics.mean(t_cw) * 1e3, 2), "GB/s": round(cw_gbs, 1),
+                                         "frac_hbm": round(cw_gbs / pk["hbm_gbs"], 4)},
+            "gemm_blockwise": {"us": round(g_ms * 1e3, 2), "TFLOP/s": round(gemm_tflops, 1),
+                               "frac_fp8": round(gemm_tflops / fp8_peak, 4)},
+        },
+        "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4), "traffic": None,
+                     "peak_source": f"{pk['source']}: 2 x bf16 burst ({pk['bf16_tflops']})"},
+        "gpu_launches": path.launches_per_step * args.steps,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                   "samples": clk["samples"]},
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(fq, path, x, w, args, world)
+    if args.sweep:
+        result["per_recipe"] = run_sweep(fq, wl, dev)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(x, w)
+    return result
+
+
+def run_e2e(fq, path, x, w, args, world):
+    """The same step through the public API with host buffers: pinned host -> device
+    copies of X and W, the three calls, and Y copied back, all inside the timed region."""
+    xh = x.cpu().pin_memory()
+    wh = w.cpu().pin_memory()
+    yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        path.x.copy_(xh, non_blocking=True)
+        path.w.copy_(wh, non_blocking=True)
+        path.cast_x()
+        path.cast_w()
+        path.gemm()
+        yh.copy_(path.y, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        path.x.copy_(xh, non_blocking=True)
+        path.w.copy_(wh, non_blocking=True)
+        path.cast_x()
+        path.cast_w()
+        path.gemm()
+        yh.copy_(path.y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    return {"value": round(world * 2.0 * M * N * K / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "h2d_bytes_per_step": int(xh.numel() * 2 + wh.numel() * 2), "d2h_bytes_per_step": int(yh.numel() * 2)}
+
+
+def _time_kernel(fn, reps=20, flush=None):
+    s = torch.cuda.current_stream()
+    es = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for _ in range(3):
+        fn()
+    for a, b in es:
+        if flush is not None:
+            flush.zero_()
+        a.record(s)
+        fn()
+        b.record(s)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in es)
+
+
+def run_sweep(fq, wl, dev):
+    """Per-recipe kernel numbers: cast-transpose GB/s at 8192^2 and 16384^2 for each
+    recipe, and GEMM TFLOP/s per recipe at 4096^3 and the MX LLaMA-7B shapes."""
+    R, F = fq.Recipe, fq.Format
+    pk = peaks()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    out = {"cast_transpose": {}, "gemm": {}}
+    for size in (8192, 16384):
+        x = wl.cfg5_sweep(size, dev)
+        scale = torch.ones(1, dtype=torch.float32, device=dev)
+        for rec in (R.TENSOR, R.BLOCK_1x128, R.BLOCK_128x128, R.MX_1x32):
+            qr, sr, qc, sc = fq.cast_transpose(x, rec, F.E4M3, scale if rec == R.TENSOR else None)
+            ms = _time_kernel(lambda: fq.fp8_cast_transpose(x, rec, F.E4M3, scale if rec == R.TENSOR else None,
+                                                            None, qr, sr, qc, sc), flush=flush)
+            extra = {R.TENSOR: 0, R.BLOCK_1x128: 2 * size * size // 128 * 4, R.BLOCK_128x128: 0,
+                     R.MX_1x32: 2 * size * size // 32}[rec]
+            gbs = (4 * size * size + extra) / (ms * 1e-3) / 1e9
+            out["cast_transpose"][f"{rec.name}_{size}"] = {"us": round(ms * 1e3, 1), "GB/s": round(gbs, 1),
+                                                          "frac_hbm": round(gbs / pk["hbm_gbs"], 4)}
+            del qr, sr, qc, sc
+        amax = torch.empty(1, dtype=torch.float32, device=dev)
+        ms = _time_kernel(lambda: fq.fp8_amax(x, amax), flush=flush)
+        gbs = 2 * size * size / (ms * 1e-3) / 1e9
+        out["cast_transpose"][f"amax_{size}"] = {"us": round(ms * 1e3, 1), "GB/s": round(gbs, 1),
+                                                 "frac_hbm": round(gbs / pk["hbm_gbs"], 4)}
+        del x
+    fp8_peak = 2.0 * pk["bf16_tflops"]
+    shapes = [("tensor_4096", R.TENSOR, R.TENSOR, (4096, 4096, 4096)),
+              ("blockwise_4096", R.BLOCK_1x128, R.BLOCK_128x128, (4096, 4096, 4096)),
+              ("mx_4096", R.MX_1x32_TILED, R.MX_1x32_TILED, (4096, 4096, 4096))]
+    shapes += [(f"mx_{k}", R.MX_1x32_TILED, R.MX_1x32_TILED, v) for k, v in wl.CFG3_SHAPES.items()]
+    for name, ra, rb, (m, n, k) in shapes:
+        a = wl.normal_bf16((m, k), 1, 1.0, dev)
+        b = wl.normal_bf16((n, k), 2, 0.02, dev)
+        sc = torch.ones(1, dtype=torch.float32, device=dev)
+        qa, sa, _, _ = fq.cast_transpose(a, ra, F.E4M3, sc if ra == R.TENSOR else None, col=False)
+        qb, sb, _, _ = fq.cast_transpose(b, rb, F.E4M3, sc if rb == R.TENSOR else None, col=False)
+        c = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        ms = _time_kernel(lambda: fq.fp8_scaled_gemm(qa, F.E4M3, ra, sa, qb, F.E4M3, rb, sb, c), flush=flush)
+        tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
+        out["gemm"][name] = {"us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1), "frac_fp8": round(tf / fp8_peak, 4)}
+        del a, b, qa, qb, c
+    torch.cuda.synchronize()
+    return out
+
+
+# ------------------------------------------------------------------ oracle (CPU) legs
+def cpu_baseline(x, w):
+    """The oracle as it stands, on the host cores: one 128-row slab of the step
+    (quantize 128 rows of X and of W, row + column copies; GEMM of 128 rows of Y
+    against all of W), the step time extrapolated x32 (M / 128)."""
+    import oracle
+    xh = x.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    wh = w.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    qw_full = oracle.quantize_rowwise(wh, oracle.KIND_128x128, oracle.E4M3)
+    t, info = _oracle_slab_time(oracle, xh, wh, 128, qw_full)
+    return {"value": round(2.0 * M * N * K / t / 1e12, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": info}
+
+
+def _oracle_slab_time(oracle, xh, wh, rows, qw_full):
+    """Time one slab of the step: quantize rows [0, rows) of X and of W (row and
+    column copies), and the GEMM of rows [0, rows) of Y against the whole
+    quantized W (quantized once beforehand).  Returns the extrapolated time of a
+    full step (x M/rows) and a description."""
+    xs = np.ascontiguousarray(xh[:rows])
+    ws = np.ascontiguousarray(wh[:rows])
+    t0 = time.perf_counter()
+    qx, sx = oracle.quantize_rowwise(xs, oracle.KIND_1x128, oracle.E4M3)
+    oracle.quantize_colwise(xs, oracle.KIND_1x128, oracle.E4M3)
+    oracle.quantize_rowwise(ws, oracle.KIND_128x128, oracle.E4M3)
+    oracle.quantize_colwise(ws, oracle.KIND_128x128, oracle.E4M3)
+    t_q = time.perf_counter() - t0
+    qw, sw = qw_full
+    t1 = time.perf_counter()
+    oracle.scaled_gemm_rows(qx, 0, oracle.KIND_1x128, sx, qw, 0, oracle.KIND_128x128, sw, np.arange(rows))
+    t_g = time.perf_counter() - t1
+    scale = M / rows
+    info = (f"{rows}-row slab of X and W quantized (row+col) in {t_q:.3f} s, GEMM of {rows} rows of Y in "
+            f"{t_g:.3f} s; full step extrapolated x{scale:.0f}; C oracle single-threaded, float64 matmul on "
+            f"the BLAS threads")
+    return (t_q + t_g) * scale, info
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is one 128-row slab of the workload
+    (1/32 of the step's work), value = the step's flops / extrapolated step time."""
+    import oracle
+    from scaled_quantize_gemm_amax_gb300 import workloads as wl
+
+    if rank != 0:
+        return None
+    x, w = wl.cfg2_blockwise("cpu")
+    xh = x.contiguous().view(torch.int16).numpy().view(np.uint16)
+    wh = w.contiguous().view(torch.int16).numpy().view(np.uint16)
+    oracle.build()
+    rows = 128
+    qw_full = oracle.quantize_rowwise(wh, oracle.KIND_128x128, oracle.E4M3)
+    for _ in range(args.warmup):
+        _oracle_slab_time(oracle, xh, wh, rows, qw_full)
+    times = []
+    info = ""
+    t_start = time.perf_counter()
+    for _ in range(args.steps):
+        t, info = _oracle_slab_time(oracle, xh, wh, rows, qw_full)
+        times.append(t)
+    wall = time.perf_counter() - t_start
+    step_s = statistics.mean(times)
+    value = 2.0 * M * N * K / step_s / 1e12
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 oracle (fp8 codes)",
+            "data": "synthetic (seeded, CPU generator)",
+            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "recipe": "blockwise 1x128 x 128x128",
+                       "parallelism": "cpu"},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": info},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(wall, 2)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, _ = dist_setup(args)
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

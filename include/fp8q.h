@@ -1,0 +1,201 @@
+/*
+ * fp8q.h -- C ABI of libfp8q: FP8 scaled quantization and the scaled FP8 GEMM
+ * that consumes it, for NVIDIA GB300 (sm_103a).
+ *
+ * The path (sources are the pages this library follows):
+ *   amax -> scale -> quantize / cast-transpose -> scaled FP8 GEMM,
+ * with four scaling recipes:
+ *   - per-tensor current scaling: scale from this tensor's max |x|
+ *     ("Colossal-AI FP8" page, "current scaling"; "FP8 quantized-training
+ *     guide" page, section "tensor-level scaling" / "instant scaling scheme");
+ *   - per-tensor delayed scaling: scale from a history of past amaxes, updated
+ *     next to the GEMM (Colossal-AI FP8 page, "delayed scaling"; guide,
+ *     "delayed scaling scheme");
+ *   - blockwise scaling: one scale per 1x128 tile (activations, gradients) or
+ *     per 128x128 tile (weights), E4M3 (guide, section "block-level scaling");
+ *   - MXFP8: one E8M0 power-of-two scale per 1x32 block (guide, section
+ *     "MXFP8 scaling").
+ * Formats: E4M3 (1-4-3, max 448, no infinity) and E5M2 (1-5-2, max 57344)
+ * (guide, section "format choice E4M3 and E5M2").  GEMM inputs are FP8, the
+ * accumulation FP32, the output BF16 (fprop / dgrad) or FP32 (wgrad) (the
+ * search-result page's mixed-precision dataflow paragraph).
+ *
+ * Conventions shared by every call:
+ *   - Ownership: the caller allocates and owns every buffer.  The library holds
+ *     no allocation.  Pointers marked "device" are device pointers.
+ *   - Asynchrony: every call is enqueued on `stream` and returns without
+ *     waiting (except fp8_get_device_status).  No call synchronizes the host.
+ *   - Layouts: matrices are dense row-major.  A "[R, C] bf16" input has R rows
+ *     of C bfloat16 values.  The column-wise copy of an [R, C] input is the
+ *     [C, R] matrix of its transpose, quantized with the recipe's blocks along
+ *     its own rows.
+ *   - Alignment: matrix pointers must be 16-byte aligned; FP32 scale arrays
+ *     4-byte aligned; GEMM-ready MX scale arrays 16-byte aligned.
+ *   - Errors: arguments are checked on the host before anything is enqueued;
+ *     a rejected call enqueues nothing and returns FP8_ERR_INVALID_ARG,
+ *     FP8_ERR_SHAPE, FP8_ERR_ALIGNMENT or FP8_ERR_UNSUPPORTED.  A CUDA launch
+ *     error returns FP8_ERR_CUDA.  Kernels never trap: a device-side failure
+ *     (a wait that ran out of time, a state argument out of range) sets a
+ *     device error word, read and cleared by fp8_get_device_status.
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FP8_OK = 0,
+  FP8_ERR_INVALID_ARG = 1, /* null pointer, bad enum, negative size */
+  FP8_ERR_SHAPE = 2,       /* a size the recipe or kernel cannot tile */
+  FP8_ERR_ALIGNMENT = 3,   /* a pointer not aligned as required */
+  FP8_ERR_UNSUPPORTED = 4, /* an operand / recipe pairing not provided */
+  FP8_ERR_CUDA = 5,        /* a CUDA runtime error */
+  FP8_ERR_TIMEOUT = 6,     /* a device wait ran out of time (see fp8_get_device_status) */
+  FP8_ERR_DEVICE_STATE = 7 /* a device-resident state argument was out of range */
+} fp8_status;
+
+typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format;
+
+typedef enum {
+  FP8_TENSOR = 0,        /* one FP32 scale for the whole tensor (current or delayed) */
+  FP8_BLOCK_1x128 = 1,   /* one FP32 scale per 128 consecutive elements of a row */
+  FP8_BLOCK_128x128 = 2, /* one FP32 scale per 128x128 tile */
+  FP8_MX_1x32 = 3,       /* one E8M0 byte per 32 consecutive elements of a row, row-major */
+  FP8_MX_1x32_TILED = 4  /* the same exponents in the GEMM-ready tiled layout (below) */
+} fp8_recipe;
+
+typedef enum { FP8_OUT_BF16 = 0, FP8_OUT_FP32 = 1 } fp8_out_dtype;
+
+/*
+ * fp8_amax -- per-tensor amax.  Colossal-AI FP8 page, "current scaling" (the
+ * scale is computed from the maximum of the current tensor).
+ *   x     device, [rows, cols] bf16 (any shape; rows * cols may be 0)
+ *   amax  device, 1 float: receives max |x| over all elements, NaN ignored
+ *         (0 for an empty tensor).  Exact, independent of reduction order.
+ */
+fp8_status fp8_amax(const void* x, int64_t rows, int64_t cols, float* amax, cudaStream_t stream);
+
+/*
+ * fp8_compute_scale -- per-tensor current-scaling scale.  Colossal-AI FP8
+ * page, "current scaling"; guide, "instant scaling scheme".
+ *   amax       device, 1 float (input)
+ *   scale      device, 1 float: FMAX / amax as one binary32 division
+ *              (FMAX = 448 for E4M3, 57344 for E5M2); 1 when amax is 0 or not
+ *              finite; FLT_MAX when the quotient overflows
+ *   scale_inv  device, 1 float: 1 / scale (binary32 division), the
+ *              dequantization multiplier the GEMM takes
+ */
+fp8_status fp8_compute_scale(const float* amax, fp8_format fmt, float* scale, float* scale_inv,
+                             cudaStream_t stream);
+
+/*
+ * amax_history_update -- one delayed-scaling step.  Colossal-AI FP8 page,
+ * "delayed scaling" (the scale comes from a past time window); guide, "delayed
+ * scaling scheme" (a buffer holding the maxima of several past steps).
+ *   hist       device, len floats: the history ring (caller initialises to 0)
+ *   len        history length, >= 1 (16 in the reference configuration)
+ *   pos        device, 1 int32: next write slot, in [0, len) (initialise to 0)
+ *   amax       device, 1 float: this step's amax (e.g. the amax_out of the cast)
+ *   scale,     device, 1 float each: the scale the NEXT step quantizes with and
+ *   scale_inv  its reciprocal (initialise to 1 and 1).
+ * Effect: hist[pos] = amax; pos = (pos + 1) mod len; m = max(hist);
+ * if 0 < m < inf: scale = FMAX / m (overflow -> FLT_MAX), scale_inv = 1 / scale;
+ * otherwise scale and scale_inv are left unchanged.  A pos outside [0, len)
+ * leaves everything unchanged and sets the device error word
+ * (FP8_ERR_DEVICE_STATE from fp8_get_device_status).
+ * The state is these four caller-owned buffers: saving and restoring them
+ * resumes the sequence bit-identically.
+ */
+fp8_status amax_history_update(float* hist, int32_t len, int32_t* pos, const float* amax, fp8_format fmt,
+                               float* scale, float* scale_inv, cudaStream_t stream);
+
+/*
+ * fp8_cast_transpose -- quantize a bf16 matrix into a row-wise and/or a
+ * column-wise FP8 copy plus their scales.  Guide, sections "tensor-level
+ * scaling", "block-level scaling" and "MXFP8 scaling"; the column-wise copy
+ * serves the backward GEMMs, which consume the operands along the other axis
+ * (the search-result page's dataflow paragraph).
+ *   x      device, [rows, cols] bf16
+ *   scale  FP8_TENSOR only: device, 1 float, the scale to multiply by (from
+ *          fp8_compute_scale, or the delayed-scaling state).  NULL otherwise.
+ *   amax_out  optional device float: receives max |x| of this input (NaN
+ *          ignored).  Delayed scaling casts with the previous scale and records
+ *          this step's amax here.
+ *   q_row  device, [rows, cols] u8 FP8 codes, or NULL to skip the row-wise copy
+ *   s_row  its dequantization multipliers:
+ *            FP8_TENSOR:        1 float (1 / scale), may be NULL
+ *            FP8_BLOCK_1x128:   float [rows, cols/128]
+ *            FP8_BLOCK_128x128: float [rows/128, cols/128]
+ *            FP8_MX_1x32:       u8 E8M0 [rows, cols/32] (exponent e stored as e + 127)
+ *            FP8_MX_1x32_TILED: u8 E8M0, (rows/128) * (cols/128) atoms of 512 B;
+ *                               exponent (r, b) at ((r/128)*(cols/128) + b/4)*512
+ *                               + (r%32)*16 + ((r%128)/32)*4 + b%4
+ *   q_col  device, [cols, rows] u8: the column-wise copy (the transpose,
+ *          quantized with blocks along its rows), or NULL to skip it
+ *   s_col  its multipliers, as s_row with rows and cols exchanged
+ *          (FP8_BLOCK_128x128: the transpose of s_row)
+ * Element rule: q = saturating round-to-nearest-even FP8 of (float(x) * s), one
+ * binary32 product, with s = FMAX / amax of the block (FP32 recipes; same edge
+ * rules as fp8_compute_scale) or s = 2^-e (MX: e the smallest integer with
+ * amax <= FMAX * 2^e, clamped to [-127, 127]; 0 for an all-zero block).
+ * Shapes: FP8_TENSOR takes any shape.  Blocked dimensions must be multiples of
+ * the block (128 for the 1x128 copy's rows, 128 for both dims of 128x128, 32
+ * for MX, 128 for both dims of MX_TILED); otherwise FP8_ERR_SHAPE.
+ */
+fp8_status fp8_cast_transpose(const void* x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
+                              const float* scale, float* amax_out, uint8_t* q_row, void* s_row, uint8_t* q_col,
+                              void* s_col, cudaStream_t stream);
+
+/*
+ * fp8_quantize -- the row-wise copy only: fp8_cast_transpose with q_col = NULL.
+ */
+fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
+                        const float* scale, float* amax_out, uint8_t* q, void* s, cudaStream_t stream);
+
+/*
+ * fp8_scaled_gemm -- C = deq(A) . deq(B)^T with FP32 accumulation.
+ * Search-result page, dataflow paragraph (FP8 inputs, FP32 accumulation, BF16
+ * output; wgrad output FP32); guide, "code changes" (the three GEMMs of a layer
+ * take quantized inputs); guide, "block-level scaling" and "MXFP8 scaling" for
+ * the scale pairings.
+ *   A   device, [M, K] u8 FP8 (format fa), K contiguous
+ *   B   device, [N, K] u8 FP8 (format fb), K contiguous
+ *   sA, sB  the multipliers written by fp8_cast_transpose for A and B
+ *   C   device, [M, N] row-major, bf16 (FP8_OUT_BF16, round to nearest) or fp32
+ * Pairings (ra, rb): (TENSOR, TENSOR); (BLOCK_1x128, BLOCK_128x128);
+ * (BLOCK_1x128, BLOCK_1x128); (MX_1x32_TILED, MX_1x32_TILED).  Others return
+ * FP8_ERR_UNSUPPORTED.  M, N, K must be multiples of 128 (FP8_ERR_SHAPE);
+ * M or N == 0 is a no-op, K == 0 writes zeros.
+ */
+fp8_status fp8_scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const void* sA, const uint8_t* B,
+                           fp8_format fb, fp8_recipe rb, const void* sB, int64_t M, int64_t N, int64_t K, void* C,
+                           fp8_out_dtype out, cudaStream_t stream);
+
+/*
+ * fp8_get_device_status -- synchronize `stream`, then read and clear the
+ * device error word of the current device.  Returns FP8_OK, FP8_ERR_TIMEOUT
+ * (some kernel gave up a wait), FP8_ERR_DEVICE_STATE, or FP8_ERR_CUDA.
+ */
+fp8_status fp8_get_device_status(cudaStream_t stream);
+
+/*
+ * fp8_debug_wait_timeout -- enqueue a one-CTA kernel that waits on a barrier
+ * nothing will complete, with the same bounded wait every kernel uses; it
+ * gives up after about one second and reports FP8_ERR_TIMEOUT through
+ * fp8_get_device_status.  Exists to test the failure path without a fault.
+ */
+fp8_status fp8_debug_wait_timeout(cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* fp8_status_string(fp8_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H */

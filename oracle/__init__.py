@@ -208,6 +208,31 @@ def quantize_colwise(x_bf16, kind: int, fmt: int, scale=None):
     return quantize_rowwise(transpose_bf16(x_bf16), kind, fmt, scale)
 
 
+# ----------------------------------------------------------------- MX tiled layout
+def mx_tiled_offsets(rows: int, cols: int) -> np.ndarray:
+    """Byte offset of exponent (r, b) (b = 32-column block) in the GEMM-ready tiled
+    layout of a row-wise MX copy [rows, cols]: atoms of 128 rows x 4 blocks, 512 B
+    each, atom (r/128, b/4) at ((r/128) * ceil(cols/128) + b/4) * 512, and inside an
+    atom (r%32)*16 + ((r%128)/32)*4 + b%4 (the 32x4x4 arrangement the block-scaled
+    MMA's scale-factor copy reads)."""
+    r = np.arange(rows, dtype=np.int64)[:, None]
+    b = np.arange(cols // 32, dtype=np.int64)[None, :]
+    apr = (cols + 127) // 128
+    return ((r // 128) * apr + b // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (b % 4)
+
+
+def mx_to_tiled(s_rowmajor: np.ndarray) -> np.ndarray:
+    rows, nb = s_rowmajor.shape
+    cols = nb * 32
+    out = np.zeros((((rows + 127) // 128) * ((cols + 127) // 128) * 512,), np.uint8)
+    out[mx_tiled_offsets(rows, cols)] = s_rowmajor
+    return out
+
+
+def mx_from_tiled(tiled: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    return np.asarray(tiled).reshape(-1)[mx_tiled_offsets(rows, cols)]
+
+
 # ----------------------------------------------------------------- GEMM
 def dequantize(q, kind: int, fmt: int, s) -> np.ndarray:
     q = np.ascontiguousarray(q, dtype=np.uint8)

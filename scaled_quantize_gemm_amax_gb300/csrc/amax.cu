@@ -1,0 +1,141 @@
+// amax.cu -- per-tensor amax reduction, per-tensor scale, and the delayed-scaling
+// amax-history update.
+//
+// amax: the maximum of |x| over a BF16 tensor, NaN ignored (Colossal-AI FP8,
+// "current scaling": the scale comes from the current tensor's maximum).  The
+// reduction is order-free (a max), so any grid shape gives the same bits.
+// History: a ring of past amaxes; the next scale comes from the window maximum
+// (Colossal-AI FP8, "delayed scaling"; guide, "delayed scaling scheme").
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "recipes.cuh"
+
+namespace fp8q {
+
+namespace {
+
+constexpr int kAmaxThreads = 256;
+constexpr int kAmaxUnroll = 8;
+
+__device__ __forceinline__ uint32_t fold16(uint32_t m, uint4 v) {
+  m = absmax_bf16x2(m, v.x);
+  m = absmax_bf16x2(m, v.y);
+  m = absmax_bf16x2(m, v.z);
+  m = absmax_bf16x2(m, v.w);
+  return m;
+}
+
+// Grid-stride max over 16-byte chunks (8 bf16 each), 8 independent loads in
+// flight per thread; the n % 8 tail is folded in by block 0.  One atomicMax per
+// block on the (non-negative) float bit pattern, which orders like the value.
+__global__ void __launch_bounds__(kAmaxThreads) k_amax(const uint4* __restrict__ x16, int64_t n16,
+                                                      const uint16_t* __restrict__ tail, int ntail,
+                                                      float* __restrict__ amax) {
+  uint32_t m = 0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + (kAmaxUnroll - 1) * stride < n16; i += kAmaxUnroll * stride) {
+    uint4 v[kAmaxUnroll];
+#pragma unroll
+    for (int u = 0; u < kAmaxUnroll; ++u) v[u] = __ldg(x16 + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < kAmaxUnroll; ++u) m = fold16(m, v[u]);
+  }
+  for (; i < n16; i += stride) m = fold16(m, __ldg(x16 + i));
+  float a = pair_max_f32(m);
+  if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < ntail)
+    a = fmaxf(a, fabsf(__uint_as_float(static_cast<uint32_t>(tail[threadIdx.x]) << 16)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+  __shared__ float red[kAmaxThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = red[0];
+    for (int w = 1; w < kAmaxThreads / 32; ++w) b = fmaxf(b, red[w]);
+    if (b > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(amax), __float_as_uint(b));
+  }
+}
+
+__global__ void k_compute_scale(const float* __restrict__ amax, int e5m2, float* __restrict__ scale,
+                                float* __restrict__ scale_inv) {
+  if (threadIdx.x != 0) return;
+  const float s = scale_from_amax(*amax, fmax_of(e5m2 != 0));
+  *scale = s;
+  *scale_inv = recip_rn(s);
+}
+
+// hist[pos] = amax; pos = (pos + 1) mod len; m = max(hist) (NaN ignored);
+// if 0 < m < inf: scale = FMAX / m (inf -> FLT_MAX), scale_inv = 1 / scale;
+// otherwise the scale is left as it is.
+__global__ void k_history_update(float* __restrict__ hist, int32_t len, int32_t* __restrict__ pos,
+                                 const float* __restrict__ amax, int e5m2, float* __restrict__ scale,
+                                 float* __restrict__ scale_inv, uint32_t* err) {
+  if (threadIdx.x != 0) return;
+  const int32_t p = *pos;
+  if (p < 0 || p >= len) {
+    atomicOr(err, kErrBadState);
+    return;
+  }
+  hist[p] = *amax;
+  *pos = (p + 1) % len;
+  float m = 0.0f;
+  for (int32_t i = 0; i < len; ++i) {
+    const float h = hist[i];
+    if (h > m) m = h;
+  }
+  if (m > 0.0f && !is_inf_or_nan(m)) {
+    float s = __fdiv_rn(fmax_of(e5m2 != 0), m);
+    if (is_inf_or_nan(s)) s = FLT_MAX;
+    *scale = s;
+    *scale_inv = recip_rn(s);
+  }
+}
+
+// One CTA waits for an mbarrier phase that never completes; the bounded wait
+// must give up, report kErrTimeoutTmaLoad and let the kernel return.
+__global__ void k_wait_selftest(uint32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(b, 0, err, kErrTimeoutTmaLoad, nullptr);
+  __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_amax(const void* x, int64_t n, float* amax, int num_sms, cudaStream_t s) {
+  const int64_t n16 = n / 8;
+  const int ntail = static_cast<int>(n - n16 * 8);
+  int64_t want = (n16 + static_cast<int64_t>(kAmaxThreads) * kAmaxUnroll - 1) / (kAmaxThreads * kAmaxUnroll);
+  int64_t cap = static_cast<int64_t>(num_sms) * 4;
+  int grid = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
+  k_amax<<<grid, kAmaxThreads, 0, s>>>(static_cast<const uint4*>(x), n16,
+                                       static_cast<const uint16_t*>(x) + n16 * 8, ntail, amax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compute_scale(const float* amax, bool e5m2, float* scale, float* scale_inv, cudaStream_t s) {
+  k_compute_scale<<<1, 32, 0, s>>>(amax, e5m2 ? 1 : 0, scale, scale_inv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_history_update(float* hist, int32_t len, int32_t* pos, const float* amax, bool e5m2, float* scale,
+                                  float* scale_inv, uint32_t* err, cudaStream_t s) {
+  k_history_update<<<1, 32, 0, s>>>(hist, len, pos, amax, e5m2 ? 1 : 0, scale, scale_inv, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t s) {
+  k_wait_selftest<<<1, 32, 0, s>>>(err);
+  return cudaGetLastError();
+}
+
+}  // namespace fp8q

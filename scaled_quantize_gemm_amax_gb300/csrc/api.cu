@@ -1,0 +1,298 @@
+// api.cu -- the C ABI (include/fp8q.h): argument checks, TMA tensor maps and
+// dispatch to the kernels.  All checks run on the host before anything is
+// enqueued, and before any CUDA call, so a rejected call has no effect.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "fp8q.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8q {
+namespace {
+
+// The device error word (one per device that loads the library).
+__device__ uint32_t g_error_word;
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  uint32_t* err = nullptr;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+fp8_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8_ERR_CUDA;
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!d.ready) {
+      int n = 0;
+      if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FP8_ERR_CUDA;
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return FP8_ERR_CUDA;
+      d.num_sms = n;
+      d.err = static_cast<uint32_t*>(p);
+      d.ready = true;
+    }
+  }
+  *out = &d;
+  return FP8_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major tensor [outer, inner] of `elem` bytes, box [box_outer, box_inner].
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t elem, const void* ptr, uint64_t inner, uint64_t outer,
+              uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * elem};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool valid_fmt(fp8_format f) { return f == FP8_E4M3 || f == FP8_E5M2; }
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;   // TMA coordinates are signed 32-bit
+
+fp8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
+
+}  // namespace
+}  // namespace fp8q
+
+using namespace fp8q;
+
+extern "C" {
+
+const char* fp8_status_string(fp8_status s) {
+  switch (s) {
+    case FP8_OK: return "FP8_OK";
+    case FP8_ERR_INVALID_ARG: return "FP8_ERR_INVALID_ARG";
+    case FP8_ERR_SHAPE: return "FP8_ERR_SHAPE";
+    case FP8_ERR_ALIGNMENT: return "FP8_ERR_ALIGNMENT";
+    case FP8_ERR_UNSUPPORTED: return "FP8_ERR_UNSUPPORTED";
+    case FP8_ERR_CUDA: return "FP8_ERR_CUDA";
+    case FP8_ERR_TIMEOUT: return "FP8_ERR_TIMEOUT";
+    case FP8_ERR_DEVICE_STATE: return "FP8_ERR_DEVICE_STATE";
+  }
+  return "FP8_ERR_UNKNOWN";
+}
+
+fp8_status fp8_amax(const void* x, int64_t rows, int64_t cols, float* amax, cudaStream_t stream) {
+  if (rows < 0 || cols < 0 || amax == nullptr) return FP8_ERR_INVALID_ARG;
+  const int64_t n = rows * cols;
+  if (n > 0 && x == nullptr) return FP8_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(amax, 4)) return FP8_ERR_ALIGNMENT;
+  DeviceInfo* d;
+  if (fp8_status st = device_info(&d)) return st;
+  if (cudaMemsetAsync(amax, 0, sizeof(float), stream) != cudaSuccess) return FP8_ERR_CUDA;
+  if (n == 0) return FP8_OK;
+  return cuda_status(launch_amax(x, n, amax, d->num_sms, stream));
+}
+
+fp8_status fp8_compute_scale(const float* amax, fp8_format fmt, float* scale, float* scale_inv,
+                             cudaStream_t stream) {
+  if (amax == nullptr || scale == nullptr || scale_inv == nullptr || !valid_fmt(fmt)) return FP8_ERR_INVALID_ARG;
+  if (!aligned(amax, 4) || !aligned(scale, 4) || !aligned(scale_inv, 4)) return FP8_ERR_ALIGNMENT;
+  return cuda_status(launch_compute_scale(amax, fmt == FP8_E5M2, scale, scale_inv, stream));
+}
+
+fp8_status amax_history_update(float* hist, int32_t len, int32_t* pos, const float* amax, fp8_format fmt,
+                               float* scale, float* scale_inv, cudaStream_t stream) {
+  if (hist == nullptr || pos == nullptr || amax == nullptr || scale == nullptr || scale_inv == nullptr || len < 1 ||
+      !valid_fmt(fmt))
+    return FP8_ERR_INVALID_ARG;
+  if (!aligned(hist, 4) || !aligned(pos, 4) || !aligned(amax, 4) || !aligned(scale, 4) || !aligned(scale_inv, 4))
+    return FP8_ERR_ALIGNMENT;
+  DeviceInfo* d;
+  if (fp8_status st = device_info(&d)) return st;
+  return cuda_status(launch_history_update(hist, len, pos, amax, fmt == FP8_E5M2, scale, scale_inv, d->err, stream));
+}
+
+fp8_status fp8_cast_transpose(const void* x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
+                              const float* scale, float* amax_out, uint8_t* q_row, void* s_row, uint8_t* q_col,
+                              void* s_col, cudaStream_t stream) {
+  if (rows < 0 || cols < 0 || !valid_fmt(fmt) || recipe < FP8_TENSOR || recipe > FP8_MX_1x32_TILED)
+    return FP8_ERR_INVALID_ARG;
+  const int64_t n = rows * cols;
+  if (n == 0) {
+    // nothing to cast (outputs of an empty tensor may be NULL); amax of nothing is 0
+    if (!aligned(amax_out, 4)) return FP8_ERR_ALIGNMENT;
+    if (amax_out != nullptr && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess)
+      return FP8_ERR_CUDA;
+    return FP8_OK;
+  }
+  const bool do_row = q_row != nullptr, do_col = q_col != nullptr;
+  if (!do_row && !do_col) return FP8_ERR_INVALID_ARG;
+  if (x == nullptr) return FP8_ERR_INVALID_ARG;
+  const bool mx = recipe == FP8_MX_1x32 || recipe == FP8_MX_1x32_TILED;
+  if (recipe == FP8_TENSOR) {
+    if (scale == nullptr) return FP8_ERR_INVALID_ARG;
+  } else {
+    if ((do_row && s_row == nullptr) || (do_col && s_col == nullptr)) return FP8_ERR_INVALID_ARG;
+  }
+  // blocked dimensions
+  switch (recipe) {
+    case FP8_BLOCK_1x128:
+      if ((do_row && cols % 128) || (do_col && rows % 128)) return FP8_ERR_SHAPE;
+      break;
+    case FP8_BLOCK_128x128:
+      if (rows % 128 || cols % 128) return FP8_ERR_SHAPE;
+      break;
+    case FP8_MX_1x32:
+      if ((do_row && cols % 32) || (do_col && rows % 32)) return FP8_ERR_SHAPE;
+      break;
+    case FP8_MX_1x32_TILED:
+      if (rows % 128 || cols % 128) return FP8_ERR_SHAPE;
+      break;
+    default:
+      break;
+  }
+  if (rows > kMaxDim || cols > kMaxDim) return FP8_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(q_row, 16) || !aligned(q_col, 16)) return FP8_ERR_ALIGNMENT;
+  if (!mx && (!aligned(s_row, 4) || !aligned(s_col, 4))) return FP8_ERR_ALIGNMENT;
+  if (recipe == FP8_MX_1x32_TILED && (!aligned(s_row, 16) || !aligned(s_col, 16))) return FP8_ERR_ALIGNMENT;
+  if (!aligned(scale, 4) || !aligned(amax_out, 4)) return FP8_ERR_ALIGNMENT;
+
+  DeviceInfo* d;
+  if (fp8_status st = device_info(&d)) return st;
+  if (amax_out != nullptr && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess) return FP8_ERR_CUDA;
+
+  CastParams p{};
+  p.R = rows;
+  p.C = cols;
+  p.recipe = mx ? kMx : static_cast<int>(recipe);
+  p.e5m2 = fmt == FP8_E5M2;
+  p.mx_tiled = recipe == FP8_MX_1x32_TILED;
+  p.do_row = do_row;
+  p.do_col = do_col;
+  p.scale = scale;
+  p.amax_out = amax_out;
+  p.q_row = q_row;
+  p.q_col = q_col;
+  p.s_row = s_row;
+  p.s_col = s_col;
+  p.err = d->err;
+  p.tiles_r = static_cast<int>((rows + 127) / 128);
+  p.tiles_c = static_cast<int>((cols + 127) / 128);
+
+  const bool tiled_ok = (cols % 16 == 0) && (!do_col || rows % 16 == 0);
+  if (!tiled_ok) {
+    // only the per-tensor recipe reaches here (block recipes imply the alignment)
+    return cuda_status(launch_cast_generic(p, x, stream));
+  }
+  CUtensorMap tm_x, tm_qr, tm_qc;
+  std::memset(&tm_qr, 0, sizeof(tm_qr));
+  std::memset(&tm_qc, 0, sizeof(tm_qc));
+  if (!make_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, cols, rows, 64, 128)) return FP8_ERR_CUDA;
+  if (do_row && !make_map(&tm_qr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q_row, cols, rows, 128, 128)) return FP8_ERR_CUDA;
+  if (do_col && !make_map(&tm_qc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q_col, rows, cols, 128, 128)) return FP8_ERR_CUDA;
+  return cuda_status(launch_cast_transpose_tiled(p, tm_x, tm_qr, tm_qc, d->num_sms, stream));
+}
+
+fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
+                        const float* scale, float* amax_out, uint8_t* q, void* s, cudaStream_t stream) {
+  if (q == nullptr && rows > 0 && cols > 0) return FP8_ERR_INVALID_ARG;
+  return fp8_cast_transpose(x, rows, cols, recipe, fmt, scale, amax_out, q, s, nullptr, nullptr, stream);
+}
+
+fp8_status fp8_scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const void* sA, const uint8_t* B,
+                           fp8_format fb, fp8_recipe rb, const void* sB, int64_t M, int64_t N, int64_t K, void* C,
+                           fp8_out_dtype out, cudaStream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || !valid_fmt(fa) || !valid_fmt(fb) || (out != FP8_OUT_BF16 && out != FP8_OUT_FP32))
+    return FP8_ERR_INVALID_ARG;
+  int kind;
+  int b_1x128 = 0;
+  if (ra == FP8_TENSOR && rb == FP8_TENSOR) {
+    kind = kTensor;
+  } else if (ra == FP8_BLOCK_1x128 && rb == FP8_BLOCK_128x128) {
+    kind = kBlock1x128;
+  } else if (ra == FP8_BLOCK_1x128 && rb == FP8_BLOCK_1x128) {
+    kind = kBlock1x128;
+    b_1x128 = 1;
+  } else if (ra == FP8_MX_1x32_TILED && rb == FP8_MX_1x32_TILED) {
+    kind = kMx;
+  } else if ((ra >= FP8_TENSOR && ra <= FP8_MX_1x32_TILED) && (rb >= FP8_TENSOR && rb <= FP8_MX_1x32_TILED)) {
+    return FP8_ERR_UNSUPPORTED;
+  } else {
+    return FP8_ERR_INVALID_ARG;
+  }
+  const int64_t outsz = out == FP8_OUT_FP32 ? 4 : 2;
+  if (M == 0 || N == 0) return FP8_OK;
+  if (C == nullptr) return FP8_ERR_INVALID_ARG;
+  if (M % 128 || N % 128 || K % 128) return FP8_ERR_SHAPE;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8_ERR_SHAPE;
+  if (!aligned(C, 16)) return FP8_ERR_ALIGNMENT;
+  if (K > 0) {
+    if (A == nullptr || B == nullptr || sA == nullptr || sB == nullptr) return FP8_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16)) return FP8_ERR_ALIGNMENT;
+    const uintptr_t sal = kind == kMx ? 16 : 4;
+    if (!aligned(sA, sal) || !aligned(sB, sal)) return FP8_ERR_ALIGNMENT;
+  }
+  DeviceInfo* d;
+  if (fp8_status st = device_info(&d)) return st;
+  if (K == 0) return cuda_status(cudaMemsetAsync(C, 0, static_cast<size_t>(M * N * outsz), stream));
+
+  CUtensorMap tm_a, tm_b;
+  if (!make_map(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128)) return FP8_ERR_CUDA;
+  if (!make_map(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, static_cast<uint32_t>(gemm_block_n(kind))))
+    return FP8_ERR_CUDA;
+  GemmParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.kind = kind;
+  p.b_1x128 = b_1x128;
+  p.e5m2_a = fa == FP8_E5M2;
+  p.e5m2_b = fb == FP8_E5M2;
+  p.out_fp32 = out == FP8_OUT_FP32;
+  p.sa = sA;
+  p.sb = sB;
+  p.c = C;
+  p.err = d->err;
+  return cuda_status(launch_gemm(p, tm_a, tm_b, d->num_sms, stream));
+}
+
+fp8_status fp8_get_device_status(cudaStream_t stream) {
+  DeviceInfo* d;
+  if (fp8_status st = device_info(&d)) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FP8_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, d->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return FP8_ERR_CUDA;
+  if (word != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(d->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FP8_ERR_CUDA;
+  }
+  if (word & (kErrTimeoutTmaLoad | kErrTimeoutMma | kErrTimeoutStage)) return FP8_ERR_TIMEOUT;
+  if (word & kErrBadState) return FP8_ERR_DEVICE_STATE;
+  return FP8_OK;
+}
+
+fp8_status fp8_debug_wait_timeout(cudaStream_t stream) {
+  DeviceInfo* d;
+  if (fp8_status st = device_info(&d)) return st;
+  return cuda_status(launch_wait_selftest(d->err, stream));
+}
+
+}  // extern "C"

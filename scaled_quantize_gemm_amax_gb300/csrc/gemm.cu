@@ -1,0 +1,423 @@
+// gemm.cu -- scaled FP8 GEMM on the 5th-generation tensor cores (tcgen05).
+//
+//   C[m, n] = sum_k deq(A)[m, k] * deq(B)[n, k],  A [M, K], B [N, K], both K-major FP8,
+//   FP32 accumulation, C row-major BF16 (fprop / dgrad) or FP32 (wgrad)
+// (mixed-precision dataflow paragraph of the search-result page: quantized inputs,
+// FP32 accumulation, BF16 output; wgrad stays FP32).  Dequantization by recipe:
+//   per-tensor  C = sA_inv * sB_inv * sum qA qB                (epilogue scale)
+//   blockwise   C = sum_kb sA[m, kb] * sB[n/128 | n, kb] * sum_{k in kb} qA qB
+//               (guide, "block-level scaling": 1x128 activations, 128x128 weights;
+//                each 128-deep partial product is promoted into FP32 registers)
+//   MXFP8       the tensor core applies 2^(eA - 127) * 2^(eB - 127) per 32-deep block
+//               (guide, "MXFP8 scaling"; kind::mxf8f6f4.block_scale)
+//
+// Structure: a persistent grid (one CTA per SM, 320 threads).
+//   warp 0      TMA producer: A / B tiles (128-byte swizzle) into a ring of stages,
+//               plus MX scale atoms by bulk copy
+//   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma (and the scale copies)
+//   warps 2..9  epilogue: tcgen05.ld from TMEM, scale, convert, store.  Warp w reads
+//               TMEM lanes 32*(w%4).. (its quarter) and half (w-2)/4 of the columns.
+// Every wait is time-bounded (ptx.cuh); a timeout sets the device error word, the
+// other roles see a shared abort flag, and the CTA drains and frees TMEM.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "recipes.cuh"
+
+namespace fp8q {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 128;               // bytes (= FP8 elements) of K per stage
+constexpr int kUmmaK = 32;             // K of one MMA instruction for 8-bit inputs
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kGroupM = 8;             // tile raster: groups of 8 M-tiles share B tiles in L2
+constexpr uint32_t kTmemCols = 512;
+
+template <int KIND>
+struct Cfg;
+template <>
+struct Cfg<kTensor> {
+  static constexpr int BN = 256, STAGES = 4, ACC = 2;
+};
+template <>
+struct Cfg<kBlock1x128> {
+  static constexpr int BN = 128, STAGES = 6, ACC = 4;   // ACC = TMEM partial buffers
+};
+template <>
+struct Cfg<kMx> {
+  static constexpr int BN = 256, STAGES = 4, ACC = 1;
+};
+
+template <int KIND>
+struct Layout {
+  static constexpr int BN = Cfg<KIND>::BN, S = Cfg<KIND>::STAGES;
+  static constexpr uint32_t A_BYTES = kBM * kBK, B_BYTES = BN * kBK;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t SF_BYTES = (KIND == kMx) ? (512 + 512 * (BN / 128)) : 0;   // per stage
+  static constexpr uint32_t OFF_SF = S * STAGE_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_SF + S * SF_BYTES;
+  // barriers: full[S], empty[S], tfull[4], tempty[4], final
+  static constexpr uint32_t OFF_FULL = OFF_BAR, OFF_EMPTY = OFF_BAR + 8 * S;
+  static constexpr uint32_t OFF_TFULL = OFF_EMPTY + 8 * S, OFF_TEMPTY = OFF_TFULL + 32;
+  static constexpr uint32_t OFF_FINAL = OFF_TEMPTY + 32;
+  static constexpr uint32_t OFF_TMEM = OFF_FINAL + 8, OFF_ABORT = OFF_TMEM + 4;
+  static constexpr uint32_t SMEM = OFF_ABORT + 64 + 1024;   // + alignment slack
+  static constexpr uint32_t TX_BYTES = STAGE_BYTES + SF_BYTES;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ void stg128(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Store 32 consecutive FP32 values (already scaled) of one output row.
+__device__ __forceinline__ void store_row32(void* c, int64_t off, const float (&v)[32], bool fp32) {
+  if (fp32) {
+    float* p = static_cast<float*>(c) + off;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      stg128(p + 4 * i, __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]), __float_as_uint(v[4 * i + 2]),
+             __float_as_uint(v[4 * i + 3]));
+  } else {
+    __nv_bfloat16* p = static_cast<__nv_bfloat16*>(c) + off;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      stg128(p + 8 * i, pack_bf16(v[8 * i], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
+             pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
+  }
+}
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
+  const int per_group = kGroupM * tiles_n;
+  const int group = t / per_group;
+  const int first_m = group * kGroupM;
+  const int gsize = min(tiles_m - first_m, kGroupM);
+  const int r = t % per_group;
+  tm = first_m + r % gsize;
+  tn = r / gsize;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, const GemmParams p) {
+  using L = Layout<KIND>;
+  constexpr int BN = L::BN, S = L::S, ACC = Cfg<KIND>::ACC;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - smem_u32(smem_raw));
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::OFF_ABORT);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int tiles_m = static_cast<int>(p.M / kBM), tiles_n = static_cast<int>((p.N + BN - 1) / BN);
+  const int ntiles = tiles_m * tiles_n;
+  const int KB = static_cast<int>(p.K / kBK);
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_b);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(base + L::OFF_FULL + 8 * s, 1);
+      mbar_init(base + L::OFF_EMPTY + 8 * s, 1);
+    }
+    for (int a = 0; a < 4; ++a) {
+      mbar_init(base + L::OFF_TFULL + 8 * a, 1);
+      mbar_init(base + L::OFF_TEMPTY + 8 * a, kEpiWarps);
+    }
+    mbar_init(base + L::OFF_FINAL, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(base + L::OFF_TMEM, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base_ptr + L::OFF_TMEM);
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ producer
+    int issued[S];
+#pragma unroll
+    for (int s = 0; s < S; ++s) issued[s] = 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      int tm, tn;
+      tile_coords(t, tiles_m, tiles_n, tm, tn);
+      for (int kb = 0; kb < KB; ++kb) {
+        const uint32_t full = base + L::OFF_FULL + 8 * stage;
+        if (!mbar_wait(base + L::OFF_EMPTY + 8 * stage, phase ^ 1u, p.err, kErrTimeoutStage, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = base + stage * L::STAGE_BYTES;
+        mbar_arrive_expect_tx(full, L::TX_BYTES);
+        tma_load_2d(sa, &tm_a, kb * kBK, tm * kBM, full);
+        tma_load_2d(sa + L::A_BYTES, &tm_b, kb * kBK, tn * BN, full);
+        if (KIND == kMx) {
+          const uint32_t sf = base + L::OFF_SF + stage * L::SF_BYTES;
+          const uint8_t* ga = static_cast<const uint8_t*>(p.sa) + (static_cast<int64_t>(tm) * KB + kb) * 512;
+          bulk_load(sf, ga, 512, full);
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h) {
+            // a tile hanging over N reuses the last real atom (its B rows are zero-filled)
+            const int64_t atom_row = min(static_cast<int64_t>(tn * (BN / 128) + h), (p.N - 1) / 128);
+            const uint8_t* gb = static_cast<const uint8_t*>(p.sb) + (atom_row * KB + kb) * 512;
+            bulk_load(sf + 512 + 512 * h, gb, 512, full);
+          }
+        }
+        ++issued[stage];
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // loads this CTA issued must land before it exits (they have, unless a consumer aborted)
+#pragma unroll
+    for (int s = 0; s < S; ++s)
+      if (issued[s] > 0)
+        mbar_wait(base + L::OFF_FULL + 8 * s, static_cast<uint32_t>(issued[s] - 1) & 1u, p.err, kErrTimeoutTmaLoad,
+                  nullptr);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------ MMA issuer
+    uint32_t idesc;
+    if (KIND == kMx) {
+      idesc = (static_cast<uint32_t>(p.e5m2_a) << 7) | (static_cast<uint32_t>(p.e5m2_b) << 10) |
+              (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(kBM >> 4) << 24);
+    } else {
+      idesc = (1u << 4) | (static_cast<uint32_t>(p.e5m2_a) << 7) | (static_cast<uint32_t>(p.e5m2_b) << 10) |
+              (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
+    }
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t acc_it = 0, part_it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      uint32_t d = tmem;
+      if (KIND != kBlock1x128) {
+        const uint32_t a = acc_it % ACC;
+        if (!mbar_wait(base + L::OFF_TEMPTY + 8 * a, ((acc_it / ACC) & 1u) ^ 1u, p.err, kErrTimeoutMma, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        d = tmem + a * BN;
+      }
+      for (int kb = 0; kb < KB; ++kb) {
+        if (KIND == kBlock1x128) {
+          const uint32_t pb = part_it % ACC;
+          if (!mbar_wait(base + L::OFF_TEMPTY + 8 * pb, ((part_it / ACC) & 1u) ^ 1u, p.err, kErrTimeoutMma,
+                         abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          d = tmem + pb * BN;
+        }
+        if (!mbar_wait(base + L::OFF_FULL + 8 * stage, phase, p.err, kErrTimeoutTmaLoad, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = base + stage * L::STAGE_BYTES;
+        const uint32_t sb = sa + L::A_BYTES;
+        if (KIND == kMx) {
+          const uint32_t sf = base + L::OFF_SF + stage * L::SF_BYTES;
+          const uint32_t sf_col = 256u + static_cast<uint32_t>(stage) * (4u + 4u * (BN / 128));
+          tc_cp_32x128b_warpx4(tmem + sf_col, sdesc_rows16(sf));
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h) tc_cp_32x128b_warpx4(tmem + sf_col + 4 + 4 * h, sdesc_rows16(sf + 512 + 512 * h));
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            const uint32_t id = idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+            tc_mma_mxf8f6f4(d, sdesc_k_sw128(sa + k * kUmmaK), sdesc_k_sw128(sb + k * kUmmaK), id, tmem + sf_col,
+                            tmem + sf_col + 4, (kb | k) != 0 ? 1u : 0u);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            const uint32_t accumulate = (KIND == kBlock1x128) ? (k != 0) : ((kb | k) != 0);
+            tc_mma_f8f6f4(d, sdesc_k_sw128(sa + k * kUmmaK), sdesc_k_sw128(sb + k * kUmmaK), idesc, accumulate);
+          }
+        }
+        tc_commit(base + L::OFF_EMPTY + 8 * stage);
+        if (KIND == kBlock1x128) {
+          tc_commit(base + L::OFF_TFULL + 8 * (part_it % ACC));
+          ++part_it;
+        }
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (KIND != kBlock1x128) {
+        tc_commit(base + L::OFF_TFULL + 8 * (acc_it % ACC));
+        ++acc_it;
+      }
+    }
+    // every MMA this thread issued has finished before TMEM is released
+    tc_commit(base + L::OFF_FINAL);
+    mbar_wait(base + L::OFF_FINAL, 0, p.err, kErrTimeoutMma, nullptr);
+  } else if (warp >= 2) {
+    // ------------------------------------------------ epilogue
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;          // column half
+    const int row = 32 * q + lane;          // row within the tile
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    const bool fp32 = p.out_fp32 != 0;
+    float tensor_scale = 1.0f;
+    if (KIND == kTensor) tensor_scale = __fmul_rn(*static_cast<const float*>(p.sa), *static_cast<const float*>(p.sb));
+    uint32_t acc_it = 0, part_it = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      int tm, tn;
+      tile_coords(t, tiles_m, tiles_n, tm, tn);
+      const int64_t grow = static_cast<int64_t>(tm) * kBM + row;
+      const int64_t gcol0 = static_cast<int64_t>(tn) * BN + h * (BN / 2);
+      if (KIND == kBlock1x128) {
+        const float* sa_row = static_cast<const float*>(p.sa) + grow * KB;
+        const float* sb_blk = static_cast<const float*>(p.sb);
+        float acc[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+        bool ok = true;
+        float sa_next = sa_row[0];
+        for (int kb = 0; kb < KB; ++kb) {
+          const float sa_v = sa_next;
+          if (kb + 1 < KB) sa_next = sa_row[kb + 1];
+          const uint32_t pb = part_it % ACC;
+          // warp-uniform decision: the TMEM loads below are .sync.aligned
+          if (!__all_sync(0xFFFFFFFFu,
+                          mbar_wait(base + L::OFF_TFULL + 8 * pb, (part_it / ACC) & 1u, p.err, kErrTimeoutMma, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t r0[32], r1[32];
+          tc_ld_32x32b_x32(lane_base + pb * BN + h * 64, r0);
+          tc_ld_32x32b_x32(lane_base + pb * BN + h * 64 + 32, r1);
+          tc_wait_ld(r0);
+          tc_wait_ld(r1);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(base + L::OFF_TEMPTY + 8 * pb);
+          ++part_it;
+          if (p.b_1x128) {
+            // per-column B scales: sB[n, kb]
+            const float* sbc = sb_blk + (gcol0)*KB + kb;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = fmaf(sa_v * __ldg(sbc + j * KB), __uint_as_float(r0[j]), acc[j]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              acc[32 + j] = fmaf(sa_v * __ldg(sbc + (32 + j) * KB), __uint_as_float(r1[j]), acc[32 + j]);
+          } else {
+            const float f = sa_v * __ldg(sb_blk + static_cast<int64_t>(tn) * KB + kb);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = fmaf(f, __uint_as_float(r0[j]), acc[j]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[32 + j] = fmaf(f, __uint_as_float(r1[j]), acc[32 + j]);
+          }
+        }
+        if (!ok) break;
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = acc[j];
+        if (gcol0 < p.N) store_row32(p.c, grow * p.N + gcol0, v, fp32);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = acc[32 + j];
+        if (gcol0 + 32 < p.N) store_row32(p.c, grow * p.N + gcol0 + 32, v, fp32);
+      } else {
+        const uint32_t a = acc_it % ACC;
+        if (!__all_sync(0xFFFFFFFFu,
+                        mbar_wait(base + L::OFF_TFULL + 8 * a, (acc_it / ACC) & 1u, p.err, kErrTimeoutMma, abort_flag)))
+          break;
+        tc_fence_after();
+        const uint32_t col_base = lane_base + a * BN + h * (BN / 2);
+        if (KIND == kMx) {
+          // pull the whole half-row into registers, free the accumulator, then store
+          uint32_t r[4][32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tc_ld_32x32b_x32(col_base + 32 * c, r[c]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tc_wait_ld(r[c]);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(base + L::OFF_TEMPTY + 8 * a);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[c][j]);
+            if (gcol0 + 32 * c < p.N) store_row32(p.c, grow * p.N + gcol0 + 32 * c, v, fp32);
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < BN / 64; ++c) {
+            uint32_t r[32];
+            tc_ld_32x32b_x32(col_base + 32 * c, r);
+            tc_wait_ld(r);
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), tensor_scale);
+            if (gcol0 + 32 * c < p.N) store_row32(p.c, grow * p.N + gcol0 + 32 * c, v, fp32);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(base + L::OFF_TEMPTY + 8 * a);
+        }
+        ++acc_it;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int KIND>
+cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int num_sms,
+                        cudaStream_t s) {
+  using L = Layout<KIND>;
+  static_assert(L::SMEM <= 232448, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(k_gemm<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(L::SMEM));
+  if (e != cudaSuccess) return e;
+  const int64_t ntiles = (p.M / kBM) * ((p.N + L::BN - 1) / L::BN);
+  const int grid = static_cast<int>(ntiles < num_sms ? ntiles : num_sms);
+  k_gemm<KIND><<<grid, kThreads, L::SMEM, s>>>(tm_a, tm_b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_block_n(int kind) {
+  return kind == kBlock1x128 ? Cfg<kBlock1x128>::BN : (kind == kMx ? Cfg<kMx>::BN : Cfg<kTensor>::BN);
+}
+
+cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int num_sms,
+                        cudaStream_t s) {
+  switch (p.kind) {
+    case kTensor: return launch_kind<kTensor>(p, tm_a, tm_b, num_sms, s);
+    case kBlock1x128: return launch_kind<kBlock1x128>(p, tm_a, tm_b, num_sms, s);
+    default: return launch_kind<kMx>(p, tm_a, tm_b, num_sms, s);
+  }
+}
+
+}  // namespace fp8q

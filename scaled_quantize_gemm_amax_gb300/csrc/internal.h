@@ -1,0 +1,59 @@
+// internal.h -- launchers shared between the C-ABI layer and the kernel files.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fp8q {
+
+enum Recipe : int { kTensor = 0, kBlock1x128 = 1, kBlock128x128 = 2, kMx = 3 };
+
+// ---- amax / scale / history (amax.cu)
+cudaError_t launch_amax(const void* x, int64_t n, float* amax, int num_sms, cudaStream_t s);
+cudaError_t launch_compute_scale(const float* amax, bool e5m2, float* scale, float* scale_inv, cudaStream_t s);
+cudaError_t launch_history_update(float* hist, int32_t len, int32_t* pos, const float* amax, bool e5m2, float* scale,
+                                  float* scale_inv, uint32_t* err, cudaStream_t s);
+
+// ---- quantize / cast-transpose (quantize.cu)
+struct CastParams {
+  int64_t R, C;          // input rows / columns (bf16, row-major)
+  int recipe;
+  int e5m2;
+  int mx_tiled;          // MX scales in the GEMM-ready tiled layout
+  int do_row, do_col;
+  const float* scale;    // per-tensor scale (device)
+  float* amax_out;       // optional (device, pre-zeroed)
+  uint8_t* q_row;        // [R, C] (generic path only; the tiled path stores through tensor maps)
+  uint8_t* q_col;        // [C, R]
+  void* s_row;
+  void* s_col;
+  uint32_t* err;
+  int tiles_r, tiles_c;
+};
+// Tiled TMA path; requires C % 16 == 0 and (when do_col) R % 16 == 0.
+cudaError_t launch_cast_transpose_tiled(const CastParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_qrow,
+                                        const CUtensorMap& tm_qcol, int num_sms, cudaStream_t s);
+// Plain path for the per-tensor recipe at any shape.
+cudaError_t launch_cast_generic(const CastParams& p, const void* x, cudaStream_t s);
+
+// ---- scaled GEMM (gemm.cu)
+struct GemmParams {
+  int64_t M, N, K;
+  int kind;              // kTensor, kBlock1x128 (A 1x128), kMx
+  int b_1x128;           // blockwise: B scales per (row, 128-K) instead of per (128 rows, 128-K)
+  int e5m2_a, e5m2_b;
+  int out_fp32;
+  const void* sa;        // per-tensor: float[1]; blockwise: float[M, K/128]; MX: tiled E8M0
+  const void* sb;        // per-tensor: float[1]; blockwise: float[N/128, K/128] or [N, K/128]; MX: tiled E8M0
+  void* c;               // [M, N] row-major, bf16 or fp32
+  uint32_t* err;
+};
+// Width (N) of one output tile of the GEMM variant (the B tensor-map box height).
+int gemm_block_n(int kind);
+cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int num_sms,
+                        cudaStream_t s);
+
+// Bounded-wait self test: one CTA waits on an mbarrier nothing arrives on.
+cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t s);
+
+}  // namespace fp8q

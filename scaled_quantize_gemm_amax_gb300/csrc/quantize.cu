@@ -1,0 +1,382 @@
+// quantize.cu -- quantize / cast-transpose of a BF16 matrix into row-wise and
+// column-wise FP8 plus scales, for the four recipes:
+//   per-tensor (current or delayed: the scale is an input),
+//   blockwise 1x128 (rows of the stored copy) and 128x128,
+//   MXFP8 1x32 with E8M0 exponents.
+// (FP8 quantized-training guide: "tensor-level scaling", "block-level scaling",
+// "MXFP8 scaling"; the column-wise copy feeds the backward GEMMs, which read the
+// operands along the other axis -- the mixed-precision dataflow paragraph.)
+//
+// Design (tiled path): a persistent grid, one CTA per SM, 256 threads.  Each CTA
+// walks 128x128 tiles of the input.  A 4-stage ring of 32 KB shared buffers is
+// filled by TMA (two 64-column boxes, 128-byte swizzle).  For each tile:
+//   row pass  -- 16-byte shared loads, 16 lanes per row; per-row / per-32 amax by
+//                warp shuffles; quantized bytes go to a swizzled 128x128 staging tile;
+//   col pass  -- ldmatrix.trans gives each lane two consecutive rows of one column;
+//                per-column amax by shuffles; bytes go to a second staging tile
+//                already transposed;
+//   both staging tiles leave through TMA stores (double-buffered).
+// The optional per-tensor amax of the input (delayed scaling records it while
+// casting with the previous scale) is a block max + one atomicMax per CTA.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "recipes.cuh"
+
+namespace fp8q {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kStages = 4;
+constexpr int kTile = 128;
+constexpr uint32_t kXBytes = kTile * kTile * 2;      // 32 KB bf16 tile
+constexpr uint32_t kQBytes = kTile * kTile;          // 16 KB fp8 tile
+constexpr uint32_t kOffOutR = kStages * kXBytes;     // 128 KB
+constexpr uint32_t kOffOutT = kOffOutR + 2 * kQBytes;
+constexpr uint32_t kOffBar = kOffOutT + 2 * kQBytes;  // 192 KB
+constexpr uint32_t kOffRed = kOffBar + 64;
+constexpr uint32_t kSmemBytes = kOffRed + 64 + 1024;  // + alignment slack
+
+// Address of 16-byte chunk `c16` (0..15) of row r in a bf16 tile held as two
+// 64-column halves, each [128 rows][128 B] with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t x_addr(uint32_t base, int r, int c16) {
+  return base + ((c16 >> 3) << 14) + (r << 7) + ((((c16 & 7) ^ (r & 7))) << 4);
+}
+// Byte (r, c) of a [128][128 B] swizzled fp8 tile, c a multiple of 2.
+__device__ __forceinline__ uint32_t q_addr(uint32_t base, int r, int c) {
+  return base + (r << 7) + ((((c >> 4) ^ (r & 7))) << 4) + (c & 15);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts64(uint32_t a, uint32_t x, uint32_t y) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void sts16(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"(static_cast<uint16_t>(v)) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t a, uint32_t (&d)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+               : "r"(a));
+}
+
+__device__ __forceinline__ float absmax_chunk(uint4 v) {
+  uint32_t m = absmax_bf16x2(absmax_bf16x2(v.x, v.y), absmax_bf16x2(v.z, v.w));
+  return pair_max_f32(m);
+}
+
+// Quantize one bf16 pair with scale s -> two FP8 bytes (low half -> low byte).
+__device__ __forceinline__ uint32_t q_pair(uint32_t w, float s, bool e5) {
+  return cvt_pair(__fmul_rn(bf16lo(w), s), __fmul_rn(bf16hi(w), s), e5);
+}
+
+__device__ __forceinline__ float block_max(float v, float* red, int warp, int lane) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) r = fmaxf(r, red[w]);
+  __syncthreads();
+  return r;
+}
+
+// Byte offset of the E8M0 exponent for (row r, 32-block b) in the GEMM-ready
+// tiled layout: 128-row x 4-block atoms of 512 B, atom (r/128, b/4) at
+// ((r/128) * atoms_per_row + b/4) * 512, inside it (r%32)*16 + ((r%128)/32)*4 + b%4.
+__device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t b, int64_t atoms_per_row) {
+  return ((r >> 7) * atoms_per_row + (b >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (b & 3);
+}
+
+template <int RECIPE>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_cast_transpose(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_qrow,
+                     const __grid_constant__ CUtensorMap tm_qcol, const CastParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - smem_u32(smem_raw));
+  float* const red = reinterpret_cast<float*>(base_ptr + kOffRed);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool e5 = p.e5m2 != 0;
+  const float fmax = fmax_of(e5);
+  const int fexp = fmax_exp_of(e5);
+  const int ntiles = p.tiles_r * p.tiles_c;
+  const int64_t nb128_c = p.C / 128, nb128_r = p.R / 128, nb32_c = p.C / 32, nb32_r = p.R / 32;
+
+  if (tid == 0) {
+    prefetch_tmap(&tm_x);
+    if (p.do_row) prefetch_tmap(&tm_qrow);
+    if (p.do_col) prefetch_tmap(&tm_qcol);
+    for (int s = 0; s < kStages; ++s) mbar_init(base + kOffBar + 8 * s, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  float g_scale = 1.0f;
+  if (RECIPE == kTensor) {
+    g_scale = *p.scale;
+    if (blockIdx.x == 0 && tid == 0) {
+      const float si = recip_rn(g_scale);
+      if (p.do_row && p.s_row) *static_cast<float*>(p.s_row) = si;
+      if (p.do_col && p.s_col) *static_cast<float*>(p.s_col) = si;
+    }
+  }
+
+  auto issue_load = [&](int it, int tile) {
+    const int s = it % kStages;
+    const uint32_t bar = base + kOffBar + 8 * s;
+    const int row0 = (tile / p.tiles_c) * kTile, col0 = (tile % p.tiles_c) * kTile;
+    mbar_arrive_expect_tx(bar, kXBytes);
+    tma_load_2d(base + s * kXBytes, &tm_x, col0, row0, bar);
+    tma_load_2d(base + s * kXBytes + kXBytes / 2, &tm_x, col0 + 64, row0, bar);
+  };
+  if (tid == 0) {
+    for (int it = 0; it < kStages; ++it) {
+      const int tile = blockIdx.x + it * gridDim.x;
+      if (tile < ntiles) issue_load(it, tile);
+    }
+  }
+
+  float thr_amax = 0.0f;
+  int it = 0;
+  bool failed = false;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+    const int s = it % kStages;
+    const uint32_t xs = base + s * kXBytes;
+    const int ob = it & 1;
+    const uint32_t outR = base + kOffOutR + ob * kQBytes;
+    const uint32_t outT = base + kOffOutT + ob * kQBytes;
+    const int tr = tile / p.tiles_c, tc = tile % p.tiles_c;
+    const int64_t row0 = static_cast<int64_t>(tr) * kTile, col0 = static_cast<int64_t>(tc) * kTile;
+
+    const bool ok = mbar_wait(base + kOffBar + 8 * s, (it / kStages) & 1, p.err, kErrTimeoutTmaLoad, nullptr);
+    if (tid == 0) bulk_wait_read<1>();  // staging buffer `ob` (used two tiles ago) has been read out
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+
+    // ---------------- row pass: thread handles row r = 16 i + 2 warp + lane/16, chunk j
+    const int j = lane & 15;
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = lds128(x_addr(xs, i * 16 + warp * 2 + (lane >> 4), j));
+
+    float tile_scale = g_scale;
+    if (RECIPE == kBlock128x128) {
+      float a = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a = fmaxf(a, absmax_chunk(v[i]));
+      const float tmax = block_max(a, red, warp, lane);
+      thr_amax = fmaxf(thr_amax, tmax);
+      tile_scale = scale_from_amax(tmax, fmax);
+      if (tid == 0) {
+        const float si = recip_rn(tile_scale);
+        if (p.do_row && p.s_row) static_cast<float*>(p.s_row)[tr * nb128_c + tc] = si;
+        if (p.do_col && p.s_col) static_cast<float*>(p.s_col)[tc * nb128_r + tr] = si;
+      }
+    }
+
+    if (p.do_row) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = i * 16 + warp * 2 + (lane >> 4);
+        const int64_t grow = row0 + r;
+        float sc = tile_scale;
+        if (RECIPE != kBlock128x128) {
+          float a = absmax_chunk(v[i]);
+          if (RECIPE == kBlock1x128) {
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+            sc = scale_from_amax(a, fmax);
+            if (j == 0 && grow < p.R) static_cast<float*>(p.s_row)[grow * nb128_c + tc] = recip_rn(sc);
+          } else if (RECIPE == kMx) {
+            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+            const int e = mx_exponent(a, fexp);
+            sc = pow2_neg(e);
+            if ((j & 3) == 0 && grow < p.R) {
+              const int64_t b = tc * 4 + (j >> 2);
+              const int64_t off = p.mx_tiled ? mx_tiled_offset(grow, b, (p.C + 127) / 128) : grow * nb32_c + b;
+              static_cast<uint8_t*>(p.s_row)[off] = static_cast<uint8_t>(e + 127);
+            }
+          }
+          thr_amax = fmaxf(thr_amax, a);
+        }
+        const uint4 w = v[i];
+        const uint32_t lo = q_pair(w.x, sc, e5) | (q_pair(w.y, sc, e5) << 16);
+        const uint32_t hi = q_pair(w.z, sc, e5) | (q_pair(w.w, sc, e5) << 16);
+        sts64(outR + (r << 7) + ((((j >> 1) ^ (r & 7))) << 4) + ((j & 1) << 3), lo, hi);
+      }
+    } else if (RECIPE != kBlock128x128) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) thr_amax = fmaxf(thr_amax, absmax_chunk(v[i]));
+    }
+
+    // ---------------- col pass: warp handles 8-column chunks g = warp, warp + 8
+    if (p.do_col) {
+#pragma unroll
+      for (int gi = 0; gi < 2; ++gi) {
+        const int g = warp + gi * 8;
+        uint32_t d[4][4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) ldsm_x4_trans(x_addr(xs, 32 * t + 8 * (lane >> 3) + (lane & 7), g), d[t]);
+        // lane holds column cc of the tile, rows 32t + 8m + 2(lane&3) + {0, 1}
+        const int cc = 8 * g + (lane >> 2);
+        const int64_t gcol = col0 + cc;
+        float sc[4] = {tile_scale, tile_scale, tile_scale, tile_scale};
+        if (RECIPE == kBlock1x128) {
+          uint32_t m = 0;
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) m = absmax_bf16x2(m, d[t][q]);
+          float a = pair_max_f32(m);
+          a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+          a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+          const float s = scale_from_amax(a, fmax);
+          sc[0] = sc[1] = sc[2] = sc[3] = s;
+          if ((lane & 3) == 0 && gcol < p.C) static_cast<float*>(p.s_col)[gcol * nb128_r + tr] = recip_rn(s);
+        } else if (RECIPE == kMx) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            uint32_t m = absmax_bf16x2(absmax_bf16x2(d[t][0], d[t][1]), absmax_bf16x2(d[t][2], d[t][3]));
+            float a = pair_max_f32(m);
+            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+            const int e = mx_exponent(a, fexp);
+            sc[t] = pow2_neg(e);
+            const int64_t b = static_cast<int64_t>(tr) * 4 + t;
+            if ((lane & 3) == 0 && gcol < p.C && b < nb32_r) {
+              const int64_t off = p.mx_tiled ? mx_tiled_offset(gcol, b, (p.R + 127) / 128) : gcol * nb32_r + b;
+              static_cast<uint8_t*>(p.s_col)[off] = static_cast<uint8_t>(e + 127);
+            }
+          }
+        }
+        if (!p.do_row && RECIPE != kBlock128x128) {
+          uint32_t m = 0;
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) m = absmax_bf16x2(m, d[t][q]);
+          thr_amax = fmaxf(thr_amax, pair_max_f32(m));
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int r0 = 32 * t + 8 * q + 2 * (lane & 3);
+            sts16(q_addr(outT, cc, r0), q_pair(d[t][q], sc[t], e5));
+          }
+      }
+    }
+
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      if (p.do_row) tma_store_2d(&tm_qrow, outR, static_cast<int>(col0), static_cast<int>(row0));
+      if (p.do_col) tma_store_2d(&tm_qcol, outT, static_cast<int>(row0), static_cast<int>(col0));
+      bulk_commit();
+      const int next = tile + kStages * gridDim.x;
+      if (next < ntiles) issue_load(it + kStages, next);
+    }
+  }
+
+  if (failed && tid == 0) {
+    // wait (bounded) for loads still in flight into this CTA's ring before leaving
+    for (int k = it; k < it + kStages; ++k) {
+      const int tile = blockIdx.x + k * gridDim.x;
+      if (tile >= ntiles) break;
+      mbar_wait(base + kOffBar + 8 * (k % kStages), (k / kStages) & 1, p.err, kErrTimeoutTmaLoad, nullptr);
+    }
+  }
+  if (tid == 0) bulk_wait_all<0>();
+
+  if (p.amax_out != nullptr) {
+    const float a = block_max(thr_amax, red, warp, lane);
+    if (tid == 0 && a > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(a));
+  }
+}
+
+// ------------------------------------------------------------------ per-tensor, any shape
+// 32x32 tiles, 256 threads: row-wise bytes straight from the input, column-wise
+// bytes through a transposed shared tile.
+__global__ void __launch_bounds__(256) k_cast_generic(const uint16_t* __restrict__ x, CastParams p) {
+  __shared__ float tile[32][33];
+  const bool e5 = p.e5m2 != 0;
+  const float s = *p.scale;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32, c0 = static_cast<int64_t>(blockIdx.x) * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  float amax = 0.0f;
+  for (int k = ty; k < 32; k += 8) {
+    const int64_t r = r0 + k, c = c0 + tx;
+    float v = 0.0f;
+    if (r < p.R && c < p.C) {
+      v = __uint_as_float(static_cast<uint32_t>(x[r * p.C + c]) << 16);
+      amax = fmaxf(amax, fabsf(v));
+      if (p.do_row) p.q_row[r * p.C + c] = static_cast<uint8_t>(cvt_pair(__fmul_rn(v, s), 0.0f, e5) & 0xFF);
+    }
+    tile[k][tx] = v;
+  }
+  __syncthreads();
+  if (p.do_col) {
+    for (int k = ty; k < 32; k += 8) {
+      const int64_t c = c0 + k, r = r0 + tx;
+      if (r < p.R && c < p.C)
+        p.q_col[c * p.R + r] = static_cast<uint8_t>(cvt_pair(__fmul_rn(tile[tx][k], s), 0.0f, e5) & 0xFF);
+    }
+  }
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    const float si = recip_rn(s);
+    if (p.do_row && p.s_row) *static_cast<float*>(p.s_row) = si;
+    if (p.do_col && p.s_col) *static_cast<float*>(p.s_col) = si;
+  }
+  if (p.amax_out != nullptr) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if (tx == 0 && amax > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(amax));
+  }
+}
+
+template <int RECIPE>
+cudaError_t launch_tiled(const CastParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_qrow,
+                         const CUtensorMap& tm_qcol, int num_sms, cudaStream_t s) {
+  static bool attr_set = false;   // per process; the attribute is per function, not per device
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_cast_transpose<RECIPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int ntiles = p.tiles_r * p.tiles_c;
+  const int grid = ntiles < num_sms ? ntiles : num_sms;
+  k_cast_transpose<RECIPE><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_qrow, tm_qcol, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_cast_transpose_tiled(const CastParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_qrow,
+                                        const CUtensorMap& tm_qcol, int num_sms, cudaStream_t s) {
+  switch (p.recipe) {
+    case kTensor: return launch_tiled<kTensor>(p, tm_x, tm_qrow, tm_qcol, num_sms, s);
+    case kBlock1x128: return launch_tiled<kBlock1x128>(p, tm_x, tm_qrow, tm_qcol, num_sms, s);
+    case kBlock128x128: return launch_tiled<kBlock128x128>(p, tm_x, tm_qrow, tm_qcol, num_sms, s);
+    default: return launch_tiled<kMx>(p, tm_x, tm_qrow, tm_qcol, num_sms, s);
+  }
+}
+
+cudaError_t launch_cast_generic(const CastParams& p, const void* x, cudaStream_t s) {
+  dim3 grid(static_cast<unsigned>((p.C + 31) / 32), static_cast<unsigned>((p.R + 31) / 32));
+  k_cast_generic<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), p);
+  return cudaGetLastError();
+}
+
+}  // namespace fp8q

@@ -1,0 +1,91 @@
+"""Helpers for the GPU parity tests (CUDA path vs the CPU oracle)."""
+import numpy as np
+import torch
+
+import oracle
+import scaled_quantize_gemm_amax_gb300 as fq
+from scaled_quantize_gemm_amax_gb300 import build as fqbuild
+
+R = fq.Recipe
+F = fq.Format
+
+KIND = {R.TENSOR: oracle.KIND_TENSOR, R.BLOCK_1x128: oracle.KIND_1x128, R.BLOCK_128x128: oracle.KIND_128x128,
+        R.MX_1x32: oracle.KIND_MX, R.MX_1x32_TILED: oracle.KIND_MX}
+
+
+def require_gpu():
+    assert torch.cuda.is_available(), "the -m gpu tests need a CUDA device"
+    fqbuild.build()
+    fq.load_library()
+
+
+def bits16(x: torch.Tensor) -> np.ndarray:
+    return x.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy()
+
+
+def f32bits(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32)).view(np.uint32)
+
+
+def assert_bytes_equal(got: np.ndarray, ref: np.ndarray, what: str):
+    got = np.asarray(got)
+    ref = np.asarray(ref)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    bad = np.argwhere(got != ref)
+    if bad.size:
+        idx = tuple(bad[0])
+        raise AssertionError(f"{what}: {len(bad)} of {ref.size} differ; first at {idx}: got {got[idx]!r} "
+                             f"ref {ref[idx]!r}")
+
+
+def assert_status_ok():
+    st = fq.fp8_get_device_status()
+    assert st == fq.Status.OK, st
+
+
+def oracle_scales_like(recipe, s_ref, rows, cols):
+    """Oracle multipliers in the layout the GPU writes (MX tiled: permuted)."""
+    if recipe == R.MX_1x32_TILED:
+        return oracle.mx_to_tiled(s_ref).reshape(((rows + 127) // 128, (cols + 127) // 128, 512))
+    return s_ref
+
+
+def check_cast(x: torch.Tensor, recipe, fmt, row=True, col=True, scale_np=None):
+    """Run the GPU cast-transpose and compare every output with the oracle.
+
+    For the per-tensor recipe the scale is the oracle's current-scaling scale of x
+    unless ``scale_np`` is given.  Returns the GPU outputs.
+    """
+    xh = bits16(x)
+    rows, cols = xh.shape
+    kind = KIND[recipe]
+    scale_t = None
+    if recipe == R.TENSOR:
+        if scale_np is None:
+            scale_np, _ = oracle.tensor_scale(oracle.amax(xh), int(fmt))
+        scale_t = torch.tensor([scale_np], dtype=torch.float32, device=x.device)
+    amax_t = torch.full((1,), 123.0, dtype=torch.float32, device=x.device)
+    qr, sr, qc, sc = fq.cast_transpose(x, recipe, fmt, scale_t, amax_t, row=row, col=col)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    assert f32bits(host(amax_t))[0] == f32bits(oracle.amax(xh)), "amax_out"
+    if row:
+        q_ref, s_ref = oracle.quantize_rowwise(xh, kind, int(fmt), scale_np)
+        assert_bytes_equal(host(qr), q_ref, "q_row")
+        _check_scales(recipe, host(sr), oracle_scales_like(recipe, s_ref, rows, cols), "s_row")
+    if col:
+        q_ref, s_ref = oracle.quantize_colwise(xh, kind, int(fmt), scale_np)
+        assert_bytes_equal(host(qc), q_ref, "q_col")
+        _check_scales(recipe, host(sc), oracle_scales_like(recipe, s_ref, cols, rows), "s_col")
+    return qr, sr, qc, sc
+
+
+def _check_scales(recipe, got, ref, what):
+    if recipe in (R.MX_1x32, R.MX_1x32_TILED):
+        assert_bytes_equal(got, ref, what)
+    else:
+        assert_bytes_equal(f32bits(got), f32bits(ref), what)

@@ -1,0 +1,133 @@
+"""GPU parity of the scaled FP8 GEMM against the oracle (dequantize exactly, float64
+matmul) within the stated bar: ||C - C_ref||_F / ||C_ref||_F <= 1e-2 and
+|C - C_ref|[m, n] <= 2e-2 * ||deq(A)[m, :]|| * ||deq(B)[n, :]|| / sqrt(K).
+
+The oracle quantizes the same BF16 bytes itself (no oracle input comes from the
+GPU); the GPU's FP8 bytes are additionally checked equal to the oracle's."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scaled_quantize_gemm_amax_gb300 as fq
+from scaled_quantize_gemm_amax_gb300 import workloads as wl
+from gpu_util import R, F, KIND, assert_bytes_equal, assert_status_ok, bits16, host, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+REL_FRO = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _quant_gpu(x, recipe, fmt, scale_np):
+    scale_t = None
+    if recipe == R.TENSOR:
+        scale_t = torch.tensor([scale_np], dtype=torch.float32, device="cuda")
+    q, s, _, _ = fq.cast_transpose(x, recipe, fmt, scale_t, None, row=True, col=False)
+    return q, s
+
+
+def _quant_oracle(xh, recipe, fmt):
+    scale_np = None
+    if recipe == R.TENSOR:
+        scale_np, _ = oracle.tensor_scale(oracle.amax(xh), int(fmt))
+    q, s = oracle.quantize_rowwise(xh, KIND[recipe], int(fmt), scale_np)
+    return q, s, scale_np
+
+
+def _oracle_recipe(recipe):
+    return KIND[recipe]
+
+
+def gemm_check(x, w, ra, rb, fa, fb, out=fq.OutDtype.BF16, rows=None):
+    """Quantize x [M, K] and w [N, K] on both sides, run the GEMM, compare.
+
+    rows: compare only these rows of C (all columns) -- for large shapes."""
+    xh, wh = bits16(x), bits16(w)
+    qa_ref, sa_ref, sca = _quant_oracle(xh, ra, fa)
+    qb_ref, sb_ref, scb = _quant_oracle(wh, rb, fb)
+    qa, sa = _quant_gpu(x, ra, fa, sca)
+    qb, sb = _quant_gpu(w, rb, fb, scb)
+    c = fq.scaled_gemm(qa, fa, ra, sa, qb, fb, rb, sb, out=out)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    assert_bytes_equal(host(qa), qa_ref, "A bytes")
+    assert_bytes_equal(host(qb), qb_ref, "B bytes")
+    c_gpu = host(c.float()).astype(np.float64)
+    ka, kb = _oracle_recipe(ra), _oracle_recipe(rb)
+    deq_b = oracle.dequantize(qb_ref, kb, int(fb), sb_ref)
+    if rows is None:
+        deq_a = oracle.dequantize(qa_ref, ka, int(fa), sa_ref)
+        c_ref = deq_a @ deq_b.T
+        c_cmp = c_gpu
+    else:
+        rows = np.asarray(rows)
+        sa_rows = sa_ref[rows] if ka in (oracle.KIND_1x128, oracle.KIND_MX) else sa_ref
+        deq_a = oracle.dequantize(qa_ref[rows], ka, int(fa), sa_rows)
+        c_ref = deq_a @ deq_b.T
+        c_cmp = c_gpu[rows]
+    rel, worst = oracle.gemm_tolerance_check(c_cmp, c_ref, deq_a, deq_b)
+    assert rel <= REL_FRO, f"relative Frobenius error {rel:.3e}"
+    assert worst <= 1.0, f"max-abs bound exceeded by x{worst:.3f}"
+    return rel, worst
+
+
+PAIRS = [(R.TENSOR, R.TENSOR), (R.BLOCK_1x128, R.BLOCK_128x128), (R.BLOCK_1x128, R.BLOCK_1x128),
+         (R.MX_1x32_TILED, R.MX_1x32_TILED)]
+
+
+@pytest.mark.parametrize("ra,rb", PAIRS)
+def test_gemm_small_single_tile(ra, rb):
+    x = wl.normal_bf16((128, 128), 10, 1.0)
+    w = wl.normal_bf16((128, 128), 11, 0.02)
+    gemm_check(x, w, ra, rb, F.E4M3, F.E4M3)
+
+
+@pytest.mark.parametrize("ra,rb", PAIRS)
+@pytest.mark.parametrize("fa,fb", [(F.E4M3, F.E4M3), (F.E5M2, F.E4M3), (F.E4M3, F.E5M2)])
+def test_gemm_multi_tile_formats(ra, rb, fa, fb):
+    # 3 x 2-or-4 tiles, 5 K blocks; N = 512 is not a multiple of every tile width
+    x = wl.normal_bf16((384, 640), 20, 1.0)
+    w = wl.normal_bf16((512, 640), 21, 0.02)
+    gemm_check(x, w, ra, rb, fa, fb)
+
+
+@pytest.mark.parametrize("ra,rb", PAIRS)
+def test_gemm_fp32_output_and_n_tail(ra, rb):
+    # N = 384: the 256-wide tiles hang over N by half a tile
+    x = wl.normal_bf16((256, 512), 30, 1.0)
+    w = wl.normal_bf16((384, 512), 31, 1e-3)
+    gemm_check(x, w, ra, rb, F.E5M2, F.E4M3, out=fq.OutDtype.FP32)
+
+
+def test_gemm_config1_per_tensor_256():
+    a, b = wl.cfg1_tensor_current("cuda")
+    gemm_check(a, b, R.TENSOR, R.TENSOR, F.E4M3, F.E4M3)
+
+
+def test_gemm_config2_blockwise_4096_full():
+    x, w = wl.cfg2_blockwise("cuda")
+    rel, worst = gemm_check(x, w, R.BLOCK_1x128, R.BLOCK_128x128, F.E4M3, F.E4M3)
+    print(f"cfg2 rel_fro={rel:.3e} worst={worst:.3f}")
+
+
+@pytest.mark.parametrize("name", ["qkv", "down"])
+def test_gemm_config3_mx_sampled_rows(name):
+    x, w = wl.cfg3_mx(name, "cuda")
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([[0, x.shape[0] - 1], rng.integers(0, x.shape[0], 126)]))
+    gemm_check(x, w, R.MX_1x32_TILED, R.MX_1x32_TILED, F.E4M3, F.E4M3, rows=rows)
+
+
+def test_gemm_k_zero_writes_zeros():
+    a = torch.empty((128, 0), dtype=torch.uint8, device="cuda")
+    b = torch.empty((256, 0), dtype=torch.uint8, device="cuda")
+    s = torch.ones(1, dtype=torch.float32, device="cuda")
+    c = torch.full((128, 256), 5.0, dtype=torch.bfloat16, device="cuda")
+    fq.fp8_scaled_gemm(a, F.E4M3, R.TENSOR, s, b, F.E4M3, R.TENSOR, s, c)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(c).item() == 0

@@ -382,3 +382,17 @@ def test_tolerance_check_detects_planted_errors():
     wrong = oracle.scaled_gemm(qa, 0, 1, sa, qb, 0, 1, sb[::-1].copy())
     rel_w, worst_w = oracle.gemm_tolerance_check(wrong, ref, da, db)
     assert rel_w > 1e-2 or worst_w > 1
+
+
+# ----------------------------------------------------------------- MX tiled layout
+def test_mx_tiled_layout_is_a_bijection_with_hand_positions():
+    R, C = 256, 384
+    off = oracle.mx_tiled_offsets(R, C)
+    assert off.shape == (256, 12)
+    assert np.array_equal(np.sort(off.ravel()), np.arange(R * C // 32))
+    # hand-computed: row 0 block 0 -> 0; row 1 -> 16; row 32 -> 4; row 96 block 3 -> 15;
+    # row 31 block 2 -> 31*16 + 2; row 128 block 0 -> atom (1, 0) -> 3*512; block 4 -> atom (0, 1) -> 512
+    assert off[0, 0] == 0 and off[1, 0] == 16 and off[32, 0] == 4 and off[96, 3] == 15
+    assert off[31, 2] == 31 * 16 + 2 and off[128, 0] == 3 * 512 and off[0, 4] == 512
+    s = np.random.default_rng(0).integers(0, 255, (R, C // 32), dtype=np.uint8)
+    np.testing.assert_array_equal(oracle.mx_from_tiled(oracle.mx_to_tiled(s), R, C), s)
