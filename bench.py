@@ -440,8 +440,61 @@ def run_reference(args, rank, world):
             "wall_s": round(wall, 2)}
 
 
+CASES = ("cast_tensor", "cast_1x128", "cast_128x128", "cast_mx", "amax", "gemm_tensor", "gemm_block", "gemm_mx")
+
+
+def run_case(args):
+    """One kernel in a loop (for profiling): cast cases on a size x size input of the
+    bandwidth sweep, GEMM cases at size^3.  Prints the median time as JSON."""
+    import scaled_quantize_gemm_amax_gb300 as fq
+    from scaled_quantize_gemm_amax_gb300 import build as fqbuild
+    from scaled_quantize_gemm_amax_gb300 import workloads as wl
+
+    fqbuild.build()
+    fq.load_library()
+    R, F = fq.Recipe, fq.Format
+    dev = torch.device("cuda", 0)
+    s = args.size
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    pk = peaks()
+    if args.case.startswith("cast") or args.case == "amax":
+        x = wl.cfg5_sweep(s, dev) if s in wl.CFG5_SIZES else wl.normal_bf16((s, s), 5, 1.0, dev)
+        rec = {"cast_tensor": R.TENSOR, "cast_1x128": R.BLOCK_1x128, "cast_128x128": R.BLOCK_128x128,
+               "cast_mx": R.MX_1x32_TILED, "amax": None}[args.case]
+        if rec is None:
+            amax = torch.empty(1, dtype=torch.float32, device=dev)
+            fn = lambda: fq.fp8_amax(x, amax)
+            nbytes = 2 * s * s
+        else:
+            scale = torch.ones(1, dtype=torch.float32, device=dev) if rec == R.TENSOR else None
+            qr, sr, qc, sc = fq.cast_transpose(x, rec, F.E4M3, scale)
+            fn = lambda: fq.fp8_cast_transpose(x, rec, F.E4M3, scale, None, qr, sr, qc, sc)
+            nbytes = 4 * s * s
+        ms = _time_kernel(fn, reps=args.steps, flush=flush)
+        res = {"case": args.case, "size": s, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+        res["frac_hbm"] = round(res["GB/s"] / pk["hbm_gbs"], 4)
+    else:
+        ra = {"gemm_tensor": R.TENSOR, "gemm_block": R.BLOCK_1x128, "gemm_mx": R.MX_1x32_TILED}[args.case]
+        rb = {"gemm_tensor": R.TENSOR, "gemm_block": R.BLOCK_128x128, "gemm_mx": R.MX_1x32_TILED}[args.case]
+        a = wl.normal_bf16((s, s), 1, 1.0, dev)
+        b = wl.normal_bf16((s, s), 2, 0.02, dev)
+        sc1 = torch.ones(1, dtype=torch.float32, device=dev)
+        qa, sa, _, _ = fq.cast_transpose(a, ra, F.E4M3, sc1 if ra == R.TENSOR else None, col=False)
+        qb, sb, _, _ = fq.cast_transpose(b, rb, F.E4M3, sc1 if rb == R.TENSOR else None, col=False)
+        c = torch.empty((s, s), dtype=torch.bfloat16, device=dev)
+        ms = _time_kernel(lambda: fq.fp8_scaled_gemm(qa, F.E4M3, ra, sa, qb, F.E4M3, rb, sb, c), reps=args.steps,
+                          flush=flush)
+        tf = 2.0 * s ** 3 / (ms * 1e-3) / 1e12
+        res = {"case": args.case, "size": s, "us": round(ms * 1e3, 2), "TFLOP/s": round(tf, 1),
+               "frac_fp8": round(tf / (2 * pk["bf16_tflops"]), 4)}
+    assert fq.fp8_get_device_status() == fq.Status.OK
+    print(json.dumps(res), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--case", choices=CASES, default=None, help="time one kernel in a loop (profiling)")
+    ap.add_argument("--size", type=int, default=4096)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=20)
@@ -452,6 +505,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.case is not None:
+        run_case(args)
+        return
     rank, world, _ = dist_setup(args)
     if args.impl == "reference":
         res = run_reference(args, rank, world)
