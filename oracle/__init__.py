@@ -36,7 +36,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fp8_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
-_CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
            "-fexcess-precision=standard", "-Wall", "-Wextra"]
 
 _lib = None
@@ -44,13 +44,19 @@ _lock = threading.Lock()
 
 
 def build(force: bool = False) -> str:
-    """Compile the C oracle into ``oracle/_build/liboracle.so`` (if stale)."""
+    """Compile the C oracle into ``oracle/_build/liboracle.so`` (if stale).
+
+    FP8_ORACLE_LIB, when set, names an already-built oracle library to load
+    instead (the mutation test loads deliberately broken copies this way)."""
+    alt = os.environ.get("FP8_ORACLE_LIB")
+    if alt:
+        return alt
     os.makedirs(_BUILD, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", *_CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+    subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 

@@ -75,6 +75,26 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return d;
 }
 
+// Packed pairs of binary32 (Blackwell's f32x2 arithmetic: one instruction, two lanes).
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t pack_f32x2(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 __device__ __forceinline__ void stg128(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -290,14 +310,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (KIND == kBlock1x128) {
         const float* sa_row = static_cast<const float*>(p.sa) + grow * KB;
         const float* sb_blk = static_cast<const float*>(p.sb);
-        float acc[64];
+        const float* sb_tile = sb_blk + static_cast<int64_t>(tn) * KB;   // 128x128 B: one factor per k-block
+        uint64_t acc[32];                    // column pairs (2j, 2j+1) of this thread's 64 columns
 #pragma unroll
-        for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+        for (int j = 0; j < 32; ++j) acc[j] = 0;
         bool ok = true;
-        float sa_next = sa_row[0];
+        // scale factors are fetched two k-blocks ahead, off the promotion's critical path
+        float sa0 = sa_row[0], sa1 = KB > 1 ? sa_row[1] : 0.0f;
+        float sb0 = p.b_1x128 ? 0.0f : __ldg(sb_tile), sb1 = (!p.b_1x128 && KB > 1) ? __ldg(sb_tile + 1) : 0.0f;
         for (int kb = 0; kb < KB; ++kb) {
-          const float sa_v = sa_next;
-          if (kb + 1 < KB) sa_next = sa_row[kb + 1];
+          const float sa_v = sa0, sb_v = sb0;
+          sa0 = sa1;
+          sb0 = sb1;
+          if (kb + 2 < KB) {
+            sa1 = sa_row[kb + 2];
+            if (!p.b_1x128) sb1 = __ldg(sb_tile + kb + 2);
+          }
           const uint32_t pb = part_it % ACC;
           // warp-uniform decision: the TMEM loads below are .sync.aligned
           if (!__all_sync(0xFFFFFFFFu,
@@ -319,25 +347,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             // per-column B scales: sB[n, kb]
             const float* sbc = sb_blk + (gcol0)*KB + kb;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = fmaf(sa_v * __ldg(sbc + j * KB), __uint_as_float(r0[j]), acc[j]);
+            for (int j = 0; j < 16; ++j) {
+              const uint64_t f = pack_f32x2(sa_v * __ldg(sbc + (2 * j) * KB), sa_v * __ldg(sbc + (2 * j + 1) * KB));
+              acc[j] = fma_f32x2(f, pack_f32x2(r0[2 * j], r0[2 * j + 1]), acc[j]);
+            }
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              acc[32 + j] = fmaf(sa_v * __ldg(sbc + (32 + j) * KB), __uint_as_float(r1[j]), acc[32 + j]);
+            for (int j = 0; j < 16; ++j) {
+              const uint64_t f =
+                  pack_f32x2(sa_v * __ldg(sbc + (32 + 2 * j) * KB), sa_v * __ldg(sbc + (33 + 2 * j) * KB));
+              acc[16 + j] = fma_f32x2(f, pack_f32x2(r1[2 * j], r1[2 * j + 1]), acc[16 + j]);
+            }
           } else {
-            const float f = sa_v * __ldg(sb_blk + static_cast<int64_t>(tn) * KB + kb);
+            const float f1 = sa_v * sb_v;
+            const uint64_t f = pack_f32x2(f1, f1);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = fmaf(f, __uint_as_float(r0[j]), acc[j]);
+            for (int j = 0; j < 16; ++j) acc[j] = fma_f32x2(f, pack_f32x2(r0[2 * j], r0[2 * j + 1]), acc[j]);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[32 + j] = fmaf(f, __uint_as_float(r1[j]), acc[32 + j]);
+            for (int j = 0; j < 16; ++j) acc[16 + j] = fma_f32x2(f, pack_f32x2(r1[2 * j], r1[2 * j + 1]), acc[16 + j]);
           }
         }
         if (!ok) break;
         float v[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = acc[j];
+        for (int j = 0; j < 16; ++j) unpack_f32x2(acc[j], v[2 * j], v[2 * j + 1]);
         if (gcol0 < p.N) store_row32(p.c, grow * p.N + gcol0, v, fp32);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = acc[32 + j];
+        for (int j = 0; j < 16; ++j) unpack_f32x2(acc[16 + j], v[2 * j], v[2 * j + 1]);
         if (gcol0 + 32 < p.N) store_row32(p.c, grow * p.N + gcol0 + 32, v, fp32);
       } else {
         const uint32_t a = acc_it % ACC;

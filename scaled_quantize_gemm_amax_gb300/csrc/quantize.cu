@@ -7,11 +7,12 @@
 // "MXFP8 scaling"; the column-wise copy feeds the backward GEMMs, which read the
 // operands along the other axis -- the mixed-precision dataflow paragraph.)
 //
-// Design (tiled path): a persistent grid, one CTA per SM, 256 threads.  Each CTA
+// Design (tiled path): a persistent grid, one CTA per SM, 512 threads.  Each CTA
 // walks 128x128 tiles of the input.  A 4-stage ring of 32 KB shared buffers is
 // filled by TMA (two 64-column boxes, 128-byte swizzle).  For each tile:
 //   row pass  -- 16-byte shared loads, 16 lanes per row; per-row / per-32 amax by
-//                warp shuffles; quantized bytes go to a swizzled 128x128 staging tile;
+//                a shuffle reduce-scatter, so each lane derives one block scale and
+//                the others receive it; quantized bytes go to a swizzled staging tile;
 //   col pass  -- ldmatrix.trans gives each lane two consecutive rows of one column;
 //                per-column amax by shuffles; bytes go to a second staging tile
 //                already transposed;
@@ -28,7 +29,8 @@ namespace fp8q {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
 constexpr int kStages = 4;
 constexpr int kTile = 128;
 constexpr uint32_t kXBytes = kTile * kTile * 2;      // 32 KB bf16 tile
@@ -37,7 +39,7 @@ constexpr uint32_t kOffOutR = kStages * kXBytes;     // 128 KB
 constexpr uint32_t kOffOutT = kOffOutR + 2 * kQBytes;
 constexpr uint32_t kOffBar = kOffOutT + 2 * kQBytes;  // 192 KB
 constexpr uint32_t kOffRed = kOffBar + 64;
-constexpr uint32_t kSmemBytes = kOffRed + 64 + 1024;  // + alignment slack
+constexpr uint32_t kSmemBytes = kOffRed + 128 + 1024;  // + alignment slack
 
 // Address of 16-byte chunk `c16` (0..15) of row r in a bf16 tile held as two
 // 64-column halves, each [128 rows][128 B] with the 128-byte swizzle.
@@ -66,14 +68,50 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t a, uint32_t (&d)[4]) {
                : "r"(a));
 }
 
+// Running max of |.| over bf16 pairs: the magnitude of max.xorsign.abs is
+// max(|a|, |b|) (its sign bit is meaningless and masked at the end); NaN inputs
+// are ignored.
+__device__ __forceinline__ uint32_t xabs_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float pair_abs_f32(uint32_t m) { return pair_max_f32(m & 0x7FFF7FFFu); }
 __device__ __forceinline__ float absmax_chunk(uint4 v) {
-  uint32_t m = absmax_bf16x2(absmax_bf16x2(v.x, v.y), absmax_bf16x2(v.z, v.w));
-  return pair_max_f32(m);
+  return pair_abs_f32(xabs_max(xabs_max(v.x, v.y), xabs_max(v.z, v.w)));
 }
 
-// Quantize one bf16 pair with scale s -> two FP8 bytes (low half -> low byte).
+// Quantize one bf16 pair with scale s -> two FP8 bytes (low half -> low byte):
+// both binary32 products in one packed multiply, then the saturating cast.
 __device__ __forceinline__ uint32_t q_pair(uint32_t w, float s, bool e5) {
-  return cvt_pair(__fmul_rn(bf16lo(w), s), __fmul_rn(bf16hi(w), s), e5);
+  uint64_t x2, s2, p2;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x2) : "r"(w << 16), "r"(w & 0xFFFF0000u));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(s2) : "f"(s));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p2) : "l"(x2), "l"(s2));
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p2));
+  return cvt_pair(lo, hi, e5);
+}
+// Eight bf16 (one 16-byte chunk) -> eight FP8 bytes.
+__device__ __forceinline__ uint2 q_chunk(uint4 w, float s, bool e5) {
+  uint2 r;
+  r.x = q_pair(w.x, s, e5) | (q_pair(w.y, s, e5) << 16);
+  r.y = q_pair(w.z, s, e5) | (q_pair(w.w, s, e5) << 16);
+  return r;
+}
+
+// Reduce-scatter of four per-lane maxima a[0..3] over the four lanes
+// {l, l^hi, l^lo, l^hi^lo}: afterwards lane l holds the maximum of
+// a[2*(l has hi) + (l has lo)] over those lanes (two rounds, three shuffles).
+__device__ __forceinline__ float reduce_scatter4(const float (&a)[4], int lane, int hi, int lo) {
+  const bool h = (lane & hi) != 0;
+  float k0 = h ? a[2] : a[0], k1 = h ? a[3] : a[1];
+  const float s0 = h ? a[0] : a[2], s1 = h ? a[1] : a[3];
+  k0 = fmaxf(k0, __shfl_xor_sync(0xFFFFFFFFu, s0, hi));
+  k1 = fmaxf(k1, __shfl_xor_sync(0xFFFFFFFFu, s1, hi));
+  const bool l = (lane & lo) != 0;
+  const float keep = l ? k1 : k0, send = l ? k0 : k1;
+  return fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, lo));
 }
 
 __device__ __forceinline__ float block_max(float v, float* red, int warp, int lane) {
@@ -83,7 +121,7 @@ __device__ __forceinline__ float block_max(float v, float* red, int warp, int la
   __syncthreads();
   float r = red[0];
 #pragma unroll
-  for (int w = 1; w < kThreads / 32; ++w) r = fmaxf(r, red[w]);
+  for (int w = 1; w < kWarps; ++w) r = fmaxf(r, red[w]);
   __syncthreads();
   return r;
 }
@@ -144,6 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // Row pass: lane j = lane % 16 of a half-warp owns 16-byte chunk j of rows
+  // r(i) = 32 i + 2 warp + lane / 16, i = 0..3.  Column pass: warp w owns the
+  // 8-column chunk w; lane holds column 8 w + lane / 4, rows 32 t + 8 q + 2 (lane % 4) + {0, 1}.
+  const int j = lane & 15;
   float thr_amax = 0.0f;
   int it = 0;
   bool failed = false;
@@ -163,18 +205,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       break;
     }
 
-    // ---------------- row pass: thread handles row r = 16 i + 2 warp + lane/16, chunk j
-    const int j = lane & 15;
-    uint4 v[8];
+    // ---------------- row pass
+    uint4 v[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = lds128(x_addr(xs, i * 16 + warp * 2 + (lane >> 4), j));
+    for (int i = 0; i < 4; ++i) v[i] = lds128(x_addr(xs, i * 32 + warp * 2 + (lane >> 4), j));
+    float a[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = absmax_chunk(v[i]);
 
     float tile_scale = g_scale;
     if (RECIPE == kBlock128x128) {
-      float a = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) a = fmaxf(a, absmax_chunk(v[i]));
-      const float tmax = block_max(a, red, warp, lane);
+      const float tmax = block_max(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), red, warp, lane);
       thr_amax = fmaxf(thr_amax, tmax);
       tile_scale = scale_from_amax(tmax, fmax);
       if (tid == 0) {
@@ -182,100 +223,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.do_row && p.s_row) static_cast<float*>(p.s_row)[tr * nb128_c + tc] = si;
         if (p.do_col && p.s_col) static_cast<float*>(p.s_col)[tc * nb128_r + tr] = si;
       }
+    } else {
+      thr_amax = fmaxf(thr_amax, fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])));
     }
 
     if (p.do_row) {
+      float sc[4] = {tile_scale, tile_scale, tile_scale, tile_scale};
+      if (RECIPE == kBlock1x128) {
+        // row i = j / 4 ends up in lanes j = 4i..4i+3 of each half-warp
+        float m = reduce_scatter4(a, lane, 8, 4);
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        const float mine = scale_from_amax(m, fmax);
+        const int64_t grow = row0 + (j >> 2) * 32 + warp * 2 + (lane >> 4);
+        if ((j & 3) == 0 && grow < p.R) static_cast<float*>(p.s_row)[grow * nb128_c + tc] = recip_rn(mine);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = i * 16 + warp * 2 + (lane >> 4);
-        const int64_t grow = row0 + r;
-        float sc = tile_scale;
-        if (RECIPE != kBlock128x128) {
-          float a = absmax_chunk(v[i]);
-          if (RECIPE == kBlock1x128) {
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-            sc = scale_from_amax(a, fmax);
-            if (j == 0 && grow < p.R) static_cast<float*>(p.s_row)[grow * nb128_c + tc] = recip_rn(sc);
-          } else if (RECIPE == kMx) {
-            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-            const int e = mx_exponent(a, fexp);
-            sc = pow2_neg(e);
-            if ((j & 3) == 0 && grow < p.R) {
-              const int64_t b = tc * 4 + (j >> 2);
-              const int64_t off = p.mx_tiled ? mx_tiled_offset(grow, b, (p.C + 127) / 128) : grow * nb32_c + b;
-              static_cast<uint8_t*>(p.s_row)[off] = static_cast<uint8_t>(e + 127);
-            }
-          }
-          thr_amax = fmaxf(thr_amax, a);
+        for (int i = 0; i < 4; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, mine, (lane & 16) | (i << 2));
+      } else if (RECIPE == kMx) {
+        // the 32-column block of lane j is lanes 4 (j/4) .. +3; row i = j % 4 ends up in lane 4 (j/4) + i
+        const float m = reduce_scatter4(a, lane, 2, 1);
+        const int e = mx_exponent(m, fexp);
+        const float mine = pow2_neg(e);
+        const int64_t grow = row0 + (j & 3) * 32 + warp * 2 + (lane >> 4);
+        const int64_t b = tc * 4 + (j >> 2);
+        if (grow < p.R && b < nb32_c) {   // a tile hanging over C has blocks past the last one
+          const int64_t off = p.mx_tiled ? mx_tiled_offset(grow, b, (p.C + 127) / 128) : grow * nb32_c + b;
+          static_cast<uint8_t*>(p.s_row)[off] = static_cast<uint8_t>(e + 127);
         }
-        const uint4 w = v[i];
-        const uint32_t lo = q_pair(w.x, sc, e5) | (q_pair(w.y, sc, e5) << 16);
-        const uint32_t hi = q_pair(w.z, sc, e5) | (q_pair(w.w, sc, e5) << 16);
-        sts64(outR + (r << 7) + ((((j >> 1) ^ (r & 7))) << 4) + ((j & 1) << 3), lo, hi);
-      }
-    } else if (RECIPE != kBlock128x128) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) thr_amax = fmaxf(thr_amax, absmax_chunk(v[i]));
+        for (int i = 0; i < 4; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, mine, (lane & ~3) | i);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = i * 32 + warp * 2 + (lane >> 4);
+        const uint2 q = q_chunk(v[i], sc[i], e5);
+        sts64(outR + (r << 7) + ((((j >> 1) ^ (r & 7))) << 4) + ((j & 1) << 3), q.x, q.y);
+      }
     }
 
-    // ---------------- col pass: warp handles 8-column chunks g = warp, warp + 8
+    // ---------------- col pass
     if (p.do_col) {
+      const int g = warp;
+      uint32_t d[4][4];
 #pragma unroll
-      for (int gi = 0; gi < 2; ++gi) {
-        const int g = warp + gi * 8;
-        uint32_t d[4][4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) ldsm_x4_trans(x_addr(xs, 32 * t + 8 * (lane >> 3) + (lane & 7), g), d[t]);
-        // lane holds column cc of the tile, rows 32t + 8m + 2(lane&3) + {0, 1}
-        const int cc = 8 * g + (lane >> 2);
-        const int64_t gcol = col0 + cc;
-        float sc[4] = {tile_scale, tile_scale, tile_scale, tile_scale};
-        if (RECIPE == kBlock1x128) {
-          uint32_t m = 0;
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) m = absmax_bf16x2(m, d[t][q]);
-          float a = pair_max_f32(m);
-          a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-          a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-          const float s = scale_from_amax(a, fmax);
-          sc[0] = sc[1] = sc[2] = sc[3] = s;
-          if ((lane & 3) == 0 && gcol < p.C) static_cast<float*>(p.s_col)[gcol * nb128_r + tr] = recip_rn(s);
-        } else if (RECIPE == kMx) {
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            uint32_t m = absmax_bf16x2(absmax_bf16x2(d[t][0], d[t][1]), absmax_bf16x2(d[t][2], d[t][3]));
-            float a = pair_max_f32(m);
-            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-            const int e = mx_exponent(a, fexp);
-            sc[t] = pow2_neg(e);
-            const int64_t b = static_cast<int64_t>(tr) * 4 + t;
-            if ((lane & 3) == 0 && gcol < p.C && b < nb32_r) {
-              const int64_t off = p.mx_tiled ? mx_tiled_offset(gcol, b, (p.R + 127) / 128) : gcol * nb32_r + b;
-              static_cast<uint8_t*>(p.s_col)[off] = static_cast<uint8_t>(e + 127);
-            }
-          }
-        }
-        if (!p.do_row && RECIPE != kBlock128x128) {
-          uint32_t m = 0;
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) m = absmax_bf16x2(m, d[t][q]);
-          thr_amax = fmaxf(thr_amax, pair_max_f32(m));
-        }
+      for (int t = 0; t < 4; ++t) ldsm_x4_trans(x_addr(xs, 32 * t + 8 * (lane >> 3) + (lane & 7), g), d[t]);
+      const int cc = 8 * g + (lane >> 2);
+      const int64_t gcol = col0 + cc;
+      float sc[4] = {tile_scale, tile_scale, tile_scale, tile_scale};
+      if (RECIPE == kBlock1x128) {
+        uint32_t m = 0;
 #pragma unroll
         for (int t = 0; t < 4; ++t)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int r0 = 32 * t + 8 * q + 2 * (lane & 3);
-            sts16(q_addr(outT, cc, r0), q_pair(d[t][q], sc[t], e5));
-          }
+          for (int q = 0; q < 4; ++q) m = xabs_max(m, d[t][q]);
+        float am = pair_abs_f32(m);
+        am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+        am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+        const float s1 = scale_from_amax(am, fmax);
+        sc[0] = sc[1] = sc[2] = sc[3] = s1;
+        if ((lane & 3) == 0 && gcol < p.C) static_cast<float*>(p.s_col)[gcol * nb128_r + tr] = recip_rn(s1);
+      } else if (RECIPE == kMx) {
+        float at[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) at[t] = pair_abs_f32(xabs_max(xabs_max(d[t][0], d[t][1]), xabs_max(d[t][2], d[t][3])));
+        // block t = lane % 4 of this column ends up in this lane
+        const float m = reduce_scatter4(at, lane, 2, 1);
+        const int e = mx_exponent(m, fexp);
+        const float mine = pow2_neg(e);
+        const int64_t b = static_cast<int64_t>(tr) * 4 + (lane & 3);
+        if (gcol < p.C && b < nb32_r) {
+          const int64_t off = p.mx_tiled ? mx_tiled_offset(gcol, b, (p.R + 127) / 128) : gcol * nb32_r + b;
+          static_cast<uint8_t*>(p.s_col)[off] = static_cast<uint8_t>(e + 127);
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) sc[t] = __shfl_sync(0xFFFFFFFFu, mine, (lane & ~3) | t);
       }
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r0 = 32 * t + 8 * q + 2 * (lane & 3);
+          sts16(q_addr(outT, cc, r0), q_pair(d[t][q], sc[t], e5));
+        }
     }
 
     fence_proxy_async_smem();
@@ -300,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) bulk_wait_all<0>();
 
   if (p.amax_out != nullptr) {
-    const float a = block_max(thr_amax, red, warp, lane);
-    if (tid == 0 && a > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(a));
+    const float am = block_max(thr_amax, red, warp, lane);
+    if (tid == 0 && am > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(am));
   }
 }
 

@@ -59,6 +59,9 @@ def test_block_recipes_with_ragged_free_dimension():
     check_cast(_x((200, 256), 302), R.BLOCK_1x128, F.E4M3, row=True, col=False)
     check_cast(_x((160, 256), 303), R.MX_1x32, F.E4M3)
     check_cast(_x((96, 160), 304), R.MX_1x32, F.E5M2)
+    # column tiles hanging over C by 1 and 3 blocks of 32 (no bytes past the last block)
+    check_cast(_x((256, 416), 305), R.MX_1x32, F.E4M3)
+    check_cast(_x((128, 352), 306), R.MX_1x32, F.E4M3, row=True, col=False)
 
 
 def test_blockwise_config_full_size():

@@ -1,0 +1,54 @@
+"""The pins catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of oracle/fp8_oracle.c (a dropped term,
+a wrong sign, bias or index, a changed tie rule), builds it on the CPU, and runs
+the oracle pin suite against it in a subprocess: the suite must fail."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+from conftest import ROOT
+
+SRC = os.path.join(ROOT, "oracle", "fp8_oracle.c")
+
+MUTANTS = {
+    "ties_away_from_even": ("else c = (lo & 1u) ? up : lo;", "else c = up;"),
+    "e4m3_bias_off_by_one": ("return ldexp((double)(8 + m), (int)e - 10);",
+                             "return ldexp((double)(8 + m), (int)e - 11);"),
+    "e5m2_subnormal_scale": ("if (e == 0) return ldexp((double)m, -16);", "if (e == 0) return ldexp((double)m, -15);"),
+    "no_saturation": ("if (saturate) return (uint8_t)(sign | maxc);", "if (0) return (uint8_t)(sign | maxc);"),
+    "decode_drops_sign": ("return sign ? -v : v;", "return v;"),
+    "amax_signed": ("float a = fabsf(bf16_to_float(x[i]));", "float a = bf16_to_float(x[i]);"),
+    "scale_inverted": ("        s = orc_fmax(fmt) / amax;", "        s = amax / orc_fmax(fmt);"),
+    "scale_zero_rule": ("if (!(amax > 0.0f) || isinf(amax)) {", "if (isinf(amax)) {"),
+    "history_window_one_slot": ("for (int32_t i = 0; i < len; ++i)\n        if (hist[i] > m)",
+                                "for (int32_t i = 0; i < 1; ++i)\n        if (hist[i] > m)"),
+    "mx_exponent_strict": ("if ((double)amax <= ldexp(fmax, e)) return e;", "if ((double)amax < ldexp(fmax, e)) return e;"),
+    "mx_scale_sign": ("float scale = pow2_neg(e);", "float scale = pow2_neg(-e);"),
+    "tile128_first_row_only": ("for (int64_t i = 0; i < 128; ++i) {\n                float a",
+                               "for (int64_t i = 0; i < 1; ++i) {\n                float a"),
+    "dequant_1x128_index": ("case 1: m = (double)sf[r * (C / 128) + c / 128]; break;",
+                            "case 1: m = (double)sf[(r / 128) * (C / 128) + c / 128]; break;"),
+    "dequant_mx_bias": ("default: m = ldexp(1.0, (int)se[r * (C / 32) + c / 32] - 127); break;",
+                        "default: m = ldexp(1.0, (int)se[r * (C / 32) + c / 32] - 128); break;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation site for {name} not found exactly once"
+    src = tmp_path / "mutant.c"
+    src.write_text(text.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", *oracle.CFLAGS, str(src), "-o", str(lib), "-lm"], check=True)
+    env = dict(os.environ, FP8_ORACLE_LIB=str(lib))
+    out = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                          os.path.join(ROOT, "tests", "test_oracle_scaling.py"),
+                          os.path.join(ROOT, "tests", "test_oracle_formats.py")],
+                         capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
+    assert out.returncode != 0, f"the pins did not catch mutant {name}"
