@@ -11,12 +11,13 @@
 //   MXFP8       the tensor core applies 2^(eA - 127) * 2^(eB - 127) per 32-deep block
 //               (guide, "MXFP8 scaling"; kind::mxf8f6f4.block_scale)
 //
-// Structure: a persistent grid (one CTA per SM, 320 threads).
+// Structure: a persistent grid (one CTA per SM).
 //   warp 0      TMA producer: A / B tiles (128-byte swizzle) into a ring of stages,
 //               plus MX scale atoms by bulk copy
 //   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma (and the scale copies)
-//   warps 2..9  epilogue: tcgen05.ld from TMEM, scale, convert, store.  Warp w reads
-//               TMEM lanes 32*(w%4).. (its quarter) and half (w-2)/4 of the columns.
+//   warps 2..   epilogue (8 warps; 16 for the blockwise promotion): tcgen05.ld from TMEM,
+//               scale, convert, store.  Warp w reads TMEM lanes 32*(w%4).. (its quarter)
+//               and column slice (w-2)/4 of the tile.
 // Every wait is time-bounded (ptx.cuh); a timeout sets the device error word, the
 // other roles see a shared abort flag, and the CTA drains and frees TMEM.
 #include <cuda_bf16.h>
@@ -32,8 +33,6 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBK = 128;               // bytes (= FP8 elements) of K per stage
 constexpr int kUmmaK = 32;             // K of one MMA instruction for 8-bit inputs
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
 constexpr int kGroupM = 8;             // tile raster: groups of 8 M-tiles share B tiles in L2
 constexpr uint32_t kTmemCols = 512;
 
@@ -41,15 +40,15 @@ template <int KIND>
 struct Cfg;
 template <>
 struct Cfg<kTensor> {
-  static constexpr int BN = 256, STAGES = 4, ACC = 2;
+  static constexpr int BN = 256, STAGES = 4, ACC = 2, EPI = 8;
 };
 template <>
 struct Cfg<kBlock1x128> {
-  static constexpr int BN = 128, STAGES = 6, ACC = 4;   // ACC = TMEM partial buffers
+  static constexpr int BN = 128, STAGES = 6, ACC = 4, EPI = 16;   // ACC = TMEM partial buffers
 };
 template <>
 struct Cfg<kMx> {
-  static constexpr int BN = 256, STAGES = 4, ACC = 1;
+  static constexpr int BN = 256, STAGES = 4, ACC = 1, EPI = 8;
 };
 
 template <int KIND>
@@ -126,11 +125,16 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   tn = r / gsize;
 }
 
+// warps 0 (producer) and 1 (MMA) plus EPI epilogue warps
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
+constexpr int threads_of() { return 32 * (2 + Cfg<KIND>::EPI); }
+
+template <int KIND>
+__global__ void __launch_bounds__(threads_of<KIND>(), 1)
     k_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, const GemmParams p) {
   using L = Layout<KIND>;
-  constexpr int BN = L::BN, S = L::S, ACC = Cfg<KIND>::ACC;
+  constexpr int BN = L::BN, S = L::S, ACC = Cfg<KIND>::ACC, EPI = Cfg<KIND>::EPI;
+  constexpr int COLS = BN / (EPI / 4);   // columns of the tile each epilogue thread owns
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - smem_u32(smem_raw));
@@ -150,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 4; ++a) {
       mbar_init(base + L::OFF_TFULL + 8 * a, 1);
-      mbar_init(base + L::OFF_TEMPTY + 8 * a, kEpiWarps);
+      mbar_init(base + L::OFF_TEMPTY + 8 * a, EPI);
     }
     mbar_init(base + L::OFF_FINAL, 1);
     *abort_flag = 0;
@@ -167,9 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------ producer
-    int issued[S];
-#pragma unroll
-    for (int s = 0; s < S; ++s) issued[s] = 0;
+    int n_issued = 0;   // loads issued so far; stage s received n_issued / S (+1 if s < n_issued % S)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -198,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_load(sf + 512 + 512 * h, gb, 512, full);
           }
         }
-        ++issued[stage];
+        ++n_issued;
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
@@ -206,11 +208,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // loads this CTA issued must land before it exits (they have, unless a consumer aborted)
-#pragma unroll
-    for (int s = 0; s < S; ++s)
-      if (issued[s] > 0)
-        mbar_wait(base + L::OFF_FULL + 8 * s, static_cast<uint32_t>(issued[s] - 1) & 1u, p.err, kErrTimeoutTmaLoad,
+    for (int s = 0; s < S; ++s) {
+      const int issued_s = n_issued / S + (s < n_issued % S ? 1 : 0);
+      if (issued_s > 0)
+        mbar_wait(base + L::OFF_FULL + 8 * s, static_cast<uint32_t>(issued_s - 1) & 1u, p.err, kErrTimeoutTmaLoad,
                   nullptr);
+    }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------ MMA issuer
     uint32_t idesc;
@@ -295,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 2) {
     // ------------------------------------------------ epilogue
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int h = (warp - 2) >> 2;          // column half
+    const int h = (warp - 2) >> 2;          // which COLS-wide slice of the tile's columns
     const int row = 32 * q + lane;          // row within the tile
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
     const bool fp32 = p.out_fp32 != 0;
@@ -306,14 +309,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tm, tn;
       tile_coords(t, tiles_m, tiles_n, tm, tn);
       const int64_t grow = static_cast<int64_t>(tm) * kBM + row;
-      const int64_t gcol0 = static_cast<int64_t>(tn) * BN + h * (BN / 2);
+      const int64_t gcol0 = static_cast<int64_t>(tn) * BN + h * COLS;
       if (KIND == kBlock1x128) {
         const float* sa_row = static_cast<const float*>(p.sa) + grow * KB;
         const float* sb_blk = static_cast<const float*>(p.sb);
         const float* sb_tile = sb_blk + static_cast<int64_t>(tn) * KB;   // 128x128 B: one factor per k-block
-        uint64_t acc[32];                    // column pairs (2j, 2j+1) of this thread's 64 columns
+        static_assert(KIND != kBlock1x128 || COLS == 32, "blockwise promotion: one 32-column chunk per thread");
+        uint64_t acc[16];                    // column pairs (2j, 2j+1) of this thread's 32 columns
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] = 0;
+        for (int j = 0; j < 16; ++j) acc[j] = 0;
         bool ok = true;
         // scale factors are fetched two k-blocks ahead, off the promotion's critical path
         float sa0 = sa_row[0], sa1 = KB > 1 ? sa_row[1] : 0.0f;
@@ -334,11 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          uint32_t r0[32], r1[32];
-          tc_ld_32x32b_x32(lane_base + pb * BN + h * 64, r0);
-          tc_ld_32x32b_x32(lane_base + pb * BN + h * 64 + 32, r1);
+          uint32_t r0[32];
+          tc_ld_32x32b_x32(lane_base + pb * BN + h * COLS, r0);
           tc_wait_ld(r0);
-          tc_wait_ld(r1);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(base + L::OFF_TEMPTY + 8 * pb);
@@ -351,19 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t f = pack_f32x2(sa_v * __ldg(sbc + (2 * j) * KB), sa_v * __ldg(sbc + (2 * j + 1) * KB));
               acc[j] = fma_f32x2(f, pack_f32x2(r0[2 * j], r0[2 * j + 1]), acc[j]);
             }
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const uint64_t f =
-                  pack_f32x2(sa_v * __ldg(sbc + (32 + 2 * j) * KB), sa_v * __ldg(sbc + (33 + 2 * j) * KB));
-              acc[16 + j] = fma_f32x2(f, pack_f32x2(r1[2 * j], r1[2 * j + 1]), acc[16 + j]);
-            }
           } else {
             const float f1 = sa_v * sb_v;
             const uint64_t f = pack_f32x2(f1, f1);
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[j] = fma_f32x2(f, pack_f32x2(r0[2 * j], r0[2 * j + 1]), acc[j]);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) acc[16 + j] = fma_f32x2(f, pack_f32x2(r1[2 * j], r1[2 * j + 1]), acc[16 + j]);
           }
         }
         if (!ok) break;
@@ -371,47 +365,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j) unpack_f32x2(acc[j], v[2 * j], v[2 * j + 1]);
         if (gcol0 < p.N) store_row32(p.c, grow * p.N + gcol0, v, fp32);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) unpack_f32x2(acc[16 + j], v[2 * j], v[2 * j + 1]);
-        if (gcol0 + 32 < p.N) store_row32(p.c, grow * p.N + gcol0 + 32, v, fp32);
       } else {
         const uint32_t a = acc_it % ACC;
         if (!__all_sync(0xFFFFFFFFu,
                         mbar_wait(base + L::OFF_TFULL + 8 * a, (acc_it / ACC) & 1u, p.err, kErrTimeoutMma, abort_flag)))
           break;
         tc_fence_after();
-        const uint32_t col_base = lane_base + a * BN + h * (BN / 2);
-        if (KIND == kMx) {
-          // pull the whole half-row into registers, free the accumulator, then store
-          uint32_t r[4][32];
+        const uint32_t col_base = lane_base + a * BN + h * COLS;
+        {
+          // pull the whole half-row into registers, free the accumulator, then scale and store
+          constexpr int CH = COLS / 32;
+          uint32_t r[CH][32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tc_ld_32x32b_x32(col_base + 32 * c, r[c]);
+          for (int c = 0; c < CH; ++c) tc_ld_32x32b_x32(col_base + 32 * c, r[c]);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tc_wait_ld(r[c]);
+          for (int c = 0; c < CH; ++c) tc_wait_ld(r[c]);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(base + L::OFF_TEMPTY + 8 * a);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < CH; ++c) {
             float v[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[c][j]);
+            for (int j = 0; j < 32; ++j)
+              v[j] = (KIND == kTensor) ? __fmul_rn(__uint_as_float(r[c][j]), tensor_scale) : __uint_as_float(r[c][j]);
             if (gcol0 + 32 * c < p.N) store_row32(p.c, grow * p.N + gcol0 + 32 * c, v, fp32);
           }
-        } else {
-#pragma unroll 1
-          for (int c = 0; c < BN / 64; ++c) {
-            uint32_t r[32];
-            tc_ld_32x32b_x32(col_base + 32 * c, r);
-            tc_wait_ld(r);
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), tensor_scale);
-            if (gcol0 + 32 * c < p.N) store_row32(p.c, grow * p.N + gcol0 + 32 * c, v, fp32);
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(base + L::OFF_TEMPTY + 8 * a);
         }
         ++acc_it;
       }
@@ -436,7 +415,7 @@ cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& tm_a, const CUte
   if (e != cudaSuccess) return e;
   const int64_t ntiles = (p.M / kBM) * ((p.N + L::BN - 1) / L::BN);
   const int grid = static_cast<int>(ntiles < num_sms ? ntiles : num_sms);
-  k_gemm<KIND><<<grid, kThreads, L::SMEM, s>>>(tm_a, tm_b, p);
+  k_gemm<KIND><<<grid, threads_of<KIND>(), L::SMEM, s>>>(tm_a, tm_b, p);
   return cudaGetLastError();
 }
 
