@@ -15,7 +15,7 @@
 //   warp 0      TMA producer: A / B tiles (128-byte swizzle) into a ring of stages,
 //               plus MX scale atoms by bulk copy
 //   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma (and the scale copies)
-//   warps 2..   epilogue (8 warps; 16 for the blockwise promotion): tcgen05.ld from TMEM,
+//   warps 2..9  epilogue: tcgen05.ld from TMEM,
 //               scale, convert, store.  Warp w reads TMEM lanes 32*(w%4).. (its quarter)
 //               and column slice (w-2)/4 of the tile.
 // Every wait is time-bounded (ptx.cuh); a timeout sets the device error word, the
@@ -36,6 +36,10 @@ constexpr int kUmmaK = 32;             // K of one MMA instruction for 8-bit inp
 constexpr int kGroupM = 8;             // tile raster: groups of 8 M-tiles share B tiles in L2
 constexpr uint32_t kTmemCols = 512;
 
+// Blockwise with per-row B scales (1x128 x 1x128, the wgrad pairing): its own
+// instantiation so the common 1x128 x 128x128 promotion carries no extra registers.
+constexpr int kBlockRowsB = 4;
+
 template <int KIND>
 struct Cfg;
 template <>
@@ -44,8 +48,10 @@ struct Cfg<kTensor> {
 };
 template <>
 struct Cfg<kBlock1x128> {
-  static constexpr int BN = 128, STAGES = 6, ACC = 4, EPI = 16;   // ACC = TMEM partial buffers
+  static constexpr int BN = 128, STAGES = 6, ACC = 4, EPI = 8;   // ACC = TMEM partial buffers
 };
+template <>
+struct Cfg<kBlockRowsB> : Cfg<kBlock1x128> {};
 template <>
 struct Cfg<kMx> {
   static constexpr int BN = 256, STAGES = 4, ACC = 1, EPI = 8;
@@ -134,6 +140,8 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     k_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, const GemmParams p) {
   using L = Layout<KIND>;
   constexpr int BN = L::BN, S = L::S, ACC = Cfg<KIND>::ACC, EPI = Cfg<KIND>::EPI;
+  constexpr bool BLOCK = (KIND == kBlock1x128 || KIND == kBlockRowsB);   // promotion path
+  constexpr bool B_ROWS = (KIND == kBlockRowsB);                         // B scales per row
   constexpr int COLS = BN / (EPI / 4);   // columns of the tile each epilogue thread owns
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -230,7 +238,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     bool ok = true;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       uint32_t d = tmem;
-      if (KIND != kBlock1x128) {
+      if (!BLOCK) {
         const uint32_t a = acc_it % ACC;
         if (!mbar_wait(base + L::OFF_TEMPTY + 8 * a, ((acc_it / ACC) & 1u) ^ 1u, p.err, kErrTimeoutMma, abort_flag)) {
           ok = false;
@@ -240,7 +248,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         d = tmem + a * BN;
       }
       for (int kb = 0; kb < KB; ++kb) {
-        if (KIND == kBlock1x128) {
+        if (BLOCK) {
           const uint32_t pb = part_it % ACC;
           if (!mbar_wait(base + L::OFF_TEMPTY + 8 * pb, ((part_it / ACC) & 1u) ^ 1u, p.err, kErrTimeoutMma,
                          abort_flag)) {
@@ -272,12 +280,12 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         } else {
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
-            const uint32_t accumulate = (KIND == kBlock1x128) ? (k != 0) : ((kb | k) != 0);
+            const uint32_t accumulate = (BLOCK) ? (k != 0) : ((kb | k) != 0);
             tc_mma_f8f6f4(d, sdesc_k_sw128(sa + k * kUmmaK), sdesc_k_sw128(sb + k * kUmmaK), idesc, accumulate);
           }
         }
         tc_commit(base + L::OFF_EMPTY + 8 * stage);
-        if (KIND == kBlock1x128) {
+        if (BLOCK) {
           tc_commit(base + L::OFF_TFULL + 8 * (part_it % ACC));
           ++part_it;
         }
@@ -287,7 +295,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         }
       }
       if (!ok) break;
-      if (KIND != kBlock1x128) {
+      if (!BLOCK) {
         tc_commit(base + L::OFF_TFULL + 8 * (acc_it % ACC));
         ++acc_it;
       }
@@ -310,61 +318,81 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
       tile_coords(t, tiles_m, tiles_n, tm, tn);
       const int64_t grow = static_cast<int64_t>(tm) * kBM + row;
       const int64_t gcol0 = static_cast<int64_t>(tn) * BN + h * COLS;
-      if (KIND == kBlock1x128) {
+      if (BLOCK) {
         const float* sa_row = static_cast<const float*>(p.sa) + grow * KB;
         const float* sb_blk = static_cast<const float*>(p.sb);
         const float* sb_tile = sb_blk + static_cast<int64_t>(tn) * KB;   // 128x128 B: one factor per k-block
-        static_assert(KIND != kBlock1x128 || COLS == 32, "blockwise promotion: one 32-column chunk per thread");
-        uint64_t acc[16];                    // column pairs (2j, 2j+1) of this thread's 32 columns
+        static_assert(!BLOCK || COLS == 64, "blockwise promotion: two 32-column halves per thread");
+        uint64_t acc[32];                    // column pairs (2j, 2j+1) of this thread's 64 columns
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] = 0;
-        bool ok = true;
+        for (int j = 0; j < 32; ++j) acc[j] = 0;
         // scale factors are fetched two k-blocks ahead, off the promotion's critical path
         float sa0 = sa_row[0], sa1 = KB > 1 ? sa_row[1] : 0.0f;
-        float sb0 = p.b_1x128 ? 0.0f : __ldg(sb_tile), sb1 = (!p.b_1x128 && KB > 1) ? __ldg(sb_tile + 1) : 0.0f;
-        for (int kb = 0; kb < KB; ++kb) {
-          const float sa_v = sa0, sb_v = sb0;
-          sa0 = sa1;
-          sb0 = sb1;
-          if (kb + 2 < KB) {
-            sa1 = sa_row[kb + 2];
-            if (!p.b_1x128) sb1 = __ldg(sb_tile + kb + 2);
-          }
+        float sb0 = B_ROWS ? 0.0f : __ldg(sb_tile), sb1 = (!B_ROWS && KB > 1) ? __ldg(sb_tile + 1) : 0.0f;
+        // Software pipeline over 32-column halves: while the FMAs of one half run,
+        // the TMEM load of the next half (same partial, or the next partial's first
+        // half) is in flight.  A partial buffer is released once both halves are in
+        // registers.
+        auto wait_full = [&]() -> bool {
           const uint32_t pb = part_it % ACC;
-          // warp-uniform decision: the TMEM loads below are .sync.aligned
+          // warp-uniform decision: the TMEM loads that follow are .sync.aligned
           if (!__all_sync(0xFFFFFFFFu,
-                          mbar_wait(base + L::OFF_TFULL + 8 * pb, (part_it / ACC) & 1u, p.err, kErrTimeoutMma, abort_flag))) {
-            ok = false;
-            break;
-          }
+                          mbar_wait(base + L::OFF_TFULL + 8 * pb, (part_it / ACC) & 1u, p.err, kErrTimeoutMma, abort_flag)))
+            return false;
           tc_fence_after();
-          uint32_t r0[32];
-          tc_ld_32x32b_x32(lane_base + pb * BN + h * COLS, r0);
-          tc_wait_ld(r0);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(base + L::OFF_TEMPTY + 8 * pb);
-          ++part_it;
-          if (p.b_1x128) {
+          return true;
+        };
+        auto promote = [&](const uint32_t (&r)[32], int half, float sa_v, float sb_v, int kb) {
+          if (B_ROWS) {
             // per-column B scales: sB[n, kb]
-            const float* sbc = sb_blk + (gcol0)*KB + kb;
+            const float* sbc = sb_blk + (gcol0 + 32 * half) * KB + kb;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const uint64_t f = pack_f32x2(sa_v * __ldg(sbc + (2 * j) * KB), sa_v * __ldg(sbc + (2 * j + 1) * KB));
-              acc[j] = fma_f32x2(f, pack_f32x2(r0[2 * j], r0[2 * j + 1]), acc[j]);
+              acc[16 * half + j] = fma_f32x2(f, pack_f32x2(r[2 * j], r[2 * j + 1]), acc[16 * half + j]);
             }
           } else {
             const float f1 = sa_v * sb_v;
             const uint64_t f = pack_f32x2(f1, f1);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = fma_f32x2(f, pack_f32x2(r0[2 * j], r0[2 * j + 1]), acc[j]);
+            for (int j = 0; j < 16; ++j)
+              acc[16 * half + j] = fma_f32x2(f, pack_f32x2(r[2 * j], r[2 * j + 1]), acc[16 * half + j]);
           }
+        };
+        uint32_t rA[32], rB[32];
+        bool ok = wait_full();
+        if (ok) tc_ld_32x32b_x32(lane_base + (part_it % ACC) * BN + h * COLS, rA);
+        for (int kb = 0; ok && kb < KB; ++kb) {
+          const uint32_t pb = part_it % ACC;
+          const float sa_v = sa0, sb_v = sb0;
+          sa0 = sa1;
+          sb0 = sb1;
+          if (kb + 2 < KB) {
+            sa1 = sa_row[kb + 2];
+            if (!B_ROWS) sb1 = __ldg(sb_tile + kb + 2);
+          }
+          tc_wait_ld(rA);                                              // first half of partial kb
+          tc_ld_32x32b_x32(lane_base + pb * BN + h * COLS + 32, rB);   // second half in flight
+          promote(rA, 0, sa_v, sb_v, kb);
+          tc_wait_ld(rB);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(base + L::OFF_TEMPTY + 8 * pb);   // partial kb fully read
+          ++part_it;
+          if (kb + 1 < KB) {
+            ok = wait_full();
+            if (ok) tc_ld_32x32b_x32(lane_base + (part_it % ACC) * BN + h * COLS, rA);   // next partial in flight
+          }
+          promote(rB, 1, sa_v, sb_v, kb);
         }
         if (!ok) break;
         float v[32];
 #pragma unroll
         for (int j = 0; j < 16; ++j) unpack_f32x2(acc[j], v[2 * j], v[2 * j + 1]);
         if (gcol0 < p.N) store_row32(p.c, grow * p.N + gcol0, v, fp32);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) unpack_f32x2(acc[16 + j], v[2 * j], v[2 * j + 1]);
+        if (gcol0 + 32 < p.N) store_row32(p.c, grow * p.N + gcol0 + 32, v, fp32);
       } else {
         const uint32_t a = acc_it % ACC;
         if (!__all_sync(0xFFFFFFFFu,
@@ -429,7 +457,9 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUte
                         cudaStream_t s) {
   switch (p.kind) {
     case kTensor: return launch_kind<kTensor>(p, tm_a, tm_b, num_sms, s);
-    case kBlock1x128: return launch_kind<kBlock1x128>(p, tm_a, tm_b, num_sms, s);
+    case kBlock1x128:
+      return p.b_1x128 ? launch_kind<kBlockRowsB>(p, tm_a, tm_b, num_sms, s)
+                       : launch_kind<kBlock1x128>(p, tm_a, tm_b, num_sms, s);
     default: return launch_kind<kMx>(p, tm_a, tm_b, num_sms, s);
   }
 }
