@@ -57,10 +57,14 @@ struct Cfg<kMx> {
   static constexpr int BN = 256, STAGES = 4, ACC = 1, EPI = 8;
 };
 
+// Stages of the 2-CTA (pair) variant: each CTA holds 128 rows of A and half of B.
 template <int KIND>
+constexpr int pair_stages() { return Cfg<KIND>::BN == 256 ? 6 : 8; }
+
+template <int KIND, bool PAIR>
 struct Layout {
-  static constexpr int BN = Cfg<KIND>::BN, S = Cfg<KIND>::STAGES;
-  static constexpr uint32_t A_BYTES = kBM * kBK, B_BYTES = BN * kBK;
+  static constexpr int BN = Cfg<KIND>::BN, S = PAIR ? pair_stages<KIND>() : Cfg<KIND>::STAGES;
+  static constexpr uint32_t A_BYTES = kBM * kBK, B_BYTES = (PAIR ? BN / 2 : BN) * kBK;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t SF_BYTES = (KIND == kMx) ? (512 + 512 * (BN / 128)) : 0;   // per stage
   static constexpr uint32_t OFF_SF = S * STAGE_BYTES;
@@ -71,7 +75,8 @@ struct Layout {
   static constexpr uint32_t OFF_FINAL = OFF_TEMPTY + 32;
   static constexpr uint32_t OFF_TMEM = OFF_FINAL + 8, OFF_ABORT = OFF_TMEM + 4;
   static constexpr uint32_t SMEM = OFF_ABORT + 64 + 1024;   // + alignment slack
-  static constexpr uint32_t TX_BYTES = STAGE_BYTES + SF_BYTES;
+  // bytes one stage's full barrier expects (in a pair: the leader's barrier sees both CTAs' loads)
+  static constexpr uint32_t TX_BYTES = PAIR ? 2 * STAGE_BYTES : STAGE_BYTES + SF_BYTES;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -135,10 +140,17 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
 template <int KIND>
 constexpr int threads_of() { return 32 * (2 + Cfg<KIND>::EPI); }
 
-template <int KIND>
+// PAIR: a 2-CTA cluster computes a 256-row tile with the 2-SM MMA (cta_group::2).
+// CTA rank r of the pair loads A rows [128 r, 128 r + 128) and B rows
+// [r BN/2, (r + 1) BN/2) of the tile into its own shared memory; both loads
+// signal the leader's (rank 0) stage barrier; the leader issues every MMA and
+// multicasts its commits to both CTAs; each CTA's TMEM holds its 128 rows of D,
+// and both CTAs' epilogues release an accumulator on the leader's barrier.
+template <int KIND, bool PAIR>
 __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     k_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, const GemmParams p) {
-  using L = Layout<KIND>;
+  static_assert(!PAIR || KIND != kMx, "the MX variant runs on single CTAs");
+  using L = Layout<KIND, PAIR>;
   constexpr int BN = L::BN, S = L::S, ACC = Cfg<KIND>::ACC, EPI = Cfg<KIND>::EPI;
   constexpr bool BLOCK = (KIND == kBlock1x128 || KIND == kBlockRowsB);   // promotion path
   constexpr bool B_ROWS = (KIND == kBlockRowsB);                         // B scales per row
@@ -149,9 +161,15 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::OFF_ABORT);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int tiles_m = static_cast<int>(p.M / kBM), tiles_n = static_cast<int>((p.N + BN - 1) / BN);
+  constexpr int TM = PAIR ? 2 * kBM : kBM;                  // rows of one tile
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;      // 0 = the pair's leader
+  const bool leader = rank == 0;
+  const int tiles_m = static_cast<int>(p.M / TM), tiles_n = static_cast<int>((p.N + BN - 1) / BN);
   const int ntiles = tiles_m * tiles_n;
   const int KB = static_cast<int>(p.K / kBK);
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);   // tile-walker index
+  const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int64_t row_off = static_cast<int64_t>(rank) * kBM;   // this CTA's rows within a tile
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tm_a);
@@ -162,18 +180,24 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     }
     for (int a = 0; a < 4; ++a) {
       mbar_init(base + L::OFF_TFULL + 8 * a, 1);
-      mbar_init(base + L::OFF_TEMPTY + 8 * a, EPI);
+      mbar_init(base + L::OFF_TEMPTY + 8 * a, PAIR ? 2 * EPI : EPI);
     }
     mbar_init(base + L::OFF_FINAL, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(base + L::OFF_TMEM, kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(base + L::OFF_TMEM, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(base + L::OFF_TMEM, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();   // the peer's barriers are initialised before anyone signals them
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base_ptr + L::OFF_TMEM);
 
@@ -183,19 +207,26 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+    for (int t = unit0; t < ntiles && ok; t += units) {
       int tm, tn;
       tile_coords(t, tiles_m, tiles_n, tm, tn);
       for (int kb = 0; kb < KB; ++kb) {
         const uint32_t full = base + L::OFF_FULL + 8 * stage;
+        const uint32_t full_sig = PAIR ? mapa_shared(full, 0) : full;   // the barrier the loads signal
         if (!mbar_wait(base + L::OFF_EMPTY + 8 * stage, phase ^ 1u, p.err, kErrTimeoutStage, abort_flag)) {
           ok = false;
           break;
         }
         const uint32_t sa = base + stage * L::STAGE_BYTES;
-        mbar_arrive_expect_tx(full, L::TX_BYTES);
-        tma_load_2d(sa, &tm_a, kb * kBK, tm * kBM, full);
-        tma_load_2d(sa + L::A_BYTES, &tm_b, kb * kBK, tn * BN, full);
+        if (PAIR) {
+          if (leader) mbar_arrive_expect_tx(full, L::TX_BYTES);
+          tma_load_2d_pair(sa, &tm_a, kb * kBK, tm * TM + static_cast<int>(row_off), full_sig);
+          tma_load_2d_pair(sa + L::A_BYTES, &tm_b, kb * kBK, tn * BN + static_cast<int>(rank) * (BN / 2), full_sig);
+        } else {
+          mbar_arrive_expect_tx(full, L::TX_BYTES);
+          tma_load_2d(sa, &tm_a, kb * kBK, tm * kBM, full);
+          tma_load_2d(sa + L::A_BYTES, &tm_b, kb * kBK, tn * BN, full);
+        }
         if (KIND == kMx) {
           const uint32_t sf = base + L::OFF_SF + stage * L::SF_BYTES;
           const uint8_t* ga = static_cast<const uint8_t*>(p.sa) + (static_cast<int64_t>(tm) * KB + kb) * 512;
@@ -215,13 +246,23 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         }
       }
     }
-    // loads this CTA issued must land before it exits (they have, unless a consumer aborted)
+    // loads this CTA issued must land before it exits (they have, unless a consumer aborted).
+    // A pair's loads complete on the leader's barrier, so there the stage's release by the
+    // MMA (which follows the loads) is awaited instead.
     for (int s = 0; s < S; ++s) {
       const int issued_s = n_issued / S + (s < n_issued % S ? 1 : 0);
-      if (issued_s > 0)
-        mbar_wait(base + L::OFF_FULL + 8 * s, static_cast<uint32_t>(issued_s - 1) & 1u, p.err, kErrTimeoutTmaLoad,
-                  nullptr);
+      if (issued_s > 0) {
+        if (PAIR)
+          mbar_wait(base + L::OFF_EMPTY + 8 * s, static_cast<uint32_t>(issued_s - 1) & 1u, p.err, kErrTimeoutStage,
+                    abort_flag);
+        else
+          mbar_wait(base + L::OFF_FULL + 8 * s, static_cast<uint32_t>(issued_s - 1) & 1u, p.err, kErrTimeoutTmaLoad,
+                    nullptr);
+      }
     }
+  } else if (warp == 1 && lane == 0 && !leader) {
+    // ------------------------------------------------ pair peer: no MMAs; wait for the leader's last one
+    mbar_wait(base + L::OFF_FINAL, 0, p.err, kErrTimeoutMma, abort_flag);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------ MMA issuer
     uint32_t idesc;
@@ -230,17 +271,26 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
               (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(kBM >> 4) << 24);
     } else {
       idesc = (1u << 4) | (static_cast<uint32_t>(p.e5m2_a) << 7) | (static_cast<uint32_t>(p.e5m2_b) << 10) |
-              (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
+              (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(TM >> 4) << 24);
     }
+    // a stage / accumulator barrier wait on the leader: the peer CTA arrives on it too
+    auto wait_free = [&](uint32_t bar, uint32_t parity) -> bool {
+      return PAIR ? mbar_wait_cluster(bar, parity, p.err, kErrTimeoutMma, abort_flag)
+                  : mbar_wait(bar, parity, p.err, kErrTimeoutMma, abort_flag);
+    };
+    auto commit = [&](uint32_t bar) {
+      if (PAIR) tc_commit_pair_mc(bar, 3);
+      else tc_commit(bar);
+    };
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc_it = 0, part_it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+    for (int t = unit0; t < ntiles && ok; t += units) {
       uint32_t d = tmem;
       if (!BLOCK) {
         const uint32_t a = acc_it % ACC;
-        if (!mbar_wait(base + L::OFF_TEMPTY + 8 * a, ((acc_it / ACC) & 1u) ^ 1u, p.err, kErrTimeoutMma, abort_flag)) {
+        if (!wait_free(base + L::OFF_TEMPTY + 8 * a, ((acc_it / ACC) & 1u) ^ 1u)) {
           ok = false;
           break;
         }
@@ -250,8 +300,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
       for (int kb = 0; kb < KB; ++kb) {
         if (BLOCK) {
           const uint32_t pb = part_it % ACC;
-          if (!mbar_wait(base + L::OFF_TEMPTY + 8 * pb, ((part_it / ACC) & 1u) ^ 1u, p.err, kErrTimeoutMma,
-                         abort_flag)) {
+          if (!wait_free(base + L::OFF_TEMPTY + 8 * pb, ((part_it / ACC) & 1u) ^ 1u)) {
             ok = false;
             break;
           }
@@ -281,12 +330,15 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             const uint32_t accumulate = (BLOCK) ? (k != 0) : ((kb | k) != 0);
-            tc_mma_f8f6f4(d, sdesc_k_sw128(sa + k * kUmmaK), sdesc_k_sw128(sb + k * kUmmaK), idesc, accumulate);
+            if (PAIR)
+              tc_mma_f8f6f4_pair(d, sdesc_k_sw128(sa + k * kUmmaK), sdesc_k_sw128(sb + k * kUmmaK), idesc, accumulate);
+            else
+              tc_mma_f8f6f4(d, sdesc_k_sw128(sa + k * kUmmaK), sdesc_k_sw128(sb + k * kUmmaK), idesc, accumulate);
           }
         }
-        tc_commit(base + L::OFF_EMPTY + 8 * stage);
+        commit(base + L::OFF_EMPTY + 8 * stage);
         if (BLOCK) {
-          tc_commit(base + L::OFF_TFULL + 8 * (part_it % ACC));
+          commit(base + L::OFF_TFULL + 8 * (part_it % ACC));
           ++part_it;
         }
         if (++stage == S) {
@@ -296,12 +348,12 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
       }
       if (!ok) break;
       if (!BLOCK) {
-        tc_commit(base + L::OFF_TFULL + 8 * (acc_it % ACC));
+        commit(base + L::OFF_TFULL + 8 * (acc_it % ACC));
         ++acc_it;
       }
     }
-    // every MMA this thread issued has finished before TMEM is released
-    tc_commit(base + L::OFF_FINAL);
+    // every MMA this thread issued has finished before TMEM is released (in both CTAs of a pair)
+    commit(base + L::OFF_FINAL);
     mbar_wait(base + L::OFF_FINAL, 0, p.err, kErrTimeoutMma, nullptr);
   } else if (warp >= 2) {
     // ------------------------------------------------ epilogue
@@ -312,11 +364,16 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     const bool fp32 = p.out_fp32 != 0;
     float tensor_scale = 1.0f;
     if (KIND == kTensor) tensor_scale = __fmul_rn(*static_cast<const float*>(p.sa), *static_cast<const float*>(p.sb));
+    // release of an accumulator / partial buffer: on the leader's barrier (remote for the peer)
+    auto release = [&](uint32_t bar) {
+      if (PAIR) mbar_arrive_cluster(mapa_shared(bar, 0));
+      else mbar_arrive(bar);
+    };
     uint32_t acc_it = 0, part_it = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    for (int t = unit0; t < ntiles; t += units) {
       int tm, tn;
       tile_coords(t, tiles_m, tiles_n, tm, tn);
-      const int64_t grow = static_cast<int64_t>(tm) * kBM + row;
+      const int64_t grow = static_cast<int64_t>(tm) * TM + row_off + row;
       const int64_t gcol0 = static_cast<int64_t>(tn) * BN + h * COLS;
       if (BLOCK) {
         const float* sa_row = static_cast<const float*>(p.sa) + grow * KB;
@@ -377,7 +434,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           tc_wait_ld(rB);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(base + L::OFF_TEMPTY + 8 * pb);   // partial kb fully read
+          if (lane == 0) release(base + L::OFF_TEMPTY + 8 * pb);   // partial kb fully read
           ++part_it;
           if (kb + 1 < KB) {
             ok = wait_full();
@@ -410,7 +467,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           for (int c = 0; c < CH; ++c) tc_wait_ld(r[c]);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(base + L::OFF_TEMPTY + 8 * a);
+          if (lane == 0) release(base + L::OFF_TEMPTY + 8 * a);
 #pragma unroll
           for (int c = 0; c < CH; ++c) {
             float v[32];
@@ -427,23 +484,60 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();   // no CTA leaves while its peer may still signal its barriers
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if (PAIR) tmem_dealloc_pair(tmem, kTmemCols);
+    else tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 template <int KIND>
 cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int num_sms,
                         cudaStream_t s) {
-  using L = Layout<KIND>;
+  using L = Layout<KIND, false>;
   static_assert(L::SMEM <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(k_gemm<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(k_gemm<KIND, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(L::SMEM));
   if (e != cudaSuccess) return e;
   const int64_t ntiles = (p.M / kBM) * ((p.N + L::BN - 1) / L::BN);
   const int grid = static_cast<int>(ntiles < num_sms ? ntiles : num_sms);
-  k_gemm<KIND><<<grid, threads_of<KIND>(), L::SMEM, s>>>(tm_a, tm_b, p);
+  k_gemm<KIND, false><<<grid, threads_of<KIND>(), L::SMEM, s>>>(tm_a, tm_b, p);
+  return cudaGetLastError();
+}
+
+// 2-CTA clusters; the grid is as many pairs as can be resident at once (at most
+// one per two SMs), each walking the 256-row tiles with a stride of the pair count.
+template <int KIND>
+cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int num_sms,
+                        cudaStream_t s) {
+  using L = Layout<KIND, true>;
+  static_assert(L::SMEM <= 232448, "shared memory budget");
+  auto kern = k_gemm<KIND, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::SMEM));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(threads_of<KIND>());
+  cfg.dynamicSmemBytes = L::SMEM;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int64_t ntiles = (p.M / (2 * kBM)) * ((p.N + L::BN - 1) / L::BN);
+  int64_t pairs = num_sms / 2;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  int max_clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) == cudaSuccess && max_clusters > 0 &&
+      max_clusters < pairs)
+    pairs = max_clusters;
+  if (ntiles < pairs) pairs = ntiles;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  e = cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -453,10 +547,20 @@ int gemm_block_n(int kind) {
   return kind == kBlock1x128 ? Cfg<kBlock1x128>::BN : (kind == kMx ? Cfg<kMx>::BN : Cfg<kTensor>::BN);
 }
 
+// The per-tensor GEMM runs on CTA pairs.  The blockwise GEMM stays on single CTAs:
+// its promotion hands every 128-deep partial from the MMA to the epilogue and
+// back, and across two SMs that round trip (about a microsecond, measured) costs
+// far more than the halved operand traffic saves.
+bool gemm_uses_pair(int kind, int64_t M) { return kind == kTensor && M % (2 * kBM) == 0; }
+
+int gemm_b_box_rows(int kind, int64_t M) { return gemm_uses_pair(kind, M) ? gemm_block_n(kind) / 2 : gemm_block_n(kind); }
+
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int num_sms,
                         cudaStream_t s) {
   switch (p.kind) {
-    case kTensor: return launch_kind<kTensor>(p, tm_a, tm_b, num_sms, s);
+    case kTensor:
+      return gemm_uses_pair(kTensor, p.M) ? launch_pair<kTensor>(p, tm_a, tm_b, num_sms, s)
+                                          : launch_kind<kTensor>(p, tm_a, tm_b, num_sms, s);
     case kBlock1x128:
       return p.b_1x128 ? launch_kind<kBlockRowsB>(p, tm_a, tm_b, num_sms, s)
                        : launch_kind<kBlock1x128>(p, tm_a, tm_b, num_sms, s);

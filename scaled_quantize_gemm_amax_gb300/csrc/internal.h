@@ -48,8 +48,12 @@ struct GemmParams {
   void* c;               // [M, N] row-major, bf16 or fp32
   uint32_t* err;
 };
-// Width (N) of one output tile of the GEMM variant (the B tensor-map box height).
+// Width (N) of one output tile of the GEMM variant.
 int gemm_block_n(int kind);
+// Whether the GEMM runs on 2-CTA pairs (256-row tiles) for this M.
+bool gemm_uses_pair(int kind, int64_t M);
+// Rows of B one TMA box carries (the tile width, or half of it for a pair).
+int gemm_b_box_rows(int kind, int64_t M);
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int num_sms,
                         cudaStream_t s);
 
