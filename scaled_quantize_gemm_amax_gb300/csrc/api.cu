@@ -60,16 +60,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2-D row-major tensor [outer, inner] of `elem` bytes, box [box_outer, box_inner].
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t elem, const void* ptr, uint64_t inner, uint64_t outer,
-              uint32_t box_inner, uint32_t box_outer) {
+              uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * elem};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -258,6 +257,16 @@ fp8_status fp8_scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const
   if (!make_map(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128)) return FP8_ERR_CUDA;
   if (!make_map(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, static_cast<uint32_t>(gemm_b_box_rows(kind, M))))
     return FP8_ERR_CUDA;
+  // MX: the tiled scale buffers as rows of 256 bytes, two rows (one 512-byte atom) per box
+  CUtensorMap tm_sfa, tm_sfb;
+  std::memset(&tm_sfa, 0, sizeof(tm_sfa));
+  std::memset(&tm_sfb, 0, sizeof(tm_sfb));
+  if (kind == kMx) {
+    const uint64_t atoms_a = static_cast<uint64_t>(M / 128) * (K / 128), atoms_b = static_cast<uint64_t>(N / 128) * (K / 128);
+    if (!make_map(&tm_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sA, 256, 2 * atoms_a, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tm_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sB, 256, 2 * atoms_b, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return FP8_ERR_CUDA;
+  }
   GemmParams p{};
   p.M = M;
   p.N = N;
@@ -271,7 +280,7 @@ fp8_status fp8_scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const
   p.sb = sB;
   p.c = C;
   p.err = d->err;
-  return cuda_status(launch_gemm(p, tm_a, tm_b, d->num_sms, stream));
+  return cuda_status(launch_gemm(p, tm_a, tm_b, tm_sfa, tm_sfb, d->num_sms, stream));
 }
 
 fp8_status fp8_get_device_status(cudaStream_t stream) {

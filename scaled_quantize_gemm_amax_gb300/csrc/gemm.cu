@@ -66,7 +66,8 @@ struct Layout {
   static constexpr int BN = Cfg<KIND>::BN, S = PAIR ? pair_stages<KIND>() : Cfg<KIND>::STAGES;
   static constexpr uint32_t A_BYTES = kBM * kBK, B_BYTES = (PAIR ? BN / 2 : BN) * kBK;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr uint32_t SF_BYTES = (KIND == kMx) ? (512 + 512 * (BN / 128)) : 0;   // per stage
+  // MX scale atoms per stage: this CTA's rows of A and all BN rows of B
+  static constexpr uint32_t SF_BYTES = (KIND == kMx) ? 512 + 512 * (BN / 128) : 0;
   static constexpr uint32_t OFF_SF = S * STAGE_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_SF + S * SF_BYTES;
   // barriers: full[S], empty[S], tfull[4], tempty[4], final
@@ -76,7 +77,7 @@ struct Layout {
   static constexpr uint32_t OFF_TMEM = OFF_FINAL + 8, OFF_ABORT = OFF_TMEM + 4;
   static constexpr uint32_t SMEM = OFF_ABORT + 64 + 1024;   // + alignment slack
   // bytes one stage's full barrier expects (in a pair: the leader's barrier sees both CTAs' loads)
-  static constexpr uint32_t TX_BYTES = PAIR ? 2 * STAGE_BYTES : STAGE_BYTES + SF_BYTES;
+  static constexpr uint32_t TX_BYTES = PAIR ? 2 * (STAGE_BYTES + SF_BYTES) : STAGE_BYTES + SF_BYTES;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -148,8 +149,8 @@ constexpr int threads_of() { return 32 * (2 + Cfg<KIND>::EPI); }
 // and both CTAs' epilogues release an accumulator on the leader's barrier.
 template <int KIND, bool PAIR>
 __global__ void __launch_bounds__(threads_of<KIND>(), 1)
-    k_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, const GemmParams p) {
-  static_assert(!PAIR || KIND != kMx, "the MX variant runs on single CTAs");
+    k_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+           const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb, const GemmParams p) {
   using L = Layout<KIND, PAIR>;
   constexpr int BN = L::BN, S = L::S, ACC = Cfg<KIND>::ACC, EPI = Cfg<KIND>::EPI;
   constexpr bool BLOCK = (KIND == kBlock1x128 || KIND == kBlockRowsB);   // promotion path
@@ -227,7 +228,18 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           tma_load_2d(sa, &tm_a, kb * kBK, tm * kBM, full);
           tma_load_2d(sa + L::A_BYTES, &tm_b, kb * kBK, tn * BN, full);
         }
-        if (KIND == kMx) {
+        if (KIND == kMx && PAIR) {
+          // this CTA's A-scale atom and the B-scale atoms of the whole tile width, each a
+          // 2 x 256-byte box of the tiled scale buffer, signalled on the leader's barrier
+          const uint32_t sf = base + L::OFF_SF + stage * L::SF_BYTES;
+          const int atom_a = (tm * 2 + static_cast<int>(rank)) * KB + kb;
+          tma_load_2d_pair(sf, &tm_sfa, 0, 2 * atom_a, full_sig);
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h) {
+            const int brow = min(tn * (BN / 128) + h, static_cast<int>((p.N - 1) / 128));
+            tma_load_2d_pair(sf + 512 + 512 * h, &tm_sfb, 0, 2 * (brow * KB + kb), full_sig);
+          }
+        } else if (KIND == kMx) {
           const uint32_t sf = base + L::OFF_SF + stage * L::SF_BYTES;
           const uint8_t* ga = static_cast<const uint8_t*>(p.sa) + (static_cast<int64_t>(tm) * KB + kb) * 512;
           bulk_load(sf, ga, 512, full);
@@ -268,7 +280,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     uint32_t idesc;
     if (KIND == kMx) {
       idesc = (static_cast<uint32_t>(p.e5m2_a) << 7) | (static_cast<uint32_t>(p.e5m2_b) << 10) |
-              (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(kBM >> 4) << 24);
+              (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(TM >> 4) << 24);
     } else {
       idesc = (1u << 4) | (static_cast<uint32_t>(p.e5m2_a) << 7) | (static_cast<uint32_t>(p.e5m2_b) << 10) |
               (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(TM >> 4) << 24);
@@ -314,7 +326,21 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         tc_fence_after();
         const uint32_t sa = base + stage * L::STAGE_BYTES;
         const uint32_t sb = sa + L::A_BYTES;
-        if (KIND == kMx) {
+        if (KIND == kMx && PAIR) {
+          // each CTA's atoms go to the same TMEM columns of its own TMEM
+          const uint32_t sf = base + L::OFF_SF + stage * L::SF_BYTES;
+          const uint32_t sf_col = 256u + static_cast<uint32_t>(stage) * (4u + 4u * (BN / 128));
+          tc_cp_32x128b_warpx4_pair(tmem + sf_col, sdesc_rows16(sf));
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)
+            tc_cp_32x128b_warpx4_pair(tmem + sf_col + 4 + 4 * h, sdesc_rows16(sf + 512 + 512 * h));
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            const uint32_t id = idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+            tc_mma_mxf8f6f4_pair(d, sdesc_k_sw128(sa + k * kUmmaK), sdesc_k_sw128(sb + k * kUmmaK), id, tmem + sf_col,
+                                 tmem + sf_col + 4, (kb | k) != 0 ? 1u : 0u);
+          }
+        } else if (KIND == kMx) {
           const uint32_t sf = base + L::OFF_SF + stage * L::SF_BYTES;
           const uint32_t sf_col = 256u + static_cast<uint32_t>(stage) * (4u + 4u * (BN / 128));
           tc_cp_32x128b_warpx4(tmem + sf_col, sdesc_rows16(sf));
@@ -493,8 +519,8 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
 }
 
 template <int KIND>
-cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int num_sms,
-                        cudaStream_t s) {
+cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
+                        const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s) {
   using L = Layout<KIND, false>;
   static_assert(L::SMEM <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(k_gemm<KIND, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -502,15 +528,15 @@ cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& tm_a, const CUte
   if (e != cudaSuccess) return e;
   const int64_t ntiles = (p.M / kBM) * ((p.N + L::BN - 1) / L::BN);
   const int grid = static_cast<int>(ntiles < num_sms ? ntiles : num_sms);
-  k_gemm<KIND, false><<<grid, threads_of<KIND>(), L::SMEM, s>>>(tm_a, tm_b, p);
+  k_gemm<KIND, false><<<grid, threads_of<KIND>(), L::SMEM, s>>>(tm_a, tm_b, tm_sfa, tm_sfb, p);
   return cudaGetLastError();
 }
 
 // 2-CTA clusters; the grid is as many pairs as can be resident at once (at most
 // one per two SMs), each walking the 256-row tiles with a stride of the pair count.
 template <int KIND>
-cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int num_sms,
-                        cudaStream_t s) {
+cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
+                        const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s) {
   using L = Layout<KIND, true>;
   static_assert(L::SMEM <= 232448, "shared memory budget");
   auto kern = k_gemm<KIND, true>;
@@ -536,7 +562,7 @@ cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUte
     pairs = max_clusters;
   if (ntiles < pairs) pairs = ntiles;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-  e = cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, p);
+  e = cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, tm_sfa, tm_sfb, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -551,20 +577,22 @@ int gemm_block_n(int kind) {
 // its promotion hands every 128-deep partial from the MMA to the epilogue and
 // back, and across two SMs that round trip (about a microsecond, measured) costs
 // far more than the halved operand traffic saves.
-bool gemm_uses_pair(int kind, int64_t M) { return kind == kTensor && M % (2 * kBM) == 0; }
+bool gemm_uses_pair(int kind, int64_t M) { return (kind == kTensor || kind == kMx) && M % (2 * kBM) == 0; }
 
 int gemm_b_box_rows(int kind, int64_t M) { return gemm_uses_pair(kind, M) ? gemm_block_n(kind) / 2 : gemm_block_n(kind); }
 
-cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int num_sms,
-                        cudaStream_t s) {
+cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
+                        const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s) {
   switch (p.kind) {
     case kTensor:
-      return gemm_uses_pair(kTensor, p.M) ? launch_pair<kTensor>(p, tm_a, tm_b, num_sms, s)
-                                          : launch_kind<kTensor>(p, tm_a, tm_b, num_sms, s);
+      return gemm_uses_pair(kTensor, p.M) ? launch_pair<kTensor>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
+                                          : launch_kind<kTensor>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
     case kBlock1x128:
-      return p.b_1x128 ? launch_kind<kBlockRowsB>(p, tm_a, tm_b, num_sms, s)
-                       : launch_kind<kBlock1x128>(p, tm_a, tm_b, num_sms, s);
-    default: return launch_kind<kMx>(p, tm_a, tm_b, num_sms, s);
+      return p.b_1x128 ? launch_kind<kBlockRowsB>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
+                       : launch_kind<kBlock1x128>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
+    default:
+      return gemm_uses_pair(kMx, p.M) ? launch_pair<kMx>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
+                                      : launch_kind<kMx>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
   }
 }
 

@@ -54,8 +54,9 @@ int gemm_block_n(int kind);
 bool gemm_uses_pair(int kind, int64_t M);
 // Rows of B one TMA box carries (the tile width, or half of it for a pair).
 int gemm_b_box_rows(int kind, int64_t M);
-cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int num_sms,
-                        cudaStream_t s);
+// tm_sfa / tm_sfb: MX only (the tiled E8M0 buffers as [atoms * 2, 256] bytes, box 2 x 256).
+cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
+                        const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s);
 
 // Bounded-wait self test: one CTA waits on an mbarrier nothing arrives on.
 cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t s);

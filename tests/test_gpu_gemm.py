@@ -133,10 +133,10 @@ def test_gemm_k_zero_writes_zeros():
     assert torch.count_nonzero(c).item() == 0
 
 
-@pytest.mark.parametrize("ra,rb", PAIRS[:3])
+@pytest.mark.parametrize("ra,rb", PAIRS)
 @pytest.mark.parametrize("m,n,k", [(256, 256, 128), (512, 640, 384), (768, 384, 256)])
 def test_gemm_cta_pair_tiles(ra, rb, m, n, k):
-    # M a multiple of 256: the per-tensor and blockwise GEMMs run on 2-CTA pairs
+    # M a multiple of 256: the per-tensor and MX GEMMs run on 2-CTA pairs (blockwise: single CTAs)
     x = wl.normal_bf16((m, k), 40, 1.0)
     w = wl.normal_bf16((n, k), 41, 0.02)
     gemm_check(x, w, ra, rb, F.E4M3, F.E5M2 if k == 384 else F.E4M3,
