@@ -44,17 +44,26 @@ template <int KIND>
 struct Cfg;
 template <>
 struct Cfg<kTensor> {
-  static constexpr int BN = 256, STAGES = 4, ACC = 2, EPI = 8;
+  static constexpr int BN = 256, STAGES = 4, ACC = 2, EPI = 8, KSUB = 1;
 };
 template <>
 struct Cfg<kBlock1x128> {
-  static constexpr int BN = 128, STAGES = 6, ACC = 4, EPI = 8;   // ACC = TMEM partial buffers
+  static constexpr int BN = 128, STAGES = 6, ACC = 4, EPI = 8, KSUB = 1;   // ACC = TMEM partial buffers
 };
 template <>
 struct Cfg<kBlockRowsB> : Cfg<kBlock1x128> {};
+// Blockwise with 256-deep stages: two 128-deep partials per stage, handed to the
+// promotion as one group (one commit, one release).  Every barrier operation of
+// the MMA-issuing thread stalls its next MMA while the tensor core streams shared
+// memory (measured), so halving them per MMA matters most for 128-wide tiles.
+constexpr int kBlockK2 = 5;
+template <>
+struct Cfg<kBlockK2> {
+  static constexpr int BN = 128, STAGES = 3, ACC = 4, EPI = 8, KSUB = 2;
+};
 template <>
 struct Cfg<kMx> {
-  static constexpr int BN = 256, STAGES = 4, ACC = 1, EPI = 8;
+  static constexpr int BN = 256, STAGES = 4, ACC = 1, EPI = 8, KSUB = 1;
 };
 
 // Stages of the 2-CTA (pair) variant: each CTA holds 128 rows of A and half of B.
@@ -64,7 +73,10 @@ constexpr int pair_stages() { return Cfg<KIND>::BN == 256 ? 6 : 8; }
 template <int KIND, bool PAIR>
 struct Layout {
   static constexpr int BN = Cfg<KIND>::BN, S = PAIR ? pair_stages<KIND>() : Cfg<KIND>::STAGES;
-  static constexpr uint32_t A_BYTES = kBM * kBK, B_BYTES = (PAIR ? BN / 2 : BN) * kBK;
+  static constexpr int KSUB = Cfg<KIND>::KSUB;
+  // per K sub-block: A [128 rows][128 B], B [BN (or BN/2) rows][128 B]; a stage holds KSUB of each
+  static constexpr uint32_t A_SUB = kBM * kBK, B_SUB = (PAIR ? BN / 2 : BN) * kBK;
+  static constexpr uint32_t A_BYTES = A_SUB * KSUB, B_BYTES = B_SUB * KSUB;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   // MX scale atoms per stage: this CTA's rows of A and all BN rows of B
   static constexpr uint32_t SF_BYTES = (KIND == kMx) ? 512 + 512 * (BN / 128) : 0;
@@ -153,7 +165,13 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
            const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb, const GemmParams p) {
   using L = Layout<KIND, PAIR>;
   constexpr int BN = L::BN, S = L::S, ACC = Cfg<KIND>::ACC, EPI = Cfg<KIND>::EPI;
-  constexpr bool BLOCK = (KIND == kBlock1x128 || KIND == kBlockRowsB);   // promotion path
+  constexpr bool BLOCK = (KIND == kBlock1x128 || KIND == kBlockRowsB || KIND == kBlockK2);   // promotion path
+  constexpr int KSUB = L::KSUB;
+  constexpr int GROUPS = ACC / KSUB;   // partial-buffer groups (blockwise)
+  static_assert(KSUB == 1 || (BLOCK && !PAIR), "multi-block stages: blockwise, single CTA");
+  // Blockwise, single CTA: a stage's full barrier also counts the epilogue's release of
+  // the partial group that stage will write, so the MMA thread waits once per stage.
+  constexpr bool GATED = BLOCK && !PAIR;
   constexpr bool B_ROWS = (KIND == kBlockRowsB);                         // B scales per row
   constexpr int COLS = BN / (EPI / 4);   // columns of the tile each epilogue thread owns
   extern __shared__ uint8_t smem_raw[];
@@ -168,6 +186,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   const int tiles_m = static_cast<int>(p.M / TM), tiles_n = static_cast<int>((p.N + BN - 1) / BN);
   const int ntiles = tiles_m * tiles_n;
   const int KB = static_cast<int>(p.K / kBK);
+  const int NG = KB / KSUB;   // stages per tile (K / 128 is a multiple of KSUB)
   const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);   // tile-walker index
   const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int64_t row_off = static_cast<int64_t>(rank) * kBM;   // this CTA's rows within a tile
@@ -176,7 +195,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     prefetch_tmap(&tm_a);
     prefetch_tmap(&tm_b);
     for (int s = 0; s < S; ++s) {
-      mbar_init(base + L::OFF_FULL + 8 * s, 1);
+      mbar_init(base + L::OFF_FULL + 8 * s, GATED ? 1 + EPI : 1);
       mbar_init(base + L::OFF_EMPTY + 8 * s, 1);
     }
     for (int a = 0; a < 4; ++a) {
@@ -211,7 +230,8 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     for (int t = unit0; t < ntiles && ok; t += units) {
       int tm, tn;
       tile_coords(t, tiles_m, tiles_n, tm, tn);
-      for (int kb = 0; kb < KB; ++kb) {
+      for (int kg = 0; kg < NG; ++kg) {
+        const int kb = kg * KSUB;   // first 128-deep K block of this stage
         const uint32_t full = base + L::OFF_FULL + 8 * stage;
         const uint32_t full_sig = PAIR ? mapa_shared(full, 0) : full;   // the barrier the loads signal
         if (!mbar_wait(base + L::OFF_EMPTY + 8 * stage, phase ^ 1u, p.err, kErrTimeoutStage, abort_flag)) {
@@ -225,8 +245,11 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           tma_load_2d_pair(sa + L::A_BYTES, &tm_b, kb * kBK, tn * BN + static_cast<int>(rank) * (BN / 2), full_sig);
         } else {
           mbar_arrive_expect_tx(full, L::TX_BYTES);
-          tma_load_2d(sa, &tm_a, kb * kBK, tm * kBM, full);
-          tma_load_2d(sa + L::A_BYTES, &tm_b, kb * kBK, tn * BN, full);
+#pragma unroll
+          for (int sub = 0; sub < KSUB; ++sub) {
+            tma_load_2d(sa + sub * L::A_SUB, &tm_a, (kb + sub) * kBK, tm * kBM, full);
+            tma_load_2d(sa + L::A_BYTES + sub * L::B_SUB, &tm_b, (kb + sub) * kBK, tn * BN, full);
+          }
         }
         if (KIND == kMx && PAIR) {
           // this CTA's A-scale atom and the B-scale atoms of the whole tile width, each a
@@ -309,15 +332,18 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         tc_fence_after();
         d = tmem + a * BN;
       }
-      for (int kb = 0; kb < KB; ++kb) {
+      for (int kg = 0; kg < NG; ++kg) {
+        const int kb = kg * KSUB;
         if (BLOCK) {
-          const uint32_t pb = part_it % ACC;
-          if (!wait_free(base + L::OFF_TEMPTY + 8 * pb, ((part_it / ACC) & 1u) ^ 1u)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          d = tmem + pb * BN;
+          const uint32_t pb = part_it % GROUPS;   // partial group: buffers pb*KSUB .. +KSUB-1
+          if (!GATED) {
+            if (!wait_free(base + L::OFF_TEMPTY + 8 * pb, ((part_it / GROUPS) & 1u) ^ 1u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }   // gated: the full-barrier wait below also covers the group's release
+          d = tmem + pb * KSUB * BN;
         }
         if (!mbar_wait(base + L::OFF_FULL + 8 * stage, phase, p.err, kErrTimeoutTmaLoad, abort_flag)) {
           ok = false;
@@ -354,17 +380,22 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           }
         } else {
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k) {
-            const uint32_t accumulate = (BLOCK) ? (k != 0) : ((kb | k) != 0);
-            if (PAIR)
-              tc_mma_f8f6f4_pair(d, sdesc_k_sw128(sa + k * kUmmaK), sdesc_k_sw128(sb + k * kUmmaK), idesc, accumulate);
-            else
-              tc_mma_f8f6f4(d, sdesc_k_sw128(sa + k * kUmmaK), sdesc_k_sw128(sb + k * kUmmaK), idesc, accumulate);
+          for (int sub = 0; sub < KSUB; ++sub) {
+            const uint32_t dsub = d + (BLOCK ? sub * BN : 0);   // blockwise: one partial per sub-block
+#pragma unroll
+            for (int k = 0; k < kBK / kUmmaK; ++k) {
+              const uint32_t accumulate = (BLOCK) ? (k != 0) : ((kb | k) != 0);
+              const uint32_t a_k = sa + sub * L::A_SUB + k * kUmmaK, b_k = sb + sub * L::B_SUB + k * kUmmaK;
+              if (PAIR)
+                tc_mma_f8f6f4_pair(dsub, sdesc_k_sw128(a_k), sdesc_k_sw128(b_k), idesc, accumulate);
+              else
+                tc_mma_f8f6f4(dsub, sdesc_k_sw128(a_k), sdesc_k_sw128(b_k), idesc, accumulate);
+            }
           }
         }
         commit(base + L::OFF_EMPTY + 8 * stage);
         if (BLOCK) {
-          commit(base + L::OFF_TFULL + 8 * (part_it % ACC));
+          commit(base + L::OFF_TFULL + 8 * (part_it % GROUPS));
           ++part_it;
         }
         if (++stage == S) {
@@ -396,6 +427,13 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
       else mbar_arrive(bar);
     };
     uint32_t acc_it = 0, part_it = 0;
+    // stages (partial groups) this CTA runs in all; gated: the first GROUPS stages find
+    // their partial groups free
+    const uint32_t my_tiles = unit0 < ntiles ? static_cast<uint32_t>((ntiles - unit0 + units - 1) / units) : 0u;
+    const uint32_t total_groups = my_tiles * static_cast<uint32_t>(NG);
+    if (GATED && lane == 0) {
+      for (uint32_t g = 0; g < static_cast<uint32_t>(GROUPS) && g < total_groups; ++g) mbar_arrive(base + L::OFF_FULL + 8 * (g % S));
+    }
     for (int t = unit0; t < ntiles; t += units) {
       int tm, tn;
       tile_coords(t, tiles_m, tiles_n, tm, tn);
@@ -404,78 +442,104 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
       if (BLOCK) {
         const float* sa_row = static_cast<const float*>(p.sa) + grow * KB;
         const float* sb_blk = static_cast<const float*>(p.sb);
-        const float* sb_tile = sb_blk + static_cast<int64_t>(tn) * KB;   // 128x128 B: one factor per k-block
-        static_assert(!BLOCK || COLS == 64, "blockwise promotion: two 32-column halves per thread");
-        uint64_t acc[32];                    // column pairs (2j, 2j+1) of this thread's 64 columns
+        // Promotion: TMEM loads of CW columns (32, or 16 when a thread owns 128 columns, to
+        // fit the registers), software-pipelined: while the FMAs of one chunk run, the
+        // load of the next chunk (of this partial, or the first of the next partial) is in
+        // flight.  A partial buffer is released once all its chunks are in registers.
+        constexpr int CW = (COLS >= 128) ? 16 : 32;
+        constexpr int NC = COLS / CW;
+        static_assert(!BLOCK || (NC % 2 == 0 && COLS % 32 == 0), "blockwise promotion chunking");
+        const float* sb_tile = sb_blk + (gcol0 / 128) * KB;   // 128x128 B: one factor per k-block
+        uint64_t acc[COLS / 2];              // column pairs (2j, 2j+1) of this thread's columns
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] = 0;
+        for (int j = 0; j < COLS / 2; ++j) acc[j] = 0;
         // scale factors are fetched two k-blocks ahead, off the promotion's critical path
         float sa0 = sa_row[0], sa1 = KB > 1 ? sa_row[1] : 0.0f;
         float sb0 = B_ROWS ? 0.0f : __ldg(sb_tile), sb1 = (!B_ROWS && KB > 1) ? __ldg(sb_tile + 1) : 0.0f;
-        // Software pipeline over 32-column halves: while the FMAs of one half run,
-        // the TMEM load of the next half (same partial, or the next partial's first
-        // half) is in flight.  A partial buffer is released once both halves are in
-        // registers.
         auto wait_full = [&]() -> bool {
-          const uint32_t pb = part_it % ACC;
+          const uint32_t pb = part_it % GROUPS;
           // warp-uniform decision: the TMEM loads that follow are .sync.aligned
           if (!__all_sync(0xFFFFFFFFu,
-                          mbar_wait(base + L::OFF_TFULL + 8 * pb, (part_it / ACC) & 1u, p.err, kErrTimeoutMma, abort_flag)))
+                          mbar_wait(base + L::OFF_TFULL + 8 * pb, (part_it / GROUPS) & 1u, p.err, kErrTimeoutMma, abort_flag)))
             return false;
           tc_fence_after();
           return true;
         };
-        auto promote = [&](const uint32_t (&r)[32], int half, float sa_v, float sb_v, int kb) {
+        auto promote = [&](const uint32_t (&r)[CW], int c, float sa_v, float sb_v, int kb) {
           if (B_ROWS) {
             // per-column B scales: sB[n, kb]
-            const float* sbc = sb_blk + (gcol0 + 32 * half) * KB + kb;
+            const float* sbc = sb_blk + (gcol0 + CW * c) * KB + kb;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < CW / 2; ++j) {
               const uint64_t f = pack_f32x2(sa_v * __ldg(sbc + (2 * j) * KB), sa_v * __ldg(sbc + (2 * j + 1) * KB));
-              acc[16 * half + j] = fma_f32x2(f, pack_f32x2(r[2 * j], r[2 * j + 1]), acc[16 * half + j]);
+              acc[(CW / 2) * c + j] = fma_f32x2(f, pack_f32x2(r[2 * j], r[2 * j + 1]), acc[(CW / 2) * c + j]);
             }
           } else {
             const float f1 = sa_v * sb_v;
             const uint64_t f = pack_f32x2(f1, f1);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              acc[16 * half + j] = fma_f32x2(f, pack_f32x2(r[2 * j], r[2 * j + 1]), acc[16 * half + j]);
+            for (int j = 0; j < CW / 2; ++j)
+              acc[(CW / 2) * c + j] = fma_f32x2(f, pack_f32x2(r[2 * j], r[2 * j + 1]), acc[(CW / 2) * c + j]);
           }
         };
-        uint32_t rA[32], rB[32];
+        uint32_t rbuf[2][CW];
+        // column offset in TMEM of chunk c of sub-block `sub` of partial group `pb`
+        auto chunk_col = [&](uint32_t pb, int sub, int c) -> uint32_t {
+          return lane_base + (pb * KSUB + sub) * BN + h * COLS + CW * c;
+        };
         bool ok = wait_full();
-        if (ok) tc_ld_32x32b_x32(lane_base + (part_it % ACC) * BN + h * COLS, rA);
-        for (int kb = 0; ok && kb < KB; ++kb) {
-          const uint32_t pb = part_it % ACC;
-          const float sa_v = sa0, sb_v = sb0;
-          sa0 = sa1;
-          sb0 = sb1;
-          if (kb + 2 < KB) {
-            sa1 = sa_row[kb + 2];
-            if (!B_ROWS) sb1 = __ldg(sb_tile + kb + 2);
+        if (ok) tc_ld_32x32b(chunk_col(part_it % GROUPS, 0, 0), rbuf[0]);
+        for (int kg = 0; ok && kg < NG; ++kg) {
+          const uint32_t group_seq = part_it;   // stages (= partial groups) this CTA has used before
+          const uint32_t pb = part_it % GROUPS;
+#pragma unroll
+          for (int sub = 0; sub < KSUB; ++sub) {
+            const int kb = kg * KSUB + sub;
+            const float sa_v = sa0, sb_v = sb0;
+            sa0 = sa1;
+            sb0 = sb1;
+            if (kb + 2 < KB) {
+              sa1 = sa_row[kb + 2];
+              if (!B_ROWS) sb1 = __ldg(sb_tile + kb + 2);
+            }
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+              const int i = sub * NC + c;   // chunk index within the group (NC is even)
+              tc_wait_ld(rbuf[i & 1]);
+              if (c + 1 < NC) {
+                tc_ld_32x32b(chunk_col(pb, sub, c + 1), rbuf[(i + 1) & 1]);
+              } else if (sub + 1 < KSUB) {
+                tc_ld_32x32b(chunk_col(pb, sub + 1, 0), rbuf[(i + 1) & 1]);
+              } else {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                  if (GATED) {
+                    // the stage that reuses this group is GROUPS stages later
+                    const uint32_t next = group_seq + GROUPS;
+                    if (next < total_groups) mbar_arrive(base + L::OFF_FULL + 8 * (next % S));
+                  } else {
+                    release(base + L::OFF_TEMPTY + 8 * pb);   // the group's partials fully read
+                  }
+                }
+                ++part_it;
+                if (kg + 1 < NG) {
+                  ok = wait_full();
+                  if (ok) tc_ld_32x32b(chunk_col(part_it % GROUPS, 0, 0), rbuf[(i + 1) & 1]);
+                }
+              }
+              promote(rbuf[i & 1], c, sa_v, sb_v, kb);
+            }
           }
-          tc_wait_ld(rA);                                              // first half of partial kb
-          tc_ld_32x32b_x32(lane_base + pb * BN + h * COLS + 32, rB);   // second half in flight
-          promote(rA, 0, sa_v, sb_v, kb);
-          tc_wait_ld(rB);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) release(base + L::OFF_TEMPTY + 8 * pb);   // partial kb fully read
-          ++part_it;
-          if (kb + 1 < KB) {
-            ok = wait_full();
-            if (ok) tc_ld_32x32b_x32(lane_base + (part_it % ACC) * BN + h * COLS, rA);   // next partial in flight
-          }
-          promote(rB, 1, sa_v, sb_v, kb);
         }
         if (!ok) break;
-        float v[32];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) unpack_f32x2(acc[j], v[2 * j], v[2 * j + 1]);
-        if (gcol0 < p.N) store_row32(p.c, grow * p.N + gcol0, v, fp32);
+        for (int c32 = 0; c32 < COLS / 32; ++c32) {
+          float v[32];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) unpack_f32x2(acc[16 + j], v[2 * j], v[2 * j + 1]);
-        if (gcol0 + 32 < p.N) store_row32(p.c, grow * p.N + gcol0 + 32, v, fp32);
+          for (int j = 0; j < 16; ++j) unpack_f32x2(acc[16 * c32 + j], v[2 * j], v[2 * j + 1]);
+          if (gcol0 + 32 * c32 < p.N) store_row32(p.c, grow * p.N + gcol0 + 32 * c32, v, fp32);
+        }
       } else {
         const uint32_t a = acc_it % ACC;
         if (!__all_sync(0xFFFFFFFFu,
@@ -588,8 +652,9 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUte
       return gemm_uses_pair(kTensor, p.M) ? launch_pair<kTensor>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
                                           : launch_kind<kTensor>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
     case kBlock1x128:
-      return p.b_1x128 ? launch_kind<kBlockRowsB>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
-                       : launch_kind<kBlock1x128>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
+      if (p.b_1x128) return launch_kind<kBlockRowsB>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
+      return (p.K / kBK) % 2 == 0 ? launch_kind<kBlockK2>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
+                                  : launch_kind<kBlock1x128>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
     default:
       return gemm_uses_pair(kMx, p.M) ? launch_pair<kMx>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
                                       : launch_kind<kMx>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
