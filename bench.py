@@ -36,6 +36,9 @@ WORKLOAD = "blockwise fprop 4096x4096x4096: X 1x128 E4M3 (row+col), W 128x128 E4
 METRIC = "FP8 scaled-GEMM TFLOPS & quantize GB/s per recipe, % of GB300 roofline"
 UNIT = "TFLOP/s"
 FLUSH_BYTES = 256 << 20
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one blockwise GEMM launch at
+# 4096^3 from an ncu capture of the current kernel version; None when not captured for it
+TRAFFIC_GEMM = None
 
 
 def peaks():
@@ -179,6 +182,21 @@ def bytes_cast_128x128(r, c):
     return r * c * 4 + 2 * (r * c // 16384) * 4
 
 
+def _capture(fn):
+    """Capture `fn` (a sequence of C-ABI calls on the current stream) in a CUDA graph."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()                     # warm: attributes and caches set outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
 def run_ours(args, rank, world):
     import scaled_quantize_gemm_amax_gb300 as fq
     from scaled_quantize_gemm_amax_gb300 import build as fqbuild
@@ -192,15 +210,22 @@ def run_ours(args, rank, world):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    for _ in range(args.warmup):
+    def step():
         path.cast_x()
         path.cast_w()
         path.gemm()
+
+    # the timed step is one CUDA graph of the three launches (no host launch cost inside it);
+    # per-kernel times come from one graph per kernel, timed the same way
+    g_step = _capture(step)
+    g_parts = [_capture(path.cast_x), _capture(path.cast_w), _capture(path.gemm)]
+    for _ in range(args.warmup):
+        g_step.replay()
         flush.zero_()
     torch.cuda.synchronize()
     assert fq.fp8_get_device_status() == fq.Status.OK
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = ClockSampler(torch.cuda.current_device(), os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
     clocks.start()
@@ -208,34 +233,38 @@ def run_ours(args, rank, world):
     barrier(world)
     torch.cuda.synchronize()
     for i in range(args.steps):
-        e = ev[i]
-        e[0].record(stream)
-        path.cast_x()
-        e[1].record(stream)
-        path.cast_w()
-        e[2].record(stream)
-        path.gemm()
-        e[3].record(stream)
+        ev[i][0].record(stream)
+        g_step.replay()
+        ev[i][1].record(stream)
         flush.zero_()          # outside the step's events: L2 does not carry inputs across steps
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
     st = fq.fp8_get_device_status()
     assert st == fq.Status.OK, st
-
-    t_cx = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
-    t_cw = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    t_g = [ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps)]
-    step_ms_local = sum(ev[i][0].elapsed_time(ev[i][3]) for i in range(args.steps)) / args.steps
+    step_ms_local = statistics.mean(a.elapsed_time(b) for a, b in ev)
     step_ms = max_over_ranks(step_ms_local, world)
+
+    # per-kernel breakdown (same flush discipline, each kernel's own graph)
+    reps = max(5, min(args.steps, 100))
+    part_ms = []
+    for g in g_parts:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        part_ms.append(statistics.mean(a.elapsed_time(b) for a, b in evs))
+    t_cx, t_cw, g_ms = part_ms
 
     flops = 2.0 * M * N * K
     pk = peaks()
     fp8_peak = 2.0 * pk["bf16_tflops"]           # FP8 dense = 2 x BF16 dense (nominal 4.5 / 2.25 PF)
-    g_ms = statistics.mean(t_g)
     gemm_tflops = flops / (g_ms * 1e-3) / 1e12
-    cx_gbs = bytes_cast_1x128(M, K) / (statistics.mean(t_cx) * 1e-3) / 1e9
-    cw_gbs = bytes_cast_128x128(N, K) / (statistics.mean(t_cw) * 1e-3) / 1e9
+    cx_gbs = bytes_cast_1x128(M, K) / (t_cx * 1e-3) / 1e9
+    cw_gbs = bytes_cast_128x128(N, K) / (t_cw * 1e-3) / 1e9
     value = world * flops / (step_ms * 1e-3) / 1e12
 
     result = {
@@ -244,24 +273,25 @@ def run_ours(args, rank, world):
         "vs_baseline": None, "dtype": "fp8-e4m3 (fp32 accumulate, bf16 out)",
         "data": "synthetic (seeded N(0,1) + 1% columns x100 / N(0,0.02))",
         "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "recipe": "blockwise 1x128 x 128x128",
-                   "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
+                   "l2": "flushed between steps (256 MiB write)", "launch": "one CUDA graph per step",
+                   "parallelism": f"replicas x{world}"},
         "kernels": {
-            "cast_transpose_x_1x128": {"us": round(statistics.mean(t_cx) * 1e3, 2), "GB/s": round(cx_gbs, 1),
+            "cast_transpose_x_1x128": {"us": round(t_cx * 1e3, 2), "GB/s": round(cx_gbs, 1),
                                        "frac_hbm": round(cx_gbs / pk["hbm_gbs"], 4)},
-            "cast_transpose_w_128x128": {"us": round(statistics.mean(t_cw) * 1e3, 2), "GB/s": round(cw_gbs, 1),
+            "cast_transpose_w_128x128": {"us": round(t_cw * 1e3, 2), "GB/s": round(cw_gbs, 1),
                                          "frac_hbm": round(cw_gbs / pk["hbm_gbs"], 4)},
             "gemm_blockwise": {"us": round(g_ms * 1e3, 2), "TFLOP/s": round(gemm_tflops, 1),
                                "frac_fp8": round(gemm_tflops / fp8_peak, 4)},
         },
         "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
-                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4), "traffic": TRAFFIC_GEMM,
                      "peak_source": f"{pk['source']}: 2 x bf16 burst ({pk['bf16_tflops']})"},
         "gpu_launches": path.launches_per_step * args.steps,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                    "samples": clk["samples"]},
     }
     if not args.no_e2e:
-        result["e2e"] = run_e2e(fq, path, x, w, args, world)
+        result["e2e"] = run_e2e(fq, x, w, args, world)
     if args.sweep:
         result["per_recipe"] = run_sweep(fq, wl, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -269,39 +299,62 @@ def run_ours(args, rank, world):
     return result
 
 
-def run_e2e(fq, path, x, w, args, world):
-    """The same step through the public API with host buffers: pinned host -> device
-    copies of X and W, the three calls, and Y copied back, all inside the timed region."""
+def run_e2e(fq, x, w, args, world):
+    """The same step through the public API with host buffers: every step copies X and W
+    from pinned host memory, runs the three calls, and copies Y back to pinned host
+    memory, all inside the timed region.  Consecutive steps overlap on three streams
+    (copy in, compute, copy out) with two sets of device buffers."""
     xh = x.cpu().pin_memory()
     wh = w.cpu().pin_memory()
-    yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
-    stream = torch.cuda.current_stream()
-    steps = max(3, min(args.steps, 50))
-    for _ in range(2):
-        path.x.copy_(xh, non_blocking=True)
-        path.w.copy_(wh, non_blocking=True)
-        path.cast_x()
-        path.cast_w()
-        path.gemm()
-        yh.copy_(path.y, non_blocking=True)
+    dev = x.device
+    paths = [Path(fq, torch.empty_like(x), torch.empty_like(w)) for _ in range(2)]
+    yh = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    comp = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event()
+    in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    steps = max(4, min(args.steps, 64))
+
+    def run(n):
+        for i in range(n):
+            b = i % 2
+            p = paths[b]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(comp_done[b])          # buffer b's previous step has been consumed
+                p.x.copy_(xh, non_blocking=True)
+                p.w.copy_(wh, non_blocking=True)
+                in_done[b].record(s_in)
+            comp.wait_event(in_done[b])
+            if i >= 2:
+                comp.wait_event(out_done[b])              # buffer b's previous result has left
+            p.cast_x()
+            p.cast_w()
+            p.gemm()
+            comp_done[b].record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[b])
+                yh[b].copy_(p.y, non_blocking=True)
+                out_done[b].record(s_out)
+
+    run(4)
     torch.cuda.synchronize()
     barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        path.x.copy_(xh, non_blocking=True)
-        path.w.copy_(wh, non_blocking=True)
-        path.cast_x()
-        path.cast_w()
-        path.gemm()
-        yh.copy_(path.y, non_blocking=True)
-    e1.record(stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(comp)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    run(steps)
+    comp.wait_stream(s_in)
+    comp.wait_stream(s_out)
+    e1.record(comp)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    # the last results did reach the host
+    assert torch.equal(yh[(steps - 1) % 2], paths[(steps - 1) % 2].y.cpu())
     return {"value": round(world * 2.0 * M * N * K / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
-            "ms_per_step": round(ms, 4), "steps": steps,
-            "h2d_bytes_per_step": int(xh.numel() * 2 + wh.numel() * 2), "d2h_bytes_per_step": int(yh.numel() * 2)}
+            "ms_per_step": round(ms, 4), "steps": steps, "overlap": "copy-in / compute / copy-out streams",
+            "h2d_bytes_per_step": int(xh.numel() * 2 + wh.numel() * 2), "d2h_bytes_per_step": int(M * N * 2)}
 
 
 def _time_kernel(fn, reps=20, flush=None):

@@ -16,7 +16,6 @@ namespace {
 // The device error word (one per device that loads the library).
 __device__ uint32_t g_error_word;
 
-constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;

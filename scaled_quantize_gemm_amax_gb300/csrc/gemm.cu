@@ -587,8 +587,8 @@ cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& tm_a, const CUte
                         const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s) {
   using L = Layout<KIND, false>;
   static_assert(L::SMEM <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(k_gemm<KIND, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(L::SMEM));
+  static bool attr_done[kMaxDevices] = {};
+  cudaError_t e = ensure_smem_limit(k_gemm<KIND, false>, static_cast<int>(L::SMEM), attr_done);
   if (e != cudaSuccess) return e;
   const int64_t ntiles = (p.M / kBM) * ((p.N + L::BN - 1) / L::BN);
   const int grid = static_cast<int>(ntiles < num_sms ? ntiles : num_sms);
@@ -604,7 +604,8 @@ cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUte
   using L = Layout<KIND, true>;
   static_assert(L::SMEM <= 232448, "shared memory budget");
   auto kern = k_gemm<KIND, true>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::SMEM));
+  static bool attr_done[kMaxDevices] = {};
+  cudaError_t e = ensure_smem_limit(kern, static_cast<int>(L::SMEM), attr_done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -620,10 +621,16 @@ cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUte
   const int64_t ntiles = (p.M / (2 * kBM)) * ((p.N + L::BN - 1) / L::BN);
   int64_t pairs = num_sms / 2;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-  int max_clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) == cudaSuccess && max_clusters > 0 &&
-      max_clusters < pairs)
-    pairs = max_clusters;
+  // resident pairs: queried once per device
+  static int max_clusters[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (max_clusters[dev] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = static_cast<int>(pairs);
+    max_clusters[dev] = n;
+  }
+  if (max_clusters[dev] < pairs) pairs = max_clusters[dev];
   if (ntiles < pairs) pairs = ntiles;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
   e = cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, tm_sfa, tm_sfb, p);

@@ -8,6 +8,22 @@ namespace fp8q {
 
 enum Recipe : int { kTensor = 0, kBlock1x128 = 1, kBlock128x128 = 2, kMx = 3 };
 
+constexpr int kMaxDevices = 64;
+
+// Raise a kernel's dynamic shared-memory limit once per device (the setting is
+// per function and device); `done` is the caller's per-kernel flag array.
+template <typename Kernel>
+inline cudaError_t ensure_smem_limit(Kernel* fn, int bytes, bool (&done)[kMaxDevices]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
+}
+
 // ---- amax / scale / history (amax.cu)
 cudaError_t launch_amax(const void* x, int64_t n, float* amax, int num_sms, cudaStream_t s);
 cudaError_t launch_compute_scale(const float* amax, bool e5m2, float* scale, float* scale_inv, cudaStream_t s);

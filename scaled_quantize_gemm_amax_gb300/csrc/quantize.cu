@@ -377,13 +377,9 @@ __global__ void __launch_bounds__(256) k_cast_generic(const uint16_t* __restrict
 template <int RECIPE>
 cudaError_t launch_tiled(const CastParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_qrow,
                          const CUtensorMap& tm_qcol, int num_sms, cudaStream_t s) {
-  static bool attr_set = false;   // per process; the attribute is per function, not per device
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_cast_transpose<RECIPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static bool attr_done[kMaxDevices] = {};
+  cudaError_t e = ensure_smem_limit(k_cast_transpose<RECIPE>, static_cast<int>(kSmemBytes), attr_done);
+  if (e != cudaSuccess) return e;
   const int ntiles = p.tiles_r * p.tiles_c;
   const int grid = ntiles < num_sms ? ntiles : num_sms;
   k_cast_transpose<RECIPE><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_qrow, tm_qcol, p);
