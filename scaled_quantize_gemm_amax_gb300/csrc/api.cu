@@ -252,20 +252,6 @@ fp8_status fp8_scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const
   if (fp8_status st = device_info(&d)) return st;
   if (K == 0) return cuda_status(cudaMemsetAsync(C, 0, static_cast<size_t>(M * N * outsz), stream));
 
-  CUtensorMap tm_a, tm_b;
-  if (!make_map(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128)) return FP8_ERR_CUDA;
-  if (!make_map(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, static_cast<uint32_t>(gemm_b_box_rows(kind, M))))
-    return FP8_ERR_CUDA;
-  // MX: the tiled scale buffers as rows of 256 bytes, two rows (one 512-byte atom) per box
-  CUtensorMap tm_sfa, tm_sfb;
-  std::memset(&tm_sfa, 0, sizeof(tm_sfa));
-  std::memset(&tm_sfb, 0, sizeof(tm_sfb));
-  if (kind == kMx) {
-    const uint64_t atoms_a = static_cast<uint64_t>(M / 128) * (K / 128), atoms_b = static_cast<uint64_t>(N / 128) * (K / 128);
-    if (!make_map(&tm_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sA, 256, 2 * atoms_a, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&tm_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sB, 256, 2 * atoms_b, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
-      return FP8_ERR_CUDA;
-  }
   GemmParams p{};
   p.M = M;
   p.N = N;
@@ -279,6 +265,20 @@ fp8_status fp8_scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const
   p.sb = sB;
   p.c = C;
   p.err = d->err;
+  CUtensorMap tm_a, tm_b;
+  if (!make_map(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128)) return FP8_ERR_CUDA;
+  if (!make_map(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, static_cast<uint32_t>(gemm_b_box_rows(p))))
+    return FP8_ERR_CUDA;
+  // MX: the tiled scale buffers as rows of 256 bytes, two rows (one 512-byte atom) per box
+  CUtensorMap tm_sfa, tm_sfb;
+  std::memset(&tm_sfa, 0, sizeof(tm_sfa));
+  std::memset(&tm_sfb, 0, sizeof(tm_sfb));
+  if (kind == kMx) {
+    const uint64_t atoms_a = static_cast<uint64_t>(M / 128) * (K / 128), atoms_b = static_cast<uint64_t>(N / 128) * (K / 128);
+    if (!make_map(&tm_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sA, 256, 2 * atoms_a, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tm_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sB, 256, 2 * atoms_b, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return FP8_ERR_CUDA;
+  }
   return cuda_status(launch_gemm(p, tm_a, tm_b, tm_sfa, tm_sfb, d->num_sms, stream));
 }
 

@@ -66,9 +66,10 @@ struct Cfg<kMx> {
   static constexpr int BN = 256, STAGES = 4, ACC = 1, EPI = 8, KSUB = 1;
 };
 
-// Stages of the 2-CTA (pair) variant: each CTA holds 128 rows of A and half of B.
+// Stages of the 2-CTA (pair) variant: each CTA holds 128 rows of A and half of B
+// (blockwise with 256-deep stages: 48 KB a stage).
 template <int KIND>
-constexpr int pair_stages() { return Cfg<KIND>::BN == 256 ? 6 : 8; }
+constexpr int pair_stages() { return Cfg<KIND>::KSUB == 2 ? 4 : (Cfg<KIND>::BN == 256 ? 6 : 8); }
 
 template <int KIND, bool PAIR>
 struct Layout {
@@ -168,10 +169,11 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   constexpr bool BLOCK = (KIND == kBlock1x128 || KIND == kBlockRowsB || KIND == kBlockK2);   // promotion path
   constexpr int KSUB = L::KSUB;
   constexpr int GROUPS = ACC / KSUB;   // partial-buffer groups (blockwise)
-  static_assert(KSUB == 1 || (BLOCK && !PAIR), "multi-block stages: blockwise, single CTA");
-  // Blockwise, single CTA: a stage's full barrier also counts the epilogue's release of
-  // the partial group that stage will write, so the MMA thread waits once per stage.
-  constexpr bool GATED = BLOCK && !PAIR;
+  static_assert(KSUB == 1 || BLOCK, "multi-block stages: blockwise only");
+  // Blockwise: a stage's full barrier also counts the epilogue's release of the partial
+  // group that stage will write (in a pair, both CTAs' epilogues release on the
+  // leader's barrier), so the MMA thread waits once per stage.
+  constexpr bool GATED = BLOCK;
   constexpr bool B_ROWS = (KIND == kBlockRowsB);                         // B scales per row
   constexpr int COLS = BN / (EPI / 4);   // columns of the tile each epilogue thread owns
   extern __shared__ uint8_t smem_raw[];
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     prefetch_tmap(&tm_a);
     prefetch_tmap(&tm_b);
     for (int s = 0; s < S; ++s) {
-      mbar_init(base + L::OFF_FULL + 8 * s, GATED ? 1 + EPI : 1);
+      mbar_init(base + L::OFF_FULL + 8 * s, GATED ? 1 + (PAIR ? 2 : 1) * EPI : 1);
       mbar_init(base + L::OFF_EMPTY + 8 * s, 1);
     }
     for (int a = 0; a < 4; ++a) {
@@ -241,8 +243,12 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         const uint32_t sa = base + stage * L::STAGE_BYTES;
         if (PAIR) {
           if (leader) mbar_arrive_expect_tx(full, L::TX_BYTES);
-          tma_load_2d_pair(sa, &tm_a, kb * kBK, tm * TM + static_cast<int>(row_off), full_sig);
-          tma_load_2d_pair(sa + L::A_BYTES, &tm_b, kb * kBK, tn * BN + static_cast<int>(rank) * (BN / 2), full_sig);
+#pragma unroll
+          for (int sub = 0; sub < KSUB; ++sub) {
+            tma_load_2d_pair(sa + sub * L::A_SUB, &tm_a, (kb + sub) * kBK, tm * TM + static_cast<int>(row_off), full_sig);
+            tma_load_2d_pair(sa + L::A_BYTES + sub * L::B_SUB, &tm_b, (kb + sub) * kBK,
+                             tn * BN + static_cast<int>(rank) * (BN / 2), full_sig);
+          }
         } else {
           mbar_arrive_expect_tx(full, L::TX_BYTES);
 #pragma unroll
@@ -423,7 +429,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     if (KIND == kTensor) tensor_scale = __fmul_rn(*static_cast<const float*>(p.sa), *static_cast<const float*>(p.sb));
     // release of an accumulator / partial buffer: on the leader's barrier (remote for the peer)
     auto release = [&](uint32_t bar) {
-      if (PAIR) mbar_arrive_cluster(mapa_shared(bar, 0));
+      if (PAIR && !leader) mbar_arrive_remote(mapa_shared(bar, 0));
       else mbar_arrive(bar);
     };
     uint32_t acc_it = 0, part_it = 0;
@@ -432,7 +438,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     const uint32_t my_tiles = unit0 < ntiles ? static_cast<uint32_t>((ntiles - unit0 + units - 1) / units) : 0u;
     const uint32_t total_groups = my_tiles * static_cast<uint32_t>(NG);
     if (GATED && lane == 0) {
-      for (uint32_t g = 0; g < static_cast<uint32_t>(GROUPS) && g < total_groups; ++g) mbar_arrive(base + L::OFF_FULL + 8 * (g % S));
+      for (uint32_t g = 0; g < static_cast<uint32_t>(GROUPS) && g < total_groups; ++g) release(base + L::OFF_FULL + 8 * (g % S));
     }
     for (int t = unit0; t < ntiles; t += units) {
       int tm, tn;
@@ -517,7 +523,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
                   if (GATED) {
                     // the stage that reuses this group is GROUPS stages later
                     const uint32_t next = group_seq + GROUPS;
-                    if (next < total_groups) mbar_arrive(base + L::OFF_FULL + 8 * (next % S));
+                    if (next < total_groups) release(base + L::OFF_FULL + 8 * (next % S));
                   } else {
                     release(base + L::OFF_TEMPTY + 8 * pb);   // the group's partials fully read
                   }
@@ -644,26 +650,33 @@ int gemm_block_n(int kind) {
   return kind == kBlock1x128 ? Cfg<kBlock1x128>::BN : (kind == kMx ? Cfg<kMx>::BN : Cfg<kTensor>::BN);
 }
 
-// The per-tensor GEMM runs on CTA pairs.  The blockwise GEMM stays on single CTAs:
-// its promotion hands every 128-deep partial from the MMA to the epilogue and
-// back, and across two SMs that round trip (about a microsecond, measured) costs
-// far more than the halved operand traffic saves.
-bool gemm_uses_pair(int kind, int64_t M) { return (kind == kTensor || kind == kMx) && M % (2 * kBM) == 0; }
+// CTA pairs need M a multiple of 256.  Blockwise runs on pairs only with 256-deep
+// stages (K / 128 even) and 128x128 B scales: there each stage's two partials go to
+// the promotion as one group, so the cross-SM release is paid once per 8 MMAs.  The
+// release is a CTA-scope arrive on the leader's barrier: with cluster-scope release
+// semantics each arrive also waited for the epilogue's earlier global stores, which
+// made the blockwise pair 40 % slower (measured).
+bool gemm_uses_pair(const GemmParams& p) {
+  if (p.M % (2 * kBM) != 0) return false;
+  if (p.kind == kBlock1x128) return !p.b_1x128 && (p.K / kBK) % 2 == 0;
+  return true;
+}
 
-int gemm_b_box_rows(int kind, int64_t M) { return gemm_uses_pair(kind, M) ? gemm_block_n(kind) / 2 : gemm_block_n(kind); }
+int gemm_b_box_rows(const GemmParams& p) { return gemm_uses_pair(p) ? gemm_block_n(p.kind) / 2 : gemm_block_n(p.kind); }
 
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
                         const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s) {
   switch (p.kind) {
     case kTensor:
-      return gemm_uses_pair(kTensor, p.M) ? launch_pair<kTensor>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
+      return gemm_uses_pair(p) ? launch_pair<kTensor>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
                                           : launch_kind<kTensor>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
     case kBlock1x128:
       if (p.b_1x128) return launch_kind<kBlockRowsB>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
+      if (gemm_uses_pair(p)) return launch_pair<kBlockK2>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
       return (p.K / kBK) % 2 == 0 ? launch_kind<kBlockK2>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
                                   : launch_kind<kBlock1x128>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
     default:
-      return gemm_uses_pair(kMx, p.M) ? launch_pair<kMx>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
+      return gemm_uses_pair(p) ? launch_pair<kMx>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
                                       : launch_kind<kMx>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
   }
 }

@@ -66,10 +66,10 @@ struct GemmParams {
 };
 // Width (N) of one output tile of the GEMM variant.
 int gemm_block_n(int kind);
-// Whether the GEMM runs on 2-CTA pairs (256-row tiles) for this M.
-bool gemm_uses_pair(int kind, int64_t M);
+// Whether the GEMM runs on 2-CTA pairs (256-row tiles) for these parameters.
+bool gemm_uses_pair(const GemmParams& p);
 // Rows of B one TMA box carries (the tile width, or half of it for a pair).
-int gemm_b_box_rows(int kind, int64_t M);
+int gemm_b_box_rows(const GemmParams& p);
 // tm_sfa / tm_sfb: MX only (the tiled E8M0 buffers as [atoms * 2, 256] bytes, box 2 x 256).
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
                         const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s);

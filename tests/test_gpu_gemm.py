@@ -141,3 +141,12 @@ def test_gemm_cta_pair_tiles(ra, rb, m, n, k):
     w = wl.normal_bf16((n, k), 41, 0.02)
     gemm_check(x, w, ra, rb, F.E4M3, F.E5M2 if k == 384 else F.E4M3,
                out=fq.OutDtype.FP32 if m == 768 else fq.OutDtype.BF16)
+
+
+@pytest.mark.parametrize("m,n,k", [(2048, 1536, 512), (512, 256, 2048)])
+def test_gemm_blockwise_pairs_many_tiles(m, n, k):
+    # blockwise on CTA pairs (M % 256 == 0, K / 128 even): more 256x128 tiles than pairs
+    # (each pair walks several tiles), and a long K that wraps the stage ring many times
+    x = wl.normal_bf16((m, k), 50, 1.0)
+    w = wl.normal_bf16((n, k), 51, 0.02)
+    gemm_check(x, w, R.BLOCK_1x128, R.BLOCK_128x128, F.E4M3, F.E4M3)
