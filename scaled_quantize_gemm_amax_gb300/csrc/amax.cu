@@ -33,6 +33,8 @@ __device__ __forceinline__ uint32_t fold16(uint32_t m, uint4 v) {
 __global__ void __launch_bounds__(kAmaxThreads) k_amax(const uint4* __restrict__ x16, int64_t n16,
                                                       const uint16_t* __restrict__ tail, int ntail,
                                                       float* __restrict__ amax) {
+  pdl_wait();
+  pdl_launch_dependents();
   uint32_t m = 0;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -62,6 +64,8 @@ __global__ void __launch_bounds__(kAmaxThreads) k_amax(const uint4* __restrict__
 
 __global__ void k_compute_scale(const float* __restrict__ amax, int e5m2, float* __restrict__ scale,
                                 float* __restrict__ scale_inv) {
+  pdl_wait();
+  pdl_launch_dependents();
   if (threadIdx.x != 0) return;
   const float s = scale_from_amax(*amax, fmax_of(e5m2 != 0));
   *scale = s;
@@ -74,6 +78,8 @@ __global__ void k_compute_scale(const float* __restrict__ amax, int e5m2, float*
 __global__ void k_history_update(float* __restrict__ hist, int32_t len, int32_t* __restrict__ pos,
                                  const float* __restrict__ amax, int e5m2, float* __restrict__ scale,
                                  float* __restrict__ scale_inv, uint32_t* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   if (threadIdx.x != 0) return;
   const int32_t p = *pos;
   if (p < 0 || p >= len) {
@@ -117,20 +123,18 @@ cudaError_t launch_amax(const void* x, int64_t n, float* amax, int num_sms, cuda
   int64_t want = (n16 + static_cast<int64_t>(kAmaxThreads) * kAmaxUnroll - 1) / (kAmaxThreads * kAmaxUnroll);
   int64_t cap = static_cast<int64_t>(num_sms) * 4;
   int grid = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
-  k_amax<<<grid, kAmaxThreads, 0, s>>>(static_cast<const uint4*>(x), n16,
-                                       static_cast<const uint16_t*>(x) + n16 * 8, ntail, amax);
-  return cudaGetLastError();
+  return launch_pdl(k_amax, dim3(grid), dim3(kAmaxThreads), 0, s, 1, static_cast<const uint4*>(x), n16,
+                    static_cast<const uint16_t*>(x) + n16 * 8, ntail, amax);
 }
 
 cudaError_t launch_compute_scale(const float* amax, bool e5m2, float* scale, float* scale_inv, cudaStream_t s) {
-  k_compute_scale<<<1, 32, 0, s>>>(amax, e5m2 ? 1 : 0, scale, scale_inv);
-  return cudaGetLastError();
+  return launch_pdl(k_compute_scale, dim3(1), dim3(32), 0, s, 1, amax, e5m2 ? 1 : 0, scale, scale_inv);
 }
 
 cudaError_t launch_history_update(float* hist, int32_t len, int32_t* pos, const float* amax, bool e5m2, float* scale,
                                   float* scale_inv, uint32_t* err, cudaStream_t s) {
-  k_history_update<<<1, 32, 0, s>>>(hist, len, pos, amax, e5m2 ? 1 : 0, scale, scale_inv, err);
-  return cudaGetLastError();
+  return launch_pdl(k_history_update, dim3(1), dim3(32), 0, s, 1, hist, len, pos, amax, e5m2 ? 1 : 0, scale, scale_inv,
+                    err);
 }
 
 cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t s) {

@@ -221,10 +221,12 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   __syncthreads();
   if (PAIR) cluster_sync();   // the peer's barriers are initialised before anyone signals them
   tc_fence_after();
+  pdl_launch_dependents();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base_ptr + L::OFF_TMEM);
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------ producer
+    pdl_wait();   // operands may come from the previous kernel in the stream
     int n_issued = 0;   // loads issued so far; stage s received n_issued / S (+1 if s < n_issued % S)
     int stage = 0;
     uint32_t phase = 0;
@@ -420,6 +422,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     mbar_wait(base + L::OFF_FINAL, 0, p.err, kErrTimeoutMma, nullptr);
   } else if (warp >= 2) {
     // ------------------------------------------------ epilogue
+    pdl_wait();   // scales and C: ordered after the previous kernel in the stream
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
     const int h = (warp - 2) >> 2;          // which COLS-wide slice of the tile's columns
     const int row = 32 * q + lane;          // row within the tile
@@ -448,11 +451,11 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
       if (BLOCK) {
         const float* sa_row = static_cast<const float*>(p.sa) + grow * KB;
         const float* sb_blk = static_cast<const float*>(p.sb);
-        // Promotion: TMEM loads of CW columns (32, or 16 when a thread owns 128 columns, to
-        // fit the registers), software-pipelined: while the FMAs of one chunk run, the
+        // Promotion: TMEM loads of CW columns (32, or 16 when a thread owns 128 columns or
+        // loads a B scale per column, to fit the registers), software-pipelined: while the FMAs of one chunk run, the
         // load of the next chunk (of this partial, or the first of the next partial) is in
         // flight.  A partial buffer is released once all its chunks are in registers.
-        constexpr int CW = (COLS >= 128) ? 16 : 32;
+        constexpr int CW = (COLS >= 128 || B_ROWS) ? 16 : 32;
         constexpr int NC = COLS / CW;
         static_assert(!BLOCK || (NC % 2 == 0 && COLS % 32 == 0), "blockwise promotion chunking");
         const float* sb_tile = sb_blk + (gcol0 / 128) * KB;   // 128x128 B: one factor per k-block
@@ -598,8 +601,7 @@ cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& tm_a, const CUte
   if (e != cudaSuccess) return e;
   const int64_t ntiles = (p.M / kBM) * ((p.N + L::BN - 1) / L::BN);
   const int grid = static_cast<int>(ntiles < num_sms ? ntiles : num_sms);
-  k_gemm<KIND, false><<<grid, threads_of<KIND>(), L::SMEM, s>>>(tm_a, tm_b, tm_sfa, tm_sfb, p);
-  return cudaGetLastError();
+  return launch_pdl(k_gemm<KIND, false>, dim3(grid), dim3(threads_of<KIND>()), L::SMEM, s, 1, tm_a, tm_b, tm_sfa, tm_sfb, p);
 }
 
 // 2-CTA clusters; the grid is as many pairs as can be resident at once (at most
@@ -639,9 +641,7 @@ cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUte
   if (max_clusters[dev] < pairs) pairs = max_clusters[dev];
   if (ntiles < pairs) pairs = ntiles;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-  e = cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, tm_sfa, tm_sfb, p);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return launch_pdl(kern, cfg.gridDim, cfg.blockDim, L::SMEM, s, 2, tm_a, tm_b, tm_sfa, tm_sfb, p);
 }
 
 }  // namespace

@@ -24,6 +24,37 @@ inline cudaError_t ensure_smem_limit(Kernel* fn, int bytes, bool (&done)[kMaxDev
   return e;
 }
 
+// Launch with programmatic stream serialization: the kernel may be scheduled while the
+// kernel before it in the stream drains.  Every kernel of this library executes
+// griddepcontrol.wait (pdl_wait) before its first global-memory access, which returns
+// once the preceding kernel has completed and its writes are visible, so stream order
+// holds for all data; only launch latency and set-up (barriers, TMEM, tensor-map
+// prefetch) overlap.  cluster_x > 1 adds a cluster dimension.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster_x,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ---- amax / scale / history (amax.cu)
 cudaError_t launch_amax(const void* x, int64_t n, float* amax, int num_sms, cudaStream_t s);
 cudaError_t launch_compute_scale(const float* amax, bool e5m2, float* scale, float* scale_inv, cudaStream_t s);

@@ -215,6 +215,14 @@ __device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
 }
 
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Wait until the kernel before this one in the stream has completed and its memory
+// writes are visible (returns at once when there is none to wait for).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel in the stream be scheduled (it still waits in pdl_wait for
+// this one to complete).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // ------------------------------------------------------------------ CTA pairs (2-CTA clusters)
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

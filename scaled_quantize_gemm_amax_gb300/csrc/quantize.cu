@@ -156,6 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();   // from here on: global memory
+  pdl_launch_dependents();
 
   float g_scale = 1.0f;
   if (RECIPE == kTensor) {
@@ -339,6 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // bytes through a transposed shared tile.
 __global__ void __launch_bounds__(256) k_cast_generic(const uint16_t* __restrict__ x, CastParams p) {
   __shared__ float tile[32][33];
+  pdl_wait();
+  pdl_launch_dependents();
   const bool e5 = p.e5m2 != 0;
   const float s = *p.scale;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32, c0 = static_cast<int64_t>(blockIdx.x) * 32;
@@ -382,8 +386,7 @@ cudaError_t launch_tiled(const CastParams& p, const CUtensorMap& tm_x, const CUt
   if (e != cudaSuccess) return e;
   const int ntiles = p.tiles_r * p.tiles_c;
   const int grid = ntiles < num_sms ? ntiles : num_sms;
-  k_cast_transpose<RECIPE><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_qrow, tm_qcol, p);
-  return cudaGetLastError();
+  return launch_pdl(k_cast_transpose<RECIPE>, dim3(grid), dim3(kThreads), kSmemBytes, s, 1, tm_x, tm_qrow, tm_qcol, p);
 }
 
 }  // namespace
@@ -400,8 +403,7 @@ cudaError_t launch_cast_transpose_tiled(const CastParams& p, const CUtensorMap& 
 
 cudaError_t launch_cast_generic(const CastParams& p, const void* x, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>((p.C + 31) / 32), static_cast<unsigned>((p.R + 31) / 32));
-  k_cast_generic<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), p);
-  return cudaGetLastError();
+  return launch_pdl(k_cast_generic, grid, dim3(256), 0, s, 1, static_cast<const uint16_t*>(x), p);
 }
 
 }  // namespace fp8q
