@@ -492,7 +492,8 @@ def run_reference(args, rank, world):
             "wall_s": round(wall, 2)}
 
 
-CASES = ("cast_tensor", "cast_1x128", "cast_128x128", "cast_mx", "amax", "gemm_tensor", "gemm_block", "gemm_mx")
+CASES = ("cast_tensor", "cast_1x128", "cast_128x128", "cast_mx", "amax", "gemm_tensor", "gemm_block", "gemm_mx",
+         "gemm_amax")
 
 
 def run_case(args):
@@ -525,6 +526,31 @@ def run_case(args):
         ms = _time_kernel(fn, reps=args.steps, flush=flush)
         res = {"case": args.case, "size": s, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
         res["frac_hbm"] = round(res["GB/s"] / pk["hbm_gbs"], 4)
+    elif args.case == "gemm_amax":
+        # per-tensor GEMM whose epilogue writes C's FP8 copy (delayed scale) and amax, against
+        # the unfused chain: GEMM to bf16, then amax and the per-tensor cast of C
+        a = wl.normal_bf16((s, s), 1, 1.0, dev)
+        b = wl.normal_bf16((s, s), 2, 0.02, dev)
+        sc1 = torch.ones(1, dtype=torch.float32, device=dev)
+        qa, sa, _, _ = fq.cast_transpose(a, R.TENSOR, F.E4M3, sc1, col=False)
+        qb, sb, _, _ = fq.cast_transpose(b, R.TENSOR, F.E4M3, sc1, col=False)
+        c = torch.empty((s, s), dtype=torch.bfloat16, device=dev)
+        c_q = torch.empty((s, s), dtype=torch.uint8, device=dev)
+        c_amax = torch.empty(1, dtype=torch.float32, device=dev)
+        c_sinv = torch.empty(1, dtype=torch.float32, device=dev)
+        c_scale = torch.full((1,), 64.0, dtype=torch.float32, device=dev)
+        fused = lambda: fq.fp8_scaled_gemm_amax(qa, F.E4M3, R.TENSOR, sa, qb, F.E4M3, R.TENSOR, sb, None,
+                                                fq.OutDtype.BF16, c_amax, c_scale, F.E4M3, c_q, c_sinv)
+
+        def unfused():
+            fq.fp8_scaled_gemm(qa, F.E4M3, R.TENSOR, sa, qb, F.E4M3, R.TENSOR, sb, c)
+            fq.fp8_quantize(c, R.TENSOR, F.E4M3, c_scale, c_amax, c_q, c_sinv)
+
+        ms = _time_kernel(fused, reps=args.steps, flush=flush)
+        ms_u = _time_kernel(unfused, reps=args.steps, flush=flush)
+        tf = 2.0 * s ** 3 / (ms * 1e-3) / 1e12
+        res = {"case": args.case, "size": s, "us": round(ms * 1e3, 2), "TFLOP/s": round(tf, 1),
+               "frac_fp8": round(tf / (2 * pk["bf16_tflops"]), 4), "unfused_us": round(ms_u * 1e3, 2)}
     else:
         ra = {"gemm_tensor": R.TENSOR, "gemm_block": R.BLOCK_1x128, "gemm_mx": R.MX_1x32_TILED}[args.case]
         rb = {"gemm_tensor": R.TENSOR, "gemm_block": R.BLOCK_128x128, "gemm_mx": R.MX_1x32_TILED}[args.case]

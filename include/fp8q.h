@@ -177,6 +177,31 @@ fp8_status fp8_scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const
                            fp8_out_dtype out, cudaStream_t stream);
 
 /*
+ * fp8_scaled_gemm_amax -- fp8_scaled_gemm with the next layer's per-tensor
+ * quantization fused into its epilogue.  Colossal-AI FP8 article, "delayed
+ * scaling": the scale comes from a window of past maxima and its update is
+ * fused with the GEMM; guide, "delayed scaling scheme".  With y the value the
+ * plain GEMM stores in C (rounded to bf16 for FP8_OUT_BF16, the FP32 value
+ * for FP8_OUT_FP32):
+ *   C           device, nullable: as fp8_scaled_gemm
+ *   c_amax      device float[1], nullable: overwritten with max |y| (NaN
+ *               ignored) -- the value the scale history records
+ *   c_scale     device float[1]: the per-tensor scale of C's FP8 copy (a
+ *               delayed-scaling state's scale); required with C_q
+ *   fc, C_q     device [M, N] u8 row-major, nullable: encode_sat(y * c_scale),
+ *               round-to-nearest-even, the bytes fp8_quantize(TENSOR) writes
+ *               for C with that scale
+ *   c_scale_inv device float[1], nullable (only with C_q): 1 / c_scale
+ * At least one of c_amax and C_q (FP8_ERR_INVALID_ARG); C and C_q 16-byte
+ * aligned.  Shapes, pairings and errors as fp8_scaled_gemm; M, N or K == 0
+ * give amax 0 and all-zero codes.
+ */
+fp8_status fp8_scaled_gemm_amax(const uint8_t* A, fp8_format fa, fp8_recipe ra, const void* sA, const uint8_t* B,
+                                fp8_format fb, fp8_recipe rb, const void* sB, int64_t M, int64_t N, int64_t K, void* C,
+                                fp8_out_dtype out, float* c_amax, const float* c_scale, fp8_format fc, uint8_t* C_q,
+                                float* c_scale_inv, cudaStream_t stream);
+
+/*
  * fp8_get_device_status -- synchronize `stream`, then read and clear the
  * device error word of the current device.  Returns FP8_OK, FP8_ERR_TIMEOUT
  * (some kernel gave up a wait), FP8_ERR_DEVICE_STATE, or FP8_ERR_CUDA.

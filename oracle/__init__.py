@@ -76,6 +76,7 @@ def _load():
             "orc_decode_array": (None, [P, I64, ctypes.c_int, P]),
             "orc_encode_array": (None, [P, I64, ctypes.c_int, ctypes.c_int, P]),
             "orc_amax_bf16": (F, [P, I64]),
+            "orc_amax_f32": (F, [P, I64]),
             "orc_tensor_scale": (None, [F, ctypes.c_int, P, P]),
             "orc_history_step": (None, [P, I32, P, F, ctypes.c_int, P, P]),
             "orc_mx_exponent": (ctypes.c_int, [F, ctypes.c_int]),
@@ -132,6 +133,12 @@ def encode(values, fmt: int, saturate: bool) -> np.ndarray:
 def amax(x_bf16) -> np.float32:
     x = _bf16_bits(x_bf16)
     return np.float32(_load().orc_amax_bf16(_ptr(x), x.size))
+
+
+def amax_f32(values) -> np.float32:
+    """max |v| over float32 values, NaN ignored (fp8_oracle.c: orc_amax_f32)."""
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    return np.float32(_load().orc_amax_f32(_ptr(v), v.size))
 
 
 def tensor_scale(amax_value, fmt: int):

@@ -155,6 +155,21 @@ float orc_amax_bf16(const uint16_t* x, int64_t n)
 }
 
 /*
+ * The same maximum over binary32 values: the amax of a GEMM output that the
+ * delayed-scaling history records when the output stays in FP32 (Colossal-AI
+ * FP8 article, "delayed scaling").
+ */
+float orc_amax_f32(const float* x, int64_t n)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    return amax;
+}
+
+/*
  * Per-tensor (and per-tile) scale rule: scale = FMAX / amax, one binary32
  * division; scale_inv = 1 / scale.  Readings (pages silent): amax == 0 or
  * non-finite gives scale 1; a quotient that overflows to inf becomes FLT_MAX;

@@ -83,6 +83,7 @@ _SIGNATURES = {
     "fp8_cast_transpose": [_P, _I64, _I64, _E, _E, _P, _P, _P, _P, _P, _P, _P],
     "fp8_quantize": [_P, _I64, _I64, _E, _E, _P, _P, _P, _P, _P],
     "fp8_scaled_gemm": [_P, _E, _E, _P, _P, _E, _E, _P, _I64, _I64, _I64, _P, _E, _P],
+    "fp8_scaled_gemm_amax": [_P, _E, _E, _P, _P, _E, _E, _P, _I64, _I64, _I64, _P, _E, _P, _P, _E, _P, _P, _P],
     "fp8_get_device_status": [_P],
     "fp8_debug_wait_timeout": [_P],
     "fp8_status_string": [_E],
@@ -173,6 +174,15 @@ def fp8_scaled_gemm(a, fa, ra, sa, b, fb, rb, sb, c, out=OutDtype.BF16, stream=N
                                           M, N, K, _ptr(c), int(out), _stream(stream)))
 
 
+def fp8_scaled_gemm_amax(a, fa, ra, sa, b, fb, rb, sb, c, out, c_amax, c_scale, fc, c_q, c_scale_inv, stream=None):
+    M, K = a.shape
+    N = b.shape[0]
+    _check("fp8_scaled_gemm_amax",
+           load_library().fp8_scaled_gemm_amax(_ptr(a), int(fa), int(ra), _ptr(sa), _ptr(b), int(fb), int(rb),
+                                               _ptr(sb), M, N, K, _ptr(c), int(out), _ptr(c_amax), _ptr(c_scale),
+                                               int(fc), _ptr(c_q), _ptr(c_scale_inv), _stream(stream)))
+
+
 def fp8_get_device_status(stream=None) -> Status:
     return Status(load_library().fp8_get_device_status(_stream(stream)))
 
@@ -222,6 +232,24 @@ def scaled_gemm(a, fa, ra, sa, b, fb, rb, sb, out=OutDtype.BF16, stream=None):
     c = torch.empty((M, N), dtype=torch.float32 if out == OutDtype.FP32 else torch.bfloat16, device=a.device)
     fp8_scaled_gemm(a, fa, ra, sa, b, fb, rb, sb, c, out, stream)
     return c
+
+
+def scaled_gemm_amax(a, fa, ra, sa, b, fb, rb, sb, c_scale, fc=Format.E4M3, out=OutDtype.BF16, keep_c=True,
+                     stream=None):
+    """Allocate outputs and run fp8_scaled_gemm_amax.
+
+    Returns (c or None, c_amax, c_q, c_scale_inv): C's FP8 copy with the given
+    per-tensor scale (e.g. a DelayedScaling state's) and the amax of C."""
+    M, N = a.shape[0], b.shape[0]
+    dev = a.device
+    c = None
+    if keep_c:
+        c = torch.empty((M, N), dtype=torch.float32 if out == OutDtype.FP32 else torch.bfloat16, device=dev)
+    c_amax = torch.empty(1, dtype=torch.float32, device=dev)
+    c_q = torch.empty((M, N), dtype=torch.uint8, device=dev)
+    c_scale_inv = torch.empty(1, dtype=torch.float32, device=dev)
+    fp8_scaled_gemm_amax(a, fa, ra, sa, b, fb, rb, sb, c, out, c_amax, c_scale, fc, c_q, c_scale_inv, stream)
+    return c, c_amax, c_q, c_scale_inv
 
 
 class DelayedScaling:

@@ -101,6 +101,12 @@ __global__ void k_history_update(float* __restrict__ hist, int32_t len, int32_t*
   }
 }
 
+__global__ void k_reciprocal(const float* __restrict__ in, float* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) *out = recip_rn(*in);
+}
+
 // One CTA waits for an mbarrier phase that never completes; the bounded wait
 // must give up, report kErrTimeoutTmaLoad and let the kernel return.
 __global__ void k_wait_selftest(uint32_t* err) {
@@ -135,6 +141,10 @@ cudaError_t launch_history_update(float* hist, int32_t len, int32_t* pos, const 
                                   float* scale_inv, uint32_t* err, cudaStream_t s) {
   return launch_pdl(k_history_update, dim3(1), dim3(32), 0, s, 1, hist, len, pos, amax, e5m2 ? 1 : 0, scale, scale_inv,
                     err);
+}
+
+cudaError_t launch_reciprocal(const float* in, float* out, cudaStream_t s) {
+  return launch_pdl(k_reciprocal, dim3(1), dim3(32), 0, s, 1, in, out);
 }
 
 cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t s) {

@@ -81,6 +81,109 @@ fp8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8_OK : FP8_E
 
 using namespace fp8q;
 
+namespace {
+
+// Optional outputs of the fused epilogue (all null for the plain GEMM).
+struct GemmExtra {
+  float* c_amax = nullptr;
+  const float* c_scale = nullptr;
+  fp8_format fc = FP8_E4M3;
+  uint8_t* cq = nullptr;
+  float* c_scale_inv = nullptr;
+};
+
+fp8_status scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const void* sA, const uint8_t* B, fp8_format fb,
+                       fp8_recipe rb, const void* sB, int64_t M, int64_t N, int64_t K, void* C, fp8_out_dtype out,
+                       const GemmExtra& x, cudaStream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || !valid_fmt(fa) || !valid_fmt(fb) || (out != FP8_OUT_BF16 && out != FP8_OUT_FP32))
+    return FP8_ERR_INVALID_ARG;
+  int kind;
+  int b_1x128 = 0;
+  if (ra == FP8_TENSOR && rb == FP8_TENSOR) {
+    kind = kTensor;
+  } else if (ra == FP8_BLOCK_1x128 && rb == FP8_BLOCK_128x128) {
+    kind = kBlock1x128;
+  } else if (ra == FP8_BLOCK_1x128 && rb == FP8_BLOCK_1x128) {
+    kind = kBlock1x128;
+    b_1x128 = 1;
+  } else if (ra == FP8_MX_1x32_TILED && rb == FP8_MX_1x32_TILED) {
+    kind = kMx;
+  } else if ((ra >= FP8_TENSOR && ra <= FP8_MX_1x32_TILED) && (rb >= FP8_TENSOR && rb <= FP8_MX_1x32_TILED)) {
+    return FP8_ERR_UNSUPPORTED;
+  } else {
+    return FP8_ERR_INVALID_ARG;
+  }
+  const bool fused = x.c_amax != nullptr || x.cq != nullptr;
+  const int64_t outsz = out == FP8_OUT_FP32 ? 4 : 2;
+  if (fused) {
+    if (!valid_fmt(x.fc)) return FP8_ERR_INVALID_ARG;
+    if (x.cq != nullptr && x.c_scale == nullptr) return FP8_ERR_INVALID_ARG;
+    if (x.c_scale_inv != nullptr && x.cq == nullptr) return FP8_ERR_INVALID_ARG;
+  } else if (C == nullptr && M > 0 && N > 0) {
+    return FP8_ERR_INVALID_ARG;
+  }
+  if (M % 128 || N % 128 || K % 128) return FP8_ERR_SHAPE;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8_ERR_SHAPE;
+  if ((C != nullptr && !aligned(C, 16)) || (x.cq != nullptr && !aligned(x.cq, 16))) return FP8_ERR_ALIGNMENT;
+  if (x.c_amax != nullptr && !aligned(x.c_amax, 4)) return FP8_ERR_ALIGNMENT;
+  if (K > 0 && M > 0 && N > 0) {
+    if (A == nullptr || B == nullptr || sA == nullptr || sB == nullptr) return FP8_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16)) return FP8_ERR_ALIGNMENT;
+    const uintptr_t sal = kind == kMx ? 16 : 4;
+    if (!aligned(sA, sal) || !aligned(sB, sal)) return FP8_ERR_ALIGNMENT;
+  }
+  if (!fused && (M == 0 || N == 0)) return FP8_OK;
+  DeviceInfo* d;
+  if (fp8_status st = device_info(&d)) return st;
+  if (x.c_amax != nullptr) {
+    if (cudaMemsetAsync(x.c_amax, 0, sizeof(float), stream) != cudaSuccess) return FP8_ERR_CUDA;
+  }
+  if (M == 0 || N == 0 || K == 0) {
+    // C = 0: amax 0 (set above), FP8 copy all +0 codes, scale_inv still written
+    const size_t mn = static_cast<size_t>(M * N);
+    if (C != nullptr && mn && cudaMemsetAsync(C, 0, mn * outsz, stream) != cudaSuccess) return FP8_ERR_CUDA;
+    if (x.cq != nullptr && mn && cudaMemsetAsync(x.cq, 0, mn, stream) != cudaSuccess) return FP8_ERR_CUDA;
+    if (x.c_scale_inv != nullptr) return cuda_status(launch_reciprocal(x.c_scale, x.c_scale_inv, stream));
+    return FP8_OK;
+  }
+
+  GemmParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.kind = kind;
+  p.b_1x128 = b_1x128;
+  p.e5m2_a = fa == FP8_E5M2;
+  p.e5m2_b = fb == FP8_E5M2;
+  p.out_fp32 = out == FP8_OUT_FP32;
+  p.sa = sA;
+  p.sb = sB;
+  p.c = C;
+  p.c_amax = x.c_amax;
+  p.c_scale = x.c_scale;
+  p.cq = x.cq;
+  p.c_scale_inv = x.c_scale_inv;
+  p.e5m2_c = x.fc == FP8_E5M2;
+  p.err = d->err;
+  CUtensorMap tm_a, tm_b;
+  if (!make_map(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128)) return FP8_ERR_CUDA;
+  if (!make_map(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, static_cast<uint32_t>(gemm_b_box_rows(p))))
+    return FP8_ERR_CUDA;
+  // MX: the tiled scale buffers as rows of 256 bytes, two rows (one 512-byte atom) per box
+  CUtensorMap tm_sfa, tm_sfb;
+  std::memset(&tm_sfa, 0, sizeof(tm_sfa));
+  std::memset(&tm_sfb, 0, sizeof(tm_sfb));
+  if (kind == kMx) {
+    const uint64_t atoms_a = static_cast<uint64_t>(M / 128) * (K / 128), atoms_b = static_cast<uint64_t>(N / 128) * (K / 128);
+    if (!make_map(&tm_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sA, 256, 2 * atoms_a, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tm_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sB, 256, 2 * atoms_b, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return FP8_ERR_CUDA;
+  }
+  return cuda_status(launch_gemm(p, tm_a, tm_b, tm_sfa, tm_sfb, d->num_sms, stream));
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* fp8_status_string(fp8_status s) {
@@ -218,68 +321,21 @@ fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, fp8_recipe re
 fp8_status fp8_scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const void* sA, const uint8_t* B,
                            fp8_format fb, fp8_recipe rb, const void* sB, int64_t M, int64_t N, int64_t K, void* C,
                            fp8_out_dtype out, cudaStream_t stream) {
-  if (M < 0 || N < 0 || K < 0 || !valid_fmt(fa) || !valid_fmt(fb) || (out != FP8_OUT_BF16 && out != FP8_OUT_FP32))
-    return FP8_ERR_INVALID_ARG;
-  int kind;
-  int b_1x128 = 0;
-  if (ra == FP8_TENSOR && rb == FP8_TENSOR) {
-    kind = kTensor;
-  } else if (ra == FP8_BLOCK_1x128 && rb == FP8_BLOCK_128x128) {
-    kind = kBlock1x128;
-  } else if (ra == FP8_BLOCK_1x128 && rb == FP8_BLOCK_1x128) {
-    kind = kBlock1x128;
-    b_1x128 = 1;
-  } else if (ra == FP8_MX_1x32_TILED && rb == FP8_MX_1x32_TILED) {
-    kind = kMx;
-  } else if ((ra >= FP8_TENSOR && ra <= FP8_MX_1x32_TILED) && (rb >= FP8_TENSOR && rb <= FP8_MX_1x32_TILED)) {
-    return FP8_ERR_UNSUPPORTED;
-  } else {
-    return FP8_ERR_INVALID_ARG;
-  }
-  const int64_t outsz = out == FP8_OUT_FP32 ? 4 : 2;
-  if (M == 0 || N == 0) return FP8_OK;
-  if (C == nullptr) return FP8_ERR_INVALID_ARG;
-  if (M % 128 || N % 128 || K % 128) return FP8_ERR_SHAPE;
-  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8_ERR_SHAPE;
-  if (!aligned(C, 16)) return FP8_ERR_ALIGNMENT;
-  if (K > 0) {
-    if (A == nullptr || B == nullptr || sA == nullptr || sB == nullptr) return FP8_ERR_INVALID_ARG;
-    if (!aligned(A, 16) || !aligned(B, 16)) return FP8_ERR_ALIGNMENT;
-    const uintptr_t sal = kind == kMx ? 16 : 4;
-    if (!aligned(sA, sal) || !aligned(sB, sal)) return FP8_ERR_ALIGNMENT;
-  }
-  DeviceInfo* d;
-  if (fp8_status st = device_info(&d)) return st;
-  if (K == 0) return cuda_status(cudaMemsetAsync(C, 0, static_cast<size_t>(M * N * outsz), stream));
+  return scaled_gemm(A, fa, ra, sA, B, fb, rb, sB, M, N, K, C, out, GemmExtra{}, stream);
+}
 
-  GemmParams p{};
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.kind = kind;
-  p.b_1x128 = b_1x128;
-  p.e5m2_a = fa == FP8_E5M2;
-  p.e5m2_b = fb == FP8_E5M2;
-  p.out_fp32 = out == FP8_OUT_FP32;
-  p.sa = sA;
-  p.sb = sB;
-  p.c = C;
-  p.err = d->err;
-  CUtensorMap tm_a, tm_b;
-  if (!make_map(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128)) return FP8_ERR_CUDA;
-  if (!make_map(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, static_cast<uint32_t>(gemm_b_box_rows(p))))
-    return FP8_ERR_CUDA;
-  // MX: the tiled scale buffers as rows of 256 bytes, two rows (one 512-byte atom) per box
-  CUtensorMap tm_sfa, tm_sfb;
-  std::memset(&tm_sfa, 0, sizeof(tm_sfa));
-  std::memset(&tm_sfb, 0, sizeof(tm_sfb));
-  if (kind == kMx) {
-    const uint64_t atoms_a = static_cast<uint64_t>(M / 128) * (K / 128), atoms_b = static_cast<uint64_t>(N / 128) * (K / 128);
-    if (!make_map(&tm_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sA, 256, 2 * atoms_a, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&tm_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sB, 256, 2 * atoms_b, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
-      return FP8_ERR_CUDA;
-  }
-  return cuda_status(launch_gemm(p, tm_a, tm_b, tm_sfa, tm_sfb, d->num_sms, stream));
+fp8_status fp8_scaled_gemm_amax(const uint8_t* A, fp8_format fa, fp8_recipe ra, const void* sA, const uint8_t* B,
+                                fp8_format fb, fp8_recipe rb, const void* sB, int64_t M, int64_t N, int64_t K, void* C,
+                                fp8_out_dtype out, float* c_amax, const float* c_scale, fp8_format fc, uint8_t* C_q,
+                                float* c_scale_inv, cudaStream_t stream) {
+  if (c_amax == nullptr && C_q == nullptr) return FP8_ERR_INVALID_ARG;
+  GemmExtra x;
+  x.c_amax = c_amax;
+  x.c_scale = c_scale;
+  x.fc = fc;
+  x.cq = C_q;
+  x.c_scale_inv = c_scale_inv;
+  return scaled_gemm(A, fa, ra, sA, B, fb, rb, sB, M, N, K, C, out, x, stream);
 }
 
 fp8_status fp8_get_device_status(cudaStream_t stream) {

@@ -160,7 +160,9 @@ constexpr int threads_of() { return 32 * (2 + Cfg<KIND>::EPI); }
 // signal the leader's (rank 0) stage barrier; the leader issues every MMA and
 // multicasts its commits to both CTAs; each CTA's TMEM holds its 128 rows of D,
 // and both CTAs' epilogues release an accumulator on the leader's barrier.
-template <int KIND, bool PAIR>
+// QOUT: the epilogue may also write C's FP8 copy and amax (a separate instantiation, so
+// the plain GEMM's epilogue carries none of it).
+template <int KIND, bool PAIR, bool QOUT>
 __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     k_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
            const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb, const GemmParams p) {
@@ -430,6 +432,37 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     const bool fp32 = p.out_fp32 != 0;
     float tensor_scale = 1.0f;
     if (KIND == kTensor) tensor_scale = __fmul_rn(*static_cast<const float*>(p.sa), *static_cast<const float*>(p.sb));
+    // Fused output quantization: the next layer's per-tensor cast of y (the value stored
+    // in C, bf16-rounded for bf16 output) with a scale known before the GEMM (delayed
+    // scaling), and the amax of y that feeds that scale's history.
+    const bool want_q = QOUT && p.cq != nullptr, want_amax = QOUT && p.c_amax != nullptr;
+    const float c_scale = want_q ? *p.c_scale : 1.0f;
+    const bool e5_c = p.e5m2_c != 0;
+    float y_amax = 0.0f;
+    if (want_q && p.c_scale_inv != nullptr && blockIdx.x == 0 && warp == 2 && lane == 0)
+      *p.c_scale_inv = recip_rn(c_scale);
+    // 32 consecutive output values of one row, starting at column gcol
+    auto emit = [&](const float (&v)[32], int64_t grow_, int64_t gcol) {
+      const int64_t off = grow_ * p.N + gcol;
+      if (p.c != nullptr) store_row32(p.c, off, v, fp32);
+      if (QOUT && (want_q || want_amax)) {
+        float y[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          y[j] = fp32 ? v[j] : __bfloat162float(__float2bfloat16_rn(v[j]));
+          y_amax = fmaxf(y_amax, fabsf(y[j]));   // NaN ignored
+        }
+        if (want_q) {
+          uint32_t w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            w[i] = cvt_pair(__fmul_rn(y[4 * i], c_scale), __fmul_rn(y[4 * i + 1], c_scale), e5_c) |
+                   (cvt_pair(__fmul_rn(y[4 * i + 2], c_scale), __fmul_rn(y[4 * i + 3], c_scale), e5_c) << 16);
+          stg128(p.cq + off, w[0], w[1], w[2], w[3]);
+          stg128(p.cq + off + 16, w[4], w[5], w[6], w[7]);
+        }
+      }
+    };
     // release of an accumulator / partial buffer: on the leader's barrier (remote for the peer)
     auto release = [&](uint32_t bar) {
       if (PAIR && !leader) mbar_arrive_remote(mapa_shared(bar, 0));
@@ -547,7 +580,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           float v[32];
 #pragma unroll
           for (int j = 0; j < 16; ++j) unpack_f32x2(acc[16 * c32 + j], v[2 * j], v[2 * j + 1]);
-          if (gcol0 + 32 * c32 < p.N) store_row32(p.c, grow * p.N + gcol0 + 32 * c32, v, fp32);
+          if (gcol0 + 32 * c32 < p.N) emit(v, grow, gcol0 + 32 * c32);
         }
       } else {
         const uint32_t a = acc_it % ACC;
@@ -573,11 +606,17 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               v[j] = (KIND == kTensor) ? __fmul_rn(__uint_as_float(r[c][j]), tensor_scale) : __uint_as_float(r[c][j]);
-            if (gcol0 + 32 * c < p.N) store_row32(p.c, grow * p.N + gcol0 + 32 * c, v, fp32);
+            if (gcol0 + 32 * c < p.N) emit(v, grow, gcol0 + 32 * c);
           }
         }
         ++acc_it;
       }
+    }
+    if (QOUT && want_amax) {
+      // one atomic per warp, on the (non-negative) float bits, which order like the values
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) y_amax = fmaxf(y_amax, __shfl_xor_sync(0xFFFFFFFFu, y_amax, o));
+      if (lane == 0 && y_amax > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(p.c_amax), __float_as_uint(y_amax));
     }
   }
 
@@ -591,27 +630,27 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   }
 }
 
-template <int KIND>
+template <int KIND, bool QOUT>
 cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
                         const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s) {
   using L = Layout<KIND, false>;
   static_assert(L::SMEM <= 232448, "shared memory budget");
   static bool attr_done[kMaxDevices] = {};
-  cudaError_t e = ensure_smem_limit(k_gemm<KIND, false>, static_cast<int>(L::SMEM), attr_done);
+  cudaError_t e = ensure_smem_limit(k_gemm<KIND, false, QOUT>, static_cast<int>(L::SMEM), attr_done);
   if (e != cudaSuccess) return e;
   const int64_t ntiles = (p.M / kBM) * ((p.N + L::BN - 1) / L::BN);
   const int grid = static_cast<int>(ntiles < num_sms ? ntiles : num_sms);
-  return launch_pdl(k_gemm<KIND, false>, dim3(grid), dim3(threads_of<KIND>()), L::SMEM, s, 1, tm_a, tm_b, tm_sfa, tm_sfb, p);
+  return launch_pdl(k_gemm<KIND, false, QOUT>, dim3(grid), dim3(threads_of<KIND>()), L::SMEM, s, 1, tm_a, tm_b, tm_sfa, tm_sfb, p);
 }
 
 // 2-CTA clusters; the grid is as many pairs as can be resident at once (at most
 // one per two SMs), each walking the 256-row tiles with a stride of the pair count.
-template <int KIND>
+template <int KIND, bool QOUT>
 cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
                         const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s) {
   using L = Layout<KIND, true>;
   static_assert(L::SMEM <= 232448, "shared memory budget");
-  auto kern = k_gemm<KIND, true>;
+  auto kern = k_gemm<KIND, true, QOUT>;
   static bool attr_done[kMaxDevices] = {};
   cudaError_t e = ensure_smem_limit(kern, static_cast<int>(L::SMEM), attr_done);
   if (e != cudaSuccess) return e;
@@ -664,21 +703,28 @@ bool gemm_uses_pair(const GemmParams& p) {
 
 int gemm_b_box_rows(const GemmParams& p) { return gemm_uses_pair(p) ? gemm_block_n(p.kind) / 2 : gemm_block_n(p.kind); }
 
-cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
-                        const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s) {
+template <bool QOUT>
+cudaError_t launch_gemm_q(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
+                          const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s) {
   switch (p.kind) {
     case kTensor:
-      return gemm_uses_pair(p) ? launch_pair<kTensor>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
-                                          : launch_kind<kTensor>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
+      return gemm_uses_pair(p) ? launch_pair<kTensor, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
+                               : launch_kind<kTensor, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
     case kBlock1x128:
-      if (p.b_1x128) return launch_kind<kBlockRowsB>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
-      if (gemm_uses_pair(p)) return launch_pair<kBlockK2>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
-      return (p.K / kBK) % 2 == 0 ? launch_kind<kBlockK2>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
-                                  : launch_kind<kBlock1x128>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
+      if (p.b_1x128) return launch_kind<kBlockRowsB, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
+      if (gemm_uses_pair(p)) return launch_pair<kBlockK2, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
+      return (p.K / kBK) % 2 == 0 ? launch_kind<kBlockK2, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
+                                  : launch_kind<kBlock1x128, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
     default:
-      return gemm_uses_pair(p) ? launch_pair<kMx>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
-                                      : launch_kind<kMx>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
+      return gemm_uses_pair(p) ? launch_pair<kMx, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
+                               : launch_kind<kMx, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
   }
+}
+
+cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
+                        const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s) {
+  if (p.cq != nullptr || p.c_amax != nullptr) return launch_gemm_q<true>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
+  return launch_gemm_q<false>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
 }
 
 }  // namespace fp8q

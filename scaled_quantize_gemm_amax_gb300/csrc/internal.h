@@ -56,6 +56,7 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 }
 
 // ---- amax / scale / history (amax.cu)
+cudaError_t launch_reciprocal(const float* in, float* out, cudaStream_t s);
 cudaError_t launch_amax(const void* x, int64_t n, float* amax, int num_sms, cudaStream_t s);
 cudaError_t launch_compute_scale(const float* amax, bool e5m2, float* scale, float* scale_inv, cudaStream_t s);
 cudaError_t launch_history_update(float* hist, int32_t len, int32_t* pos, const float* amax, bool e5m2, float* scale,
@@ -92,7 +93,14 @@ struct GemmParams {
   int out_fp32;
   const void* sa;        // per-tensor: float[1]; blockwise: float[M, K/128]; MX: tiled E8M0
   const void* sb;        // per-tensor: float[1]; blockwise: float[N/128, K/128] or [N, K/128]; MX: tiled E8M0
-  void* c;               // [M, N] row-major, bf16 or fp32
+  void* c;               // [M, N] row-major, bf16 or fp32; null: not stored
+  // fused output quantization (all null: off).  y = the value stored in c (bf16-rounded
+  // for bf16 output): c_amax = max |y|, cq = encode_sat(y * c_scale), c_scale_inv = 1 / c_scale
+  float* c_amax;         // float[1], zeroed by the caller's stream before the launch
+  const float* c_scale;  // float[1]
+  uint8_t* cq;           // [M, N] row-major FP8 (format e5m2_c)
+  float* c_scale_inv;    // float[1]
+  int e5m2_c;
   uint32_t* err;
 };
 // Width (N) of one output tile of the GEMM variant.

@@ -117,3 +117,21 @@ def test_gemm_rejects(lib):
 def test_binding_raises_without_library(tmp_path):
     with pytest.raises(OSError):
         fq.load_library(str(tmp_path / "missing.so"))
+
+
+def test_gemm_amax_rejects(lib):
+    g = lib.fp8_scaled_gemm_amax
+    T, B1 = 0, 1
+
+    def args(ra=T, rb=T, M=256, N=256, K=256, c=FAKE, amax=FAKE, scale=FAKE, fc=0, cq=FAKE, sinv=FAKE):
+        return (FAKE, 0, ra, FAKE, FAKE, 0, rb, FAKE, M, N, K, c, 0, amax, scale, fc, cq, sinv, None)
+
+    assert g(*args(amax=None, cq=None)) == INVALID           # nothing fused requested
+    assert g(*args(scale=None)) == INVALID                   # the FP8 copy needs its scale
+    assert g(*args(cq=None)) == INVALID                      # scale_inv only with the FP8 copy
+    assert g(*args(fc=4)) == INVALID
+    assert g(*args(T, B1)) == UNSUP
+    assert g(*args(M=200)) == SHAPE
+    assert g(*args(cq=FAKE + 8)) == ALIGN
+    assert g(*args(amax=FAKE + 2)) == ALIGN
+    assert g(*args(c=FAKE + 4)) == ALIGN

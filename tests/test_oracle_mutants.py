@@ -22,6 +22,7 @@ MUTANTS = {
     "no_saturation": ("if (saturate) return (uint8_t)(sign | maxc);", "if (0) return (uint8_t)(sign | maxc);"),
     "decode_drops_sign": ("return sign ? -v : v;", "return v;"),
     "amax_signed": ("float a = fabsf(bf16_to_float(x[i]));", "float a = bf16_to_float(x[i]);"),
+    "amax_f32_signed": ("float a = fabsf(x[i]);", "float a = x[i];"),
     "scale_inverted": ("        s = orc_fmax(fmt) / amax;", "        s = amax / orc_fmax(fmt);"),
     "scale_zero_rule": ("if (!(amax > 0.0f) || isinf(amax)) {", "if (isinf(amax)) {"),
     "history_window_one_slot": ("for (int32_t i = 0; i < len; ++i)\n        if (hist[i] > m)",

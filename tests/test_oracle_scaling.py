@@ -63,6 +63,22 @@ def test_amax_ignores_nan_and_handles_specials():
     assert oracle.amax(np.zeros(0, np.uint16)) == 0.0
 
 
+def test_amax_f32_agrees_with_bf16_amax_and_is_order_free():
+    # on bf16-representable values the float32 amax must equal the (pinned) bf16 one
+    x = randn_bf16((129, 65), 3, 50.0)
+    v = bf16_to_f32(x)
+    assert oracle.amax_f32(v) == oracle.amax(x)
+    rng = np.random.default_rng(4)
+    w = (rng.standard_normal(4099) * 1e3).astype(np.float32)   # full float32 mantissas
+    ref = np.max(np.abs(w))
+    assert oracle.amax_f32(w) == ref
+    assert oracle.amax_f32(-w[rng.permutation(w.size)]) == ref
+    specials = np.array([np.nan, -0.0, 0.0, -7.5, np.float32(1e-45), -np.nan], np.float32)
+    assert oracle.amax_f32(specials) == np.float32(7.5)
+    assert np.isinf(oracle.amax_f32(np.array([1.0, -np.inf], np.float32)))
+    assert oracle.amax_f32(np.zeros(0, np.float32)) == 0.0
+
+
 # ----------------------------------------------------------------- scale
 def test_tensor_scale_golden():
     for fmt, amax_b, s_b, si_b, *_ in golden_rows("tensor_scale.txt"):
