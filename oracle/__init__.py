@@ -77,6 +77,8 @@ def _load():
             "orc_encode_array": (None, [P, I64, ctypes.c_int, ctypes.c_int, P]),
             "orc_amax_bf16": (F, [P, I64]),
             "orc_amax_f32": (F, [P, I64]),
+            "orc_round_bf16": (ctypes.c_uint16, [ctypes.c_double]),
+            "orc_dequantize_bf16": (None, [P, I64, I64, ctypes.c_int, ctypes.c_int, P, P]),
             "orc_tensor_scale": (None, [F, ctypes.c_int, P, P]),
             "orc_history_step": (None, [P, I32, P, F, ctypes.c_int, P, P]),
             "orc_mx_exponent": (ctypes.c_int, [F, ctypes.c_int]),
@@ -253,6 +255,23 @@ def dequantize(q, kind: int, fmt: int, s) -> np.ndarray:
     s = np.ascontiguousarray(s, dtype=np.uint8 if kind == KIND_MX else np.float32)
     out = np.empty((R, C), np.float64)
     _load().orc_dequantize(_ptr(q), R, C, fmt, kind, _ptr(s), _ptr(out))
+    return out
+
+
+def round_bf16(values) -> np.ndarray:
+    """float64 values -> bfloat16 bit patterns (uint16), one rounding, ties to even."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    f = _load().orc_round_bf16
+    return np.array([f(float(x)) for x in v.reshape(-1)], dtype=np.uint16).reshape(v.shape)
+
+
+def dequantize_bf16(q, kind: int, fmt: int, s) -> np.ndarray:
+    """FP8 codes + multipliers -> bfloat16 bit patterns: the exact product rounded once."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    R, C = q.shape
+    s = np.ascontiguousarray(s, dtype=np.uint8 if kind == KIND_MX else np.float32)
+    out = np.empty((R, C), np.uint16)
+    _load().orc_dequantize_bf16(_ptr(q), R, C, fmt, kind, _ptr(s), _ptr(out))
     return out
 
 

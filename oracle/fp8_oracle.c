@@ -30,6 +30,7 @@
 #include <float.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define ORC_E4M3 0
@@ -320,7 +321,10 @@ void orc_transpose_bf16(const uint16_t* x, int64_t R, int64_t C, uint16_t* xt)
  *   kind 0 (per tensor):  s[0]
  *   kind 1 (1 x 128):     s[r * (C/128) + c/128]
  *   kind 2 (128 x 128):   s[(r/128) * (C/128) + c/128]
- *   kind 3 (MX 1 x 32):   2^(e8m0[r * (C/32) + c/32] - 127)
+ *   kind 3 (MX 1 x 32):   2^(e8m0[r * (C/32) + c/32] - 127); the byte 0xFF is
+ *                         the E8M0 NaN (reading: the guide names the E8M0
+ *                         format only; its all-ones code is NaN, and the
+ *                         quantizer never writes it)
  * All products are exact in double (4-bit by 24-bit significands).
  */
 void orc_dequantize(const uint8_t* q, int64_t R, int64_t C, int fmt, int kind,
@@ -336,9 +340,73 @@ void orc_dequantize(const uint8_t* q, int64_t R, int64_t C, int fmt, int kind,
             case 0: m = (double)sf[0]; break;
             case 1: m = (double)sf[r * (C / 128) + c / 128]; break;
             case 2: m = (double)sf[(r / 128) * (C / 128) + c / 128]; break;
-            default: m = ldexp(1.0, (int)se[r * (C / 32) + c / 32] - 127); break;
+            default: {
+                const int e = (int)se[r * (C / 32) + c / 32];
+                m = e == 255 ? NAN : ldexp(1.0, e - 127);
+                break;
+            }
             }
             out[r * C + c] = v * m;
         }
     }
+}
+
+/*
+ * Round a double to the nearest bfloat16 (8 significant bits, 8 exponent
+ * bits, bias 127), ties to even, with gradual underflow (spacing 2^-133 below
+ * 2^-126) and overflow to infinity at max + half an ulp; returns the bit
+ * pattern.  NaN gives the quiet NaN 0x7FC0 with the input's sign.
+ */
+uint16_t orc_round_bf16(double v)
+{
+    const uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    if (isnan(v)) return (uint16_t)(sign | 0x7FC0u);
+    double a = fabs(v);
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80u);
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);               /* a = f * 2^e, f in [0.5, 1): a in [2^(e-1), 2^e) */
+    int ex = e - 1;
+    if (ex < -126) ex = -126;   /* subnormal range: fixed spacing */
+    const double quantum = ldexp(1.0, ex - 7);
+    const double k = a / quantum;                 /* exact: division by a power of two */
+    double n = floor(k);
+    const double frac = k - n;
+    if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) != 0.0)) n += 1.0;
+    const double res = n * quantum;
+    if (res >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80u);
+    const float f = (float)res;                   /* exact: every bfloat16 is a binary32 */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return (uint16_t)(sign | (bits >> 16));
+}
+
+/*
+ * Dequantize to bfloat16 (the FP8 -> BF16 conversion, e.g. of weights): the
+ * exact product decode(q) * multiplier of orc_dequantize, rounded once to
+ * bfloat16 (reading: the pages give no rounding for this step; one rounding
+ * of the exact value is the plain definition).
+ */
+void orc_dequantize_bf16(const uint8_t* q, int64_t R, int64_t C, int fmt, int kind,
+                         const void* s, uint16_t* out)
+{
+    /* 128-row slabs through orc_dequantize (a slab starts on a 128-row block,
+       so every kind's multiplier array is offset by whole rows of blocks) */
+    double* buf = (double*)malloc((size_t)(C > 0 ? C : 1) * 128 * sizeof(double));
+    if (buf == NULL) return;
+    const float* sf = (const float*)s;
+    const uint8_t* se = (const uint8_t*)s;
+    for (int64_t r0 = 0; r0 < R; r0 += 128) {
+        const int64_t rows = R - r0 < 128 ? R - r0 : 128;
+        const void* sb;
+        switch (kind) {
+        case 0: sb = sf; break;
+        case 1: sb = sf + r0 * (C / 128); break;
+        case 2: sb = sf + (r0 / 128) * (C / 128); break;
+        default: sb = se + r0 * (C / 32); break;
+        }
+        orc_dequantize(q + r0 * C, rows, C, fmt, kind, sb, buf);
+        for (int64_t i = 0; i < rows * C; ++i) out[r0 * C + i] = orc_round_bf16(buf[i]);
+    }
+    free(buf);
 }

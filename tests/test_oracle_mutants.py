@@ -35,6 +35,11 @@ MUTANTS = {
                             "case 1: m = (double)sf[(r / 128) * (C / 128) + c / 128]; break;"),
     "dequant_mx_bias": ("default: m = ldexp(1.0, (int)se[r * (C / 32) + c / 32] - 127); break;",
                         "default: m = ldexp(1.0, (int)se[r * (C / 32) + c / 32] - 128); break;"),
+    "bf16_ties_away": ("if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) != 0.0)) n += 1.0;", "if (frac >= 0.5) n += 1.0;"),
+    "bf16_subnormal_spacing": ("if (ex < -126) ex = -126;", "if (ex < -127) ex = -127;"),
+    "bf16_overflow_early": ("if (res >= ldexp(1.0, 128)) return", "if (res >= ldexp(1.0, 127)) return"),
+    "mx_nan_byte_ignored": ("                m = e == 255 ? NAN : ldexp(1.0, e - 127);\n                break;\n            }\n            }\n            out[r * C + c] = v * m;",
+                            "                m = ldexp(1.0, e - 127);\n                break;\n            }\n            }\n            out[r * C + c] = v * m;"),
 }
 
 
@@ -50,6 +55,7 @@ def test_pins_reject_mutant(name, tmp_path):
     env = dict(os.environ, FP8_ORACLE_LIB=str(lib))
     out = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                           os.path.join(ROOT, "tests", "test_oracle_scaling.py"),
-                          os.path.join(ROOT, "tests", "test_oracle_formats.py")],
+                          os.path.join(ROOT, "tests", "test_oracle_formats.py"),
+                          os.path.join(ROOT, "tests", "test_oracle_dequant.py")],
                          capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
     assert out.returncode != 0, f"the pins did not catch mutant {name}"
