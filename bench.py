@@ -493,7 +493,7 @@ def run_reference(args, rank, world):
 
 
 CASES = ("cast_tensor", "cast_1x128", "cast_128x128", "cast_mx", "amax", "gemm_tensor", "gemm_block", "gemm_mx",
-         "gemm_amax")
+         "gemm_amax", "dequant_tensor", "dequant_1x128", "dequant_128x128", "dequant_mx")
 
 
 def run_case(args):
@@ -524,6 +524,18 @@ def run_case(args):
             fn = lambda: fq.fp8_cast_transpose(x, rec, F.E4M3, scale, None, qr, sr, qc, sc)
             nbytes = 4 * s * s
         ms = _time_kernel(fn, reps=args.steps, flush=flush)
+        res = {"case": args.case, "size": s, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+        res["frac_hbm"] = round(res["GB/s"] / pk["hbm_gbs"], 4)
+    elif args.case.startswith("dequant"):
+        # FP8 -> BF16 of an s x s row-wise copy: 1 B read + 2 B written per element (+ scales)
+        x = wl.cfg5_sweep(s, dev) if s in wl.CFG5_SIZES else wl.normal_bf16((s, s), 5, 1.0, dev)
+        rec = {"dequant_tensor": R.TENSOR, "dequant_1x128": R.BLOCK_1x128, "dequant_128x128": R.BLOCK_128x128,
+               "dequant_mx": R.MX_1x32_TILED}[args.case]
+        scale = torch.ones(1, dtype=torch.float32, device=dev) if rec == R.TENSOR else None
+        q, sq, _, _ = fq.cast_transpose(x, rec, F.E4M3, scale, col=False)
+        y = torch.empty((s, s), dtype=torch.bfloat16, device=dev)
+        ms = _time_kernel(lambda: fq.fp8_dequantize(q, rec, F.E4M3, sq, y), reps=args.steps, flush=flush)
+        nbytes = 3 * s * s + sq.numel() * sq.element_size()
         res = {"case": args.case, "size": s, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
         res["frac_hbm"] = round(res["GB/s"] / pk["hbm_gbs"], 4)
     elif args.case == "gemm_amax":

@@ -158,6 +158,27 @@ fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, fp8_recipe re
                         const float* scale, float* amax_out, uint8_t* q, void* s, cudaStream_t stream);
 
 /*
+ * fp8_dequantize -- FP8 -> BF16 (e.g. FP8 weights to BF16; search-result page,
+ * the FP8-to-BF16 weight conversion; guide, "block-level scaling" and "MXFP8
+ * scaling" for the multipliers).
+ *   q       device, [rows, cols] u8 FP8 codes (format fmt), row-major: a
+ *           row-wise copy, or a column-wise copy passed as its own [rows, cols]
+ *   recipe  how q was quantized; s holds the multipliers (scale_inv) exactly as
+ *           fp8_cast_transpose wrote them for that copy:
+ *           TENSOR float[1]; BLOCK_1x128 float[rows, cols/128];
+ *           BLOCK_128x128 float[rows/128, cols/128]; MX_1x32 u8 E8M0
+ *           [rows, cols/32]; MX_1x32_TILED the GEMM-ready atoms
+ *   y       device, [rows, cols] bf16: the exact product decode(q) * multiplier
+ *           rounded once to bfloat16 (nearest, ties to even; gradual underflow;
+ *           overflow to inf).  E8M0 byte 0xFF (its NaN) gives NaN.
+ * q and y 16-byte aligned (FP8_ERR_ALIGNMENT).  Shapes: TENSOR any; 1x128
+ * cols % 128; 128x128 and MX_1x32_TILED rows and cols % 128; MX_1x32 cols % 32
+ * (FP8_ERR_SHAPE).  rows or cols == 0 is a no-op.
+ */
+fp8_status fp8_dequantize(const uint8_t* q, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
+                          const void* s, void* y, cudaStream_t stream);
+
+/*
  * fp8_scaled_gemm -- C = deq(A) . deq(B)^T with FP32 accumulation.
  * Search-result page, dataflow paragraph (FP8 inputs, FP32 accumulation, BF16
  * output; wgrad output FP32); guide, "code changes" (the three GEMMs of a layer

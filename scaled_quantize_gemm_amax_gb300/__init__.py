@@ -82,6 +82,7 @@ _SIGNATURES = {
     "amax_history_update": [_P, _I32, _P, _P, _E, _P, _P, _P],
     "fp8_cast_transpose": [_P, _I64, _I64, _E, _E, _P, _P, _P, _P, _P, _P, _P],
     "fp8_quantize": [_P, _I64, _I64, _E, _E, _P, _P, _P, _P, _P],
+    "fp8_dequantize": [_P, _I64, _I64, _E, _E, _P, _P, _P],
     "fp8_scaled_gemm": [_P, _E, _E, _P, _P, _E, _E, _P, _I64, _I64, _I64, _P, _E, _P],
     "fp8_scaled_gemm_amax": [_P, _E, _E, _P, _P, _E, _E, _P, _I64, _I64, _I64, _P, _E, _P, _P, _E, _P, _P, _P],
     "fp8_get_device_status": [_P],
@@ -164,6 +165,20 @@ def fp8_quantize(x, recipe, fmt, scale, amax_out, q, s, stream=None):
     _check("fp8_quantize",
            load_library().fp8_quantize(_ptr(x), rows, cols, int(recipe), int(fmt), _ptr(scale), _ptr(amax_out),
                                        _ptr(q), _ptr(s), _stream(stream)))
+
+
+def fp8_dequantize(q, recipe, fmt, s, y, stream=None):
+    rows, cols = q.shape
+    _check("fp8_dequantize",
+           load_library().fp8_dequantize(_ptr(q), rows, cols, int(recipe), int(fmt), _ptr(s), _ptr(y),
+                                         _stream(stream)))
+
+
+def dequantize(q, recipe, fmt, s, stream=None):
+    """Allocate y [rows, cols] bf16 and run fp8_dequantize."""
+    y = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    fp8_dequantize(q, recipe, fmt, s, y, stream)
+    return y
 
 
 def fp8_scaled_gemm(a, fa, ra, sa, b, fb, rb, sb, c, out=OutDtype.BF16, stream=None):

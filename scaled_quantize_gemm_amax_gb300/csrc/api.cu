@@ -318,6 +318,38 @@ fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, fp8_recipe re
   return fp8_cast_transpose(x, rows, cols, recipe, fmt, scale, amax_out, q, s, nullptr, nullptr, stream);
 }
 
+fp8_status fp8_dequantize(const uint8_t* q, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
+                          const void* s, void* y, cudaStream_t stream) {
+  if (rows < 0 || cols < 0 || !valid_fmt(fmt) || recipe < FP8_TENSOR || recipe > FP8_MX_1x32_TILED)
+    return FP8_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return FP8_OK;
+  if (q == nullptr || s == nullptr || y == nullptr) return FP8_ERR_INVALID_ARG;
+  if (rows > kMaxDim || cols > kMaxDim) return FP8_ERR_SHAPE;
+  switch (recipe) {
+    case FP8_BLOCK_1x128:
+      if (cols % 128) return FP8_ERR_SHAPE;
+      break;
+    case FP8_BLOCK_128x128:
+    case FP8_MX_1x32_TILED:
+      if (rows % 128 || cols % 128) return FP8_ERR_SHAPE;
+      break;
+    case FP8_MX_1x32:
+      if (cols % 32) return FP8_ERR_SHAPE;
+      break;
+    default:
+      break;
+  }
+  if (!aligned(q, 16) || !aligned(y, 16)) return FP8_ERR_ALIGNMENT;
+  const bool mx = recipe == FP8_MX_1x32 || recipe == FP8_MX_1x32_TILED;
+  if (!mx && !aligned(s, 4)) return FP8_ERR_ALIGNMENT;
+  DeviceInfo* d;
+  if (fp8_status st = device_info(&d)) return st;
+  const int kind = recipe == FP8_TENSOR ? kTensor : recipe == FP8_BLOCK_1x128 ? kBlock1x128
+                   : recipe == FP8_BLOCK_128x128 ? kBlock128x128 : kMx;
+  return cuda_status(launch_dequantize(q, rows, cols, kind, recipe == FP8_MX_1x32_TILED, fmt == FP8_E5M2, s, y,
+                                       d->num_sms, stream));
+}
+
 fp8_status fp8_scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const void* sA, const uint8_t* B,
                            fp8_format fb, fp8_recipe rb, const void* sB, int64_t M, int64_t N, int64_t K, void* C,
                            fp8_out_dtype out, cudaStream_t stream) {

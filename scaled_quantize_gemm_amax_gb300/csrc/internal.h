@@ -84,6 +84,10 @@ cudaError_t launch_cast_transpose_tiled(const CastParams& p, const CUtensorMap& 
 // Plain path for the per-tensor recipe at any shape.
 cudaError_t launch_cast_generic(const CastParams& p, const void* x, cudaStream_t s);
 
+// ---- dequantize (dequantize.cu): y bf16 [R, C] = RN_bf16(decode(q) * multiplier)
+cudaError_t launch_dequantize(const uint8_t* q, int64_t R, int64_t C, int recipe, bool mx_tiled, bool e5m2,
+                              const void* s, void* y, int num_sms, cudaStream_t stream);
+
 // ---- scaled GEMM (gemm.cu)
 struct GemmParams {
   int64_t M, N, K;

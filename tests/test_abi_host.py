@@ -135,3 +135,20 @@ def test_gemm_amax_rejects(lib):
     assert g(*args(cq=FAKE + 8)) == ALIGN
     assert g(*args(amax=FAKE + 2)) == ALIGN
     assert g(*args(c=FAKE + 4)) == ALIGN
+
+
+def test_dequantize_rejects(lib):
+    dq = lib.fp8_dequantize
+    T, B1, B128, MX, MXT = 0, 1, 2, 3, 4
+    assert dq(FAKE, 128, 128, 9, 0, FAKE, FAKE, None) == INVALID        # bad recipe
+    assert dq(FAKE, 128, 128, T, 2, FAKE, FAKE, None) == INVALID        # bad format
+    assert dq(None, 128, 128, T, 0, FAKE, FAKE, None) == INVALID
+    assert dq(FAKE, 128, 128, T, 0, None, FAKE, None) == INVALID
+    assert dq(FAKE, 128, 100, B1, 0, FAKE, FAKE, None) == SHAPE
+    assert dq(FAKE, 100, 128, B128, 0, FAKE, FAKE, None) == SHAPE
+    assert dq(FAKE, 128, 48, MX, 0, FAKE, FAKE, None) == SHAPE
+    assert dq(FAKE, 160, 128, MXT, 0, FAKE, FAKE, None) == SHAPE
+    assert dq(FAKE + 8, 128, 128, T, 0, FAKE, FAKE, None) == ALIGN
+    assert dq(FAKE, 128, 128, T, 0, FAKE, FAKE + 2, None) == ALIGN
+    assert dq(FAKE, 128, 128, B1, 0, FAKE + 1, FAKE, None) == ALIGN
+    assert dq(FAKE, 0, 128, T, 0, None, None, None) == OK                # empty: no-op
