@@ -9,8 +9,11 @@ output tensors with torch.  There is no fallback: every call raises when
 Entry points with the C names take tensors (or None for NULL) and raise
 ``FP8Error`` on a non-OK status: ``fp8_amax``, ``fp8_compute_scale``,
 ``amax_history_update``, ``fp8_quantize``, ``fp8_cast_transpose``,
-``fp8_scaled_gemm``, ``fp8_get_device_status``, ``fp8_debug_wait_timeout``.
-``cast_transpose`` / ``scaled_gemm`` are allocation helpers over them.
+``fp8_dequantize``, ``fp8_scaled_gemm``, ``fp8_scaled_gemm_amax``,
+``fp8_get_device_status``, ``fp8_debug_wait_timeout``.  ``cast_transpose`` /
+``dequantize`` / ``scaled_gemm`` / ``scaled_gemm_amax`` are allocation helpers
+over them; ``linear`` holds the FP8 linear layer and the autocast scope built
+on these calls.
 """
 from __future__ import annotations
 
@@ -23,8 +26,9 @@ import torch
 __all__ = [
     "Status", "Format", "Recipe", "OutDtype", "FP8Error", "lib_path", "load_library",
     "fp8_amax", "fp8_compute_scale", "amax_history_update", "fp8_quantize", "fp8_cast_transpose",
-    "fp8_scaled_gemm", "fp8_get_device_status", "fp8_debug_wait_timeout", "fp8_status_string",
-    "scale_shape", "cast_transpose", "scaled_gemm", "DelayedScaling",
+    "fp8_dequantize", "fp8_scaled_gemm", "fp8_scaled_gemm_amax", "fp8_get_device_status",
+    "fp8_debug_wait_timeout", "fp8_status_string",
+    "scale_shape", "cast_transpose", "dequantize", "scaled_gemm", "scaled_gemm_amax", "DelayedScaling",
 ]
 
 

@@ -1,0 +1,101 @@
+"""GPU parity of the FP8 linear layer (fprop, dgrad, wgrad through the C ABI)
+against the oracle: the oracle quantizes the same BF16 operands with the recipe's
+rules and computes each GEMM in float64; every output is held to the GEMM bar."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from scaled_quantize_gemm_amax_gb300 import Format
+from scaled_quantize_gemm_amax_gb300 import linear as L
+from scaled_quantize_gemm_amax_gb300 import workloads as wl
+from gpu_util import assert_status_ok, bits16, host, require_gpu
+import scaled_quantize_gemm_amax_gb300 as fq
+
+pytestmark = pytest.mark.gpu
+
+M, K, N = 256, 384, 512
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def oracle_copies(xh, kind, fmt, scale=None):
+    q_r, s_r = oracle.quantize_rowwise(xh, kind, fmt, scale)
+    q_c, s_c = oracle.quantize_colwise(xh, kind, fmt, scale)
+    return (q_r, s_r), (q_c, s_c)
+
+
+def deq(qs, kind, fmt):
+    return oracle.dequantize(qs[0], kind, fmt, qs[1])
+
+
+def check(c_gpu, a_deq, b_deq, what):
+    c_ref = a_deq @ b_deq.T
+    rel, worst = oracle.gemm_tolerance_check(host(c_gpu.float()).astype(np.float64), c_ref, a_deq, b_deq)
+    assert rel <= 1e-2 and worst <= 1.0, f"{what}: rel {rel:.3e} worst {worst:.3f}"
+
+
+def run_layer(recipe, seed, steps=1):
+    torch.manual_seed(seed + 5000)   # weights independent of the seeded inputs' streams
+    layer = L.FP8Linear(K, N, device="cuda")
+    outs = []
+    for step in range(steps):
+        x = wl.normal_bf16((M, K), seed + 10 * step, 1.0).requires_grad_(True)
+        dy = wl.normal_bf16((M, N), seed + 10 * step + 1, 1e-3)
+        layer.weight.grad = None
+        with L.fp8_autocast(fp8_recipe=recipe):
+            y = layer(x)
+        y.backward(dy)
+        torch.cuda.synchronize()
+        assert_status_ok()
+        assert x.grad.dtype == torch.bfloat16 and layer.weight.grad.dtype == torch.float32
+        outs.append((x.detach(), dy, layer.weight.detach().to(torch.bfloat16), y.detach(), x.grad.clone(),
+                     layer.weight.grad.clone()))
+    return outs
+
+
+KINDS = {"current": (oracle.KIND_TENSOR, oracle.KIND_TENSOR), "block": (oracle.KIND_1x128, oracle.KIND_128x128),
+         "mx": (oracle.KIND_MX, oracle.KIND_MX)}
+
+
+@pytest.mark.parametrize("name,recipe", [("current", L.Float8CurrentScaling()), ("block", L.Float8BlockScaling()),
+                                         ("mx", L.MXFP8BlockScaling())])
+def test_fp8_linear_three_gemms(name, recipe):
+    (x, dy, w16, y, dx, dw), = run_layer(recipe, 80)
+    kx, kw = KINDS[name]
+    fx, fdy = int(recipe.fwd_format), int(recipe.bwd_format)
+    xh, wh, dyh = bits16(x), bits16(w16), bits16(dy)
+    sx = sw = sdy = None
+    if name == "current":
+        sx, _ = oracle.tensor_scale(oracle.amax(xh), fx)
+        sw, _ = oracle.tensor_scale(oracle.amax(wh), fx)
+        sdy, _ = oracle.tensor_scale(oracle.amax(dyh), fdy)
+    x_r, x_c = oracle_copies(xh, kx, fx, sx)
+    w_r, w_c = oracle_copies(wh, kw, fx, sw)
+    dy_r, dy_c = oracle_copies(dyh, kx, fdy, sdy)
+    check(y, deq(x_r, kx, fx), deq(w_r, kw, fx), "fprop")
+    check(dx, deq(dy_r, kx, fdy), deq(w_c, kw, fx), "dgrad")
+    check(dw, deq(dy_c, kx, fdy), deq(x_c, kx, fx), "wgrad")
+
+
+def test_fp8_linear_delayed_scaling_steps():
+    # delayed scaling: step t quantizes with the scale the history held before t (1 at t = 0)
+    recipe = L.Float8DelayedScaling(history_len=16)
+    outs = run_layer(recipe, 90, steps=3)
+    st = {"x": oracle.DelayedState(16, oracle.E4M3), "w": oracle.DelayedState(16, oracle.E4M3),
+          "dy": oracle.DelayedState(16, oracle.E5M2)}
+    for step, (x, dy, w16, y, dx, dw) in enumerate(outs):
+        xh, wh, dyh = bits16(x), bits16(w16), bits16(dy)
+        x_r, x_c = oracle_copies(xh, 0, oracle.E4M3, st["x"].scale[0])
+        w_r, w_c = oracle_copies(wh, 0, oracle.E4M3, st["w"].scale[0])
+        dy_r, dy_c = oracle_copies(dyh, 0, oracle.E5M2, st["dy"].scale[0])
+        check(y, deq(x_r, 0, oracle.E4M3), deq(w_r, 0, oracle.E4M3), f"fprop step {step}")
+        check(dx, deq(dy_r, 0, oracle.E5M2), deq(w_c, 0, oracle.E4M3), f"dgrad step {step}")
+        check(dw, deq(dy_c, 0, oracle.E5M2), deq(x_c, 0, oracle.E4M3), f"wgrad step {step}")
+        st["x"].step(oracle.amax(xh))
+        st["w"].step(oracle.amax(wh))
+        st["dy"].step(oracle.amax(dyh))
+
