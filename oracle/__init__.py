@@ -78,6 +78,7 @@ def _load():
             "orc_amax_bf16": (F, [P, I64]),
             "orc_amax_f32": (F, [P, I64]),
             "orc_round_bf16": (ctypes.c_uint16, [ctypes.c_double]),
+            "orc_allreduce_sum": (None, [P, I32, I64, ctypes.c_int, P, P, P, P]),
             "orc_dequantize_bf16": (None, [P, I64, I64, ctypes.c_int, ctypes.c_int, P, P]),
             "orc_tensor_scale": (None, [F, ctypes.c_int, P, P]),
             "orc_history_step": (None, [P, I32, P, F, ctypes.c_int, P, P]),
@@ -273,6 +274,20 @@ def dequantize_bf16(q, kind: int, fmt: int, s) -> np.ndarray:
     out = np.empty((R, C), np.uint16)
     _load().orc_dequantize_bf16(_ptr(q), R, C, fmt, kind, _ptr(s), _ptr(out))
     return out
+
+
+def allreduce_sum(g_bf16, fmt: int):
+    """FP8 all-reduce of k rank gradients (rows of g [k, n] bf16) with a shared scale.
+
+    Returns (amax, q [k, n] uint8, scale_inv, out [n] float32)."""
+    g = _bf16_bits(g_bf16)
+    k, n = g.shape
+    q = np.empty((k, n), np.uint8)
+    out = np.empty(n, np.float32)
+    a = np.zeros(1, np.float32)
+    si = np.zeros(1, np.float32)
+    _load().orc_allreduce_sum(_ptr(g), k, n, fmt, _ptr(a), _ptr(q), _ptr(si), _ptr(out))
+    return a[0], q, si[0], out
 
 
 def scaled_gemm(qa, fa, ka, sa, qb, fb, kb, sb) -> np.ndarray:

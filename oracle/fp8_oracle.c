@@ -410,3 +410,31 @@ void orc_dequantize_bf16(const uint8_t* q, int64_t R, int64_t C, int fmt, int ki
     }
     free(buf);
 }
+
+/*
+ * FP8 gradient all-reduce with a shared scale, for k data-parallel ranks whose
+ * gradients are the k rows of g [k, n] (FP8-LM news article, "automatic
+ * scaling": the gradient's scaling factor is adjusted so that its values stay
+ * within FP8's range during the all-reduce).  Reading (the pages give no
+ * formula): the ranks agree on the global amax A (an all-reduce MAX), all use
+ * the per-tensor scale s = FMAX / A (orc_tensor_scale's rule), each sends
+ * encode_sat(g_r * s), and the reduction sums the decoded payloads in rank
+ * order in binary32, then multiplies once by scale_inv = 1 / s:
+ *   out[i] = (((decode(q[0,i]) + decode(q[1,i])) + ...) + decode(q[k-1,i])) * scale_inv
+ * q is [k, n]; *amax_out = A; *scale_inv_out = 1 / s.
+ */
+void orc_allreduce_sum(const uint16_t* g, int32_t k, int64_t n, int fmt, float* amax_out, uint8_t* q,
+                       float* scale_inv_out, float* out)
+{
+    const float a = orc_amax_bf16(g, (int64_t)k * n);
+    float s, si;
+    orc_tensor_scale(a, fmt, &s, &si);
+    orc_quantize_tensor(g, k, n, fmt, s, q);
+    for (int64_t i = 0; i < n; ++i) {
+        float acc = 0.0f;
+        for (int32_t r = 0; r < k; ++r) acc = acc + (float)orc_decode(q[(int64_t)r * n + i], fmt);
+        out[i] = acc * si;
+    }
+    *amax_out = a;
+    *scale_inv_out = si;
+}

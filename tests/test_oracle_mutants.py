@@ -35,6 +35,8 @@ MUTANTS = {
                             "case 1: m = (double)sf[(r / 128) * (C / 128) + c / 128]; break;"),
     "dequant_mx_bias": ("default: m = ldexp(1.0, (int)se[r * (C / 32) + c / 32] - 127); break;",
                         "default: m = ldexp(1.0, (int)se[r * (C / 32) + c / 32] - 128); break;"),
+    "allreduce_drops_last_rank": ("for (int32_t r = 0; r < k; ++r) acc = acc +", "for (int32_t r = 0; r < k - 1; ++r) acc = acc +"),
+    "allreduce_local_amax": ("const float a = orc_amax_bf16(g, (int64_t)k * n);", "const float a = orc_amax_bf16(g, n);"),
     "bf16_ties_away": ("if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) != 0.0)) n += 1.0;", "if (frac >= 0.5) n += 1.0;"),
     "bf16_subnormal_spacing": ("if (ex < -126) ex = -126;", "if (ex < -127) ex = -127;"),
     "bf16_overflow_early": ("if (res >= ldexp(1.0, 128)) return", "if (res >= ldexp(1.0, 127)) return"),
@@ -56,6 +58,7 @@ def test_pins_reject_mutant(name, tmp_path):
     out = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                           os.path.join(ROOT, "tests", "test_oracle_scaling.py"),
                           os.path.join(ROOT, "tests", "test_oracle_formats.py"),
-                          os.path.join(ROOT, "tests", "test_oracle_dequant.py")],
+                          os.path.join(ROOT, "tests", "test_oracle_dequant.py"),
+                          os.path.join(ROOT, "tests", "test_oracle_allreduce.py")],
                          capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
     assert out.returncode != 0, f"the pins did not catch mutant {name}"
