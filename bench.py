@@ -493,7 +493,7 @@ def run_reference(args, rank, world):
 
 
 CASES = ("cast_tensor", "cast_1x128", "cast_128x128", "cast_mx", "amax", "gemm_tensor", "gemm_block", "gemm_mx",
-         "gemm_amax", "dequant_tensor", "dequant_1x128", "dequant_128x128", "dequant_mx")
+         "gemm_amax", "dequant_tensor", "dequant_1x128", "dequant_128x128", "dequant_mx", "allreduce")
 
 
 def run_case(args):
@@ -537,6 +537,21 @@ def run_case(args):
         ms = _time_kernel(lambda: fq.fp8_dequantize(q, rec, F.E4M3, sq, y), reps=args.steps, flush=flush)
         nbytes = 3 * s * s + sq.numel() * sq.element_size()
         res = {"case": args.case, "size": s, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+        res["frac_hbm"] = round(res["GB/s"] / pk["hbm_gbs"], 4)
+    elif args.case == "allreduce":
+        # 8 ranks' size x size gradients: amax pass (2 B/elem) + cast and sum (2 B read, 1 B payload per
+        # rank element, 4 B per reduced element)
+        k, n = 8, s * s
+        g = (torch.randn((k, n), generator=torch.Generator(device=dev).manual_seed(9), device=dev) * 1e-3).to(
+            torch.bfloat16)
+        amax = torch.empty(1, dtype=torch.float32, device=dev)
+        q = torch.empty((k, n), dtype=torch.uint8, device=dev)
+        si = torch.empty(1, dtype=torch.float32, device=dev)
+        out = torch.empty(n, dtype=torch.float32, device=dev)
+        ms = _time_kernel(lambda: fq.fp8_allreduce_sum(g, F.E5M2, amax, q, si, out), reps=args.steps, flush=flush)
+        nbytes = k * n * 2 + k * n * 3 + 4 * n
+        res = {"case": args.case, "size": s, "ranks": k, "us": round(ms * 1e3, 2),
+               "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
         res["frac_hbm"] = round(res["GB/s"] / pk["hbm_gbs"], 4)
     elif args.case == "gemm_amax":
         # per-tensor GEMM whose epilogue writes C's FP8 copy (delayed scale) and amax, against

@@ -179,6 +179,26 @@ fp8_status fp8_dequantize(const uint8_t* q, int64_t rows, int64_t cols, fp8_reci
                           const void* s, void* y, cudaStream_t stream);
 
 /*
+ * fp8_allreduce_sum -- FP8 gradient all-reduce with a shared scale (FP8-LM news
+ * article, "automatic scaling": the gradient's scaling factor keeps its values
+ * inside FP8's range through the all-reduce), for k data-parallel ranks whose
+ * gradients are held on this device as the rows of g.  The ranks agree on the
+ * global amax A (the all-reduce MAX), all use the per-tensor scale
+ * s = FMAX / A (fp8_compute_scale's rule), and the reduction sums the decoded
+ * FP8 payloads in rank order in binary32, then multiplies once by 1 / s.
+ *   g          device, [k, n] bf16 row-major (rank r's gradient in row r)
+ *   amax       device float[1], overwritten with A
+ *   q          device, [k, n] u8: rank r's payload encode_sat(g[r] * s) (fmt)
+ *   scale_inv  device float[1]: 1 / s
+ *   out        device, [n] fp32: the reduced gradient
+ * k >= 1; n % 8 == 0 (FP8_ERR_SHAPE); g and out 16-byte aligned, q 8-byte
+ * aligned (FP8_ERR_ALIGNMENT).  n == 0 is a no-op.  For E4M3 and k <= 64 the
+ * sum is exact, so out does not depend on the rank order.
+ */
+fp8_status fp8_allreduce_sum(const void* g, int32_t k, int64_t n, fp8_format fmt, float* amax, uint8_t* q,
+                             float* scale_inv, float* out, cudaStream_t stream);
+
+/*
  * fp8_scaled_gemm -- C = deq(A) . deq(B)^T with FP32 accumulation.
  * Search-result page, dataflow paragraph (FP8 inputs, FP32 accumulation, BF16
  * output; wgrad output FP32); guide, "code changes" (the three GEMMs of a layer

@@ -9,7 +9,7 @@ output tensors with torch.  There is no fallback: every call raises when
 Entry points with the C names take tensors (or None for NULL) and raise
 ``FP8Error`` on a non-OK status: ``fp8_amax``, ``fp8_compute_scale``,
 ``amax_history_update``, ``fp8_quantize``, ``fp8_cast_transpose``,
-``fp8_dequantize``, ``fp8_scaled_gemm``, ``fp8_scaled_gemm_amax``,
+``fp8_dequantize``, ``fp8_allreduce_sum``, ``fp8_scaled_gemm``, ``fp8_scaled_gemm_amax``,
 ``fp8_get_device_status``, ``fp8_debug_wait_timeout``.  ``cast_transpose`` /
 ``dequantize`` / ``scaled_gemm`` / ``scaled_gemm_amax`` are allocation helpers
 over them; ``linear`` holds the FP8 linear layer and the autocast scope built
@@ -26,9 +26,10 @@ import torch
 __all__ = [
     "Status", "Format", "Recipe", "OutDtype", "FP8Error", "lib_path", "load_library",
     "fp8_amax", "fp8_compute_scale", "amax_history_update", "fp8_quantize", "fp8_cast_transpose",
-    "fp8_dequantize", "fp8_scaled_gemm", "fp8_scaled_gemm_amax", "fp8_get_device_status",
+    "fp8_dequantize", "fp8_allreduce_sum", "fp8_scaled_gemm", "fp8_scaled_gemm_amax", "fp8_get_device_status",
     "fp8_debug_wait_timeout", "fp8_status_string",
-    "scale_shape", "cast_transpose", "dequantize", "scaled_gemm", "scaled_gemm_amax", "DelayedScaling",
+    "scale_shape", "cast_transpose", "dequantize", "allreduce_sum", "scaled_gemm", "scaled_gemm_amax",
+    "DelayedScaling",
 ]
 
 
@@ -87,6 +88,7 @@ _SIGNATURES = {
     "fp8_cast_transpose": [_P, _I64, _I64, _E, _E, _P, _P, _P, _P, _P, _P, _P],
     "fp8_quantize": [_P, _I64, _I64, _E, _E, _P, _P, _P, _P, _P],
     "fp8_dequantize": [_P, _I64, _I64, _E, _E, _P, _P, _P],
+    "fp8_allreduce_sum": [_P, _I32, _I64, _E, _P, _P, _P, _P, _P],
     "fp8_scaled_gemm": [_P, _E, _E, _P, _P, _E, _E, _P, _I64, _I64, _I64, _P, _E, _P],
     "fp8_scaled_gemm_amax": [_P, _E, _E, _P, _P, _E, _E, _P, _I64, _I64, _I64, _P, _E, _P, _P, _E, _P, _P, _P],
     "fp8_get_device_status": [_P],
@@ -176,6 +178,27 @@ def fp8_dequantize(q, recipe, fmt, s, y, stream=None):
     _check("fp8_dequantize",
            load_library().fp8_dequantize(_ptr(q), rows, cols, int(recipe), int(fmt), _ptr(s), _ptr(y),
                                          _stream(stream)))
+
+
+def fp8_allreduce_sum(g, fmt, amax, q, scale_inv, out, stream=None):
+    k, n = g.shape
+    _check("fp8_allreduce_sum",
+           load_library().fp8_allreduce_sum(_ptr(g), k, n, int(fmt), _ptr(amax), _ptr(q), _ptr(scale_inv), _ptr(out),
+                                            _stream(stream)))
+
+
+def allreduce_sum(g, fmt=Format.E5M2, stream=None):
+    """Allocate outputs and run fp8_allreduce_sum on g [k, n] (rank r's gradient in row r).
+
+    Returns (out [n] fp32, q [k, n] u8, scale_inv, amax)."""
+    k, n = g.shape
+    dev = g.device
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
+    q = torch.empty((k, n), dtype=torch.uint8, device=dev)
+    scale_inv = torch.empty(1, dtype=torch.float32, device=dev)
+    out = torch.empty(n, dtype=torch.float32, device=dev)
+    fp8_allreduce_sum(g, fmt, amax, q, scale_inv, out, stream)
+    return out, q, scale_inv, amax
 
 
 def dequantize(q, recipe, fmt, s, stream=None):

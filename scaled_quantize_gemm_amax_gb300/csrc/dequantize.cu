@@ -34,19 +34,6 @@ namespace {
 constexpr int kDqThreads = 256;
 constexpr int kDqUnroll = 4;
 
-// Two FP8 codes (low byte first) -> two binary32 values, exact (via f16x2).
-__device__ __forceinline__ void decode_pair(uint32_t two, bool e5, float& lo, float& hi) {
-  uint32_t h2;
-  const uint16_t t = static_cast<uint16_t>(two);
-  if (e5)
-    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(t));
-  else
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(t));
-  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(h2));
-}
-
 // round-to-odd binary32 of d * m (fast path: the product and its residual are normal)
 __device__ __forceinline__ float mul_odd_fast(float d, float m) {
   const float p = __fmul_rz(d, m);

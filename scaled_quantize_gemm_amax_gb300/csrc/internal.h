@@ -88,6 +88,11 @@ cudaError_t launch_cast_generic(const CastParams& p, const void* x, cudaStream_t
 cudaError_t launch_dequantize(const uint8_t* q, int64_t R, int64_t C, int recipe, bool mx_tiled, bool e5m2,
                               const void* s, void* y, int num_sms, cudaStream_t stream);
 
+// ---- FP8 gradient all-reduce of k ranks held as rows of g [k, n] (allreduce.cu);
+// *amax must hold the global amax when the kernel runs
+cudaError_t launch_allreduce(const void* g, int k, int64_t n, const float* amax, bool e5m2, uint8_t* q,
+                             float* scale_inv, float* out, int num_sms, cudaStream_t s);
+
 // ---- scaled GEMM (gemm.cu)
 struct GemmParams {
   int64_t M, N, K;

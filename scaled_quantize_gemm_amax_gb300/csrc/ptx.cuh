@@ -343,5 +343,18 @@ __device__ __forceinline__ uint32_t cvt_pair_e5m2(float lo, float hi) {
 __device__ __forceinline__ uint32_t cvt_pair(float lo, float hi, bool e5m2) {
   return e5m2 ? cvt_pair_e5m2(lo, hi) : cvt_pair_e4m3(lo, hi);
 }
+// Two FP8 codes (low byte first) -> two binary32 values, exact (through f16x2,
+// which holds every E4M3 and E5M2 value, infinities and NaN included).
+__device__ __forceinline__ void decode_pair(uint32_t two, bool e5m2, float& lo, float& hi) {
+  uint32_t h2;
+  const uint16_t t = static_cast<uint16_t>(two);
+  if (e5m2)
+    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(t));
+  else
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(t));
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+}
 
 }  // namespace fp8q

@@ -152,3 +152,15 @@ def test_dequantize_rejects(lib):
     assert dq(FAKE, 128, 128, T, 0, FAKE, FAKE + 2, None) == ALIGN
     assert dq(FAKE, 128, 128, B1, 0, FAKE + 1, FAKE, None) == ALIGN
     assert dq(FAKE, 0, 128, T, 0, None, None, None) == OK                # empty: no-op
+
+
+def test_allreduce_rejects(lib):
+    ar = lib.fp8_allreduce_sum
+    assert ar(FAKE, 0, 64, 0, FAKE, FAKE, FAKE, FAKE, None) == INVALID        # no ranks
+    assert ar(FAKE, 2, 64, 5, FAKE, FAKE, FAKE, FAKE, None) == INVALID        # bad format
+    assert ar(None, 2, 64, 0, FAKE, FAKE, FAKE, FAKE, None) == INVALID
+    assert ar(FAKE, 2, 60, 0, FAKE, FAKE, FAKE, FAKE, None) == SHAPE          # n % 8
+    assert ar(FAKE + 8, 2, 64, 0, FAKE, FAKE, FAKE, FAKE, None) == ALIGN
+    assert ar(FAKE, 2, 64, 0, FAKE, FAKE + 4, FAKE, FAKE, None) == ALIGN
+    assert ar(FAKE, 2, 64, 0, FAKE, FAKE, FAKE, FAKE + 8, None) == ALIGN
+    assert ar(FAKE, 2, 0, 0, None, None, None, None, None) == OK               # empty: no-op
