@@ -33,8 +33,7 @@ MUTANTS = {
                                "for (int64_t i = 0; i < 1; ++i) {\n                float a"),
     "dequant_1x128_index": ("case 1: m = (double)sf[r * (C / 128) + c / 128]; break;",
                             "case 1: m = (double)sf[(r / 128) * (C / 128) + c / 128]; break;"),
-    "dequant_mx_bias": ("default: m = ldexp(1.0, (int)se[r * (C / 32) + c / 32] - 127); break;",
-                        "default: m = ldexp(1.0, (int)se[r * (C / 32) + c / 32] - 128); break;"),
+    "dequant_mx_bias": ("m = e == 255 ? NAN : ldexp(1.0, e - 127);", "m = e == 255 ? NAN : ldexp(1.0, e - 128);"),
     "allreduce_drops_last_rank": ("for (int32_t r = 0; r < k; ++r) acc = acc +", "for (int32_t r = 0; r < k - 1; ++r) acc = acc +"),
     "allreduce_local_amax": ("const float a = orc_amax_bf16(g, (int64_t)k * n);", "const float a = orc_amax_bf16(g, n);"),
     "bf16_ties_away": ("if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) != 0.0)) n += 1.0;", "if (frac >= 0.5) n += 1.0;"),
