@@ -14,10 +14,12 @@
 // Structure: a persistent grid (one CTA per SM).
 //   warp 0      TMA producer: A / B tiles (128-byte swizzle) into a ring of stages,
 //               plus MX scale atoms by bulk copy
-//   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma (and the scale copies)
+//   warp 1      TMEM allocation; lane 0 issues the tcgen05.mma (and the scale copies)
 //   warps 2..9  epilogue: tcgen05.ld from TMEM,
 //               scale, convert, store.  Warp w reads TMEM lanes 32*(w%4).. (its quarter)
 //               and column slice (w-2)/4 of the tile.
+//   warp 10     (blockwise with 256-deep stages) lane 0 issues the MMAs of each
+//               stage's second partial
 // Every wait is time-bounded (ptx.cuh); a timeout sets the device error word, the
 // other roles see a shared abort flag, and the CTA drains and frees TMEM.
 #include <cuda_bf16.h>
@@ -61,6 +63,15 @@ template <>
 struct Cfg<kBlockK2> {
   static constexpr int BN = 128, STAGES = 3, ACC = 4, EPI = 8, KSUB = 2;
 };
+
+// MMA-issuing threads.  One thread needs about 74 cycles to issue a 256x128x32 MMA
+// (measured by a clock trace), close to the 88 cycles the MMA runs, so with 128-wide
+// tiles a single issuer starves the tensor core once it also waits and commits.  With
+// 256-deep stages the two 128-deep partials of a stage go to different TMEM buffers
+// and need no ordering between them: each gets its own issuing thread (warp 1 and the
+// warp after the epilogue warps), and both commit every stage.
+template <int KIND>
+__host__ __device__ constexpr int issuers_of() { return KIND == kBlockK2 ? 2 : 1; }
 template <>
 struct Cfg<kMx> {
   static constexpr int BN = 256, STAGES = 4, ACC = 1, EPI = 8, KSUB = 1;
@@ -150,9 +161,9 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   tn = r / gsize;
 }
 
-// warps 0 (producer) and 1 (MMA) plus EPI epilogue warps
+// warps 0 (producer) and 1 (MMA), EPI epilogue warps, then the second MMA issuer if any
 template <int KIND>
-constexpr int threads_of() { return 32 * (2 + Cfg<KIND>::EPI); }
+constexpr int threads_of() { return 32 * (2 + Cfg<KIND>::EPI + issuers_of<KIND>() - 1); }
 
 // PAIR: a 2-CTA cluster computes a 256-row tile with the 2-SM MMA (cta_group::2).
 // CTA rank r of the pair loads A rows [128 r, 128 r + 128) and B rows
@@ -178,6 +189,8 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   constexpr bool GATED = BLOCK;
   constexpr bool B_ROWS = (KIND == kBlockRowsB);                         // B scales per row
   constexpr int COLS = BN / (EPI / 4);   // columns of the tile each epilogue thread owns
+  constexpr int NISS = issuers_of<KIND>();
+  static_assert(NISS == 1 || NISS == KSUB, "one issuing thread per partial of a stage");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - smem_u32(smem_raw));
@@ -200,13 +213,13 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     prefetch_tmap(&tm_b);
     for (int s = 0; s < S; ++s) {
       mbar_init(base + L::OFF_FULL + 8 * s, GATED ? 1 + (PAIR ? 2 : 1) * EPI : 1);
-      mbar_init(base + L::OFF_EMPTY + 8 * s, 1);
+      mbar_init(base + L::OFF_EMPTY + 8 * s, NISS);
     }
     for (int a = 0; a < 4; ++a) {
-      mbar_init(base + L::OFF_TFULL + 8 * a, 1);
+      mbar_init(base + L::OFF_TFULL + 8 * a, NISS);
       mbar_init(base + L::OFF_TEMPTY + 8 * a, PAIR ? 2 * EPI : EPI);
     }
-    mbar_init(base + L::OFF_FINAL, 1);
+    mbar_init(base + L::OFF_FINAL, NISS);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -305,11 +318,12 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
                     nullptr);
       }
     }
-  } else if (warp == 1 && lane == 0 && !leader) {
-    // ------------------------------------------------ pair peer: no MMAs; wait for the leader's last one
+  } else if ((warp == 1 || (NISS > 1 && warp == 2 + EPI)) && lane == 0 && !leader) {
+    // ------------------------------------------------ pair peer: no MMAs; wait for the leader's last ones
     mbar_wait(base + L::OFF_FINAL, 0, p.err, kErrTimeoutMma, abort_flag);
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------ MMA issuer
+  } else if ((warp == 1 || (NISS > 1 && warp == 2 + EPI)) && lane == 0) {
+    // ------------------------------------------------ MMA issuer(s)
+    const int my_sub = warp == 1 ? 0 : 1;   // with two issuers: the partial of the stage this thread issues
     uint32_t idesc;
     if (KIND == kMx) {
       idesc = (static_cast<uint32_t>(p.e5m2_a) << 7) | (static_cast<uint32_t>(p.e5m2_b) << 10) |
@@ -391,6 +405,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         } else {
 #pragma unroll
           for (int sub = 0; sub < KSUB; ++sub) {
+            if (NISS > 1 && sub != my_sub) continue;
             const uint32_t dsub = d + (BLOCK ? sub * BN : 0);   // blockwise: one partial per sub-block
 #pragma unroll
             for (int k = 0; k < kBK / kUmmaK; ++k) {
@@ -419,10 +434,11 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         ++acc_it;
       }
     }
-    // every MMA this thread issued has finished before TMEM is released (in both CTAs of a pair)
+    // every MMA this thread issued has finished before TMEM is released (in both CTAs of a
+    // pair); with two issuers the barrier completes once both have committed
     commit(base + L::OFF_FINAL);
     mbar_wait(base + L::OFF_FINAL, 0, p.err, kErrTimeoutMma, nullptr);
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 2 + EPI) {
     // ------------------------------------------------ epilogue
     pdl_wait();   // scales and C: ordered after the previous kernel in the stream
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
