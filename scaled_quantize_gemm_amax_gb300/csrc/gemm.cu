@@ -18,8 +18,9 @@
 //   warps 2..9  epilogue: tcgen05.ld from TMEM,
 //               scale, convert, store.  Warp w reads TMEM lanes 32*(w%4).. (its quarter)
 //               and column slice (w-2)/4 of the tile.
-//   warp 10     (blockwise with 256-deep stages) lane 0 issues the MMAs of each
-//               stage's second partial
+//   blockwise with 256-deep stages: warps 0..3 are the control warpgroup (warp 2's lane
+//               0 issues the MMAs of each stage's second partial) and warps 4..11 the
+//               epilogue, with registers moved from the former to the latter
 // Every wait is time-bounded (ptx.cuh); a timeout sets the device error word, the
 // other roles see a shared abort flag, and the CTA drains and frees TMEM.
 #include <cuda_bf16.h>
@@ -46,11 +47,11 @@ template <int KIND>
 struct Cfg;
 template <>
 struct Cfg<kTensor> {
-  static constexpr int BN = 256, STAGES = 4, ACC = 2, EPI = 8, KSUB = 1;
+  static constexpr int BN = 256, STAGES = 4, ACC = 2, EPI = 8, KSUB = 1, CTRL = 2;
 };
 template <>
 struct Cfg<kBlock1x128> {
-  static constexpr int BN = 128, STAGES = 6, ACC = 4, EPI = 8, KSUB = 1;   // ACC = TMEM partial buffers
+  static constexpr int BN = 128, STAGES = 6, ACC = 4, EPI = 8, KSUB = 1, CTRL = 2;   // ACC = TMEM partial buffers
 };
 template <>
 struct Cfg<kBlockRowsB> : Cfg<kBlock1x128> {};
@@ -61,7 +62,7 @@ struct Cfg<kBlockRowsB> : Cfg<kBlock1x128> {};
 constexpr int kBlockK2 = 5;
 template <>
 struct Cfg<kBlockK2> {
-  static constexpr int BN = 128, STAGES = 3, ACC = 4, EPI = 8, KSUB = 2;
+  static constexpr int BN = 128, STAGES = 3, ACC = 4, EPI = 8, KSUB = 2, CTRL = 4;
 };
 
 // MMA-issuing threads.  One thread needs about 74 cycles to issue a 256x128x32 MMA
@@ -74,8 +75,17 @@ template <int KIND>
 __host__ __device__ constexpr int issuers_of() { return KIND == kBlockK2 ? 2 : 1; }
 template <>
 struct Cfg<kMx> {
-  static constexpr int BN = 256, STAGES = 4, ACC = 1, EPI = 8, KSUB = 1;
+  static constexpr int BN = 256, STAGES = 4, ACC = 1, EPI = 8, KSUB = 1, CTRL = 2;
 };
+
+// CTRL = 4: warps 0..3 (producer, the two MMA issuers, an idle warp) form a warpgroup
+// that gives registers to the two epilogue warpgroups (warps 4..11) with setmaxnreg, so
+// that the promotion can keep a whole 128-deep partial of its columns in flight per
+// TMEM wait.  The kernel must be launched with kSplitLaunchRegs a thread (checked on the
+// host before the first launch: an increase beyond the launch pool is never granted).
+constexpr int kSplitLaunchRegs = 168, kCtrlRegs = 72, kEpiRegs = 216;
+static_assert(128 * kCtrlRegs + 256 * kEpiRegs <= 384 * kSplitLaunchRegs, "register split exceeds the launch pool");
+static_assert(kCtrlRegs + 2 * kEpiRegs <= 512, "register split exceeds a sub-partition");
 
 // Stages of the 2-CTA (pair) variant: each CTA holds 128 rows of A and half of B
 // (blockwise with 256-deep stages: 48 KB a stage).
@@ -161,9 +171,11 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   tn = r / gsize;
 }
 
-// warps 0 (producer) and 1 (MMA), EPI epilogue warps, then the second MMA issuer if any
+// control warps (producer, MMA), EPI epilogue warps, then (CTRL = 2) the second MMA issuer if any
 template <int KIND>
-constexpr int threads_of() { return 32 * (2 + Cfg<KIND>::EPI + issuers_of<KIND>() - 1); }
+constexpr int threads_of() {
+  return 32 * (Cfg<KIND>::CTRL + Cfg<KIND>::EPI + (Cfg<KIND>::CTRL == 2 ? issuers_of<KIND>() - 1 : 0));
+}
 
 // PAIR: a 2-CTA cluster computes a 256-row tile with the 2-SM MMA (cta_group::2).
 // CTA rank r of the pair loads A rows [128 r, 128 r + 128) and B rows
@@ -191,6 +203,10 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   constexpr int COLS = BN / (EPI / 4);   // columns of the tile each epilogue thread owns
   constexpr int NISS = issuers_of<KIND>();
   static_assert(NISS == 1 || NISS == KSUB, "one issuing thread per partial of a stage");
+  constexpr int CTRL = Cfg<KIND>::CTRL;                 // warps before the epilogue warps
+  constexpr int ISS1 = CTRL == 4 ? 2 : 2 + EPI;         // warp of the second MMA issuer
+  constexpr bool WIDE = CTRL == 4;                      // 64-column partial loads (see Cfg)
+  static_assert(!WIDE || (BLOCK && KSUB == 2 && COLS == 64 && !B_ROWS), "wide promotion layout");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - smem_u32(smem_raw));
@@ -239,6 +255,8 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   pdl_launch_dependents();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base_ptr + L::OFF_TMEM);
 
+  if (warp < CTRL || (CTRL == 2 && NISS > 1 && warp == ISS1)) {
+  if constexpr (WIDE) setmaxnreg_dec<kCtrlRegs>();
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------ producer
     pdl_wait();   // operands may come from the previous kernel in the stream
@@ -318,10 +336,10 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
                     nullptr);
       }
     }
-  } else if ((warp == 1 || (NISS > 1 && warp == 2 + EPI)) && lane == 0 && !leader) {
+  } else if ((warp == 1 || (NISS > 1 && warp == ISS1)) && lane == 0 && !leader) {
     // ------------------------------------------------ pair peer: no MMAs; wait for the leader's last ones
     mbar_wait(base + L::OFF_FINAL, 0, p.err, kErrTimeoutMma, abort_flag);
-  } else if ((warp == 1 || (NISS > 1 && warp == 2 + EPI)) && lane == 0) {
+  } else if ((warp == 1 || (NISS > 1 && warp == ISS1)) && lane == 0) {
     // ------------------------------------------------ MMA issuer(s)
     const int my_sub = warp == 1 ? 0 : 1;   // with two issuers: the partial of the stage this thread issues
     uint32_t idesc;
@@ -438,11 +456,13 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     // pair); with two issuers the barrier completes once both have committed
     commit(base + L::OFF_FINAL);
     mbar_wait(base + L::OFF_FINAL, 0, p.err, kErrTimeoutMma, nullptr);
-  } else if (warp >= 2 && warp < 2 + EPI) {
+  }
+  } else if (warp >= CTRL && warp < CTRL + EPI) {
     // ------------------------------------------------ epilogue
+    if constexpr (WIDE) setmaxnreg_inc<kEpiRegs>();
     pdl_wait();   // scales and C: ordered after the previous kernel in the stream
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int h = (warp - 2) >> 2;          // which COLS-wide slice of the tile's columns
+    const int h = (warp - CTRL) >> 2;       // which COLS-wide slice of the tile's columns
     const int row = 32 * q + lane;          // row within the tile
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
     const bool fp32 = p.out_fp32 != 0;
@@ -455,7 +475,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     const float c_scale = want_q ? *p.c_scale : 1.0f;
     const bool e5_c = p.e5m2_c != 0;
     float y_amax = 0.0f;
-    if (want_q && p.c_scale_inv != nullptr && blockIdx.x == 0 && warp == 2 && lane == 0)
+    if (want_q && p.c_scale_inv != nullptr && blockIdx.x == 0 && warp == CTRL && lane == 0)
       *p.c_scale_inv = recip_rn(c_scale);
     // 32 consecutive output values of one row, starting at column gcol
     auto emit = [&](const float (&v)[32], int64_t grow_, int64_t gcol) {
@@ -497,7 +517,79 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
       tile_coords(t, tiles_m, tiles_n, tm, tn);
       const int64_t grow = static_cast<int64_t>(tm) * TM + row_off + row;
       const int64_t gcol0 = static_cast<int64_t>(tn) * BN + h * COLS;
-      if (BLOCK) {
+      if constexpr (WIDE) {
+        // Promotion, one 128-deep partial (this thread's 64 columns: two 32-column
+        // loads) per TMEM wait: while partial 0 of a group is promoted the loads of
+        // partial 1 are in flight, and while partial 1 is promoted those of the next
+        // group's partial 0.  Buffers pa / pb hold the group's two partials.
+        const float* sa_row = static_cast<const float*>(p.sa) + grow * KB;
+        const float* sb_tile = static_cast<const float*>(p.sb) + (gcol0 / 128) * KB;
+        uint64_t acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0;
+        uint32_t pa[2][32], pb[2][32];
+        auto wait_full = [&]() -> bool {
+          const uint32_t g = part_it % GROUPS;
+          // warp-uniform decision: the TMEM loads that follow are .sync.aligned
+          if (!__all_sync(0xFFFFFFFFu,
+                          mbar_wait(base + L::OFF_TFULL + 8 * g, (part_it / GROUPS) & 1u, p.err, kErrTimeoutMma, abort_flag)))
+            return false;
+          tc_fence_after();
+          return true;
+        };
+        auto load64 = [&](int sub, uint32_t (&r)[2][32]) {
+          const uint32_t col = lane_base + ((part_it % GROUPS) * KSUB + sub) * BN + h * COLS;
+          tc_ld_32x32b_x32(col, r[0]);
+          tc_ld_32x32b_x32(col + 32, r[1]);
+        };
+        auto promote64 = [&](const uint32_t (&r)[2][32], float f) {
+          const uint64_t f2 = pack_f32x2(f, f);
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[16 * c + j] = fma_f32x2(f2, pack_f32x2(r[c][2 * j], r[c][2 * j + 1]), acc[16 * c + j]);
+        };
+        // scale factors of the group being promoted and (loads in flight) of the next
+        float sa0 = sa_row[0], sa1 = sa_row[1], sb0 = __ldg(sb_tile), sb1 = __ldg(sb_tile + 1);
+        bool ok = wait_full();
+        if (ok) load64(0, pa);
+        for (int kg = 0; ok && kg < NG; ++kg) {
+          const float f0 = sa0 * sb0, f1 = sa1 * sb1;
+          if (kg + 1 < NG) {
+            sa0 = sa_row[2 * kg + 2];
+            sa1 = sa_row[2 * kg + 3];
+            sb0 = __ldg(sb_tile + 2 * kg + 2);
+            sb1 = __ldg(sb_tile + 2 * kg + 3);
+          }
+          tc_wait_ld(pa[0]);          // partial 0 of this group has landed
+          tc_tie(pa[1]);
+          load64(1, pb);              // partial 1 in flight
+          promote64(pa, f0);
+          tc_wait_ld(pb[0]);          // partial 1 has landed: the group's TMEM is read
+          tc_tie(pb[1]);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            // the stage that reuses this group is GROUPS stages later
+            const uint32_t next = part_it + GROUPS;
+            if (next < total_groups) release(base + L::OFF_FULL + 8 * (next % S));
+          }
+          ++part_it;
+          if (kg + 1 < NG) {
+            ok = wait_full();
+            if (ok) load64(0, pa);    // the next group's partial 0 in flight
+          }
+          promote64(pb, f1);
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int c32 = 0; c32 < 2; ++c32) {
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) unpack_f32x2(acc[16 * c32 + j], v[2 * j], v[2 * j + 1]);
+          if (gcol0 + 32 * c32 < p.N) emit(v, grow, gcol0 + 32 * c32);
+        }
+      } else if (BLOCK) {
         const float* sa_row = static_cast<const float*>(p.sa) + grow * KB;
         const float* sb_blk = static_cast<const float*>(p.sb);
         // Promotion: TMEM loads of CW columns (32, or 16 when a thread owns 128 columns or
@@ -646,6 +738,25 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   }
 }
 
+// A kernel that moves registers between warpgroups must have been given exactly the
+// launch registers the split was sized for (with fewer, an increase would never be
+// granted and the epilogue warps would not start).  Checked once per device.
+template <class K>
+cudaError_t check_split_regs(K kern, bool split, bool (&checked)[kMaxDevices]) {
+  if (!split) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (checked[dev]) return cudaSuccess;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kSplitLaunchRegs) return cudaErrorInvalidConfiguration;
+  checked[dev] = true;
+  return cudaSuccess;
+}
+
 template <int KIND, bool QOUT>
 cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
                         const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s) {
@@ -653,6 +764,9 @@ cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& tm_a, const CUte
   static_assert(L::SMEM <= 232448, "shared memory budget");
   static bool attr_done[kMaxDevices] = {};
   cudaError_t e = ensure_smem_limit(k_gemm<KIND, false, QOUT>, static_cast<int>(L::SMEM), attr_done);
+  if (e != cudaSuccess) return e;
+  static bool regs_checked[kMaxDevices] = {};
+  e = check_split_regs(k_gemm<KIND, false, QOUT>, Cfg<KIND>::CTRL == 4, regs_checked);
   if (e != cudaSuccess) return e;
   const int64_t ntiles = (p.M / kBM) * ((p.N + L::BN - 1) / L::BN);
   const int grid = static_cast<int>(ntiles < num_sms ? ntiles : num_sms);
@@ -669,6 +783,9 @@ cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUte
   auto kern = k_gemm<KIND, true, QOUT>;
   static bool attr_done[kMaxDevices] = {};
   cudaError_t e = ensure_smem_limit(kern, static_cast<int>(L::SMEM), attr_done);
+  if (e != cudaSuccess) return e;
+  static bool regs_checked[kMaxDevices] = {};
+  e = check_split_regs(kern, Cfg<KIND>::CTRL == 4, regs_checked);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];

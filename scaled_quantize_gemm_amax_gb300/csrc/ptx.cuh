@@ -184,6 +184,11 @@ __device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[16]) {
                :
                : "memory");
 }
+// Orders later uses of `r` after a preceding tc_wait_ld (the wait's operands tie only one array).
+__device__ __forceinline__ void tc_tie(uint32_t (&r)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
 __device__ __forceinline__ void tc_ld_32x32b(uint32_t taddr, uint32_t (&r)[32]) { tc_ld_32x32b_x32(taddr, r); }
 __device__ __forceinline__ void tc_ld_32x32b(uint32_t taddr, uint32_t (&r)[16]) { tc_ld_32x32b_x16(taddr, r); }
 
@@ -222,6 +227,19 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // Let the next kernel in the stream be scheduled (it still waits in pdl_wait for
 // this one to complete).
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// ------------------------------------------------------------------ register budget per warpgroup
+// Every thread of the executing warpgroup must issue these together.  An increase
+// waits until the CTA's pool (threads x registers at launch) has room, so the
+// decreases and increases of all warpgroups must sum to at most that pool.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 // ------------------------------------------------------------------ CTA pairs (2-CTA clusters)
 __device__ __forceinline__ uint32_t cluster_ctarank() {
