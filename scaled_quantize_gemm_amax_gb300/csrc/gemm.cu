@@ -72,7 +72,7 @@ struct Cfg<kBlockK2> {
 // and need no ordering between them: each gets its own issuing thread (warp 1 and the
 // warp after the epilogue warps), and both commit every stage.
 template <int KIND>
-__host__ __device__ constexpr int issuers_of() { return KIND == kBlockK2 ? 2 : 1; }
+__host__ __device__ constexpr int issuers_of() { return (KIND == kBlockK2 || KIND == kMx) ? 2 : 1; }
 template <>
 struct Cfg<kMx> {
   static constexpr int BN = 256, STAGES = 4, ACC = 1, EPI = 8, KSUB = 1, CTRL = 2;
@@ -108,7 +108,8 @@ struct Layout {
   static constexpr uint32_t OFF_FULL = OFF_BAR, OFF_EMPTY = OFF_BAR + 8 * S;
   static constexpr uint32_t OFF_TFULL = OFF_EMPTY + 8 * S, OFF_TEMPTY = OFF_TFULL + 32;
   static constexpr uint32_t OFF_FINAL = OFF_TEMPTY + 32;
-  static constexpr uint32_t OFF_TMEM = OFF_FINAL + 8, OFF_ABORT = OFF_TMEM + 4;
+  static constexpr uint32_t OFF_SFR = OFF_FINAL + 8;   // MX: a stage's scale factors are in TMEM
+  static constexpr uint32_t OFF_TMEM = OFF_SFR + 8 * S, OFF_ABORT = OFF_TMEM + 4;
   static constexpr uint32_t SMEM = OFF_ABORT + 64 + 1024;   // + alignment slack
   // bytes one stage's full barrier expects (in a pair: the leader's barrier sees both CTAs' loads)
   static constexpr uint32_t TX_BYTES = PAIR ? 2 * (STAGE_BYTES + SF_BYTES) : STAGE_BYTES + SF_BYTES;
@@ -202,7 +203,10 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   constexpr bool B_ROWS = (KIND == kBlockRowsB);                         // B scales per row
   constexpr int COLS = BN / (EPI / 4);   // columns of the tile each epilogue thread owns
   constexpr int NISS = issuers_of<KIND>();
-  static_assert(NISS == 1 || NISS == KSUB, "one issuing thread per partial of a stage");
+  // MX with two issuers: the second thread copies each stage's scale factors into TMEM
+  // (tcgen05.cp) and signals the MMA thread, which then only issues MMAs
+  constexpr bool SFCP = KIND == kMx && NISS > 1;
+  static_assert(NISS == 1 || NISS == KSUB || SFCP, "MMA issuers");
   constexpr int CTRL = Cfg<KIND>::CTRL;                 // warps before the epilogue warps
   constexpr int ISS1 = CTRL == 4 ? 2 : 2 + EPI;         // warp of the second MMA issuer
   constexpr bool WIDE = CTRL == 4;                      // 64-column partial loads (see Cfg)
@@ -229,10 +233,11 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     prefetch_tmap(&tm_b);
     for (int s = 0; s < S; ++s) {
       mbar_init(base + L::OFF_FULL + 8 * s, GATED ? 1 + (PAIR ? 2 : 1) * EPI : 1);
-      mbar_init(base + L::OFF_EMPTY + 8 * s, NISS);
+      mbar_init(base + L::OFF_EMPTY + 8 * s, SFCP ? 1 : NISS);
+      mbar_init(base + L::OFF_SFR + 8 * s, 1);
     }
     for (int a = 0; a < 4; ++a) {
-      mbar_init(base + L::OFF_TFULL + 8 * a, NISS);
+      mbar_init(base + L::OFF_TFULL + 8 * a, SFCP ? 1 : NISS);
       mbar_init(base + L::OFF_TEMPTY + 8 * a, PAIR ? 2 * EPI : EPI);
     }
     mbar_init(base + L::OFF_FINAL, NISS);
@@ -339,6 +344,47 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   } else if ((warp == 1 || (NISS > 1 && warp == ISS1)) && lane == 0 && !leader) {
     // ------------------------------------------------ pair peer: no MMAs; wait for the leader's last ones
     mbar_wait(base + L::OFF_FINAL, 0, p.err, kErrTimeoutMma, abort_flag);
+  } else if (SFCP && warp == ISS1 && lane == 0) {
+    // ------------------------------------------------ MX scale-factor copies (leader)
+    auto commit_sfr = [&](uint32_t bar) {
+      if (PAIR) tc_commit_pair_mc(bar, 1);   // the leader's MMA thread waits on it
+      else tc_commit(bar);
+    };
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = unit0; t < ntiles && ok; t += units) {
+      for (int kg = 0; kg < NG; ++kg) {
+        if (!mbar_wait(base + L::OFF_FULL + 8 * stage, phase, p.err, kErrTimeoutTmaLoad, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // the slot of this stage was last read by the MMAs of the stage's previous use,
+        // which finished before the producer could refill the stage (and so before the
+        // wait above returned)
+        const uint32_t sf = base + L::OFF_SF + stage * L::SF_BYTES;
+        const uint32_t sf_col = 256u + static_cast<uint32_t>(stage) * (4u + 4u * (BN / 128));
+        if (PAIR) {
+          tc_cp_32x128b_warpx4_pair(tmem + sf_col, sdesc_rows16(sf));
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)
+            tc_cp_32x128b_warpx4_pair(tmem + sf_col + 4 + 4 * h, sdesc_rows16(sf + 512 + 512 * h));
+        } else {
+          tc_cp_32x128b_warpx4(tmem + sf_col, sdesc_rows16(sf));
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h) tc_cp_32x128b_warpx4(tmem + sf_col + 4 + 4 * h, sdesc_rows16(sf + 512 + 512 * h));
+        }
+        commit_sfr(base + L::OFF_SFR + 8 * stage);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (PAIR) tc_commit_pair_mc(base + L::OFF_FINAL, 3);
+    else tc_commit(base + L::OFF_FINAL);
+    mbar_wait(base + L::OFF_FINAL, 0, p.err, kErrTimeoutMma, nullptr);
   } else if ((warp == 1 || (NISS > 1 && warp == ISS1)) && lane == 0) {
     // ------------------------------------------------ MMA issuer(s)
     const int my_sub = warp == 1 ? 0 : 1;   // with two issuers: the partial of the stage this thread issues
@@ -387,7 +433,9 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           }   // gated: the full-barrier wait below also covers the group's release
           d = tmem + pb * KSUB * BN;
         }
-        if (!mbar_wait(base + L::OFF_FULL + 8 * stage, phase, p.err, kErrTimeoutTmaLoad, abort_flag)) {
+        // MX with a copying thread: its signal implies the stage's data and scale factors
+        if (!mbar_wait(base + (SFCP ? L::OFF_SFR : L::OFF_FULL) + 8 * stage, phase, p.err, kErrTimeoutTmaLoad,
+                       abort_flag)) {
           ok = false;
           break;
         }
@@ -398,10 +446,12 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           // each CTA's atoms go to the same TMEM columns of its own TMEM
           const uint32_t sf = base + L::OFF_SF + stage * L::SF_BYTES;
           const uint32_t sf_col = 256u + static_cast<uint32_t>(stage) * (4u + 4u * (BN / 128));
-          tc_cp_32x128b_warpx4_pair(tmem + sf_col, sdesc_rows16(sf));
+          if (!SFCP) {
+            tc_cp_32x128b_warpx4_pair(tmem + sf_col, sdesc_rows16(sf));
 #pragma unroll
-          for (int h = 0; h < BN / 128; ++h)
-            tc_cp_32x128b_warpx4_pair(tmem + sf_col + 4 + 4 * h, sdesc_rows16(sf + 512 + 512 * h));
+            for (int h = 0; h < BN / 128; ++h)
+              tc_cp_32x128b_warpx4_pair(tmem + sf_col + 4 + 4 * h, sdesc_rows16(sf + 512 + 512 * h));
+          }
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             const uint32_t id = idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
@@ -411,9 +461,12 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         } else if (KIND == kMx) {
           const uint32_t sf = base + L::OFF_SF + stage * L::SF_BYTES;
           const uint32_t sf_col = 256u + static_cast<uint32_t>(stage) * (4u + 4u * (BN / 128));
-          tc_cp_32x128b_warpx4(tmem + sf_col, sdesc_rows16(sf));
+          if (!SFCP) {
+            tc_cp_32x128b_warpx4(tmem + sf_col, sdesc_rows16(sf));
 #pragma unroll
-          for (int h = 0; h < BN / 128; ++h) tc_cp_32x128b_warpx4(tmem + sf_col + 4 + 4 * h, sdesc_rows16(sf + 512 + 512 * h));
+            for (int h = 0; h < BN / 128; ++h)
+              tc_cp_32x128b_warpx4(tmem + sf_col + 4 + 4 * h, sdesc_rows16(sf + 512 + 512 * h));
+          }
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             const uint32_t id = idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
