@@ -199,6 +199,26 @@ fp8_status fp8_allreduce_sum(const void* g, int32_t k, int64_t n, fp8_format fmt
                              float* scale_inv, float* out, cudaStream_t stream);
 
 /*
+ * fp8_allreduce_sum_noalloc -- fp8_allreduce_sum without its amax argument: the
+ * per-rank and global amaxes live in scratch the library owns, so a caller that
+ * cannot provide device memory beyond the buffers it reduces (a gradient-reduction
+ * hook in a runtime without a device allocator of its own, or a process whose
+ * device memory a caching allocator has reserved in full) needs none.  The pages
+ * have no counterpart; results are bit-identical to fp8_allreduce_sum's (the
+ * maximum is exact and order-free).
+ *   g, k, n, fmt, q, scale_inv, out   as fp8_allreduce_sum
+ * Scratch: a file-scope device array of 1025 floats (4 KB) per device, one amax
+ * per rank and the global one, so k <= 1024 (FP8_ERR_SHAPE beyond).  Nothing in
+ * it has to start at zero: each call clears the slots it uses first.  All calls on
+ * a device share it: calls whose executions overlap (other streams, other host
+ * threads) race and must be ordered by the caller.  The first call on a device
+ * looks up the scratch address (cudaGetSymbolAddress, with that device current)
+ * and keeps it; make that first call before any stream capture.
+ */
+fp8_status fp8_allreduce_sum_noalloc(const void* g, int32_t k, int64_t n, fp8_format fmt, uint8_t* q, float* scale_inv,
+                                     float* out, cudaStream_t stream);
+
+/*
  * fp8_scaled_gemm -- C = deq(A) . deq(B)^T with FP32 accumulation.
  * Search-result page, dataflow paragraph (FP8 inputs, FP32 accumulation, BF16
  * output; wgrad output FP32); guide, "code changes" (the three GEMMs of a layer

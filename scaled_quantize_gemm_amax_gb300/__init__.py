@@ -26,7 +26,7 @@ import torch
 __all__ = [
     "Status", "Format", "Recipe", "OutDtype", "FP8Error", "lib_path", "load_library",
     "fp8_amax", "fp8_compute_scale", "amax_history_update", "fp8_quantize", "fp8_cast_transpose",
-    "fp8_dequantize", "fp8_allreduce_sum", "fp8_scaled_gemm", "fp8_scaled_gemm_amax", "fp8_get_device_status",
+    "fp8_dequantize", "fp8_allreduce_sum", "fp8_allreduce_sum_noalloc", "fp8_scaled_gemm", "fp8_scaled_gemm_amax", "fp8_get_device_status",
     "fp8_debug_wait_timeout", "fp8_status_string",
     "scale_shape", "cast_transpose", "dequantize", "allreduce_sum", "scaled_gemm", "scaled_gemm_amax",
     "DelayedScaling",
@@ -89,6 +89,7 @@ _SIGNATURES = {
     "fp8_quantize": [_P, _I64, _I64, _E, _E, _P, _P, _P, _P, _P],
     "fp8_dequantize": [_P, _I64, _I64, _E, _E, _P, _P, _P],
     "fp8_allreduce_sum": [_P, _I32, _I64, _E, _P, _P, _P, _P, _P],
+    "fp8_allreduce_sum_noalloc": [_P, _I32, _I64, _E, _P, _P, _P, _P],
     "fp8_scaled_gemm": [_P, _E, _E, _P, _P, _E, _E, _P, _I64, _I64, _I64, _P, _E, _P],
     "fp8_scaled_gemm_amax": [_P, _E, _E, _P, _P, _E, _E, _P, _I64, _I64, _I64, _P, _E, _P, _P, _E, _P, _P, _P],
     "fp8_get_device_status": [_P],
@@ -185,6 +186,13 @@ def fp8_allreduce_sum(g, fmt, amax, q, scale_inv, out, stream=None):
     _check("fp8_allreduce_sum",
            load_library().fp8_allreduce_sum(_ptr(g), k, n, int(fmt), _ptr(amax), _ptr(q), _ptr(scale_inv), _ptr(out),
                                             _stream(stream)))
+
+
+def fp8_allreduce_sum_noalloc(g, fmt, q, scale_inv, out, stream=None):
+    k, n = g.shape
+    _check("fp8_allreduce_sum_noalloc",
+           load_library().fp8_allreduce_sum_noalloc(_ptr(g), k, n, int(fmt), _ptr(q), _ptr(scale_inv), _ptr(out),
+                                                    _stream(stream)))
 
 
 def allreduce_sum(g, fmt=Format.E5M2, stream=None):

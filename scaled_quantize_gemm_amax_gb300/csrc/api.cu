@@ -366,6 +366,17 @@ fp8_status fp8_allreduce_sum(const void* g, int32_t k, int64_t n, fp8_format fmt
   return cuda_status(launch_allreduce(g, k, n, amax, fmt == FP8_E5M2, q, scale_inv, out, d->num_sms, stream));
 }
 
+fp8_status fp8_allreduce_sum_noalloc(const void* g, int32_t k, int64_t n, fp8_format fmt, uint8_t* q, float* scale_inv,
+                                     float* out, cudaStream_t stream) {
+  if (k < 1 || n < 0 || !valid_fmt(fmt)) return FP8_ERR_INVALID_ARG;
+  if (k > noalloc_max_ranks()) return FP8_ERR_SHAPE;   // more ranks than the scratch has slots
+  if (n == 0) return FP8_OK;
+  if (g == nullptr || q == nullptr || scale_inv == nullptr || out == nullptr) return FP8_ERR_INVALID_ARG;
+  if (n % 8 || n > kMaxDim) return FP8_ERR_SHAPE;
+  if (!aligned(g, 16) || !aligned(out, 16) || !aligned(q, 8) || !aligned(scale_inv, 4)) return FP8_ERR_ALIGNMENT;
+  return cuda_status(launch_allreduce_noalloc(g, k, n, fmt == FP8_E5M2, q, scale_inv, out, stream));
+}
+
 fp8_status fp8_scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const void* sA, const uint8_t* B,
                            fp8_format fb, fp8_recipe rb, const void* sB, int64_t M, int64_t N, int64_t K, void* C,
                            fp8_out_dtype out, cudaStream_t stream) {

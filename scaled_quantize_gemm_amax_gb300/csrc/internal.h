@@ -93,6 +93,11 @@ cudaError_t launch_dequantize(const uint8_t* q, int64_t R, int64_t C, int recipe
 cudaError_t launch_allreduce(const void* g, int k, int64_t n, const float* amax, bool e5m2, uint8_t* q,
                              float* scale_inv, float* out, int num_sms, cudaStream_t s);
 
+// ---- the all-reduce with its amax in library-owned scratch (noalloc.cu)
+int noalloc_max_ranks();
+cudaError_t launch_allreduce_noalloc(const void* g, int k, int64_t n, bool e5m2, uint8_t* q, float* scale_inv,
+                                     float* out, cudaStream_t s);
+
 // ---- scaled GEMM (gemm.cu)
 struct GemmParams {
   int64_t M, N, K;

@@ -164,3 +164,13 @@ def test_allreduce_rejects(lib):
     assert ar(FAKE, 2, 64, 0, FAKE, FAKE + 4, FAKE, FAKE, None) == ALIGN
     assert ar(FAKE, 2, 64, 0, FAKE, FAKE, FAKE, FAKE + 8, None) == ALIGN
     assert ar(FAKE, 2, 0, 0, None, None, None, None, None) == OK               # empty: no-op
+
+
+def test_allreduce_noalloc_rejects(lib):
+    ar = lib.fp8_allreduce_sum_noalloc
+    assert ar(FAKE, 1025, 64, 0, FAKE, FAKE, FAKE, None) == SHAPE       # more ranks than the scratch holds
+    assert ar(FAKE, 0, 64, 0, FAKE, FAKE, FAKE, None) == INVALID
+    assert ar(FAKE, 2, 64, 3, FAKE, FAKE, FAKE, None) == INVALID        # bad format
+    assert ar(FAKE, 2, 60, 0, FAKE, FAKE, FAKE, None) == SHAPE          # n % 8
+    assert ar(FAKE + 8, 2, 64, 0, FAKE, FAKE, FAKE, None) == ALIGN
+    assert ar(FAKE, 2, 0, 0, None, None, None, None) == OK               # empty: no-op

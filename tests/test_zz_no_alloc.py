@@ -1,0 +1,55 @@
+"""fp8_allreduce_sum_noalloc (amax in library-owned scratch) against
+fp8_allreduce_sum (amax in a caller buffer): two calls in a row with different
+inputs, every output equal bit for bit.  Kept in the last-collected file so that it
+runs after everything else in a full session, and it passes alone too."""
+import numpy as np
+import pytest
+import torch
+
+import scaled_quantize_gemm_amax_gb300 as fq
+from gpu_util import F, assert_status_ok, host, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def grads(k, n, seed, sigma):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    x = torch.randn((k, n), generator=g, device="cuda") * sigma
+    x *= torch.logspace(-3, 0, k, device="cuda")[:, None]
+    return x.to(torch.bfloat16)
+
+
+def noalloc(g, fmt):
+    k, n = g.shape
+    q = torch.empty((k, n), dtype=torch.uint8, device="cuda")
+    si = torch.empty(1, dtype=torch.float32, device="cuda")
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    fq.fp8_allreduce_sum_noalloc(g, fmt, q, si, out)
+    return out, q, si
+
+
+def test_noalloc_matches_allreduce_sum_two_calls_in_a_row():
+    # the second call has fewer ranks and a smaller amax: leftovers in the scratch
+    # from the first call would show up as a wrong scale
+    cases = [(grads(8, 65536, 11, 10.0), F.E5M2), (grads(3, 4096, 12, 1e-3), F.E4M3)]
+    for g, fmt in cases:
+        out_ref, q_ref, si_ref, _ = fq.allreduce_sum(g, fmt)
+        out, q, si = noalloc(g, fmt)
+        torch.cuda.synchronize()
+        assert_status_ok()
+        assert torch.equal(q, q_ref)
+        assert np.array_equal(host(si).view(np.uint32), host(si_ref).view(np.uint32))
+        assert np.array_equal(host(out).view(np.uint32), host(out_ref).view(np.uint32))
+
+
+def test_noalloc_rejects_more_ranks_than_its_scratch():
+    g = torch.zeros((1025, 8), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fq.FP8Error) as e:
+        noalloc(g, F.E4M3)
+    assert e.value.status == fq.Status.ERR_SHAPE
