@@ -152,6 +152,33 @@ fp8_status fp8_cast_transpose(const void* x, int64_t rows, int64_t cols, fp8_rec
                               void* s_col, cudaStream_t stream);
 
 /*
+ * fp8_cast_transpose_multi -- several fp8_cast_transpose calls in one launch (e.g.
+ * the activation and the weight of a layer, each with its own recipe): the tiles
+ * of all jobs are spread over one persistent grid, so the fixed cost of a launch
+ * (the first loads, the last stores) is paid once.  Same results as calling
+ * fp8_cast_transpose on each job in order.  Guide, "tensor-level scaling",
+ * "block-level scaling", "MXFP8 scaling" (as fp8_cast_transpose).
+ *   jobs    host array of n_jobs descriptions; each field as the argument of the
+ *           same name of fp8_cast_transpose
+ *   n_jobs  0..4 (FP8_ERR_INVALID_ARG beyond)
+ * Every job is checked (as fp8_cast_transpose checks its arguments) before any
+ * device work; the first failing job's status is returned.
+ */
+typedef struct fp8_cast_job {
+  const void* x;
+  int64_t rows, cols;
+  fp8_recipe recipe;
+  fp8_format fmt;
+  const float* scale;
+  float* amax_out;
+  uint8_t* q_row;
+  void* s_row;
+  uint8_t* q_col;
+  void* s_col;
+} fp8_cast_job;
+fp8_status fp8_cast_transpose_multi(const fp8_cast_job* jobs, int32_t n_jobs, cudaStream_t stream);
+
+/*
  * fp8_quantize -- the row-wise copy only: fp8_cast_transpose with q_col = NULL.
  */
 fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,

@@ -8,7 +8,7 @@ output tensors with torch.  There is no fallback: every call raises when
 
 Entry points with the C names take tensors (or None for NULL) and raise
 ``FP8Error`` on a non-OK status: ``fp8_amax``, ``fp8_compute_scale``,
-``amax_history_update``, ``fp8_quantize``, ``fp8_cast_transpose``,
+``amax_history_update``, ``fp8_quantize``, ``fp8_cast_transpose``, ``fp8_cast_transpose_multi``,
 ``fp8_dequantize``, ``fp8_allreduce_sum``, ``fp8_scaled_gemm``, ``fp8_scaled_gemm_amax``,
 ``fp8_get_device_status``, ``fp8_debug_wait_timeout``.  ``cast_transpose`` /
 ``dequantize`` / ``scaled_gemm`` / ``scaled_gemm_amax`` are allocation helpers
@@ -26,9 +26,10 @@ import torch
 __all__ = [
     "Status", "Format", "Recipe", "OutDtype", "FP8Error", "lib_path", "load_library",
     "fp8_amax", "fp8_compute_scale", "amax_history_update", "fp8_quantize", "fp8_cast_transpose",
+    "fp8_cast_transpose_multi", "CastJob",
     "fp8_dequantize", "fp8_allreduce_sum", "fp8_allreduce_sum_noalloc", "fp8_scaled_gemm", "fp8_scaled_gemm_amax", "fp8_get_device_status",
     "fp8_debug_wait_timeout", "fp8_status_string",
-    "scale_shape", "cast_transpose", "dequantize", "allreduce_sum", "scaled_gemm", "scaled_gemm_amax",
+    "scale_shape", "cast_transpose", "cast_transpose_multi", "dequantize", "allreduce_sum", "scaled_gemm", "scaled_gemm_amax",
     "DelayedScaling",
 ]
 
@@ -81,12 +82,21 @@ _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 _I32 = ctypes.c_int32
 _E = ctypes.c_int
+class CastJob(ctypes.Structure):
+    """C layout of fp8_cast_job."""
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("recipe", ctypes.c_int), ("fmt", ctypes.c_int), ("scale", ctypes.c_void_p),
+                ("amax_out", ctypes.c_void_p), ("q_row", ctypes.c_void_p), ("s_row", ctypes.c_void_p),
+                ("q_col", ctypes.c_void_p), ("s_col", ctypes.c_void_p)]
+
+
 _SIGNATURES = {
     "fp8_amax": [_P, _I64, _I64, _P, _P],
     "fp8_compute_scale": [_P, _E, _P, _P, _P],
     "amax_history_update": [_P, _I32, _P, _P, _E, _P, _P, _P],
     "fp8_cast_transpose": [_P, _I64, _I64, _E, _E, _P, _P, _P, _P, _P, _P, _P],
     "fp8_quantize": [_P, _I64, _I64, _E, _E, _P, _P, _P, _P, _P],
+    "fp8_cast_transpose_multi": [_P, _I32, _P],
     "fp8_dequantize": [_P, _I64, _I64, _E, _E, _P, _P, _P],
     "fp8_allreduce_sum": [_P, _I32, _I64, _E, _P, _P, _P, _P, _P],
     "fp8_allreduce_sum_noalloc": [_P, _I32, _I64, _E, _P, _P, _P, _P],
@@ -165,6 +175,17 @@ def fp8_cast_transpose(x, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_c
            load_library().fp8_cast_transpose(_ptr(x), rows, cols, int(recipe), int(fmt), _ptr(scale),
                                              _ptr(amax_out), _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col),
                                              _stream(stream)))
+
+
+def fp8_cast_transpose_multi(jobs, stream=None):
+    """jobs: sequence of (x, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_col), as fp8_cast_transpose."""
+    arr = (CastJob * max(len(jobs), 1))()
+    for i, (x, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_col) in enumerate(jobs):
+        rows, cols = x.shape
+        arr[i] = CastJob(_ptr(x), rows, cols, int(recipe), int(fmt), _ptr(scale), _ptr(amax_out), _ptr(q_row),
+                         _ptr(s_row), _ptr(q_col), _ptr(s_col))
+    _check("fp8_cast_transpose_multi",
+           load_library().fp8_cast_transpose_multi(ctypes.cast(arr, ctypes.c_void_p), len(jobs), _stream(stream)))
 
 
 def fp8_quantize(x, recipe, fmt, scale, amax_out, q, s, stream=None):
@@ -274,6 +295,26 @@ def cast_transpose(x, recipe, fmt, scale=None, amax_out=None, row=True, col=True
         s_col = torch.empty(shp, dtype=dt, device=dev)
     fp8_cast_transpose(x, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_col, stream)
     return q_row, s_row, q_col, s_col
+
+
+def cast_transpose_multi(specs, stream=None):
+    """specs: sequence of (x, recipe, fmt, scale, amax_out).  Allocates every job's outputs
+    with torch and runs them in one fp8_cast_transpose_multi launch; returns a list of
+    (q_row, s_row, q_col, s_col) per job."""
+    outs, jobs = [], []
+    for x, recipe, fmt, scale, amax_out in specs:
+        rows, cols = x.shape
+        dev = x.device
+        q_row = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+        shp, dt = scale_shape(recipe, rows, cols)
+        s_row = torch.empty(shp, dtype=dt, device=dev)
+        q_col = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+        shp, dt = scale_shape(recipe, cols, rows)
+        s_col = torch.empty(shp, dtype=dt, device=dev)
+        outs.append((q_row, s_row, q_col, s_col))
+        jobs.append((x, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_col))
+    fp8_cast_transpose_multi(jobs, stream)
+    return outs
 
 
 def scaled_gemm(a, fa, ra, sa, b, fb, rb, sb, out=OutDtype.BF16, stream=None):

@@ -83,6 +83,85 @@ using namespace fp8q;
 
 namespace {
 
+// Validation and launch parameters of one cast; no device work.  fp8_cast_transpose and
+// every job of fp8_cast_transpose_multi go through the same checks.
+struct CastPlan {
+  bool empty = false;   // no elements: nothing to launch
+  bool tiled = false;   // the TMA path (else the plain per-tensor path)
+  CastParams p{};
+  CUtensorMap tm_x, tm_qr, tm_qc;
+};
+
+fp8_status plan_cast(const void* x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt, const float* scale,
+                     float* amax_out, uint8_t* q_row, void* s_row, uint8_t* q_col, void* s_col, CastPlan* plan) {
+  if (rows < 0 || cols < 0 || !valid_fmt(fmt) || recipe < FP8_TENSOR || recipe > FP8_MX_1x32_TILED)
+    return FP8_ERR_INVALID_ARG;
+  if (rows * cols == 0) {
+    if (!aligned(amax_out, 4)) return FP8_ERR_ALIGNMENT;
+    plan->empty = true;
+    return FP8_OK;
+  }
+  const bool do_row = q_row != nullptr, do_col = q_col != nullptr;
+  if (!do_row && !do_col) return FP8_ERR_INVALID_ARG;
+  if (x == nullptr) return FP8_ERR_INVALID_ARG;
+  const bool mx = recipe == FP8_MX_1x32 || recipe == FP8_MX_1x32_TILED;
+  if (recipe == FP8_TENSOR) {
+    if (scale == nullptr) return FP8_ERR_INVALID_ARG;
+  } else {
+    if ((do_row && s_row == nullptr) || (do_col && s_col == nullptr)) return FP8_ERR_INVALID_ARG;
+  }
+  // blocked dimensions
+  switch (recipe) {
+    case FP8_BLOCK_1x128:
+      if ((do_row && cols % 128) || (do_col && rows % 128)) return FP8_ERR_SHAPE;
+      break;
+    case FP8_BLOCK_128x128:
+      if (rows % 128 || cols % 128) return FP8_ERR_SHAPE;
+      break;
+    case FP8_MX_1x32:
+      if ((do_row && cols % 32) || (do_col && rows % 32)) return FP8_ERR_SHAPE;
+      break;
+    case FP8_MX_1x32_TILED:
+      if (rows % 128 || cols % 128) return FP8_ERR_SHAPE;
+      break;
+    default:
+      break;
+  }
+  if (rows > kMaxDim || cols > kMaxDim) return FP8_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(q_row, 16) || !aligned(q_col, 16)) return FP8_ERR_ALIGNMENT;
+  if (!mx && (!aligned(s_row, 4) || !aligned(s_col, 4))) return FP8_ERR_ALIGNMENT;
+  if (recipe == FP8_MX_1x32_TILED && (!aligned(s_row, 16) || !aligned(s_col, 16))) return FP8_ERR_ALIGNMENT;
+  if (!aligned(scale, 4) || !aligned(amax_out, 4)) return FP8_ERR_ALIGNMENT;
+
+  CastParams& p = plan->p;
+  p.R = rows;
+  p.C = cols;
+  p.recipe = mx ? kMx : static_cast<int>(recipe);
+  p.e5m2 = fmt == FP8_E5M2;
+  p.mx_tiled = recipe == FP8_MX_1x32_TILED;
+  p.do_row = do_row;
+  p.do_col = do_col;
+  p.scale = scale;
+  p.amax_out = amax_out;
+  p.q_row = q_row;
+  p.q_col = q_col;
+  p.s_row = s_row;
+  p.s_col = s_col;
+  p.tiles_r = static_cast<int>((rows + 127) / 128);
+  p.tiles_c = static_cast<int>((cols + 127) / 128);
+  plan->tiled = (cols % 16 == 0) && (!do_col || rows % 16 == 0);
+  if (plan->tiled) {
+    std::memset(&plan->tm_qr, 0, sizeof(plan->tm_qr));
+    std::memset(&plan->tm_qc, 0, sizeof(plan->tm_qc));
+    if (!make_map(&plan->tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, cols, rows, 64, 128)) return FP8_ERR_CUDA;
+    if (do_row && !make_map(&plan->tm_qr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q_row, cols, rows, 128, 128))
+      return FP8_ERR_CUDA;
+    if (do_col && !make_map(&plan->tm_qc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q_col, rows, cols, 128, 128))
+      return FP8_ERR_CUDA;
+  }
+  return FP8_OK;
+}
+
 // Optional outputs of the fused epilogue (all null for the plain GEMM).
 struct GemmExtra {
   float* c_amax = nullptr;
@@ -234,82 +313,57 @@ fp8_status amax_history_update(float* hist, int32_t len, int32_t* pos, const flo
 fp8_status fp8_cast_transpose(const void* x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
                               const float* scale, float* amax_out, uint8_t* q_row, void* s_row, uint8_t* q_col,
                               void* s_col, cudaStream_t stream) {
-  if (rows < 0 || cols < 0 || !valid_fmt(fmt) || recipe < FP8_TENSOR || recipe > FP8_MX_1x32_TILED)
-    return FP8_ERR_INVALID_ARG;
-  const int64_t n = rows * cols;
-  if (n == 0) {
+  CastPlan plan;
+  if (fp8_status st = plan_cast(x, rows, cols, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_col, &plan))
+    return st;
+  if (plan.empty) {
     // nothing to cast (outputs of an empty tensor may be NULL); amax of nothing is 0
-    if (!aligned(amax_out, 4)) return FP8_ERR_ALIGNMENT;
     if (amax_out != nullptr && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess)
       return FP8_ERR_CUDA;
     return FP8_OK;
   }
-  const bool do_row = q_row != nullptr, do_col = q_col != nullptr;
-  if (!do_row && !do_col) return FP8_ERR_INVALID_ARG;
-  if (x == nullptr) return FP8_ERR_INVALID_ARG;
-  const bool mx = recipe == FP8_MX_1x32 || recipe == FP8_MX_1x32_TILED;
-  if (recipe == FP8_TENSOR) {
-    if (scale == nullptr) return FP8_ERR_INVALID_ARG;
-  } else {
-    if ((do_row && s_row == nullptr) || (do_col && s_col == nullptr)) return FP8_ERR_INVALID_ARG;
-  }
-  // blocked dimensions
-  switch (recipe) {
-    case FP8_BLOCK_1x128:
-      if ((do_row && cols % 128) || (do_col && rows % 128)) return FP8_ERR_SHAPE;
-      break;
-    case FP8_BLOCK_128x128:
-      if (rows % 128 || cols % 128) return FP8_ERR_SHAPE;
-      break;
-    case FP8_MX_1x32:
-      if ((do_row && cols % 32) || (do_col && rows % 32)) return FP8_ERR_SHAPE;
-      break;
-    case FP8_MX_1x32_TILED:
-      if (rows % 128 || cols % 128) return FP8_ERR_SHAPE;
-      break;
-    default:
-      break;
-  }
-  if (rows > kMaxDim || cols > kMaxDim) return FP8_ERR_SHAPE;
-  if (!aligned(x, 16) || !aligned(q_row, 16) || !aligned(q_col, 16)) return FP8_ERR_ALIGNMENT;
-  if (!mx && (!aligned(s_row, 4) || !aligned(s_col, 4))) return FP8_ERR_ALIGNMENT;
-  if (recipe == FP8_MX_1x32_TILED && (!aligned(s_row, 16) || !aligned(s_col, 16))) return FP8_ERR_ALIGNMENT;
-  if (!aligned(scale, 4) || !aligned(amax_out, 4)) return FP8_ERR_ALIGNMENT;
-
   DeviceInfo* d;
   if (fp8_status st = device_info(&d)) return st;
   if (amax_out != nullptr && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess) return FP8_ERR_CUDA;
+  plan.p.err = d->err;
+  // only the per-tensor recipe can miss the tiled path (block recipes imply its alignment)
+  if (!plan.tiled) return cuda_status(launch_cast_generic(plan.p, x, stream));
+  return cuda_status(launch_cast_transpose_tiled(plan.p, plan.tm_x, plan.tm_qr, plan.tm_qc, d->num_sms, stream));
+}
 
-  CastParams p{};
-  p.R = rows;
-  p.C = cols;
-  p.recipe = mx ? kMx : static_cast<int>(recipe);
-  p.e5m2 = fmt == FP8_E5M2;
-  p.mx_tiled = recipe == FP8_MX_1x32_TILED;
-  p.do_row = do_row;
-  p.do_col = do_col;
-  p.scale = scale;
-  p.amax_out = amax_out;
-  p.q_row = q_row;
-  p.q_col = q_col;
-  p.s_row = s_row;
-  p.s_col = s_col;
-  p.err = d->err;
-  p.tiles_r = static_cast<int>((rows + 127) / 128);
-  p.tiles_c = static_cast<int>((cols + 127) / 128);
-
-  const bool tiled_ok = (cols % 16 == 0) && (!do_col || rows % 16 == 0);
-  if (!tiled_ok) {
-    // only the per-tensor recipe reaches here (block recipes imply the alignment)
-    return cuda_status(launch_cast_generic(p, x, stream));
+fp8_status fp8_cast_transpose_multi(const fp8_cast_job* jobs, int32_t n_jobs, cudaStream_t stream) {
+  if (n_jobs < 0 || n_jobs > kMaxCastJobs || (n_jobs > 0 && jobs == nullptr)) return FP8_ERR_INVALID_ARG;
+  CastPlan plans[kMaxCastJobs];
+  // every job is checked before any device work
+  for (int i = 0; i < n_jobs; ++i) {
+    const fp8_cast_job& j = jobs[i];
+    if (fp8_status st = plan_cast(j.x, j.rows, j.cols, j.recipe, j.fmt, j.scale, j.amax_out, j.q_row, j.s_row, j.q_col,
+                                  j.s_col, &plans[i]))
+      return st;
   }
-  CUtensorMap tm_x, tm_qr, tm_qc;
-  std::memset(&tm_qr, 0, sizeof(tm_qr));
-  std::memset(&tm_qc, 0, sizeof(tm_qc));
-  if (!make_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, cols, rows, 64, 128)) return FP8_ERR_CUDA;
-  if (do_row && !make_map(&tm_qr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q_row, cols, rows, 128, 128)) return FP8_ERR_CUDA;
-  if (do_col && !make_map(&tm_qc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q_col, rows, cols, 128, 128)) return FP8_ERR_CUDA;
-  return cuda_status(launch_cast_transpose_tiled(p, tm_x, tm_qr, tm_qc, d->num_sms, stream));
+  if (n_jobs == 0) return FP8_OK;
+  DeviceInfo* d;
+  if (fp8_status st = device_info(&d)) return st;
+  CastJobs launch{};
+  for (int i = 0; i < n_jobs; ++i) {
+    CastPlan& pl = plans[i];
+    if (jobs[i].amax_out != nullptr && cudaMemsetAsync(jobs[i].amax_out, 0, sizeof(float), stream) != cudaSuccess)
+      return FP8_ERR_CUDA;
+    if (pl.empty) continue;
+    pl.p.err = d->err;
+    if (!pl.tiled) {
+      if (fp8_status st = cuda_status(launch_cast_generic(pl.p, jobs[i].x, stream))) return st;
+      continue;
+    }
+    launch.p[launch.n] = pl.p;
+    launch.m[launch.n].x = pl.tm_x;
+    launch.m[launch.n].qrow = pl.tm_qr;
+    launch.m[launch.n].qcol = pl.tm_qc;
+    launch.tile_start[launch.n + 1] = launch.tile_start[launch.n] + pl.p.tiles_r * pl.p.tiles_c;
+    ++launch.n;
+  }
+  if (launch.n == 0) return FP8_OK;
+  return cuda_status(launch_cast_jobs(launch, d->num_sms, stream));
 }
 
 fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,

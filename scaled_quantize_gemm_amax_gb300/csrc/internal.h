@@ -83,6 +83,18 @@ cudaError_t launch_cast_transpose_tiled(const CastParams& p, const CUtensorMap& 
                                         const CUtensorMap& tm_qcol, int num_sms, cudaStream_t s);
 // Plain path for the per-tensor recipe at any shape.
 cudaError_t launch_cast_generic(const CastParams& p, const void* x, cudaStream_t s);
+// Several tiled casts in one launch: job j owns tiles [tile_start[j], tile_start[j+1]).
+constexpr int kMaxCastJobs = 4;
+struct CastJobMaps {
+  CUtensorMap x, qrow, qcol;
+};
+struct CastJobs {
+  CastJobMaps m[kMaxCastJobs];
+  CastParams p[kMaxCastJobs];
+  int tile_start[kMaxCastJobs + 1];
+  int n;
+};
+cudaError_t launch_cast_jobs(const CastJobs& jobs, int num_sms, cudaStream_t s);
 
 // ---- dequantize (dequantize.cu): y bf16 [R, C] = RN_bf16(decode(q) * multiplier)
 cudaError_t launch_dequantize(const uint8_t* q, int64_t R, int64_t C, int recipe, bool mx_tiled, bool e5m2,

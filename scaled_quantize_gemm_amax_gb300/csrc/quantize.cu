@@ -133,6 +133,122 @@ __device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t b, int64_t
   return ((r >> 7) * atoms_per_row + (b >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (b & 3);
 }
 
+// One 128x128 tile already in shared memory (stage buffer xs): both passes, scales
+// written to global memory, quantized bytes staged in outR (row-wise) and outT
+// (column-wise) for the TMA stores.  thr_amax accumulates this thread's |x| maximum.
+template <int RECIPE>
+__device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs, uint32_t outR, uint32_t outT, int tr,
+                                               int tc, int64_t row0, int64_t col0, float g_scale, float& thr_amax,
+                                               float* red, int tid, int warp, int lane) {
+  const bool e5 = p.e5m2 != 0;
+  const float fmax = fmax_of(e5);
+  const int fexp = fmax_exp_of(e5);
+  const int64_t nb128_c = p.C / 128, nb128_r = p.R / 128, nb32_c = p.C / 32, nb32_r = p.R / 32;
+  const int j = lane & 15;
+  // ---------------- row pass
+  uint4 v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = lds128(x_addr(xs, i * 32 + warp * 2 + (lane >> 4), j));
+  float a[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) a[i] = absmax_chunk(v[i]);
+
+  float tile_scale = g_scale;
+  if (RECIPE == kBlock128x128) {
+    const float tmax = block_max(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), red, warp, lane);
+    thr_amax = fmaxf(thr_amax, tmax);
+    tile_scale = scale_from_amax(tmax, fmax);
+    if (tid == 0) {
+      const float si = recip_rn(tile_scale);
+      if (p.do_row && p.s_row) static_cast<float*>(p.s_row)[tr * nb128_c + tc] = si;
+      if (p.do_col && p.s_col) static_cast<float*>(p.s_col)[tc * nb128_r + tr] = si;
+    }
+  } else {
+    thr_amax = fmaxf(thr_amax, fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])));
+  }
+
+  if (p.do_row) {
+    float sc[4] = {tile_scale, tile_scale, tile_scale, tile_scale};
+    if (RECIPE == kBlock1x128) {
+      // row i = j / 4 ends up in lanes j = 4i..4i+3 of each half-warp
+      float m = reduce_scatter4(a, lane, 8, 4);
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      const float mine = scale_from_amax(m, fmax);
+      const int64_t grow = row0 + (j >> 2) * 32 + warp * 2 + (lane >> 4);
+      if ((j & 3) == 0 && grow < p.R) static_cast<float*>(p.s_row)[grow * nb128_c + tc] = recip_rn(mine);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, mine, (lane & 16) | (i << 2));
+    } else if (RECIPE == kMx) {
+      // the 32-column block of lane j is lanes 4 (j/4) .. +3; row i = j % 4 ends up in lane 4 (j/4) + i
+      const float m = reduce_scatter4(a, lane, 2, 1);
+      const int e = mx_exponent(m, fexp);
+      const float mine = pow2_neg(e);
+      const int64_t grow = row0 + (j & 3) * 32 + warp * 2 + (lane >> 4);
+      const int64_t b = tc * 4 + (j >> 2);
+      if (grow < p.R && b < nb32_c) {   // a tile hanging over C has blocks past the last one
+        const int64_t off = p.mx_tiled ? mx_tiled_offset(grow, b, (p.C + 127) / 128) : grow * nb32_c + b;
+        static_cast<uint8_t*>(p.s_row)[off] = static_cast<uint8_t>(e + 127);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, mine, (lane & ~3) | i);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = i * 32 + warp * 2 + (lane >> 4);
+      const uint2 q = q_chunk(v[i], sc[i], e5);
+      sts64(outR + (r << 7) + ((((j >> 1) ^ (r & 7))) << 4) + ((j & 1) << 3), q.x, q.y);
+    }
+  }
+
+  // ---------------- col pass
+  if (p.do_col) {
+    const int g = warp;
+    uint32_t d[4][4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) ldsm_x4_trans(x_addr(xs, 32 * t + 8 * (lane >> 3) + (lane & 7), g), d[t]);
+    const int cc = 8 * g + (lane >> 2);
+    const int64_t gcol = col0 + cc;
+    float sc[4] = {tile_scale, tile_scale, tile_scale, tile_scale};
+    if (RECIPE == kBlock1x128) {
+      uint32_t m = 0;
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) m = xabs_max(m, d[t][q]);
+      float am = pair_abs_f32(m);
+      am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+      am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+      const float s1 = scale_from_amax(am, fmax);
+      sc[0] = sc[1] = sc[2] = sc[3] = s1;
+      if ((lane & 3) == 0 && gcol < p.C) static_cast<float*>(p.s_col)[gcol * nb128_r + tr] = recip_rn(s1);
+    } else if (RECIPE == kMx) {
+      float at[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) at[t] = pair_abs_f32(xabs_max(xabs_max(d[t][0], d[t][1]), xabs_max(d[t][2], d[t][3])));
+      // block t = lane % 4 of this column ends up in this lane
+      const float m = reduce_scatter4(at, lane, 2, 1);
+      const int e = mx_exponent(m, fexp);
+      const float mine = pow2_neg(e);
+      const int64_t b = static_cast<int64_t>(tr) * 4 + (lane & 3);
+      if (gcol < p.C && b < nb32_r) {
+        const int64_t off = p.mx_tiled ? mx_tiled_offset(gcol, b, (p.R + 127) / 128) : gcol * nb32_r + b;
+        static_cast<uint8_t*>(p.s_col)[off] = static_cast<uint8_t>(e + 127);
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) sc[t] = __shfl_sync(0xFFFFFFFFu, mine, (lane & ~3) | t);
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r0 = 32 * t + 8 * q + 2 * (lane & 3);
+        sts16(q_addr(outT, cc, r0), q_pair(d[t][q], sc[t], e5));
+      }
+  }
+
+}
+
 template <int RECIPE>
 __global__ void __launch_bounds__(kThreads, 1)
     k_cast_transpose(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_qrow,
@@ -142,11 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* const base_ptr = smem_raw + (base - smem_u32(smem_raw));
   float* const red = reinterpret_cast<float*>(base_ptr + kOffRed);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool e5 = p.e5m2 != 0;
-  const float fmax = fmax_of(e5);
-  const int fexp = fmax_exp_of(e5);
   const int ntiles = p.tiles_r * p.tiles_c;
-  const int64_t nb128_c = p.C / 128, nb128_r = p.R / 128, nb32_c = p.C / 32, nb32_r = p.R / 32;
 
   if (tid == 0) {
     prefetch_tmap(&tm_x);
@@ -187,7 +299,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Row pass: lane j = lane % 16 of a half-warp owns 16-byte chunk j of rows
   // r(i) = 32 i + 2 warp + lane / 16, i = 0..3.  Column pass: warp w owns the
   // 8-column chunk w; lane holds column 8 w + lane / 4, rows 32 t + 8 q + 2 (lane % 4) + {0, 1}.
-  const int j = lane & 15;
   float thr_amax = 0.0f;
   int it = 0;
   bool failed = false;
@@ -207,107 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       break;
     }
 
-    // ---------------- row pass
-    uint4 v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = lds128(x_addr(xs, i * 32 + warp * 2 + (lane >> 4), j));
-    float a[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = absmax_chunk(v[i]);
-
-    float tile_scale = g_scale;
-    if (RECIPE == kBlock128x128) {
-      const float tmax = block_max(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), red, warp, lane);
-      thr_amax = fmaxf(thr_amax, tmax);
-      tile_scale = scale_from_amax(tmax, fmax);
-      if (tid == 0) {
-        const float si = recip_rn(tile_scale);
-        if (p.do_row && p.s_row) static_cast<float*>(p.s_row)[tr * nb128_c + tc] = si;
-        if (p.do_col && p.s_col) static_cast<float*>(p.s_col)[tc * nb128_r + tr] = si;
-      }
-    } else {
-      thr_amax = fmaxf(thr_amax, fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])));
-    }
-
-    if (p.do_row) {
-      float sc[4] = {tile_scale, tile_scale, tile_scale, tile_scale};
-      if (RECIPE == kBlock1x128) {
-        // row i = j / 4 ends up in lanes j = 4i..4i+3 of each half-warp
-        float m = reduce_scatter4(a, lane, 8, 4);
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-        const float mine = scale_from_amax(m, fmax);
-        const int64_t grow = row0 + (j >> 2) * 32 + warp * 2 + (lane >> 4);
-        if ((j & 3) == 0 && grow < p.R) static_cast<float*>(p.s_row)[grow * nb128_c + tc] = recip_rn(mine);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, mine, (lane & 16) | (i << 2));
-      } else if (RECIPE == kMx) {
-        // the 32-column block of lane j is lanes 4 (j/4) .. +3; row i = j % 4 ends up in lane 4 (j/4) + i
-        const float m = reduce_scatter4(a, lane, 2, 1);
-        const int e = mx_exponent(m, fexp);
-        const float mine = pow2_neg(e);
-        const int64_t grow = row0 + (j & 3) * 32 + warp * 2 + (lane >> 4);
-        const int64_t b = tc * 4 + (j >> 2);
-        if (grow < p.R && b < nb32_c) {   // a tile hanging over C has blocks past the last one
-          const int64_t off = p.mx_tiled ? mx_tiled_offset(grow, b, (p.C + 127) / 128) : grow * nb32_c + b;
-          static_cast<uint8_t*>(p.s_row)[off] = static_cast<uint8_t>(e + 127);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, mine, (lane & ~3) | i);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = i * 32 + warp * 2 + (lane >> 4);
-        const uint2 q = q_chunk(v[i], sc[i], e5);
-        sts64(outR + (r << 7) + ((((j >> 1) ^ (r & 7))) << 4) + ((j & 1) << 3), q.x, q.y);
-      }
-    }
-
-    // ---------------- col pass
-    if (p.do_col) {
-      const int g = warp;
-      uint32_t d[4][4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) ldsm_x4_trans(x_addr(xs, 32 * t + 8 * (lane >> 3) + (lane & 7), g), d[t]);
-      const int cc = 8 * g + (lane >> 2);
-      const int64_t gcol = col0 + cc;
-      float sc[4] = {tile_scale, tile_scale, tile_scale, tile_scale};
-      if (RECIPE == kBlock1x128) {
-        uint32_t m = 0;
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) m = xabs_max(m, d[t][q]);
-        float am = pair_abs_f32(m);
-        am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-        am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
-        const float s1 = scale_from_amax(am, fmax);
-        sc[0] = sc[1] = sc[2] = sc[3] = s1;
-        if ((lane & 3) == 0 && gcol < p.C) static_cast<float*>(p.s_col)[gcol * nb128_r + tr] = recip_rn(s1);
-      } else if (RECIPE == kMx) {
-        float at[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) at[t] = pair_abs_f32(xabs_max(xabs_max(d[t][0], d[t][1]), xabs_max(d[t][2], d[t][3])));
-        // block t = lane % 4 of this column ends up in this lane
-        const float m = reduce_scatter4(at, lane, 2, 1);
-        const int e = mx_exponent(m, fexp);
-        const float mine = pow2_neg(e);
-        const int64_t b = static_cast<int64_t>(tr) * 4 + (lane & 3);
-        if (gcol < p.C && b < nb32_r) {
-          const int64_t off = p.mx_tiled ? mx_tiled_offset(gcol, b, (p.R + 127) / 128) : gcol * nb32_r + b;
-          static_cast<uint8_t*>(p.s_col)[off] = static_cast<uint8_t>(e + 127);
-        }
-#pragma unroll
-        for (int t = 0; t < 4; ++t) sc[t] = __shfl_sync(0xFFFFFFFFu, mine, (lane & ~3) | t);
-      }
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int r0 = 32 * t + 8 * q + 2 * (lane & 3);
-          sts16(q_addr(outT, cc, r0), q_pair(d[t][q], sc[t], e5));
-        }
-    }
+    cast_tile_body<RECIPE>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red, tid, warp, lane);
 
     fence_proxy_async_smem();
     __syncthreads();
@@ -378,6 +389,129 @@ __global__ void __launch_bounds__(256) k_cast_generic(const uint16_t* __restrict
   }
 }
 
+// Several casts in one persistent grid: the tiles of job 0, then job 1, ... are dealt
+// round-robin to the CTAs as in k_cast_transpose; each tile runs the body of its
+// job's recipe and leaves through its job's tensor maps.  A CTA meets the jobs in
+// order, so it folds its amax of a job into that job's amax_out when it moves on.
+__global__ void __launch_bounds__(kThreads, 1) k_cast_jobs(const __grid_constant__ CastJobs J) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - smem_u32(smem_raw));
+  float* const red = reinterpret_cast<float*>(base_ptr + kOffRed);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ntiles = J.tile_start[J.n];
+
+  if (tid == 0) {
+    for (int j = 0; j < J.n; ++j) prefetch_tmap(&J.m[j].x);
+    for (int s = 0; s < kStages; ++s) mbar_init(base + kOffBar + 8 * s, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();   // from here on: global memory
+  pdl_launch_dependents();
+
+  if (blockIdx.x == 0 && tid == 0) {
+    for (int j = 0; j < J.n; ++j) {
+      const CastParams& p = J.p[j];
+      if (p.recipe != kTensor) continue;
+      const float si = recip_rn(*p.scale);
+      if (p.do_row && p.s_row) *static_cast<float*>(p.s_row) = si;
+      if (p.do_col && p.s_col) *static_cast<float*>(p.s_col) = si;
+    }
+  }
+  auto job_of = [&](int gt) {
+    int j = 0;
+    while (j + 1 < J.n && gt >= J.tile_start[j + 1]) ++j;
+    return j;
+  };
+  auto issue_load = [&](int it, int gt) {
+    const int j = job_of(gt);
+    const int lt = gt - J.tile_start[j];
+    const int s = it % kStages;
+    const uint32_t bar = base + kOffBar + 8 * s;
+    const int row0 = (lt / J.p[j].tiles_c) * kTile, col0 = (lt % J.p[j].tiles_c) * kTile;
+    mbar_arrive_expect_tx(bar, kXBytes);
+    tma_load_2d(base + s * kXBytes, &J.m[j].x, col0, row0, bar);
+    tma_load_2d(base + s * kXBytes + kXBytes / 2, &J.m[j].x, col0 + 64, row0, bar);
+  };
+  if (tid == 0) {
+    for (int it = 0; it < kStages; ++it) {
+      const int gt = blockIdx.x + it * gridDim.x;
+      if (gt < ntiles) issue_load(it, gt);
+    }
+  }
+  // fold this CTA's |x| maximum of job j into its amax_out (all threads take part)
+  auto flush_amax = [&](int j, float thr_amax) {
+    if (J.p[j].amax_out == nullptr) return;
+    const float am = block_max(thr_amax, red, warp, lane);
+    if (tid == 0 && am > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(J.p[j].amax_out), __float_as_uint(am));
+  };
+
+  float thr_amax = 0.0f, g_scale = 1.0f;
+  int cur = -1;
+  int it = 0;
+  bool failed = false;
+  for (int gt = blockIdx.x; gt < ntiles; gt += gridDim.x, ++it) {
+    const int j = job_of(gt);
+    if (j != cur) {
+      if (cur >= 0) flush_amax(cur, thr_amax);
+      cur = j;
+      thr_amax = 0.0f;
+      g_scale = J.p[j].recipe == kTensor ? *J.p[j].scale : 1.0f;
+    }
+    const CastParams& p = J.p[j];
+    const int lt = gt - J.tile_start[j];
+    const int s = it % kStages;
+    const uint32_t xs = base + s * kXBytes;
+    const int ob = it & 1;
+    const uint32_t outR = base + kOffOutR + ob * kQBytes;
+    const uint32_t outT = base + kOffOutT + ob * kQBytes;
+    const int tr = lt / p.tiles_c, tc = lt % p.tiles_c;
+    const int64_t row0 = static_cast<int64_t>(tr) * kTile, col0 = static_cast<int64_t>(tc) * kTile;
+
+    const bool ok = mbar_wait(base + kOffBar + 8 * s, (it / kStages) & 1, p.err, kErrTimeoutTmaLoad, nullptr);
+    if (tid == 0) bulk_wait_read<1>();  // staging buffer `ob` (used two tiles ago) has been read out
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+    switch (p.recipe) {
+      case kTensor:
+        cast_tile_body<kTensor>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red, tid, warp, lane);
+        break;
+      case kBlock1x128:
+        cast_tile_body<kBlock1x128>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red, tid, warp, lane);
+        break;
+      case kBlock128x128:
+        cast_tile_body<kBlock128x128>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red, tid, warp, lane);
+        break;
+      default:
+        cast_tile_body<kMx>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red, tid, warp, lane);
+        break;
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      if (p.do_row) tma_store_2d(&J.m[j].qrow, outR, static_cast<int>(col0), static_cast<int>(row0));
+      if (p.do_col) tma_store_2d(&J.m[j].qcol, outT, static_cast<int>(row0), static_cast<int>(col0));
+      bulk_commit();
+      const int next = gt + kStages * gridDim.x;
+      if (next < ntiles) issue_load(it + kStages, next);
+    }
+  }
+
+  if (failed && tid == 0) {
+    // wait (bounded) for loads still in flight into this CTA's ring before leaving
+    for (int k = it; k < it + kStages; ++k) {
+      const int gt = blockIdx.x + k * gridDim.x;
+      if (gt >= ntiles) break;
+      mbar_wait(base + kOffBar + 8 * (k % kStages), (k / kStages) & 1, J.p[0].err, kErrTimeoutTmaLoad, nullptr);
+    }
+  }
+  if (tid == 0) bulk_wait_all<0>();
+  if (!failed && cur >= 0) flush_amax(cur, thr_amax);
+}
+
 template <int RECIPE>
 cudaError_t launch_tiled(const CastParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_qrow,
                          const CUtensorMap& tm_qcol, int num_sms, cudaStream_t s) {
@@ -399,6 +533,15 @@ cudaError_t launch_cast_transpose_tiled(const CastParams& p, const CUtensorMap& 
     case kBlock128x128: return launch_tiled<kBlock128x128>(p, tm_x, tm_qrow, tm_qcol, num_sms, s);
     default: return launch_tiled<kMx>(p, tm_x, tm_qrow, tm_qcol, num_sms, s);
   }
+}
+
+cudaError_t launch_cast_jobs(const CastJobs& jobs, int num_sms, cudaStream_t s) {
+  static bool attr_done[kMaxDevices] = {};
+  cudaError_t e = ensure_smem_limit(k_cast_jobs, static_cast<int>(kSmemBytes), attr_done);
+  if (e != cudaSuccess) return e;
+  const int ntiles = jobs.tile_start[jobs.n];
+  const int grid = ntiles < num_sms ? ntiles : num_sms;
+  return launch_pdl(k_cast_jobs, dim3(grid), dim3(kThreads), kSmemBytes, s, 1, jobs);
 }
 
 cudaError_t launch_cast_generic(const CastParams& p, const void* x, cudaStream_t s) {

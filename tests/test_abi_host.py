@@ -174,3 +174,19 @@ def test_allreduce_noalloc_rejects(lib):
     assert ar(FAKE, 2, 60, 0, FAKE, FAKE, FAKE, None) == SHAPE          # n % 8
     assert ar(FAKE + 8, 2, 64, 0, FAKE, FAKE, FAKE, None) == ALIGN
     assert ar(FAKE, 2, 0, 0, None, None, None, None) == OK               # empty: no-op
+
+
+def test_cast_multi_rejects(lib):
+    job = fq.CastJob
+    T, B1 = 0, 1
+    good = job(FAKE, 128, 128, B1, 0, None, None, FAKE, FAKE, None, None)
+    bad_shape = job(FAKE, 128, 100, B1, 0, None, None, FAKE, FAKE, None, None)
+    bad_align = job(FAKE + 8, 128, 128, B1, 0, None, None, FAKE, FAKE, None, None)
+    arr = (job * 5)(good, good, good, good, good)
+    assert lib.fp8_cast_transpose_multi(arr, 5, None) == INVALID      # more than 4 jobs
+    assert lib.fp8_cast_transpose_multi(None, 1, None) == INVALID
+    assert lib.fp8_cast_transpose_multi(arr, 0, None) == OK
+    arr2 = (job * 2)(bad_shape, good)
+    assert lib.fp8_cast_transpose_multi(arr2, 2, None) == SHAPE      # checked before any device work
+    arr3 = (job * 2)(bad_align, good)
+    assert lib.fp8_cast_transpose_multi(arr3, 2, None) == ALIGN

@@ -1,0 +1,70 @@
+"""GPU parity of fp8_cast_transpose_multi: several casts (different recipes, formats,
+shapes, with and without amax) in one launch, every output compared with the oracle
+bit for bit, and with the single-job entry point."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scaled_quantize_gemm_amax_gb300 as fq
+from scaled_quantize_gemm_amax_gb300 import workloads as wl
+from gpu_util import (R, F, KIND, assert_bytes_equal, assert_status_ok, bits16, f32bits, host, oracle_scales_like,
+                      require_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def check_job(x, recipe, fmt, scale_np, outs, amax_t):
+    xh = bits16(x)
+    rows, cols = xh.shape
+    kind = KIND[recipe]
+    qr, sr, qc, sc = outs
+    if amax_t is not None:
+        assert f32bits(host(amax_t))[0] == f32bits(oracle.amax(xh))[0], "amax_out"
+    q_ref, s_ref = oracle.quantize_rowwise(xh, kind, int(fmt), scale_np)
+    assert_bytes_equal(host(qr), q_ref, f"{recipe.name} q_row")
+    s_ref = oracle_scales_like(recipe, s_ref, rows, cols)
+    got = host(sr)
+    assert_bytes_equal(got if got.dtype == np.uint8 else f32bits(got), s_ref if s_ref.dtype == np.uint8 else f32bits(s_ref),
+                       f"{recipe.name} s_row")
+    q_ref, s_ref = oracle.quantize_colwise(xh, kind, int(fmt), scale_np)
+    assert_bytes_equal(host(qc), q_ref, f"{recipe.name} q_col")
+    s_ref = oracle_scales_like(recipe, s_ref, cols, rows)
+    got = host(sc)
+    assert_bytes_equal(got if got.dtype == np.uint8 else f32bits(got), s_ref if s_ref.dtype == np.uint8 else f32bits(s_ref),
+                       f"{recipe.name} s_col")
+
+
+def test_cast_multi_four_recipes():
+    xs = [wl.normal_bf16((384, 256), 80, 1.0), wl.normal_bf16((256, 512), 81, 0.02),
+          wl.normal_bf16((256, 384), 82, 3.0), wl.normal_bf16((512, 128), 83, 1.0)]
+    xs[0][:, 7] *= 100.0
+    recipes = [R.BLOCK_1x128, R.BLOCK_128x128, R.MX_1x32_TILED, R.TENSOR]
+    fmts = [F.E4M3, F.E4M3, F.E5M2, F.E5M2]
+    scale_np = oracle.tensor_scale(oracle.amax(bits16(xs[3])), int(F.E5M2))[0]
+    scales = [None, None, None, torch.tensor([scale_np], dtype=torch.float32, device="cuda")]
+    amaxes = [torch.full((1,), 7.0, device="cuda"), None, torch.full((1,), 7.0, device="cuda"),
+              torch.full((1,), 7.0, device="cuda")]
+    outs = fq.cast_transpose_multi(list(zip(xs, recipes, fmts, scales, amaxes)))
+    torch.cuda.synchronize()
+    assert_status_ok()
+    for x, r, f, sc, am, o in zip(xs, recipes, fmts, scales, amaxes, outs):
+        check_job(x, r, f, scale_np if r == R.TENSOR else None, o, am)
+
+
+def test_cast_multi_equals_single_calls_on_the_blockwise_workload():
+    # the activation / weight pair of the blockwise fprop workload, in one launch
+    x, w = wl.cfg2_blockwise("cuda")
+    (mx_, ms_, mxt, mst), (mw, mws, mwt, mwst) = fq.cast_transpose_multi(
+        [(x, R.BLOCK_1x128, F.E4M3, None, None), (w, R.BLOCK_128x128, F.E4M3, None, None)])
+    sx = fq.cast_transpose(x, R.BLOCK_1x128, F.E4M3)
+    sw = fq.cast_transpose(w, R.BLOCK_128x128, F.E4M3)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    for a, b in zip((mx_, ms_, mxt, mst, mw, mws, mwt, mwst), sx + sw):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
