@@ -75,7 +75,7 @@ template <int KIND>
 __host__ __device__ constexpr int issuers_of() { return (KIND == kBlockK2 || KIND == kMx) ? 2 : 1; }
 template <>
 struct Cfg<kMx> {
-  static constexpr int BN = 256, STAGES = 4, ACC = 1, EPI = 8, KSUB = 1, CTRL = 2;
+  static constexpr int BN = 256, STAGES = 3, ACC = 1, EPI = 8, KSUB = 1, CTRL = 2;
 };
 
 // CTRL = 4: warps 0..3 (producer, the two MMA issuers, an idle warp) form a warpgroup
@@ -90,7 +90,9 @@ static_assert(kCtrlRegs + 2 * kEpiRegs <= 512, "register split exceeds a sub-par
 // Stages of the 2-CTA (pair) variant: each CTA holds 128 rows of A and half of B
 // (blockwise with 256-deep stages: 48 KB a stage).
 template <int KIND>
-constexpr int pair_stages() { return Cfg<KIND>::KSUB == 2 ? 4 : (Cfg<KIND>::BN == 256 ? 6 : 8); }
+constexpr int pair_stages() {
+  return Cfg<KIND>::KSUB == 2 ? 4 : (KIND == kMx ? 5 : (Cfg<KIND>::BN == 256 ? 6 : 8));
+}
 
 template <int KIND, bool PAIR>
 struct Layout {
@@ -103,7 +105,12 @@ struct Layout {
   // MX scale atoms per stage: this CTA's rows of A and all BN rows of B
   static constexpr uint32_t SF_BYTES = (KIND == kMx) ? 512 + 512 * (BN / 128) : 0;
   static constexpr uint32_t OFF_SF = S * STAGE_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_SF + S * SF_BYTES;
+  // per-tensor / MX: one 4 KB staging box per epilogue warp for the TMA stores of C
+  // (32 rows x 128 B, 128-byte swizzle; the box must start on 1024 bytes)
+  static constexpr bool TSTORE = !(KIND == kBlock1x128 || KIND == kBlockRowsB || KIND == kBlockK2);
+  static constexpr uint32_t STG_BYTES = TSTORE ? Cfg<KIND>::EPI * 4096 : 0;
+  static constexpr uint32_t OFF_STG = (OFF_SF + S * SF_BYTES + 1023) & ~1023u;
+  static constexpr uint32_t OFF_BAR = OFF_STG + STG_BYTES;
   // barriers: full[S], empty[S], tfull[4], tempty[4], final
   static constexpr uint32_t OFF_FULL = OFF_BAR, OFF_EMPTY = OFF_BAR + 8 * S;
   static constexpr uint32_t OFF_TFULL = OFF_EMPTY + 8 * S, OFF_TEMPTY = OFF_TFULL + 32;
@@ -139,6 +146,10 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
+}
+
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
 }
 
 __device__ __forceinline__ void stg128(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -189,7 +200,8 @@ constexpr int threads_of() {
 template <int KIND, bool PAIR, bool QOUT>
 __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     k_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-           const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb, const GemmParams p) {
+           const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
+           const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
   using L = Layout<KIND, PAIR>;
   constexpr int BN = L::BN, S = L::S, ACC = Cfg<KIND>::ACC, EPI = Cfg<KIND>::EPI;
   constexpr bool BLOCK = (KIND == kBlock1x128 || KIND == kBlockRowsB || KIND == kBlockK2);   // promotion path
@@ -531,9 +543,9 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     if (want_q && p.c_scale_inv != nullptr && blockIdx.x == 0 && warp == CTRL && lane == 0)
       *p.c_scale_inv = recip_rn(c_scale);
     // 32 consecutive output values of one row, starting at column gcol
-    auto emit = [&](const float (&v)[32], int64_t grow_, int64_t gcol) {
+    auto emit = [&](const float (&v)[32], int64_t grow_, int64_t gcol, bool store_c = true) {
       const int64_t off = grow_ * p.N + gcol;
-      if (p.c != nullptr) store_row32(p.c, off, v, fp32);
+      if (store_c && p.c != nullptr) store_row32(p.c, off, v, fp32);
       if (QOUT && (want_q || want_amax)) {
         float y[32];
 #pragma unroll
@@ -761,18 +773,54 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) release(base + L::OFF_TEMPTY + 8 * a);
+          // C leaves through TMA stores: this warp's 32 rows x 128 bytes (32 fp32 or 64 bf16
+          // columns) at a time are staged in its swizzled box, so that every store writes
+          // whole lines (a thread per row storing its own 16 bytes would not)
+          const uint32_t stg = base + L::OFF_STG + static_cast<uint32_t>(warp - CTRL) * 4096u;
+          const int box_row = static_cast<int>(static_cast<int64_t>(tm) * TM + row_off) + 32 * q;
 #pragma unroll
           for (int c = 0; c < CH; ++c) {
             float v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               v[j] = (KIND == kTensor) ? __fmul_rn(__uint_as_float(r[c][j]), tensor_scale) : __uint_as_float(r[c][j]);
-            if (gcol0 + 32 * c < p.N) emit(v, grow, gcol0 + 32 * c);
+            if (QOUT && (want_q || want_amax) && gcol0 + 32 * c < p.N) emit(v, grow, gcol0 + 32 * c, false);
+            if (p.c == nullptr) continue;
+            if (fp32 || (c & 1) == 0) {
+              // the box is free once the previous store from it has read it
+              if (lane == 0) bulk_wait_read<0>();
+              __syncwarp();
+            }
+            // 16-byte chunk k of this thread's row of the box sits at chunk k ^ (row % 8)
+            const uint32_t rowb = stg + static_cast<uint32_t>(lane) * 128u;
+            if (fp32) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                sts128(rowb + ((static_cast<uint32_t>(k) ^ (lane & 7u)) << 4), __float_as_uint(v[4 * k]),
+                       __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
+            } else {
+              const uint32_t k0 = (c & 1) * 4;   // 32 bf16 = chunks 0..3 (even c) or 4..7 (odd c) of the row
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                sts128(rowb + (((k0 + k) ^ (lane & 7u)) << 4), pack_bf16(v[8 * k], v[8 * k + 1]),
+                       pack_bf16(v[8 * k + 2], v[8 * k + 3]), pack_bf16(v[8 * k + 4], v[8 * k + 5]),
+                       pack_bf16(v[8 * k + 6], v[8 * k + 7]));
+            }
+            if (fp32 || (c & 1) == 1) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                const int x = static_cast<int>(fp32 ? gcol0 + 32 * c : gcol0 + 32 * (c - 1));
+                tma_store_2d(&tm_c, stg, x, box_row);
+                bulk_commit();
+              }
+            }
           }
         }
         ++acc_it;
       }
     }
+    if (L::TSTORE && lane == 0) bulk_wait_all<0>();   // this warp's TMA stores have finished
     if (QOUT && want_amax) {
       // one atomic per warp, on the (non-negative) float bits, which order like the values
 #pragma unroll
@@ -812,7 +860,7 @@ cudaError_t check_split_regs(K kern, bool split, bool (&checked)[kMaxDevices]) {
 
 template <int KIND, bool QOUT>
 cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
-                        const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s) {
+                        const CUtensorMap& tm_sfb, const CUtensorMap& tm_c, int num_sms, cudaStream_t s) {
   using L = Layout<KIND, false>;
   static_assert(L::SMEM <= 232448, "shared memory budget");
   static bool attr_done[kMaxDevices] = {};
@@ -823,14 +871,14 @@ cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& tm_a, const CUte
   if (e != cudaSuccess) return e;
   const int64_t ntiles = (p.M / kBM) * ((p.N + L::BN - 1) / L::BN);
   const int grid = static_cast<int>(ntiles < num_sms ? ntiles : num_sms);
-  return launch_pdl(k_gemm<KIND, false, QOUT>, dim3(grid), dim3(threads_of<KIND>()), L::SMEM, s, 1, tm_a, tm_b, tm_sfa, tm_sfb, p);
+  return launch_pdl(k_gemm<KIND, false, QOUT>, dim3(grid), dim3(threads_of<KIND>()), L::SMEM, s, 1, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, p);
 }
 
 // 2-CTA clusters; the grid is as many pairs as can be resident at once (at most
 // one per two SMs), each walking the 256-row tiles with a stride of the pair count.
 template <int KIND, bool QOUT>
 cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
-                        const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s) {
+                        const CUtensorMap& tm_sfb, const CUtensorMap& tm_c, int num_sms, cudaStream_t s) {
   using L = Layout<KIND, true>;
   static_assert(L::SMEM <= 232448, "shared memory budget");
   auto kern = k_gemm<KIND, true, QOUT>;
@@ -866,7 +914,7 @@ cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUte
   if (max_clusters[dev] < pairs) pairs = max_clusters[dev];
   if (ntiles < pairs) pairs = ntiles;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-  return launch_pdl(kern, cfg.gridDim, cfg.blockDim, L::SMEM, s, 2, tm_a, tm_b, tm_sfa, tm_sfb, p);
+  return launch_pdl(kern, cfg.gridDim, cfg.blockDim, L::SMEM, s, 2, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, p);
 }
 
 }  // namespace
@@ -891,26 +939,26 @@ int gemm_b_box_rows(const GemmParams& p) { return gemm_uses_pair(p) ? gemm_block
 
 template <bool QOUT>
 cudaError_t launch_gemm_q(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
-                          const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s) {
+                          const CUtensorMap& tm_sfb, const CUtensorMap& tm_c, int num_sms, cudaStream_t s) {
   switch (p.kind) {
     case kTensor:
-      return gemm_uses_pair(p) ? launch_pair<kTensor, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
-                               : launch_kind<kTensor, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
+      return gemm_uses_pair(p) ? launch_pair<kTensor, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s)
+                               : launch_kind<kTensor, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);
     case kBlock1x128:
-      if (p.b_1x128) return launch_kind<kBlockRowsB, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
-      if (gemm_uses_pair(p)) return launch_pair<kBlockK2, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
-      return (p.K / kBK) % 2 == 0 ? launch_kind<kBlockK2, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
-                                  : launch_kind<kBlock1x128, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
+      if (p.b_1x128) return launch_kind<kBlockRowsB, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);
+      if (gemm_uses_pair(p)) return launch_pair<kBlockK2, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);
+      return (p.K / kBK) % 2 == 0 ? launch_kind<kBlockK2, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s)
+                                  : launch_kind<kBlock1x128, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);
     default:
-      return gemm_uses_pair(p) ? launch_pair<kMx, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s)
-                               : launch_kind<kMx, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
+      return gemm_uses_pair(p) ? launch_pair<kMx, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s)
+                               : launch_kind<kMx, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);
   }
 }
 
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
-                        const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s) {
-  if (p.cq != nullptr || p.c_amax != nullptr) return launch_gemm_q<true>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
-  return launch_gemm_q<false>(p, tm_a, tm_b, tm_sfa, tm_sfb, num_sms, s);
+                        const CUtensorMap& tm_sfb, const CUtensorMap& tm_c, int num_sms, cudaStream_t s) {
+  if (p.cq != nullptr || p.c_amax != nullptr) return launch_gemm_q<true>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);
+  return launch_gemm_q<false>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);
 }
 
 }  // namespace fp8q

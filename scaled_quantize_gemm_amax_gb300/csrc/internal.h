@@ -137,7 +137,7 @@ bool gemm_uses_pair(const GemmParams& p);
 int gemm_b_box_rows(const GemmParams& p);
 // tm_sfa / tm_sfb: MX only (the tiled E8M0 buffers as [atoms * 2, 256] bytes, box 2 x 256).
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
-                        const CUtensorMap& tm_sfb, int num_sms, cudaStream_t s);
+                        const CUtensorMap& tm_sfb, const CUtensorMap& tm_c, int num_sms, cudaStream_t s);
 
 // Bounded-wait self test: one CTA waits on an mbarrier nothing arrives on.
 cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t s);
