@@ -258,10 +258,11 @@ fp8_status scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const voi
         !make_map(&tm_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sB, 256, 2 * atoms_b, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
       return FP8_ERR_CUDA;
   }
-  // per-tensor / MX: C leaves through TMA stores of 32-row x 128-byte boxes
+  // C leaves through TMA stores of 32-row x 128-byte boxes (all kernels but the blockwise
+  // ones with 128-deep stages, which store directly)
   CUtensorMap tm_c;
   std::memset(&tm_c, 0, sizeof(tm_c));
-  if (C != nullptr && kind != kBlock1x128) {
+  if (C != nullptr) {
     const bool ok = out == FP8_OUT_FP32
                         ? make_map(&tm_c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, 32, 32)
                         : make_map(&tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, N, M, 64, 32);

@@ -105,9 +105,10 @@ struct Layout {
   // MX scale atoms per stage: this CTA's rows of A and all BN rows of B
   static constexpr uint32_t SF_BYTES = (KIND == kMx) ? 512 + 512 * (BN / 128) : 0;
   static constexpr uint32_t OFF_SF = S * STAGE_BYTES;
-  // per-tensor / MX: one 4 KB staging box per epilogue warp for the TMA stores of C
+  // per-tensor / MX / blockwise with 256-deep stages: one 4 KB staging box per epilogue
+  // warp for the TMA stores of C
   // (32 rows x 128 B, 128-byte swizzle; the box must start on 1024 bytes)
-  static constexpr bool TSTORE = !(KIND == kBlock1x128 || KIND == kBlockRowsB || KIND == kBlockK2);
+  static constexpr bool TSTORE = !(KIND == kBlock1x128 || KIND == kBlockRowsB);
   static constexpr uint32_t STG_BYTES = TSTORE ? Cfg<KIND>::EPI * 4096 : 0;
   static constexpr uint32_t OFF_STG = (OFF_SF + S * SF_BYTES + 1023) & ~1023u;
   static constexpr uint32_t OFF_BAR = OFF_STG + STG_BYTES;
@@ -647,12 +648,41 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           promote64(pb, f1);
         }
         if (!ok) break;
+        // C through TMA stores of this warp's staged 32-row x 128-byte box (as the other kinds)
+        const uint32_t stg = base + L::OFF_STG + static_cast<uint32_t>(warp - CTRL) * 4096u;
+        const int box_row = static_cast<int>(static_cast<int64_t>(tm) * TM + row_off) + 32 * q;
+        const uint32_t rowb = stg + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
         for (int c32 = 0; c32 < 2; ++c32) {
           float v[32];
 #pragma unroll
           for (int j = 0; j < 16; ++j) unpack_f32x2(acc[16 * c32 + j], v[2 * j], v[2 * j + 1]);
-          if (gcol0 + 32 * c32 < p.N) emit(v, grow, gcol0 + 32 * c32);
+          if (QOUT && (want_q || want_amax) && gcol0 + 32 * c32 < p.N) emit(v, grow, gcol0 + 32 * c32, false);
+          if (p.c == nullptr) continue;
+          if (fp32 || c32 == 0) {
+            if (lane == 0) bulk_wait_read<0>();   // the box's previous store has read it
+            __syncwarp();
+          }
+          if (fp32) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              sts128(rowb + ((static_cast<uint32_t>(k) ^ (lane & 7u)) << 4), __float_as_uint(v[4 * k]),
+                     __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              sts128(rowb + (((static_cast<uint32_t>(c32 * 4 + k)) ^ (lane & 7u)) << 4), pack_bf16(v[8 * k], v[8 * k + 1]),
+                     pack_bf16(v[8 * k + 2], v[8 * k + 3]), pack_bf16(v[8 * k + 4], v[8 * k + 5]),
+                     pack_bf16(v[8 * k + 6], v[8 * k + 7]));
+          }
+          if (fp32 || c32 == 1) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tm_c, stg, static_cast<int>(fp32 ? gcol0 + 32 * c32 : gcol0), box_row);
+              bulk_commit();
+            }
+          }
         }
       } else if (BLOCK) {
         const float* sa_row = static_cast<const float*>(p.sa) + grow * KB;
