@@ -38,7 +38,7 @@ UNIT = "TFLOP/s"
 FLUSH_BYTES = 256 << 20
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one blockwise GEMM launch at
 # 4096^3 from an ncu capture of the current kernel version; None when not captured for it
-TRAFFIC_GEMM = 34_152_192 + 476_160
+TRAFFIC_GEMM = 34_150_912 + 1_818_880
 
 
 def peaks():
@@ -373,7 +373,8 @@ def _time_kernel(fn, reps=20, flush=None):
 
 def run_sweep(fq, wl, dev):
     """Per-recipe kernel numbers: cast-transpose GB/s at 8192^2 and 16384^2 for each
-    recipe, and GEMM TFLOP/s per recipe at 4096^3 and the MX LLaMA-7B shapes."""
+    recipe, and GEMM TFLOP/s per recipe at 4096^3, the MX LLaMA-7B shapes and the per-tensor
+    GPT-175B linears (fprop, dgrad, wgrad)."""
     R, F = fq.Recipe, fq.Format
     pk = peaks()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -402,14 +403,22 @@ def run_sweep(fq, wl, dev):
               ("blockwise_4096", R.BLOCK_1x128, R.BLOCK_128x128, (4096, 4096, 4096)),
               ("mx_4096", R.MX_1x32_TILED, R.MX_1x32_TILED, (4096, 4096, 4096))]
     shapes += [(f"mx_{k}", R.MX_1x32_TILED, R.MX_1x32_TILED, v) for k, v in wl.CFG3_SHAPES.items()]
-    for name, ra, rb, (m, n, k) in shapes:
+    shapes = [(name, ra, rb, mnk, F.E4M3, F.E4M3, fq.OutDtype.BF16) for name, ra, rb, mnk in shapes]
+    # GPT-175B linears (2048 tokens), per-tensor: fprop E4M3 x E4M3 -> bf16, dgrad E5M2 dY x E4M3 W -> bf16,
+    # wgrad E5M2 dY^T x E4M3 X^T -> fp32
+    for lin, (fin, fout) in wl.CFG4_LINEARS.items():
+        t = wl.CFG4_TOKENS
+        shapes += [(f"gpt175b_{lin}_fprop", R.TENSOR, R.TENSOR, (t, fout, fin), F.E4M3, F.E4M3, fq.OutDtype.BF16),
+                   (f"gpt175b_{lin}_dgrad", R.TENSOR, R.TENSOR, (t, fin, fout), F.E5M2, F.E4M3, fq.OutDtype.BF16),
+                   (f"gpt175b_{lin}_wgrad", R.TENSOR, R.TENSOR, (fout, fin, t), F.E5M2, F.E4M3, fq.OutDtype.FP32)]
+    for name, ra, rb, (m, n, k), fa, fb, od in shapes:
         a = wl.normal_bf16((m, k), 1, 1.0, dev)
         b = wl.normal_bf16((n, k), 2, 0.02, dev)
         sc = torch.ones(1, dtype=torch.float32, device=dev)
-        qa, sa, _, _ = fq.cast_transpose(a, ra, F.E4M3, sc if ra == R.TENSOR else None, col=False)
-        qb, sb, _, _ = fq.cast_transpose(b, rb, F.E4M3, sc if rb == R.TENSOR else None, col=False)
-        c = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-        ms = _time_kernel(lambda: fq.fp8_scaled_gemm(qa, F.E4M3, ra, sa, qb, F.E4M3, rb, sb, c), flush=flush)
+        qa, sa, _, _ = fq.cast_transpose(a, ra, fa, sc if ra == R.TENSOR else None, col=False)
+        qb, sb, _, _ = fq.cast_transpose(b, rb, fb, sc if rb == R.TENSOR else None, col=False)
+        c = torch.empty((m, n), dtype=torch.float32 if od == fq.OutDtype.FP32 else torch.bfloat16, device=dev)
+        ms = _time_kernel(lambda: fq.fp8_scaled_gemm(qa, fa, ra, sa, qb, fb, rb, sb, c, od), flush=flush)
         tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
         out["gemm"][name] = {"us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1), "frac_fp8": round(tf / fp8_peak, 4)}
         del a, b, qa, qb, c
