@@ -54,6 +54,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same with a suspend-time hint: a thread whose phase is not complete sleeps up to
+// 1 ms in hardware (waking as soon as the phase completes) instead of returning at
+// once, so the loop below checks its abort flag and clock far less often.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed.  Gives up (returns
 // false) when *abort becomes non-zero or after kWaitTimeoutNs; a timeout ORs
 // `code` into the device error word and raises *abort for the other roles.
@@ -62,7 +77,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     if (abort_flag != nullptr && *abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
       atomicOr(err, code);
