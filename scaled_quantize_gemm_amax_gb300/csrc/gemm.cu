@@ -64,7 +64,6 @@ template <>
 struct Cfg<kBlockK2> {
   static constexpr int BN = 128, STAGES = 3, ACC = 4, EPI = 8, KSUB = 2, CTRL = 4;
 };
-
 // MMA-issuing threads.  One thread needs about 74 cycles to issue a 256x128x32 MMA
 // (measured by a clock trace), close to the 88 cycles the MMA runs, so with 128-wide
 // tiles a single issuer starves the tensor core once it also waits and commits.  With
@@ -570,6 +569,41 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
       if (PAIR && !leader) mbar_arrive_remote(mapa_shared(bar, 0));
       else mbar_arrive(bar);
     };
+    // C leaves through TMA stores: this warp's 32 rows x 128 bytes (32 fp32 or 64 bf16
+    // columns) at a time are staged in its swizzled box, so that every store writes whole
+    // lines (a thread per row storing its own 16 bytes would not).  Chunk c holds columns
+    // [gcol + 32 c, gcol + 32 c + 32) of this thread's row; bf16 chunks go out in pairs.
+    auto store_chunk = [&](const float (&v)[32], int c, int64_t gcol, int box_row) {
+      const uint32_t stg = base + L::OFF_STG + static_cast<uint32_t>(warp - CTRL) * 4096u;
+      if (fp32 || (c & 1) == 0) {
+        // the box is free once the previous store from it has read it
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+      }
+      // 16-byte chunk k of this thread's row of the box sits at chunk k ^ (row % 8)
+      const uint32_t rowb = stg + static_cast<uint32_t>(lane) * 128u;
+      if (fp32) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          sts128(rowb + ((static_cast<uint32_t>(k) ^ (lane & 7u)) << 4), __float_as_uint(v[4 * k]),
+                 __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
+      } else {
+        const uint32_t k0 = (c & 1) * 4;   // 32 bf16 = chunks 0..3 (even c) or 4..7 (odd c) of the row
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          sts128(rowb + (((k0 + k) ^ (lane & 7u)) << 4), pack_bf16(v[8 * k], v[8 * k + 1]),
+                 pack_bf16(v[8 * k + 2], v[8 * k + 3]), pack_bf16(v[8 * k + 4], v[8 * k + 5]),
+                 pack_bf16(v[8 * k + 6], v[8 * k + 7]));
+      }
+      if (fp32 || (c & 1) == 1) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tm_c, stg, static_cast<int>(fp32 ? gcol + 32 * c : gcol + 32 * (c - 1)), box_row);
+          bulk_commit();
+        }
+      }
+    };
     uint32_t acc_it = 0, part_it = 0;
     // stages (partial groups) this CTA runs in all; gated: the first GROUPS stages find
     // their partial groups free
@@ -648,41 +682,15 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           promote64(pb, f1);
         }
         if (!ok) break;
-        // C through TMA stores of this warp's staged 32-row x 128-byte box (as the other kinds)
-        const uint32_t stg = base + L::OFF_STG + static_cast<uint32_t>(warp - CTRL) * 4096u;
+        // C through TMA stores of this warp's staged box (as the other kinds)
         const int box_row = static_cast<int>(static_cast<int64_t>(tm) * TM + row_off) + 32 * q;
-        const uint32_t rowb = stg + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
         for (int c32 = 0; c32 < 2; ++c32) {
           float v[32];
 #pragma unroll
           for (int j = 0; j < 16; ++j) unpack_f32x2(acc[16 * c32 + j], v[2 * j], v[2 * j + 1]);
           if (QOUT && (want_q || want_amax) && gcol0 + 32 * c32 < p.N) emit(v, grow, gcol0 + 32 * c32, false);
-          if (p.c == nullptr) continue;
-          if (fp32 || c32 == 0) {
-            if (lane == 0) bulk_wait_read<0>();   // the box's previous store has read it
-            __syncwarp();
-          }
-          if (fp32) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              sts128(rowb + ((static_cast<uint32_t>(k) ^ (lane & 7u)) << 4), __float_as_uint(v[4 * k]),
-                     __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
-          } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              sts128(rowb + (((static_cast<uint32_t>(c32 * 4 + k)) ^ (lane & 7u)) << 4), pack_bf16(v[8 * k], v[8 * k + 1]),
-                     pack_bf16(v[8 * k + 2], v[8 * k + 3]), pack_bf16(v[8 * k + 4], v[8 * k + 5]),
-                     pack_bf16(v[8 * k + 6], v[8 * k + 7]));
-          }
-          if (fp32 || c32 == 1) {
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tm_c, stg, static_cast<int>(fp32 ? gcol0 + 32 * c32 : gcol0), box_row);
-              bulk_commit();
-            }
-          }
+          if (p.c != nullptr) store_chunk(v, c32, gcol0, box_row);
         }
       } else if (BLOCK) {
         const float* sa_row = static_cast<const float*>(p.sa) + grow * KB;
@@ -803,10 +811,6 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) release(base + L::OFF_TEMPTY + 8 * a);
-          // C leaves through TMA stores: this warp's 32 rows x 128 bytes (32 fp32 or 64 bf16
-          // columns) at a time are staged in its swizzled box, so that every store writes
-          // whole lines (a thread per row storing its own 16 bytes would not)
-          const uint32_t stg = base + L::OFF_STG + static_cast<uint32_t>(warp - CTRL) * 4096u;
           const int box_row = static_cast<int>(static_cast<int64_t>(tm) * TM + row_off) + 32 * q;
 #pragma unroll
           for (int c = 0; c < CH; ++c) {
@@ -815,36 +819,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
             for (int j = 0; j < 32; ++j)
               v[j] = (KIND == kTensor) ? __fmul_rn(__uint_as_float(r[c][j]), tensor_scale) : __uint_as_float(r[c][j]);
             if (QOUT && (want_q || want_amax) && gcol0 + 32 * c < p.N) emit(v, grow, gcol0 + 32 * c, false);
-            if (p.c == nullptr) continue;
-            if (fp32 || (c & 1) == 0) {
-              // the box is free once the previous store from it has read it
-              if (lane == 0) bulk_wait_read<0>();
-              __syncwarp();
-            }
-            // 16-byte chunk k of this thread's row of the box sits at chunk k ^ (row % 8)
-            const uint32_t rowb = stg + static_cast<uint32_t>(lane) * 128u;
-            if (fp32) {
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                sts128(rowb + ((static_cast<uint32_t>(k) ^ (lane & 7u)) << 4), __float_as_uint(v[4 * k]),
-                       __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
-            } else {
-              const uint32_t k0 = (c & 1) * 4;   // 32 bf16 = chunks 0..3 (even c) or 4..7 (odd c) of the row
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                sts128(rowb + (((k0 + k) ^ (lane & 7u)) << 4), pack_bf16(v[8 * k], v[8 * k + 1]),
-                       pack_bf16(v[8 * k + 2], v[8 * k + 3]), pack_bf16(v[8 * k + 4], v[8 * k + 5]),
-                       pack_bf16(v[8 * k + 6], v[8 * k + 7]));
-            }
-            if (fp32 || (c & 1) == 1) {
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) {
-                const int x = static_cast<int>(fp32 ? gcol0 + 32 * c : gcol0 + 32 * (c - 1));
-                tma_store_2d(&tm_c, stg, x, box_row);
-                bulk_commit();
-              }
-            }
+            if (p.c != nullptr) store_chunk(v, c, gcol0, box_row);
           }
         }
         ++acc_it;
@@ -949,8 +924,8 @@ cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUte
 
 }  // namespace
 
-int gemm_block_n(int kind) {
-  return kind == kBlock1x128 ? Cfg<kBlock1x128>::BN : (kind == kMx ? Cfg<kMx>::BN : Cfg<kTensor>::BN);
+int gemm_block_n(const GemmParams& p) {
+  return p.kind == kBlock1x128 ? Cfg<kBlock1x128>::BN : (p.kind == kMx ? Cfg<kMx>::BN : Cfg<kTensor>::BN);
 }
 
 // CTA pairs need M a multiple of 256.  Blockwise runs on pairs only with 256-deep
@@ -965,7 +940,7 @@ bool gemm_uses_pair(const GemmParams& p) {
   return true;
 }
 
-int gemm_b_box_rows(const GemmParams& p) { return gemm_uses_pair(p) ? gemm_block_n(p.kind) / 2 : gemm_block_n(p.kind); }
+int gemm_b_box_rows(const GemmParams& p) { return gemm_uses_pair(p) ? gemm_block_n(p) / 2 : gemm_block_n(p); }
 
 template <bool QOUT>
 cudaError_t launch_gemm_q(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,

@@ -129,8 +129,8 @@ struct GemmParams {
   int e5m2_c;
   uint32_t* err;
 };
-// Width (N) of one output tile of the GEMM variant.
-int gemm_block_n(int kind);
+// Width (N) of one output tile of the GEMM variant these parameters select.
+int gemm_block_n(const GemmParams& p);
 // Whether the GEMM runs on 2-CTA pairs (256-row tiles) for these parameters.
 bool gemm_uses_pair(const GemmParams& p);
 // Rows of B one TMA box carries (the tile width, or half of it for a pair).

@@ -136,17 +136,24 @@ def test_gemm_k_zero_writes_zeros():
 @pytest.mark.parametrize("ra,rb", PAIRS)
 @pytest.mark.parametrize("m,n,k", [(256, 256, 128), (512, 640, 384), (768, 384, 256)])
 def test_gemm_cta_pair_tiles(ra, rb, m, n, k):
-    # M a multiple of 256: the per-tensor and MX GEMMs run on 2-CTA pairs (blockwise: single CTAs)
+    # M a multiple of 256: 2-CTA pairs (blockwise: pairs when K / 128 is even, single CTAs
+    # for K = 128 and 384)
     x = wl.normal_bf16((m, k), 40, 1.0)
     w = wl.normal_bf16((n, k), 41, 0.02)
     gemm_check(x, w, ra, rb, F.E4M3, F.E5M2 if k == 384 else F.E4M3,
                out=fq.OutDtype.FP32 if m == 768 else fq.OutDtype.BF16)
 
 
-@pytest.mark.parametrize("m,n,k", [(2048, 1536, 512), (512, 256, 2048)])
-def test_gemm_blockwise_pairs_many_tiles(m, n, k):
-    # blockwise on CTA pairs (M % 256 == 0, K / 128 even): more 256x128 tiles than pairs
-    # (each pair walks several tiles), and a long K that wraps the stage ring many times
+@pytest.mark.parametrize("m,n,k,out", [
+    (2048, 1536, 512, fq.OutDtype.BF16),    # CTA pairs: 96 tiles of 256x128, more than pairs
+    (2048, 1408, 512, fq.OutDtype.BF16),    # CTA pairs, N % 256 == 128
+    (512, 256, 2048, fq.OutDtype.BF16),     # a long K that wraps the stage ring many times
+    (768, 1024, 640, fq.OutDtype.FP32),     # odd K blocks: single CTAs, FP32 output
+    (1536, 2304, 1152, fq.OutDtype.BF16),   # odd K blocks over 216 single-CTA tiles
+])
+def test_gemm_blockwise_pairs_many_tiles(m, n, k, out):
+    # blockwise with M % 256 == 0: CTA pairs with 256-deep stages when K / 128 is even,
+    # single CTAs otherwise; each pair (CTA) walks several tiles
     x = wl.normal_bf16((m, k), 50, 1.0)
     w = wl.normal_bf16((n, k), 51, 0.02)
-    gemm_check(x, w, R.BLOCK_1x128, R.BLOCK_128x128, F.E4M3, F.E4M3)
+    gemm_check(x, w, R.BLOCK_1x128, R.BLOCK_128x128, F.E4M3, F.E4M3, out=out)

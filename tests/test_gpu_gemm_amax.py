@@ -54,10 +54,12 @@ def check_fused(c_ref, c_amax, c_q, c_sinv, c_scale, fc, out):
 
 @pytest.mark.parametrize("ra,rb", PAIRS)
 @pytest.mark.parametrize("out", [fq.OutDtype.BF16, fq.OutDtype.FP32])
-def test_fused_output_quantization_matches_oracle(ra, rb, out):
-    # 512 x 384 output: pairs for the per-tensor / MX kernels, an N that hangs over 256-wide tiles
+@pytest.mark.parametrize("n", [384, 512])
+def test_fused_output_quantization_matches_oracle(ra, rb, out, n):
+    # 512 x n output (K = 640: 5 K blocks); N = 384 hangs over the 256-wide tiles, N = 512
+    # fills them
     x = wl.normal_bf16((512, 640), 60, 1.0)
-    w = wl.normal_bf16((384, 640), 61, 0.02)
+    w = wl.normal_bf16((n, 640), 61, 0.02)
     c_scale = 448.0 / 1.5          # outputs above 1.5 in magnitude saturate, most do not
     fc = F.E4M3
     c, c_amax, c_q, c_sinv, c_plain = run_fused(x, w, ra, rb, F.E4M3, F.E4M3, c_scale, fc, out)
