@@ -38,7 +38,7 @@ UNIT = "TFLOP/s"
 FLUSH_BYTES = 256 << 20
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one blockwise GEMM launch at
 # 4096^3 from an ncu capture of the current kernel version; None when not captured for it
-TRAFFIC_GEMM = 34_150_912 + 1_818_880
+TRAFFIC_GEMM = 34_140_416 + 1_971_200
 
 
 def peaks():
