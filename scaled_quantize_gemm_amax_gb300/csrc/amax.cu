@@ -28,8 +28,10 @@ __device__ __forceinline__ uint32_t fold16(uint32_t m, uint4 v) {
 }
 
 // Grid-stride max over 16-byte chunks (8 bf16 each), 8 independent loads in
-// flight per thread; the n % 8 tail is folded in by block 0.  One atomicMax per
-// block on the (non-negative) float bit pattern, which orders like the value.
+// flight per thread, the last round predicated (chunks past the end read as zero,
+// which leaves a max of magnitudes unchanged) so that no round has fewer loads in
+// flight; the n % 8 tail is folded in by block 0.  One atomicMax per block on the
+// (non-negative) float bit pattern, which orders like the value.
 __global__ void __launch_bounds__(kAmaxThreads) k_amax(const uint4* __restrict__ x16, int64_t n16,
                                                       const uint16_t* __restrict__ tail, int ntail,
                                                       float* __restrict__ amax) {
@@ -45,7 +47,13 @@ __global__ void __launch_bounds__(kAmaxThreads) k_amax(const uint4* __restrict__
 #pragma unroll
     for (int u = 0; u < kAmaxUnroll; ++u) m = fold16(m, v[u]);
   }
-  for (; i < n16; i += stride) m = fold16(m, __ldg(x16 + i));
+  if (i < n16) {
+    uint4 v[kAmaxUnroll];
+#pragma unroll
+    for (int u = 0; u < kAmaxUnroll; ++u) v[u] = i + u * stride < n16 ? __ldg(x16 + i + u * stride) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int u = 0; u < kAmaxUnroll; ++u) m = fold16(m, v[u]);
+  }
   float a = pair_max_f32(m);
   if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < ntail)
     a = fmaxf(a, fabsf(__uint_as_float(static_cast<uint32_t>(tail[threadIdx.x]) << 16)));
