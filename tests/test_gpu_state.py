@@ -86,3 +86,33 @@ def test_bounded_wait_times_out_and_context_survives():
     torch.cuda.synchronize()
     assert f32bits(host(amax))[0] == f32bits(oracle.amax(bits16(x)))
     assert_status_ok()
+
+
+def test_delayed_scaling_gpt175b_qkv_full_size():
+    # The GPT-175B QKV linear's X [2048, 12288] (E4M3) and dY [2048, 36864] (E5M2) over 32
+    # steps with the x10 spike at step 8, at full size: amax, history, position, scale and
+    # scale_inv bit for bit every step; the FP8 bytes on seeded rows of both copies.
+    st = {"x": fq.DelayedScaling(16, F.E4M3), "dy": fq.DelayedScaling(16, F.E5M2)}
+    ref = {"x": oracle.DelayedState(16, oracle.E4M3), "dy": oracle.DelayedState(16, oracle.E5M2)}
+    rng = np.random.default_rng(4100)
+    for t in range(32):
+        x, _, dy = wl.cfg4_step("qkv", t)
+        for key, x_t, fmt in (("x", x, F.E4M3), ("dy", dy, F.E5M2)):
+            rows, cols = x_t.shape
+            qr, _, qc, _ = fq.cast_transpose(x_t, R.TENSOR, fmt, st[key].scale, st[key].amax)
+            st[key].update()
+            torch.cuda.synchronize()
+            assert_status_ok()
+            xh = bits16(x_t)
+            r = np.unique(np.concatenate([[0, rows - 1], rng.choice(rows, 30, replace=False)]))
+            c = np.unique(np.concatenate([[0, cols - 1], rng.choice(cols, 30, replace=False)]))
+            q_r, _ = oracle.quantize_rowwise(xh[r], oracle.KIND_TENSOR, int(fmt), ref[key].scale[0])
+            q_c, _ = oracle.quantize_rowwise(np.ascontiguousarray(xh[:, c].T), oracle.KIND_TENSOR, int(fmt),
+                                             ref[key].scale[0])
+            assert_bytes_equal(host(qr[torch.as_tensor(r, device=qr.device)]), q_r, f"step {t} {key} q_row")
+            assert_bytes_equal(host(qc[torch.as_tensor(c, device=qc.device)]), q_c, f"step {t} {key} q_col")
+            ref[key].step(oracle.amax(xh))
+            assert_bytes_equal(f32bits(host(st[key].hist)), f32bits(ref[key].hist), f"step {t} {key} hist")
+            assert host(st[key].pos)[0] == ref[key].pos[0]
+            assert f32bits(host(st[key].scale))[0] == f32bits(ref[key].scale[0]), f"step {t} {key} scale"
+            assert f32bits(host(st[key].scale_inv))[0] == f32bits(ref[key].scale_inv[0]), f"step {t} {key} scale_inv"
