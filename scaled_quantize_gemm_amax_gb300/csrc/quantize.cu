@@ -114,6 +114,20 @@ __device__ __forceinline__ float reduce_scatter4(const float (&a)[4], int lane, 
   return fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, lo));
 }
 
+// The same with one barrier, for a caller that alternates between two `red` buffers: a
+// buffer is written again only two calls later, after every thread has passed the
+// caller's own barrier in between.
+__device__ __forceinline__ float block_max_1(float v, float* red, int warp, int lane) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) r = fmaxf(r, red[w]);
+  return r;
+}
+
 __device__ __forceinline__ float block_max(float v, float* red, int warp, int lane) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
@@ -136,6 +150,8 @@ __device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t b, int64_t
 // One 128x128 tile already in shared memory (stage buffer xs): both passes, scales
 // written to global memory, quantized bytes staged in outR (row-wise) and outT
 // (column-wise) for the TMA stores.  thr_amax accumulates this thread's |x| maximum.
+// `red` is this tile's block-maximum buffer (the caller alternates two), and every
+// thread of the CTA calls this (the 128x128 recipe synchronises inside).
 template <int RECIPE>
 __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs, uint32_t outR, uint32_t outT, int tr,
                                                int tc, int64_t row0, int64_t col0, float g_scale, float& thr_amax,
@@ -155,7 +171,7 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
 
   float tile_scale = g_scale;
   if (RECIPE == kBlock128x128) {
-    const float tmax = block_max(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), red, warp, lane);
+    const float tmax = block_max_1(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), red, warp, lane);
     thr_amax = fmaxf(thr_amax, tmax);
     tile_scale = scale_from_amax(tmax, fmax);
     if (tid == 0) {
@@ -311,17 +327,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tr = tile / p.tiles_c, tc = tile % p.tiles_c;
     const int64_t row0 = static_cast<int64_t>(tr) * kTile, col0 = static_cast<int64_t>(tc) * kTile;
 
+    // One barrier a tile.  Staging buffer `ob` was last read by the stores of two tiles
+    // ago, which thread 0 waited for before the previous tile's barrier.  A wait that
+    // timed out still runs the body (its results are dropped) so that every thread
+    // reaches the same barriers; the barrier then ends the loop on every thread.
     const bool ok = mbar_wait(base + kOffBar + 8 * s, (it / kStages) & 1, p.err, kErrTimeoutTmaLoad, nullptr);
-    if (tid == 0) bulk_wait_read<1>();  // staging buffer `ob` (used two tiles ago) has been read out
+
+    cast_tile_body<RECIPE>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red + (it & 1) * kWarps, tid,
+                           warp, lane);
+
+    fence_proxy_async_smem();
+    if (tid == 0) bulk_wait_read<0>();  // the previous tile's stores have read their staging buffer
     if (__syncthreads_or(!ok)) {
       failed = true;
       break;
     }
-
-    cast_tile_body<RECIPE>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red, tid, warp, lane);
-
-    fence_proxy_async_smem();
-    __syncthreads();
     if (tid == 0) {
       if (p.do_row) tma_store_2d(&tm_qrow, outR, static_cast<int>(col0), static_cast<int>(row0));
       if (p.do_col) tma_store_2d(&tm_qcol, outT, static_cast<int>(row0), static_cast<int>(col0));
@@ -469,28 +489,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_cast_jobs(const __grid_constant
     const int tr = lt / p.tiles_c, tc = lt % p.tiles_c;
     const int64_t row0 = static_cast<int64_t>(tr) * kTile, col0 = static_cast<int64_t>(tc) * kTile;
 
+    // one barrier a tile, as in k_cast_transpose
     const bool ok = mbar_wait(base + kOffBar + 8 * s, (it / kStages) & 1, p.err, kErrTimeoutTmaLoad, nullptr);
-    if (tid == 0) bulk_wait_read<1>();  // staging buffer `ob` (used two tiles ago) has been read out
+    float* const red_t = red + (it & 1) * kWarps;
+    switch (p.recipe) {
+      case kTensor:
+        cast_tile_body<kTensor>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red_t, tid, warp, lane);
+        break;
+      case kBlock1x128:
+        cast_tile_body<kBlock1x128>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red_t, tid, warp, lane);
+        break;
+      case kBlock128x128:
+        cast_tile_body<kBlock128x128>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red_t, tid, warp, lane);
+        break;
+      default:
+        cast_tile_body<kMx>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red_t, tid, warp, lane);
+        break;
+    }
+    fence_proxy_async_smem();
+    if (tid == 0) bulk_wait_read<0>();  // the previous tile's stores have read their staging buffer
     if (__syncthreads_or(!ok)) {
       failed = true;
       break;
     }
-    switch (p.recipe) {
-      case kTensor:
-        cast_tile_body<kTensor>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red, tid, warp, lane);
-        break;
-      case kBlock1x128:
-        cast_tile_body<kBlock1x128>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red, tid, warp, lane);
-        break;
-      case kBlock128x128:
-        cast_tile_body<kBlock128x128>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red, tid, warp, lane);
-        break;
-      default:
-        cast_tile_body<kMx>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red, tid, warp, lane);
-        break;
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
     if (tid == 0) {
       if (p.do_row) tma_store_2d(&J.m[j].qrow, outR, static_cast<int>(col0), static_cast<int>(row0));
       if (p.do_col) tma_store_2d(&J.m[j].qcol, outT, static_cast<int>(row0), static_cast<int>(col0));
