@@ -215,7 +215,7 @@ fp8_status scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const voi
   DeviceInfo* d;
   if (fp8_status st = device_info(&d)) return st;
   if (x.c_amax != nullptr) {
-    if (cudaMemsetAsync(x.c_amax, 0, sizeof(float), stream) != cudaSuccess) return FP8_ERR_CUDA;
+    if (launch_zero_f32(x.c_amax, 1, stream) != cudaSuccess) return FP8_ERR_CUDA;
   }
   if (M == 0 || N == 0 || K == 0) {
     // C = 0: amax 0 (set above), FP8 copy all +0 codes, scale_inv still written
@@ -296,7 +296,7 @@ fp8_status fp8_amax(const void* x, int64_t rows, int64_t cols, float* amax, cuda
   if (!aligned(x, 16) || !aligned(amax, 4)) return FP8_ERR_ALIGNMENT;
   DeviceInfo* d;
   if (fp8_status st = device_info(&d)) return st;
-  if (cudaMemsetAsync(amax, 0, sizeof(float), stream) != cudaSuccess) return FP8_ERR_CUDA;
+  if (launch_zero_f32(amax, 1, stream) != cudaSuccess) return FP8_ERR_CUDA;
   if (n == 0) return FP8_OK;
   return cuda_status(launch_amax(x, n, amax, d->num_sms, stream));
 }
@@ -328,13 +328,12 @@ fp8_status fp8_cast_transpose(const void* x, int64_t rows, int64_t cols, fp8_rec
     return st;
   if (plan.empty) {
     // nothing to cast (outputs of an empty tensor may be NULL); amax of nothing is 0
-    if (amax_out != nullptr && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess)
-      return FP8_ERR_CUDA;
+    if (amax_out != nullptr && launch_zero_f32(amax_out, 1, stream) != cudaSuccess) return FP8_ERR_CUDA;
     return FP8_OK;
   }
   DeviceInfo* d;
   if (fp8_status st = device_info(&d)) return st;
-  if (amax_out != nullptr && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess) return FP8_ERR_CUDA;
+  if (amax_out != nullptr && launch_zero_f32(amax_out, 1, stream) != cudaSuccess) return FP8_ERR_CUDA;
   plan.p.err = d->err;
   // only the per-tensor recipe can miss the tiled path (block recipes imply its alignment)
   if (!plan.tiled) return cuda_status(launch_cast_generic(plan.p, x, stream));
@@ -357,8 +356,7 @@ fp8_status fp8_cast_transpose_multi(const fp8_cast_job* jobs, int32_t n_jobs, cu
   CastJobs launch{};
   for (int i = 0; i < n_jobs; ++i) {
     CastPlan& pl = plans[i];
-    if (jobs[i].amax_out != nullptr && cudaMemsetAsync(jobs[i].amax_out, 0, sizeof(float), stream) != cudaSuccess)
-      return FP8_ERR_CUDA;
+    if (jobs[i].amax_out != nullptr && launch_zero_f32(jobs[i].amax_out, 1, stream) != cudaSuccess) return FP8_ERR_CUDA;
     if (pl.empty) continue;
     pl.p.err = d->err;
     if (!pl.tiled) {
@@ -425,7 +423,7 @@ fp8_status fp8_allreduce_sum(const void* g, int32_t k, int64_t n, fp8_format fmt
     return FP8_ERR_ALIGNMENT;
   DeviceInfo* d;
   if (fp8_status st = device_info(&d)) return st;
-  if (cudaMemsetAsync(amax, 0, sizeof(float), stream) != cudaSuccess) return FP8_ERR_CUDA;
+  if (launch_zero_f32(amax, 1, stream) != cudaSuccess) return FP8_ERR_CUDA;
   if (fp8_status st = cuda_status(launch_amax(g, static_cast<int64_t>(k) * n, amax, d->num_sms, stream))) return st;
   return cuda_status(launch_allreduce(g, k, n, amax, fmt == FP8_E5M2, q, scale_inv, out, d->num_sms, stream));
 }

@@ -57,6 +57,8 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 
 // ---- amax / scale / history (amax.cu)
 cudaError_t launch_reciprocal(const float* in, float* out, cudaStream_t s);
+// p[0 .. n) = 0 as a (programmatically launched) kernel, ahead of an atomicMax reduction
+cudaError_t launch_zero_f32(float* p, int n, cudaStream_t s);
 cudaError_t launch_amax(const void* x, int64_t n, float* amax, int num_sms, cudaStream_t s);
 cudaError_t launch_compute_scale(const float* amax, bool e5m2, float* scale, float* scale_inv, cudaStream_t s);
 cudaError_t launch_history_update(float* hist, int32_t len, int32_t* pos, const float* amax, bool e5m2, float* scale,

@@ -113,7 +113,7 @@ cudaError_t launch_allreduce_noalloc(const void* g, int k, int64_t n, bool e5m2,
   NoAllocDevice* d = nullptr;
   cudaError_t e = noalloc_device(&d);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(d->scratch, 0, static_cast<size_t>(k) * sizeof(float), s);
+  e = launch_zero_f32(d->scratch, k, s);
   if (e != cudaSuccess) return e;
   const int64_t n8 = n / 8;
   int64_t bx = (n8 + kRankAmaxThreads - 1) / kRankAmaxThreads;
