@@ -16,7 +16,9 @@
 //   col pass  -- ldmatrix.trans gives each lane two consecutive rows of one column;
 //                per-column amax by shuffles; bytes go to a second staging tile
 //                already transposed;
-//   both staging tiles leave through TMA stores (double-buffered).
+//   both staging tiles leave through TMA stores (double-buffered), and one barrier
+//   per tile separates a tile's shared-memory writes from its stores and the
+//   refill of its ring slot.
 // The optional per-tensor amax of the input (delayed scaling records it while
 // casting with the previous scale) is a block max + one atomicMax per CTA.
 #include <cuda_bf16.h>
