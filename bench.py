@@ -245,8 +245,7 @@ def run_ours(args, rank, world):
     assert fq.fp8_get_device_status() == fq.Status.OK
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clocks = ClockSampler(torch.cuda.current_device(), os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    clocks = ClockSampler(torch.cuda.current_device(), args.clocks_csv)
     clocks.start()
     time.sleep(0.2)
     barrier(world)
@@ -637,6 +636,7 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default=None, help="also write the raw clock samples of the timed region here")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
