@@ -861,18 +861,18 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
 // launch registers the split was sized for (with fewer, an increase would never be
 // granted and the epilogue warps would not start).  Checked once per device.
 template <class K>
-cudaError_t check_split_regs(K kern, bool split, bool (&checked)[kMaxDevices]) {
+cudaError_t check_split_regs(K kern, bool split, std::atomic<bool> (&checked)[kMaxDevices]) {
   if (!split) return cudaSuccess;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (checked[dev]) return cudaSuccess;
+  if (checked[dev].load(std::memory_order_acquire)) return cudaSuccess;
   cudaFuncAttributes fa;
   e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kSplitLaunchRegs) return cudaErrorInvalidConfiguration;
-  checked[dev] = true;
+  checked[dev].store(true, std::memory_order_release);
   return cudaSuccess;
 }
 
@@ -881,10 +881,10 @@ cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& tm_a, const CUte
                         const CUtensorMap& tm_sfb, const CUtensorMap& tm_c, int num_sms, cudaStream_t s) {
   using L = Layout<KIND, false>;
   static_assert(L::SMEM <= 232448, "shared memory budget");
-  static bool attr_done[kMaxDevices] = {};
+  static std::atomic<bool> attr_done[kMaxDevices] = {};
   cudaError_t e = ensure_smem_limit(k_gemm<KIND, false, QOUT>, static_cast<int>(L::SMEM), attr_done);
   if (e != cudaSuccess) return e;
-  static bool regs_checked[kMaxDevices] = {};
+  static std::atomic<bool> regs_checked[kMaxDevices] = {};
   e = check_split_regs(k_gemm<KIND, false, QOUT>, Cfg<KIND>::CTRL == 4, regs_checked);
   if (e != cudaSuccess) return e;
   const int64_t ntiles = (p.M / kBM) * ((p.N + L::BN - 1) / L::BN);
@@ -900,10 +900,10 @@ cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUte
   using L = Layout<KIND, true>;
   static_assert(L::SMEM <= 232448, "shared memory budget");
   auto kern = k_gemm<KIND, true, QOUT>;
-  static bool attr_done[kMaxDevices] = {};
+  static std::atomic<bool> attr_done[kMaxDevices] = {};
   cudaError_t e = ensure_smem_limit(kern, static_cast<int>(L::SMEM), attr_done);
   if (e != cudaSuccess) return e;
-  static bool regs_checked[kMaxDevices] = {};
+  static std::atomic<bool> regs_checked[kMaxDevices] = {};
   e = check_split_regs(kern, Cfg<KIND>::CTRL == 4, regs_checked);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

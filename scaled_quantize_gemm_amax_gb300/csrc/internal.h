@@ -1,5 +1,6 @@
 // internal.h -- launchers shared between the C-ABI layer and the kernel files.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -11,16 +12,17 @@ enum Recipe : int { kTensor = 0, kBlock1x128 = 1, kBlock128x128 = 2, kMx = 3 };
 constexpr int kMaxDevices = 64;
 
 // Raise a kernel's dynamic shared-memory limit once per device (the setting is
-// per function and device); `done` is the caller's per-kernel flag array.
+// per function and device); `done` is the caller's per-kernel flag array (atomic:
+// any host thread may launch; setting the attribute twice is harmless).
 template <typename Kernel>
-inline cudaError_t ensure_smem_limit(Kernel* fn, int bytes, bool (&done)[kMaxDevices]) {
+inline cudaError_t ensure_smem_limit(Kernel* fn, int bytes, std::atomic<bool> (&done)[kMaxDevices]) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (done[dev]) return cudaSuccess;
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done[dev] = true;
+  if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
   return e;
 }
 

@@ -538,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_cast_jobs(const __grid_constant
 template <int RECIPE>
 cudaError_t launch_tiled(const CastParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_qrow,
                          const CUtensorMap& tm_qcol, int num_sms, cudaStream_t s) {
-  static bool attr_done[kMaxDevices] = {};
+  static std::atomic<bool> attr_done[kMaxDevices] = {};
   cudaError_t e = ensure_smem_limit(k_cast_transpose<RECIPE>, static_cast<int>(kSmemBytes), attr_done);
   if (e != cudaSuccess) return e;
   const int ntiles = p.tiles_r * p.tiles_c;
@@ -559,7 +559,7 @@ cudaError_t launch_cast_transpose_tiled(const CastParams& p, const CUtensorMap& 
 }
 
 cudaError_t launch_cast_jobs(const CastJobs& jobs, int num_sms, cudaStream_t s) {
-  static bool attr_done[kMaxDevices] = {};
+  static std::atomic<bool> attr_done[kMaxDevices] = {};
   cudaError_t e = ensure_smem_limit(k_cast_jobs, static_cast<int>(kSmemBytes), attr_done);
   if (e != cudaSuccess) return e;
   const int ntiles = jobs.tile_start[jobs.n];
