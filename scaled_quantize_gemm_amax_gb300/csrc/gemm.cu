@@ -631,10 +631,13 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
       const int64_t grow = static_cast<int64_t>(tm) * TM + row_off + row;
       const int64_t gcol0 = static_cast<int64_t>(tn) * BN + h * COLS;
       if constexpr (WIDE) {
-        // Promotion, one 128-deep partial (this thread's 64 columns: two 32-column
-        // loads) per TMEM wait: while partial 0 of a group is promoted the loads of
-        // partial 1 are in flight, and while partial 1 is promoted those of the next
-        // group's partial 0.  Buffers pa / pb hold the group's two partials.
+        // Promotion, one partial group (two 128-deep partials; this thread's 64 columns
+        // of each: four 32-column loads) per TMEM wait.  All four loads are issued
+        // together and the group goes back to the MMA issuers as soon as they land;
+        // the FMAs follow, overlapping the MMAs that refill the group.  Releasing only
+        // after the FMAs (of this group's first partial and the previous group's
+        // second) left the tensor pipe idle for part of every hand-off.  Buffers
+        // pa / pb hold the group's two partials.
         const float* sa_row = static_cast<const float*>(p.sa) + grow * KB;
         const float* sb_tile = static_cast<const float*>(p.sb) + (gcol0 / 128) * KB;
         uint64_t acc[32];
@@ -664,9 +667,8 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         };
         // scale factors of the group being promoted and (loads in flight) of the next
         float sa0 = sa_row[0], sa1 = sa_row[1], sb0 = __ldg(sb_tile), sb1 = __ldg(sb_tile + 1);
-        bool ok = wait_full();
-        if (ok) load64(0, pa);
-        for (int kg = 0; ok && kg < NG; ++kg) {
+        bool ok = true;
+        for (int kg = 0; kg < NG; ++kg) {
           const float f0 = sa0 * sb0, f1 = sa1 * sb1;
           if (kg + 1 < NG) {
             sa0 = sa_row[2 * kg + 2];
@@ -674,11 +676,13 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
             sb0 = __ldg(sb_tile + 2 * kg + 2);
             sb1 = __ldg(sb_tile + 2 * kg + 3);
           }
-          tc_wait_ld(pa[0]);          // partial 0 of this group has landed
+          ok = wait_full();
+          if (!ok) break;
+          load64(0, pa);
+          load64(1, pb);
+          tc_wait_ld(pa[0]);          // both partials of the group have landed
           tc_tie(pa[1]);
-          load64(1, pb);              // partial 1 in flight
-          promote64(pa, f0);
-          tc_wait_ld(pb[0]);          // partial 1 has landed: the group's TMEM is read
+          tc_tie(pb[0]);
           tc_tie(pb[1]);
           tc_fence_before();
           __syncwarp();
@@ -688,10 +692,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
             if (next < total_groups) release(base + L::OFF_FULL + 8 * (next % S));
           }
           ++part_it;
-          if (kg + 1 < NG) {
-            ok = wait_full();
-            if (ok) load64(0, pa);    // the next group's partial 0 in flight
-          }
+          promote64(pa, f0);          // the FMAs run while the MMAs refill the group
           promote64(pb, f1);
         }
         if (!ok) break;
