@@ -665,17 +665,10 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[16 * c + j] = fma_f32x2(f2, pack_f32x2(r[c][2 * j], r[c][2 * j + 1]), acc[16 * c + j]);
         };
-        // scale factors of the group being promoted and (loads in flight) of the next
+        // scale factors of the group to promote next (loads in flight)
         float sa0 = sa_row[0], sa1 = sa_row[1], sb0 = __ldg(sb_tile), sb1 = __ldg(sb_tile + 1);
         bool ok = true;
         for (int kg = 0; kg < NG; ++kg) {
-          const float f0 = sa0 * sb0, f1 = sa1 * sb1;
-          if (kg + 1 < NG) {
-            sa0 = sa_row[2 * kg + 2];
-            sa1 = sa_row[2 * kg + 3];
-            sb0 = __ldg(sb_tile + 2 * kg + 2);
-            sb1 = __ldg(sb_tile + 2 * kg + 3);
-          }
           ok = wait_full();
           if (!ok) break;
           load64(0, pa);
@@ -692,6 +685,15 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
             if (next < total_groups) release(base + L::OFF_FULL + 8 * (next % S));
           }
           ++part_it;
+          // the scale factors are used only after the release (a tile's first ones were
+          // loaded at its start and may still be in flight)
+          const float f0 = sa0 * sb0, f1 = sa1 * sb1;
+          if (kg + 1 < NG) {
+            sa0 = sa_row[2 * kg + 2];
+            sa1 = sa_row[2 * kg + 3];
+            sb0 = __ldg(sb_tile + 2 * kg + 2);
+            sb1 = __ldg(sb_tile + 2 * kg + 3);
+          }
           promote64(pa, f0);          // the FMAs run while the MMAs refill the group
           promote64(pb, f1);
         }
