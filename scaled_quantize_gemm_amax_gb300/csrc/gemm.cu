@@ -64,6 +64,14 @@ template <>
 struct Cfg<kBlockK2> {
   static constexpr int BN = 128, STAGES = 3, ACC = 4, EPI = 8, KSUB = 2, CTRL = 4;
 };
+// The same with per-row B scales (1x128 x 1x128): each output column has its own factor
+// sB[n, kb].  The epilogue copies the tile's B scales into a shared table at each tile
+// start (per half of the tile's columns, [kb][64] floats, K / 128 <= kMaxTableKb) and
+// reads a k-block's 64 factors as broadcast 16-byte loads.
+constexpr int kBlockK2RowsB = 6;
+constexpr int kMaxTableKb = 64;
+template <>
+struct Cfg<kBlockK2RowsB> : Cfg<kBlockK2> {};
 // MMA-issuing threads.  One thread needs about 74 cycles to issue a 256x128x32 MMA
 // (measured by a clock trace), close to the 88 cycles the MMA runs, so with 128-wide
 // tiles a single issuer starves the tensor core once it also waits and commits.  With
@@ -71,7 +79,7 @@ struct Cfg<kBlockK2> {
 // and need no ordering between them: each gets its own issuing thread (warp 1 and the
 // warp after the epilogue warps), and both commit every stage.
 template <int KIND>
-__host__ __device__ constexpr int issuers_of() { return (KIND == kBlockK2 || KIND == kMx) ? 2 : 1; }
+__host__ __device__ constexpr int issuers_of() { return (KIND == kBlockK2 || KIND == kBlockK2RowsB || KIND == kMx) ? 2 : 1; }
 template <>
 struct Cfg<kMx> {
   static constexpr int BN = 256, STAGES = 3, ACC = 1, EPI = 8, KSUB = 1, CTRL = 2;
@@ -111,14 +119,19 @@ struct Layout {
   static constexpr bool TSTORE = !(KIND == kBlock1x128 || KIND == kBlockRowsB);
   static constexpr uint32_t STG_BYTES = TSTORE ? Cfg<KIND>::EPI * 4096 : 0;
   static constexpr uint32_t OFF_STG = (OFF_SF + S * SF_BYTES + 1023) & ~1023u;
-  static constexpr uint32_t OFF_BAR = OFF_STG + STG_BYTES;
+  // per-row B scales on CTA pairs: the tile's B-scale table, two halves of [kb][64] floats
+  static constexpr uint32_t TBL_HALF = KIND == kBlockK2RowsB ? kMaxTableKb * 64 * 4 : 0;
+  static constexpr uint32_t OFF_TBL = OFF_STG + STG_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_TBL + 2 * TBL_HALF;
   // barriers: full[S], empty[S], tfull[4], tempty[4], final
   static constexpr uint32_t OFF_FULL = OFF_BAR, OFF_EMPTY = OFF_BAR + 8 * S;
   static constexpr uint32_t OFF_TFULL = OFF_EMPTY + 8 * S, OFF_TEMPTY = OFF_TFULL + 32;
   static constexpr uint32_t OFF_FINAL = OFF_TEMPTY + 32;
   static constexpr uint32_t OFF_SFR = OFF_FINAL + 8;   // MX: a stage's scale factors are in TMEM
   static constexpr uint32_t OFF_TMEM = OFF_SFR + 8 * S, OFF_ABORT = OFF_TMEM + 4;
-  static constexpr uint32_t SMEM = OFF_ABORT + 64 + 1024;   // + alignment slack
+  // B-scale table barriers: tbl_full[2] (the half's table is filled), tbl_free[2] (read)
+  static constexpr uint32_t OFF_TBAR = (OFF_ABORT + 4 + 7) & ~7u;
+  static constexpr uint32_t SMEM = OFF_TBAR + 32 + 64 + 1024;   // + alignment slack
   // bytes one stage's full barrier expects (in a pair: the leader's barrier sees both CTAs' loads)
   static constexpr uint32_t TX_BYTES = PAIR ? 2 * (STAGE_BYTES + SF_BYTES) : STAGE_BYTES + SF_BYTES;
 };
@@ -151,6 +164,21 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
 
 __device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+
+__device__ __forceinline__ void sts32(uint32_t a, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+// volatile: stays after the barrier wait that precedes it
+__device__ __forceinline__ float4 lds128f(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 __device__ __forceinline__ void stg128(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -217,7 +245,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
            const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
   using L = Layout<KIND, PAIR>;
   constexpr int BN = L::BN, S = L::S, ACC = Cfg<KIND>::ACC, EPI = Cfg<KIND>::EPI;
-  constexpr bool BLOCK = (KIND == kBlock1x128 || KIND == kBlockRowsB || KIND == kBlockK2);   // promotion path
+  constexpr bool BLOCK = (KIND == kBlock1x128 || KIND == kBlockRowsB || KIND == kBlockK2 || KIND == kBlockK2RowsB);   // promotion path
   constexpr int KSUB = L::KSUB;
   constexpr int GROUPS = ACC / KSUB;   // partial-buffer groups (blockwise)
   static_assert(KSUB == 1 || BLOCK, "multi-block stages: blockwise only");
@@ -225,7 +253,8 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   // group that stage will write (in a pair, both CTAs' epilogues release on the
   // leader's barrier), so the MMA thread waits once per stage.
   constexpr bool GATED = BLOCK;
-  constexpr bool B_ROWS = (KIND == kBlockRowsB);                         // B scales per row
+  constexpr bool B_ROWS = (KIND == kBlockRowsB || KIND == kBlockK2RowsB);   // B scales per row
+  constexpr bool TABLE = (KIND == kBlockK2RowsB);                         // ... read from the shared table
   constexpr int COLS = BN / (EPI / 4);   // columns of the tile each epilogue thread owns
   constexpr int NISS = issuers_of<KIND>();
   // MX with two issuers: the second thread copies each stage's scale factors into TMEM
@@ -235,7 +264,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   constexpr int CTRL = Cfg<KIND>::CTRL;                 // warps before the epilogue warps
   constexpr int ISS1 = CTRL == 4 ? 2 : 2 + EPI;         // warp of the second MMA issuer
   constexpr bool WIDE = CTRL == 4;                      // 64-column partial loads (see Cfg)
-  static_assert(!WIDE || (BLOCK && KSUB == 2 && COLS == 64 && !B_ROWS), "wide promotion layout");
+  static_assert(!WIDE || (BLOCK && KSUB == 2 && COLS == 64 && B_ROWS == TABLE), "wide promotion layout");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - smem_u32(smem_raw));
@@ -266,6 +295,12 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
       mbar_init(base + L::OFF_TEMPTY + 8 * a, PAIR ? 2 * EPI : EPI);
     }
     mbar_init(base + L::OFF_FINAL, NISS);
+    if (TABLE) {
+      for (int hh = 0; hh < 2; ++hh) {
+        mbar_init(base + L::OFF_TBAR + 8 * hh, 4 * 32);     // every lane of the half's four warps
+        mbar_init(base + L::OFF_TBAR + 16 + 8 * hh, 4);     // one arrive per warp
+      }
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -618,6 +653,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
       }
     };
     uint32_t acc_it = 0, part_it = 0;
+    uint32_t tile_it = 0;   // tiles this CTA has finished (B-scale table phases)
     // stages (partial groups) this CTA runs in all; gated: the first GROUPS stages find
     // their partial groups free
     const uint32_t my_tiles = unit0 < ntiles ? static_cast<uint32_t>((ntiles - unit0 + units - 1) / units) : 0u;
@@ -665,8 +701,45 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[16 * c + j] = fma_f32x2(f2, pack_f32x2(r[c][2 * j], r[c][2 * j + 1]), acc[16 * c + j]);
         };
+        // per-row B scales: this half's table, and the factor of column j at k-block kb:
+        // sA[m, kb] * sB[n0 + j, kb] rounded once, then the FMA (as the single-CTA kernel)
+        const uint32_t tbl = base + L::OFF_TBL + static_cast<uint32_t>(h) * L::TBL_HALF;
+        auto promote64t = [&](const uint32_t (&r)[2][32], float sa, int kb) {
+          const uint64_t sa2 = pack_f32x2(sa, sa);
+          const uint32_t trow = tbl + static_cast<uint32_t>(kb) * 256u;
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const float4 fb = lds128f(trow + static_cast<uint32_t>(32 * c + 4 * jj) * 4u);
+              const uint64_t f01 = mul_f32x2(sa2, pack_f32x2(fb.x, fb.y));
+              const uint64_t f23 = mul_f32x2(sa2, pack_f32x2(fb.z, fb.w));
+              acc[16 * c + 2 * jj] = fma_f32x2(f01, pack_f32x2(r[c][4 * jj], r[c][4 * jj + 1]), acc[16 * c + 2 * jj]);
+              acc[16 * c + 2 * jj + 1] =
+                  fma_f32x2(f23, pack_f32x2(r[c][4 * jj + 2], r[c][4 * jj + 3]), acc[16 * c + 2 * jj + 1]);
+            }
+        };
+        if constexpr (TABLE) {
+          // The half's four warps fill its table with this tile's B scales (warp q: its 16
+          // columns, every k-block), once all four have finished reading the previous tile's.
+          const uint32_t tbar_full = base + L::OFF_TBAR + 8 * h, tbar_free = base + L::OFF_TBAR + 16 + 8 * h;
+          if (tile_it > 0 &&
+              !__all_sync(0xFFFFFFFFu, mbar_wait(tbar_free, (tile_it - 1) & 1u, p.err, kErrTimeoutMma, abort_flag)))
+            break;
+          const int cq = 16 * q + (lane & 15);
+          const float* src = static_cast<const float*>(p.sb) + (gcol0 + cq) * KB;
+#pragma unroll 4
+          for (int kb = lane >> 4; kb < KB; kb += 2) sts32(tbl + static_cast<uint32_t>(kb * 64 + cq) * 4u, __ldg(src + kb));
+          mbar_arrive(tbar_full);   // every lane: its own stores are released by its arrive
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(tbar_full, tile_it & 1u, p.err, kErrTimeoutMma, abort_flag))) break;
+        }
         // scale factors of the group to promote next (loads in flight)
-        float sa0 = sa_row[0], sa1 = sa_row[1], sb0 = __ldg(sb_tile), sb1 = __ldg(sb_tile + 1);
+        float sa0 = sa_row[0], sa1 = sa_row[1];
+        float sb0 = 0.0f, sb1 = 0.0f;
+        if constexpr (!TABLE) {
+          sb0 = __ldg(sb_tile);
+          sb1 = __ldg(sb_tile + 1);
+        }
         bool ok = true;
         for (int kg = 0; kg < NG; ++kg) {
           ok = wait_full();
@@ -687,17 +760,32 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           ++part_it;
           // the scale factors are used only after the release (a tile's first ones were
           // loaded at its start and may still be in flight)
-          const float f0 = sa0 * sb0, f1 = sa1 * sb1;
-          if (kg + 1 < NG) {
-            sa0 = sa_row[2 * kg + 2];
-            sa1 = sa_row[2 * kg + 3];
-            sb0 = __ldg(sb_tile + 2 * kg + 2);
-            sb1 = __ldg(sb_tile + 2 * kg + 3);
+          if constexpr (TABLE) {
+            const float a0 = sa0, a1 = sa1;
+            if (kg + 1 < NG) {
+              sa0 = sa_row[2 * kg + 2];
+              sa1 = sa_row[2 * kg + 3];
+            }
+            promote64t(pa, a0, 2 * kg);   // the FMAs run while the MMAs refill the group
+            promote64t(pb, a1, 2 * kg + 1);
+          } else {
+            const float f0 = sa0 * sb0, f1 = sa1 * sb1;
+            if (kg + 1 < NG) {
+              sa0 = sa_row[2 * kg + 2];
+              sa1 = sa_row[2 * kg + 3];
+              sb0 = __ldg(sb_tile + 2 * kg + 2);
+              sb1 = __ldg(sb_tile + 2 * kg + 3);
+            }
+            promote64(pa, f0);          // the FMAs run while the MMAs refill the group
+            promote64(pb, f1);
           }
-          promote64(pa, f0);          // the FMAs run while the MMAs refill the group
-          promote64(pb, f1);
         }
         if (!ok) break;
+        if constexpr (TABLE) {
+          __syncwarp();   // every lane's table reads of this tile are done
+          if (lane == 0) mbar_arrive(base + L::OFF_TBAR + 16 + 8 * h);
+          ++tile_it;
+        }
         // C through TMA stores of this warp's staged box (as the other kinds)
         const int box_row = static_cast<int>(static_cast<int64_t>(tm) * TM + row_off) + 32 * q;
 #pragma unroll
@@ -952,7 +1040,7 @@ int gemm_block_n(const GemmParams& p) {
 // made the blockwise pair 40 % slower (measured).
 bool gemm_uses_pair(const GemmParams& p) {
   if (p.M % (2 * kBM) != 0) return false;
-  if (p.kind == kBlock1x128) return !p.b_1x128 && (p.K / kBK) % 2 == 0;
+  if (p.kind == kBlock1x128) return (p.K / kBK) % 2 == 0 && (!p.b_1x128 || p.K / kBK <= kMaxTableKb);
   return true;
 }
 
@@ -966,7 +1054,9 @@ cudaError_t launch_gemm_q(const GemmParams& p, const CUtensorMap& tm_a, const CU
       return gemm_uses_pair(p) ? launch_pair<kTensor, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s)
                                : launch_kind<kTensor, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);
     case kBlock1x128:
-      if (p.b_1x128) return launch_kind<kBlockRowsB, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);
+      if (p.b_1x128)
+        return gemm_uses_pair(p) ? launch_pair<kBlockK2RowsB, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s)
+                                 : launch_kind<kBlockRowsB, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);
       if (gemm_uses_pair(p)) return launch_pair<kBlockK2, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);
       return (p.K / kBK) % 2 == 0 ? launch_kind<kBlockK2, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s)
                                   : launch_kind<kBlock1x128, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);

@@ -157,3 +157,32 @@ def test_gemm_blockwise_pairs_many_tiles(m, n, k, out):
     x = wl.normal_bf16((m, k), 50, 1.0)
     w = wl.normal_bf16((n, k), 51, 0.02)
     gemm_check(x, w, R.BLOCK_1x128, R.BLOCK_128x128, F.E4M3, F.E4M3, out=out)
+
+
+def _block_spread(t, seed):
+    """Multiply each 1x128 block of t by its own power of two (exact in BF16), so that a
+    scale taken from the wrong row, column or k-block is far off."""
+    r, c = t.shape
+    e = (torch.arange(r, device=t.device)[:, None] * 3 + torch.arange(c // 128, device=t.device)[None, :] * 5 + seed) % 7 - 3
+    return t * torch.exp2(e.float()).repeat_interleave(128, dim=1).to(t.dtype)
+
+
+@pytest.mark.parametrize("m,n,k,out,spread", [
+    (2048, 1536, 512, fq.OutDtype.FP32, True),    # CTA pairs: 96 tiles, some pairs refill their B-scale table
+    (4096, 2048, 256, fq.OutDtype.FP32, True),    # two k-blocks (the shortest pair K), 256 tiles: 3-4 a pair
+    (1280, 768, 1024, fq.OutDtype.FP32, True),    # M = 5 x 256
+    (1280, 768, 1024, fq.OutDtype.BF16, False),   # BF16 output
+    (512, 1024, 8192, fq.OutDtype.FP32, True),    # 64 k-blocks: the largest table
+    (512, 512, 8448, fq.OutDtype.FP32, True),     # 66 k-blocks: past the table, single CTAs
+])
+def test_gemm_blockwise_rows_b_many_tiles(m, n, k, out, spread):
+    # 1x128 x 1x128 (the weight-gradient pairing: a scale per row of B and k-block): CTA
+    # pairs reading B's scales from a per-tile table when K / 128 is even and at most 64,
+    # single CTAs otherwise.  The spread inputs use FP32 output: with their range, the
+    # exact product rounded to BF16 alone exceeds the max-abs bar (x1.04 at 1280x768x1024,
+    # computed with the oracle), so BF16 output is checked on plain normal inputs.
+    x = wl.normal_bf16((m, k), 60, 1.0)
+    w = wl.normal_bf16((n, k), 61, 0.02)
+    if spread:
+        x, w = _block_spread(x, 1), _block_spread(w, 4)
+    gemm_check(x, w, R.BLOCK_1x128, R.BLOCK_1x128, F.E4M3, F.E4M3, out=out)
