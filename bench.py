@@ -431,6 +431,11 @@ def run_sweep(fq, wl, dev):
         shapes += [(f"gpt175b_{lin}_fprop", R.TENSOR, R.TENSOR, (t, fout, fin), F.E4M3, F.E4M3, fq.OutDtype.BF16),
                    (f"gpt175b_{lin}_dgrad", R.TENSOR, R.TENSOR, (t, fin, fout), F.E5M2, F.E4M3, fq.OutDtype.BF16),
                    (f"gpt175b_{lin}_wgrad", R.TENSOR, R.TENSOR, (fout, fin, t), F.E5M2, F.E4M3, fq.OutDtype.FP32)]
+    # blockwise weight gradient: 1x128 x 1x128 (a scale per row of B), FP32 out
+    shapes += [("blockwise_wgrad_4096", R.BLOCK_1x128, R.BLOCK_1x128, (4096, 4096, 4096), F.E4M3, F.E4M3,
+                fq.OutDtype.FP32),
+               ("gpt175b_qkv_wgrad_blockwise", R.BLOCK_1x128, R.BLOCK_1x128,
+                (wl.CFG4_LINEARS["qkv"][1], wl.CFG4_LINEARS["qkv"][0], wl.CFG4_TOKENS), F.E5M2, F.E4M3, fq.OutDtype.FP32)]
     for name, ra, rb, (m, n, k), fa, fb, od in shapes:
         a = wl.normal_bf16((m, k), 1, 1.0, dev)
         b = wl.normal_bf16((n, k), 2, 0.02, dev)
@@ -522,7 +527,7 @@ def run_reference(args, rank, world):
 
 
 CASES = ("cast_tensor", "cast_1x128", "cast_128x128", "cast_mx", "amax", "gemm_tensor", "gemm_block", "gemm_mx",
-         "gemm_amax", "dequant_tensor", "dequant_1x128", "dequant_128x128", "dequant_mx", "allreduce")
+         "gemm_block_wgrad", "gemm_amax", "dequant_tensor", "dequant_1x128", "dequant_128x128", "dequant_mx", "allreduce")
 
 
 def run_case(args):
@@ -608,15 +613,19 @@ def run_case(args):
         res = {"case": args.case, "size": s, "us": round(ms * 1e3, 2), "TFLOP/s": round(tf, 1),
                "frac_fp8": round(tf / (2 * pk["bf16_tflops"]), 4), "unfused_us": round(ms_u * 1e3, 2)}
     else:
-        ra = {"gemm_tensor": R.TENSOR, "gemm_block": R.BLOCK_1x128, "gemm_mx": R.MX_1x32_TILED}[args.case]
-        rb = {"gemm_tensor": R.TENSOR, "gemm_block": R.BLOCK_128x128, "gemm_mx": R.MX_1x32_TILED}[args.case]
+        # gemm_block_wgrad: the weight-gradient pairing, 1x128 x 1x128 (a scale per row of B), FP32 out
+        ra = {"gemm_tensor": R.TENSOR, "gemm_block": R.BLOCK_1x128, "gemm_mx": R.MX_1x32_TILED,
+              "gemm_block_wgrad": R.BLOCK_1x128}[args.case]
+        rb = {"gemm_tensor": R.TENSOR, "gemm_block": R.BLOCK_128x128, "gemm_mx": R.MX_1x32_TILED,
+              "gemm_block_wgrad": R.BLOCK_1x128}[args.case]
+        od = fq.OutDtype.FP32 if args.case == "gemm_block_wgrad" else fq.OutDtype.BF16
         a = wl.normal_bf16((s, s), 1, 1.0, dev)
         b = wl.normal_bf16((s, s), 2, 0.02, dev)
         sc1 = torch.ones(1, dtype=torch.float32, device=dev)
         qa, sa, _, _ = fq.cast_transpose(a, ra, F.E4M3, sc1 if ra == R.TENSOR else None, col=False)
         qb, sb, _, _ = fq.cast_transpose(b, rb, F.E4M3, sc1 if rb == R.TENSOR else None, col=False)
-        c = torch.empty((s, s), dtype=torch.bfloat16, device=dev)
-        ms = _time_kernel(lambda: fq.fp8_scaled_gemm(qa, F.E4M3, ra, sa, qb, F.E4M3, rb, sb, c), reps=args.steps,
+        c = torch.empty((s, s), dtype=torch.float32 if od == fq.OutDtype.FP32 else torch.bfloat16, device=dev)
+        ms = _time_kernel(lambda: fq.fp8_scaled_gemm(qa, F.E4M3, ra, sa, qb, F.E4M3, rb, sb, c, od), reps=args.steps,
                           flush=flush)
         tf = 2.0 * s ** 3 / (ms * 1e-3) / 1e12
         res = {"case": args.case, "size": s, "us": round(ms * 1e3, 2), "TFLOP/s": round(tf, 1),
