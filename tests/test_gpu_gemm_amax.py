@@ -55,11 +55,13 @@ def check_fused(c_ref, c_amax, c_q, c_sinv, c_scale, fc, out):
 @pytest.mark.parametrize("ra,rb", PAIRS)
 @pytest.mark.parametrize("out", [fq.OutDtype.BF16, fq.OutDtype.FP32])
 @pytest.mark.parametrize("n", [384, 512])
-def test_fused_output_quantization_matches_oracle(ra, rb, out, n):
-    # 512 x n output (K = 640: 5 K blocks); N = 384 hangs over the 256-wide tiles, N = 512
-    # fills them
-    x = wl.normal_bf16((512, 640), 60, 1.0)
-    w = wl.normal_bf16((n, 640), 61, 0.02)
+@pytest.mark.parametrize("k", [640, 512])
+def test_fused_output_quantization_matches_oracle(ra, rb, out, n, k):
+    # 512 x n output; N = 384 hangs over the 256-wide tiles, N = 512 fills them.  K = 640
+    # (5 K blocks): the blockwise pairings run on single CTAs; K = 512 (4 K blocks): on CTA
+    # pairs with 256-deep stages
+    x = wl.normal_bf16((512, k), 60, 1.0)
+    w = wl.normal_bf16((n, k), 61, 0.02)
     c_scale = 448.0 / 1.5          # outputs above 1.5 in magnitude saturate, most do not
     fc = F.E4M3
     c, c_amax, c_q, c_sinv, c_plain = run_fused(x, w, ra, rb, F.E4M3, F.E4M3, c_scale, fc, out)
