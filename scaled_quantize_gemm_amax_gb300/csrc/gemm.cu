@@ -88,8 +88,9 @@ struct Cfg<kMx> {
 // CTRL = 4: warps 0..3 (producer, the two MMA issuers, an idle warp) form a warpgroup
 // that gives registers to the two epilogue warpgroups (warps 4..11) with setmaxnreg, so
 // that the promotion can hold both 128-deep partials of a group (its 64 columns of
-// each) in registers at once and hand the group back before its FMAs.  The kernel must be launched with kSplitLaunchRegs a thread (checked on the
-// host before the first launch: an increase beyond the launch pool is never granted).
+// each) in registers at once and hand the group back before its FMAs.  The kernel must
+// be launched with kSplitLaunchRegs a thread (checked on the host before the first
+// launch: an increase beyond the launch pool is never granted).
 constexpr int kSplitLaunchRegs = 168, kCtrlRegs = 72, kEpiRegs = 216;
 static_assert(128 * kCtrlRegs + 256 * kEpiRegs <= 384 * kSplitLaunchRegs, "register split exceeds the launch pool");
 static_assert(kCtrlRegs + 2 * kEpiRegs <= 512, "register split exceeds a sub-partition");
