@@ -240,7 +240,9 @@ fp8_status fp8_allreduce_sum(const void* g, int32_t k, int64_t n, fp8_format fmt
  * a device share it: calls whose executions overlap (other streams, other host
  * threads) race and must be ordered by the caller.  The first call on a device
  * looks up the scratch address (cudaGetSymbolAddress, with that device current)
- * and keeps it; make that first call before any stream capture.
+ * and keeps it; make that first call before any stream capture.  A first call
+ * made while `stream` is being captured does nothing and returns
+ * FP8_ERR_INVALID_ARG.
  */
 fp8_status fp8_allreduce_sum_noalloc(const void* g, int32_t k, int64_t n, fp8_format fmt, uint8_t* q, float* scale_inv,
                                      float* out, cudaStream_t stream);

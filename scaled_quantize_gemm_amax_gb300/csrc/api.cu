@@ -2,7 +2,9 @@
 // dispatch to the kernels.  All checks run on the host before anything is
 // enqueued, and before any CUDA call, so a rejected call has no effect.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -16,8 +18,10 @@ namespace {
 // The device error word (one per device that loads the library).
 __device__ uint32_t g_error_word;
 
+// `ready` is stored with release order once the other fields are filled in and loaded
+// with acquire order, so the unlocked check in device_info() is well defined.
 struct DeviceInfo {
-  bool ready = false;
+  std::atomic<bool> ready{false};
   int num_sms = 0;
   uint32_t* err = nullptr;
 };
@@ -28,16 +32,16 @@ fp8_status device_info(DeviceInfo** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8_ERR_CUDA;
   DeviceInfo& d = g_devices[dev];
-  if (!d.ready) {
+  if (!d.ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_relaxed)) {
       int n = 0;
       if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FP8_ERR_CUDA;
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return FP8_ERR_CUDA;
       d.num_sms = n;
       d.err = static_cast<uint32_t*>(p);
-      d.ready = true;
+      d.ready.store(true, std::memory_order_release);
     }
   }
   *out = &d;
@@ -75,6 +79,30 @@ bool valid_fmt(fp8_format f) { return f == FP8_E4M3 || f == FP8_E5M2; }
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;   // TMA coordinates are signed 32-bit
 
 fp8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
+
+// One NVTX range per C-ABI call, in the "fp8q" domain, so that a profiler's timeline
+// shows which entry point enqueued which kernels.  With no tool attached the NVTX
+// calls return at once.
+class ApiRange {
+ public:
+  explicit ApiRange(const char* name) {
+    nvtxEventAttributes_t a = {};
+    a.version = NVTX_VERSION;
+    a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+    a.message.ascii = name;
+    nvtxDomainRangePushEx(domain(), &a);
+  }
+  ~ApiRange() { nvtxDomainRangePop(domain()); }
+  ApiRange(const ApiRange&) = delete;
+  ApiRange& operator=(const ApiRange&) = delete;
+
+ private:
+  static nvtxDomainHandle_t domain() {
+    static const nvtxDomainHandle_t d = nvtxDomainCreateA("fp8q");
+    return d;
+  }
+};
 
 }  // namespace
 }  // namespace fp8q
@@ -290,6 +318,7 @@ const char* fp8_status_string(fp8_status s) {
 }
 
 fp8_status fp8_amax(const void* x, int64_t rows, int64_t cols, float* amax, cudaStream_t stream) {
+  ApiRange nvtx_range("fp8_amax");
   if (rows < 0 || cols < 0 || amax == nullptr) return FP8_ERR_INVALID_ARG;
   const int64_t n = rows * cols;
   if (n > 0 && x == nullptr) return FP8_ERR_INVALID_ARG;
@@ -303,6 +332,7 @@ fp8_status fp8_amax(const void* x, int64_t rows, int64_t cols, float* amax, cuda
 
 fp8_status fp8_compute_scale(const float* amax, fp8_format fmt, float* scale, float* scale_inv,
                              cudaStream_t stream) {
+  ApiRange nvtx_range("fp8_compute_scale");
   if (amax == nullptr || scale == nullptr || scale_inv == nullptr || !valid_fmt(fmt)) return FP8_ERR_INVALID_ARG;
   if (!aligned(amax, 4) || !aligned(scale, 4) || !aligned(scale_inv, 4)) return FP8_ERR_ALIGNMENT;
   return cuda_status(launch_compute_scale(amax, fmt == FP8_E5M2, scale, scale_inv, stream));
@@ -310,6 +340,7 @@ fp8_status fp8_compute_scale(const float* amax, fp8_format fmt, float* scale, fl
 
 fp8_status amax_history_update(float* hist, int32_t len, int32_t* pos, const float* amax, fp8_format fmt,
                                float* scale, float* scale_inv, cudaStream_t stream) {
+  ApiRange nvtx_range("amax_history_update");
   if (hist == nullptr || pos == nullptr || amax == nullptr || scale == nullptr || scale_inv == nullptr || len < 1 ||
       !valid_fmt(fmt))
     return FP8_ERR_INVALID_ARG;
@@ -323,6 +354,7 @@ fp8_status amax_history_update(float* hist, int32_t len, int32_t* pos, const flo
 fp8_status fp8_cast_transpose(const void* x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
                               const float* scale, float* amax_out, uint8_t* q_row, void* s_row, uint8_t* q_col,
                               void* s_col, cudaStream_t stream) {
+  ApiRange nvtx_range("fp8_cast_transpose");
   CastPlan plan;
   if (fp8_status st = plan_cast(x, rows, cols, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_col, &plan))
     return st;
@@ -341,6 +373,7 @@ fp8_status fp8_cast_transpose(const void* x, int64_t rows, int64_t cols, fp8_rec
 }
 
 fp8_status fp8_cast_transpose_multi(const fp8_cast_job* jobs, int32_t n_jobs, cudaStream_t stream) {
+  ApiRange nvtx_range("fp8_cast_transpose_multi");
   if (n_jobs < 0 || n_jobs > kMaxCastJobs || (n_jobs > 0 && jobs == nullptr)) return FP8_ERR_INVALID_ARG;
   CastPlan plans[kMaxCastJobs];
   // every job is checked before any device work
@@ -376,12 +409,14 @@ fp8_status fp8_cast_transpose_multi(const fp8_cast_job* jobs, int32_t n_jobs, cu
 
 fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
                         const float* scale, float* amax_out, uint8_t* q, void* s, cudaStream_t stream) {
+  ApiRange nvtx_range("fp8_quantize");
   if (q == nullptr && rows > 0 && cols > 0) return FP8_ERR_INVALID_ARG;
   return fp8_cast_transpose(x, rows, cols, recipe, fmt, scale, amax_out, q, s, nullptr, nullptr, stream);
 }
 
 fp8_status fp8_dequantize(const uint8_t* q, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
                           const void* s, void* y, cudaStream_t stream) {
+  ApiRange nvtx_range("fp8_dequantize");
   if (rows < 0 || cols < 0 || !valid_fmt(fmt) || recipe < FP8_TENSOR || recipe > FP8_MX_1x32_TILED)
     return FP8_ERR_INVALID_ARG;
   if (rows == 0 || cols == 0) return FP8_OK;
@@ -414,6 +449,7 @@ fp8_status fp8_dequantize(const uint8_t* q, int64_t rows, int64_t cols, fp8_reci
 
 fp8_status fp8_allreduce_sum(const void* g, int32_t k, int64_t n, fp8_format fmt, float* amax, uint8_t* q,
                              float* scale_inv, float* out, cudaStream_t stream) {
+  ApiRange nvtx_range("fp8_allreduce_sum");
   if (k < 1 || n < 0 || !valid_fmt(fmt)) return FP8_ERR_INVALID_ARG;
   if (n == 0) return FP8_OK;
   if (g == nullptr || amax == nullptr || q == nullptr || scale_inv == nullptr || out == nullptr)
@@ -430,18 +466,23 @@ fp8_status fp8_allreduce_sum(const void* g, int32_t k, int64_t n, fp8_format fmt
 
 fp8_status fp8_allreduce_sum_noalloc(const void* g, int32_t k, int64_t n, fp8_format fmt, uint8_t* q, float* scale_inv,
                                      float* out, cudaStream_t stream) {
+  ApiRange nvtx_range("fp8_allreduce_sum_noalloc");
   if (k < 1 || n < 0 || !valid_fmt(fmt)) return FP8_ERR_INVALID_ARG;
   if (k > noalloc_max_ranks()) return FP8_ERR_SHAPE;   // more ranks than the scratch has slots
   if (n == 0) return FP8_OK;
   if (g == nullptr || q == nullptr || scale_inv == nullptr || out == nullptr) return FP8_ERR_INVALID_ARG;
   if (n % 8 || n > kMaxDim) return FP8_ERR_SHAPE;
   if (!aligned(g, 16) || !aligned(out, 16) || !aligned(q, 8) || !aligned(scale_inv, 4)) return FP8_ERR_ALIGNMENT;
-  return cuda_status(launch_allreduce_noalloc(g, k, n, fmt == FP8_E5M2, q, scale_inv, out, stream));
+  const cudaError_t e = launch_allreduce_noalloc(g, k, n, fmt == FP8_E5M2, q, scale_inv, out, stream);
+  // the first call on a device was made inside a stream capture: refused before any work
+  if (e == cudaErrorStreamCaptureUnsupported) return FP8_ERR_INVALID_ARG;
+  return cuda_status(e);
 }
 
 fp8_status fp8_scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const void* sA, const uint8_t* B,
                            fp8_format fb, fp8_recipe rb, const void* sB, int64_t M, int64_t N, int64_t K, void* C,
                            fp8_out_dtype out, cudaStream_t stream) {
+  ApiRange nvtx_range("fp8_scaled_gemm");
   return scaled_gemm(A, fa, ra, sA, B, fb, rb, sB, M, N, K, C, out, GemmExtra{}, stream);
 }
 
@@ -449,6 +490,7 @@ fp8_status fp8_scaled_gemm_amax(const uint8_t* A, fp8_format fa, fp8_recipe ra, 
                                 fp8_format fb, fp8_recipe rb, const void* sB, int64_t M, int64_t N, int64_t K, void* C,
                                 fp8_out_dtype out, float* c_amax, const float* c_scale, fp8_format fc, uint8_t* C_q,
                                 float* c_scale_inv, cudaStream_t stream) {
+  ApiRange nvtx_range("fp8_scaled_gemm_amax");
   if (c_amax == nullptr && C_q == nullptr) return FP8_ERR_INVALID_ARG;
   GemmExtra x;
   x.c_amax = c_amax;
@@ -460,6 +502,7 @@ fp8_status fp8_scaled_gemm_amax(const uint8_t* A, fp8_format fa, fp8_recipe ra, 
 }
 
 fp8_status fp8_get_device_status(cudaStream_t stream) {
+  ApiRange nvtx_range("fp8_get_device_status");
   DeviceInfo* d;
   if (fp8_status st = device_info(&d)) return st;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return FP8_ERR_CUDA;
@@ -475,6 +518,7 @@ fp8_status fp8_get_device_status(cudaStream_t stream) {
 }
 
 fp8_status fp8_debug_wait_timeout(cudaStream_t stream) {
+  ApiRange nvtx_range("fp8_debug_wait_timeout");
   DeviceInfo* d;
   if (fp8_status st = device_info(&d)) return st;
   return cuda_status(launch_wait_selftest(d->err, stream));

@@ -13,6 +13,7 @@
 // Every call clears scratch[0..k) before use, so nothing has to start at zero.  All
 // calls on a device share the array: calls whose executions overlap (on different
 // streams or from different threads) race on it.
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -70,24 +71,31 @@ __global__ void k_max_ranks(float* __restrict__ scratch, int k) {
 }
 
 // The scratch address and SM count of each device, looked up on the first call made
-// with that device current.
+// with that device current.  `ready` is published with release order after the other
+// fields are written, and read with acquire order, so a thread that sees it set also
+// sees the address (the check outside the lock is then well defined).
 struct NoAllocDevice {
-  bool ready = false;
+  std::atomic<bool> ready{false};
   float* scratch = nullptr;
   int num_sms = 0;
 };
 NoAllocDevice g_noalloc_dev[kMaxDevices];
 std::mutex g_noalloc_mutex;
 
-cudaError_t noalloc_device(NoAllocDevice** out) {
+cudaError_t noalloc_device(NoAllocDevice** out, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   NoAllocDevice& d = g_noalloc_dev[dev];
-  if (!d.ready) {
+  if (!d.ready.load(std::memory_order_acquire)) {
+    // the set-up queries below are not allowed while the stream is being captured
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return e;
+    if (cs != cudaStreamCaptureStatusNone) return cudaErrorStreamCaptureUnsupported;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_relaxed)) {
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
       if (e != cudaSuccess) return e;
@@ -96,7 +104,7 @@ cudaError_t noalloc_device(NoAllocDevice** out) {
       if (e != cudaSuccess) return e;
       d.scratch = static_cast<float*>(p);
       d.num_sms = n;
-      d.ready = true;
+      d.ready.store(true, std::memory_order_release);
     }
   }
   *out = &d;
@@ -111,7 +119,7 @@ cudaError_t launch_allreduce_noalloc(const void* g, int k, int64_t n, bool e5m2,
                                      float* out, cudaStream_t s) {
   if (k < 1 || k > kNoAllocMaxRanks) return cudaErrorInvalidValue;
   NoAllocDevice* d = nullptr;
-  cudaError_t e = noalloc_device(&d);
+  cudaError_t e = noalloc_device(&d, s);
   if (e != cudaSuccess) return e;
   e = launch_zero_f32(d->scratch, k, s);
   if (e != cudaSuccess) return e;

@@ -48,6 +48,21 @@ def test_noalloc_matches_allreduce_sum_two_calls_in_a_row():
         assert np.array_equal(host(out).view(np.uint32), host(out_ref).view(np.uint32))
 
 
+def test_noalloc_at_its_rank_limit():
+    # k = 1024 fills every per-rank slot, the last one right beside the global-amax
+    # slot, and leaves the per-rank amax pass about one block per rank; run twice so
+    # that the second call starts from the first call's scratch contents
+    for seed, fmt in ((13, F.E4M3), (14, F.E5M2)):
+        g = grads(1024, 64, seed, 1.0)
+        out_ref, q_ref, si_ref, _ = fq.allreduce_sum(g, fmt)
+        out, q, si = noalloc(g, fmt)
+        torch.cuda.synchronize()
+        assert_status_ok()
+        assert torch.equal(q, q_ref)
+        assert np.array_equal(host(si).view(np.uint32), host(si_ref).view(np.uint32))
+        assert np.array_equal(host(out).view(np.uint32), host(out_ref).view(np.uint32))
+
+
 def test_noalloc_rejects_more_ranks_than_its_scratch():
     g = torch.zeros((1025, 8), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(fq.FP8Error) as e:
