@@ -13,8 +13,13 @@ kernel of the step).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
-bounded slab of the same workload.  --sweep adds per-recipe kernel numbers.
+Prints one JSON line (rank 0).  Besides the step it reports, by default, every
+recipe's kernels at the sizes the targets are stated for (`per_recipe`: each a
+median of >= 50 event-timed launches with L2 flushed before each), a sustained
+window of back-to-back steps for the clock record, the same step end to end
+through the C ABI with host buffers (`e2e`), and the CPU oracle timed on the
+host cores (`cpu_baseline`).  --impl reference times the CPU oracle on the
+whole step instead.
 """
 from __future__ import annotations
 
@@ -39,6 +44,8 @@ WORKLOAD = "blockwise fprop 4096x4096x4096: X 1x128 E4M3 (row+col), W 128x128 E4
 METRIC = "FP8 scaled-GEMM TFLOPS & quantize GB/s per recipe, % of GB300 roofline"
 UNIT = "TFLOP/s"
 FLUSH_BYTES = 256 << 20
+KERNEL_REPS = 50          # event-timed launches per kernel figure (median reported)
+SUSTAIN_S = 1.5           # back-to-back steps after the timed region, for the clock record
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one blockwise GEMM launch at
 # 4096^3 from an ncu capture of the current kernel version; None when not captured for it
 TRAFFIC_GEMM = 34_124_544 + 2_114_816
@@ -57,17 +64,27 @@ def peaks():
     return p
 
 
+def fp8_peak_of(pk):
+    """Dense FP8 = 2 x dense BF16 (the nominal 4.5 / 2.25 PFLOP/s ratio), from the burst figure."""
+    return 2.0 * pk["bf16_tflops"]
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
+    """nvidia-smi samples every 50 ms, each stamped with the host clock when read, so
+    that a window of the run (the timed steps, the sustained steps, the per-recipe
+    kernels) can be summarised on its own."""
+
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int, out_path: str | None):
         self.gpu = gpu_index
         self.out_path = out_path
         self.proc = None
-        self.lines = []
+        self.samples = []       # (host time, raw line)
 
     def start(self):
         try:
@@ -80,36 +97,44 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.samples.append((time.monotonic(), line.strip()))
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+            return
         time.sleep(0.12)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        if self.out_path:
+            with open(self.out_path, "w") as f:
+                f.write("\n".join(f"{t:.3f},{ln}" for t, ln in self.samples) + "\n")
+
+    def summary(self, windows):
+        """Median SM clock, max clock, power and active throttle reasons over the samples
+        read inside any of the (t0, t1) windows (host monotonic seconds)."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm, smax, pw, reasons = [], [], [], set()
+        for t, ln in self.samples:
+            if not any(a <= t <= b for a, b in windows):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
             try:
                 sm.append(float(parts[1]))
                 smax.append(float(parts[2]))
+                pw.append(float(parts[3]))
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[5:9]):
+            for nm, v in zip(self.REASONS, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
-        if self.out_path:
-            with open(self.out_path, "w") as f:
-                f.write("\n".join(self.lines) + "\n")
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # ------------------------------------------------------------------ distributed
@@ -176,13 +201,18 @@ class Path:
         self.fq.fp8_scaled_gemm(self.qx, self.F.E4M3, self.R.BLOCK_1x128, self.sx, self.qw, self.F.E4M3,
                                 self.R.BLOCK_128x128, self.sw, self.y)
 
+    def step(self):
+        self.cast_x()
+        self.cast_w()
+        self.gemm()
 
-def bytes_cast_1x128(r, c):
-    return r * c * 4 + 2 * (r * c // 128) * 4
 
-
-def bytes_cast_128x128(r, c):
-    return r * c * 4 + 2 * (r * c // 16384) * 4
+def bytes_cast(recipe_name, r, c):
+    """Algorithmic bytes of a row + column cast-transpose of an r x c bf16 matrix: 2 B read
+    and 1 B + 1 B written per element, plus the scale arrays of both copies."""
+    extra = {"TENSOR": 0, "BLOCK_1x128": 2 * (r * c // 128) * 4, "BLOCK_128x128": 2 * (r * c // 16384) * 4,
+             "MX_1x32": 2 * (r * c // 32), "MX_1x32_TILED": 2 * (r * c // 32)}[recipe_name]
+    return 4 * r * c + extra
 
 
 class L2Flush:
@@ -192,13 +222,11 @@ class L2Flush:
     cast of 268 MB)."""
 
     def __init__(self, dev):
-        import torch
         self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
         self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
         self.out = torch.empty((), dtype=torch.float32, device=dev)
 
     def __call__(self):
-        import torch
         self.w.zero_()
         torch.amax(self.r, dim=0, out=self.out)
 
@@ -218,6 +246,24 @@ def _capture(fn):
     return g
 
 
+def time_kernel(fn, reps=KERNEL_REPS, flush=None, warm=3):
+    """Median of `reps` launches, each alone between two events on the launching stream,
+    L2 flushed before each (the flush is enqueued ahead of the first event, so the host
+    enqueues the launch while the flush runs and the events see the kernel alone)."""
+    s = torch.cuda.current_stream()
+    for _ in range(warm):
+        fn()
+    es = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in es:
+        if flush is not None:
+            flush()
+        a.record(s)
+        fn()
+        b.record(s)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in es)
+
+
 def run_ours(args, rank, world):
     import scaled_quantize_gemm_amax_gb300 as fq
     from scaled_quantize_gemm_amax_gb300 import build as fqbuild
@@ -230,14 +276,11 @@ def run_ours(args, rank, world):
     path = Path(fq, x, w)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
-
-    def step():
-        path.cast_x()
-        path.cast_w()
-        path.gemm()
+    clocks = ClockSampler(torch.cuda.current_device(), args.clocks_csv)
+    clocks.start()
 
     # the timed step is one CUDA graph of the three launches (no host launch cost inside it)
-    g_step = _capture(step)
+    g_step = _capture(path.step)
     for _ in range(args.warmup):
         g_step.replay()
         flush()
@@ -245,45 +288,35 @@ def run_ours(args, rank, world):
     assert fq.fp8_get_device_status() == fq.Status.OK
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clocks = ClockSampler(torch.cuda.current_device(), args.clocks_csv)
-    clocks.start()
     time.sleep(0.2)
     barrier(world)
     torch.cuda.synchronize()
+    t_timed0 = time.monotonic()
     for i in range(args.steps):
         ev[i][0].record(stream)
         g_step.replay()
         ev[i][1].record(stream)
         flush()          # outside the step's events: L2 does not carry inputs across steps
     torch.cuda.synchronize()
+    t_timed1 = time.monotonic()
     barrier(world)
-    clk = clocks.stop()
     st = fq.fp8_get_device_status()
     assert st == fq.Status.OK, st
-    step_ms_local = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    step_ms = max_over_ranks(step_ms_local, world)
+    step_times = [a.elapsed_time(b) for a, b in ev]
+    step_ms = max_over_ranks(statistics.mean(step_times), world)
+    sustained = run_sustained(fq, wl, dev, x, w, path)
 
-    # per-kernel breakdown: each launch alone between two events, L2 flushed before it;
-    # the host-side launch is enqueued while the flush runs, so the events see the kernel
-    reps = max(5, min(args.steps, 100))
-    part_ms = []
-    for fn in (path.cast_x, path.cast_w, path.gemm):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-        for a, b in evs:
-            flush()
-            a.record(stream)
-            fn()
-            b.record(stream)
-        torch.cuda.synchronize()
-        part_ms.append(statistics.mean(a.elapsed_time(b) for a, b in evs))
-    t_cx, t_cw, g_ms = part_ms
+    # per-kernel breakdown of the step: each launch alone, L2 flushed before it
+    t_cx = time_kernel(path.cast_x, flush=flush)
+    t_cw = time_kernel(path.cast_w, flush=flush)
+    g_ms = time_kernel(path.gemm, flush=flush)
 
     flops = 2.0 * M * N * K
     pk = peaks()
-    fp8_peak = 2.0 * pk["bf16_tflops"]           # FP8 dense = 2 x BF16 dense (nominal 4.5 / 2.25 PF)
+    fp8_peak = fp8_peak_of(pk)
     gemm_tflops = flops / (g_ms * 1e-3) / 1e12
-    cx_gbs = bytes_cast_1x128(M, K) / (t_cx * 1e-3) / 1e9
-    cw_gbs = bytes_cast_128x128(N, K) / (t_cw * 1e-3) / 1e9
+    cx_gbs = bytes_cast("BLOCK_1x128", M, K) / (t_cx * 1e-3) / 1e9
+    cw_gbs = bytes_cast("BLOCK_128x128", N, K) / (t_cw * 1e-3) / 1e9
     value = world * flops / (step_ms * 1e-3) / 1e12
 
     result = {
@@ -294,7 +327,9 @@ def run_ours(args, rank, world):
         "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "recipe": "blockwise 1x128 x 128x128",
                    "l2": "flushed between steps (256 MiB write, then 256 MiB read)", "launch": "one CUDA graph per step",
                    "parallelism": f"replicas x{world}"},
+        "step_ms_median": round(statistics.median(step_times), 5),
         "kernels": {
+            "stat": f"median of {KERNEL_REPS} launches, L2 flushed before each",
             "cast_transpose_x_1x128": {"us": round(t_cx * 1e3, 2), "GB/s": round(cx_gbs, 1),
                                        "frac_hbm": round(cx_gbs / pk["hbm_gbs"], 4)},
             "cast_transpose_w_128x128": {"us": round(t_cw * 1e3, 2), "GB/s": round(cw_gbs, 1),
@@ -306,16 +341,181 @@ def run_ours(args, rank, world):
                      "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4), "traffic": TRAFFIC_GEMM,
                      "peak_source": f"{pk['source']}: 2 x bf16 burst ({pk['bf16_tflops']})"},
         "gpu_launches": path.launches_per_step * args.steps,
-        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
-                   "samples": clk["samples"]},
+        "sustained": {k: v for k, v in sustained.items() if k not in ("t0", "t1")},
     }
+    t_pr0 = time.monotonic()
+    if not args.no_per_recipe:
+        result["per_recipe"] = run_per_recipe(fq, wl, dev, flush)
+    t_pr1 = time.monotonic()
+    clocks.stop()
+    ck = clocks.summary([(t_timed0, t_timed1), (sustained["t0"], sustained["t1"])])
+    ck["window"] = "the timed steps and the sustained back-to-back steps that follow them"
+    ck["timed_region_samples"] = clocks.summary([(t_timed0, t_timed1)])["samples"]
+    result["clocks"] = ck
+    if not args.no_per_recipe:
+        result["per_recipe"]["clocks"] = clocks.summary([(t_pr0, t_pr1)])
     if not args.no_e2e:
         result["e2e"] = run_e2e(fq, x, w, args, world)
-    if args.sweep:
-        result["per_recipe"] = run_sweep(fq, wl, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(x, w)
     return result
+
+
+def run_sustained(fq, wl, dev, x, w, path):
+    """Back-to-back steps for about SUSTAIN_S seconds, rotating over four input sets
+    (the first is the timed step's own) so that each step's inputs come from HBM
+    without a flush between steps: 4 x 64 MiB of bf16 inputs plus their FP8 copies
+    exceed L2.  Timed with two events around the whole window; it gives the clock
+    sampler a window under load."""
+    paths = [path] + [Path(fq, x.roll(i, 0).contiguous(), w.roll(i, 0).contiguous()) for i in (1, 2, 3)]
+    graphs = [_capture(p.step) for p in paths]
+    stream = torch.cuda.current_stream()
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    # size the window from one round's time
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for g in graphs:
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    per_round_s = max(e0.elapsed_time(e1) * 1e-3, 1e-5)
+    rounds = max(1, int(SUSTAIN_S / per_round_s))
+    t0 = time.monotonic()
+    e0.record(stream)
+    for _ in range(rounds):
+        for g in graphs:
+            g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    assert fq.fp8_get_device_status() == fq.Status.OK
+    n = rounds * len(graphs)
+    ms = e0.elapsed_time(e1) / n
+    return {"steps": n, "seconds": round(e0.elapsed_time(e1) * 1e-3, 3), "ms_per_step": round(ms, 5),
+            "TFLOP/s": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1),
+            "inputs": "four input sets in turn (512 MiB of bf16 with their FP8 copies), no flush", "t0": t0, "t1": t1}
+
+
+def run_per_recipe(fq, wl, dev, flush):
+    """Every recipe's kernels at the sizes the targets are stated for: cast-transpose
+    (row + column copies) of each recipe and the amax at 8192^2, 16384^2 and 32768^2;
+    the GEMM of each recipe pairing at 4096^3 and 8192^3, the MXFP8 LLaMA-7B linears,
+    the blockwise weight-gradient pairing, and the per-tensor (delayed-scaling)
+    GPT-175B linears' fprop / dgrad / wgrad; dequantization, the fused output
+    quantization and the FP8 gradient all-reduce.  Each figure is the median of
+    KERNEL_REPS launches with L2 flushed before each."""
+    R, F, O = fq.Recipe, fq.Format, fq.OutDtype
+    pk = peaks()
+    hbm = pk["hbm_gbs"]
+    fp8 = fp8_peak_of(pk)
+    out = {"stat": f"median of {KERNEL_REPS} launches, L2 flushed before each",
+           "peaks": {"hbm_GB/s": hbm, "fp8_TFLOP/s": fp8, "source": pk["source"]},
+           "cast_transpose": {}, "amax": {}, "gemm": {}, "dequantize": {}, "fused_gemm_amax": {}, "allreduce": {}}
+
+    def bw(us_ms, nbytes):
+        gbs = nbytes / (us_ms * 1e-3) / 1e9
+        return {"us": round(us_ms * 1e3, 2), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)}
+
+    def tf(us_ms, flops):
+        t = flops / (us_ms * 1e-3) / 1e12
+        return {"us": round(us_ms * 1e3, 2), "TFLOP/s": round(t, 1), "frac_fp8": round(t / fp8, 4)}
+
+    one = torch.ones(1, dtype=torch.float32, device=dev)
+    # ---- cast-transpose and amax (bandwidth sweep inputs: N(0,1), 0.1 % of elements x1000)
+    for size in (8192, 16384, 32768):
+        x = wl.cfg5_sweep(size, dev)
+        for rec in (R.TENSOR, R.BLOCK_1x128, R.BLOCK_128x128, R.MX_1x32_TILED):
+            sc = one if rec == R.TENSOR else None
+            qr, sr, qc, scol = fq.cast_transpose(x, rec, F.E4M3, sc)
+            ms = time_kernel(lambda: fq.fp8_cast_transpose(x, rec, F.E4M3, sc, None, qr, sr, qc, scol), flush=flush)
+            out["cast_transpose"][f"{rec.name}_{size}"] = bw(ms, bytes_cast(rec.name, size, size))
+            del qr, sr, qc, scol
+        amax = torch.empty(1, dtype=torch.float32, device=dev)
+        ms = time_kernel(lambda: fq.fp8_amax(x, amax), flush=flush)
+        out["amax"][str(size)] = bw(ms, 2 * size * size)
+        if size == 16384:
+            for rec in (R.TENSOR, R.BLOCK_1x128, R.BLOCK_128x128, R.MX_1x32_TILED):
+                sc = one if rec == R.TENSOR else None
+                q, sq, _, _ = fq.cast_transpose(x, rec, F.E4M3, sc, col=False)
+                y = torch.empty((size, size), dtype=torch.bfloat16, device=dev)
+                ms = time_kernel(lambda: fq.fp8_dequantize(q, rec, F.E4M3, sq, y), flush=flush)
+                out["dequantize"][f"{rec.name}_{size}"] = bw(ms, 3 * size * size + sq.numel() * sq.element_size())
+                del q, sq, y
+        del x
+        torch.cuda.empty_cache()
+
+    # ---- GEMMs
+    shapes = [("tensor_4096", R.TENSOR, R.TENSOR, (4096, 4096, 4096), F.E4M3, F.E4M3, O.BF16),
+              ("tensor_8192", R.TENSOR, R.TENSOR, (8192, 8192, 8192), F.E4M3, F.E4M3, O.BF16),
+              ("blockwise_4096", R.BLOCK_1x128, R.BLOCK_128x128, (4096, 4096, 4096), F.E4M3, F.E4M3, O.BF16),
+              ("blockwise_8192", R.BLOCK_1x128, R.BLOCK_128x128, (8192, 8192, 8192), F.E4M3, F.E4M3, O.BF16),
+              ("blockwise_wgrad_4096", R.BLOCK_1x128, R.BLOCK_1x128, (4096, 4096, 4096), F.E4M3, F.E4M3, O.FP32),
+              ("blockwise_wgrad_8192", R.BLOCK_1x128, R.BLOCK_1x128, (8192, 8192, 8192), F.E4M3, F.E4M3, O.FP32),
+              ("mx_4096", R.MX_1x32_TILED, R.MX_1x32_TILED, (4096, 4096, 4096), F.E4M3, F.E4M3, O.BF16),
+              ("mx_8192", R.MX_1x32_TILED, R.MX_1x32_TILED, (8192, 8192, 8192), F.E4M3, F.E4M3, O.BF16)]
+    shapes += [(f"mx_llama7b_{k}", R.MX_1x32_TILED, R.MX_1x32_TILED, v, F.E4M3, F.E4M3, O.BF16)
+               for k, v in wl.CFG3_SHAPES.items()]
+    # GPT-175B linears (2048 tokens), per-tensor (delayed) scaling: fprop E4M3 x E4M3 -> bf16,
+    # dgrad E5M2 dY x E4M3 W -> bf16, wgrad E5M2 dY^T x E4M3 X^T -> fp32
+    t = wl.CFG4_TOKENS
+    for lin, (fin, fout) in wl.CFG4_LINEARS.items():
+        shapes += [(f"gpt175b_{lin}_fprop", R.TENSOR, R.TENSOR, (t, fout, fin), F.E4M3, F.E4M3, O.BF16),
+                   (f"gpt175b_{lin}_dgrad", R.TENSOR, R.TENSOR, (t, fin, fout), F.E5M2, F.E4M3, O.BF16),
+                   (f"gpt175b_{lin}_wgrad", R.TENSOR, R.TENSOR, (fout, fin, t), F.E5M2, F.E4M3, O.FP32)]
+    qkv_in, qkv_out = wl.CFG4_LINEARS["qkv"]
+    shapes += [("gpt175b_qkv_wgrad_blockwise", R.BLOCK_1x128, R.BLOCK_1x128, (qkv_out, qkv_in, t), F.E5M2, F.E4M3,
+                O.FP32)]
+    for name, ra, rb, (m, n, k), fa, fb, od in shapes:
+        a = wl.normal_bf16((m, k), 1, 1.0, dev)
+        b = wl.normal_bf16((n, k), 2, 0.02, dev)
+        qa, sa, _, _ = fq.cast_transpose(a, ra, fa, one if ra == R.TENSOR else None, col=False)
+        qb, sb, _, _ = fq.cast_transpose(b, rb, fb, one if rb == R.TENSOR else None, col=False)
+        del a, b
+        c = torch.empty((m, n), dtype=torch.float32 if od == O.FP32 else torch.bfloat16, device=dev)
+        ms = time_kernel(lambda: fq.fp8_scaled_gemm(qa, fa, ra, sa, qb, fb, rb, sb, c, od), flush=flush)
+        out["gemm"][name] = dict(tf(ms, 2.0 * m * n * k), M=m, N=n, K=k)
+        del qa, qb, sa, sb, c
+
+    # ---- fused output quantization (per-tensor, delayed scale) against the unfused chain
+    s = 8192
+    a = wl.normal_bf16((s, s), 1, 1.0, dev)
+    b = wl.normal_bf16((s, s), 2, 0.02, dev)
+    qa, sa, _, _ = fq.cast_transpose(a, R.TENSOR, F.E4M3, one, col=False)
+    qb, sb, _, _ = fq.cast_transpose(b, R.TENSOR, F.E4M3, one, col=False)
+    c = torch.empty((s, s), dtype=torch.bfloat16, device=dev)
+    c_q = torch.empty((s, s), dtype=torch.uint8, device=dev)
+    c_amax = torch.empty(1, dtype=torch.float32, device=dev)
+    c_sinv = torch.empty(1, dtype=torch.float32, device=dev)
+    c_scale = torch.full((1,), 64.0, dtype=torch.float32, device=dev)
+    ms = time_kernel(lambda: fq.fp8_scaled_gemm_amax(qa, F.E4M3, R.TENSOR, sa, qb, F.E4M3, R.TENSOR, sb, None,
+                                                     O.BF16, c_amax, c_scale, F.E4M3, c_q, c_sinv), flush=flush)
+
+    def unfused():
+        fq.fp8_scaled_gemm(qa, F.E4M3, R.TENSOR, sa, qb, F.E4M3, R.TENSOR, sb, c)
+        fq.fp8_quantize(c, R.TENSOR, F.E4M3, c_scale, c_amax, c_q, c_sinv)
+
+    ms_u = time_kernel(unfused, flush=flush)
+    out["fused_gemm_amax"]["tensor_8192"] = dict(tf(ms, 2.0 * s ** 3), unfused_us=round(ms_u * 1e3, 2))
+    del a, b, qa, qb, c, c_q
+
+    # ---- FP8 gradient all-reduce: 8 ranks' 8192^2 gradients ~ N(0, 1e-3): amax pass (2 B/elem),
+    # then cast and sum (2 B read + 1 B payload per rank element, 4 B per reduced element)
+    kr, n = 8, 8192 * 8192
+    g = (torch.randn((kr, n), generator=torch.Generator(device=dev).manual_seed(9), device=dev) * 1e-3).to(
+        torch.bfloat16)
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
+    q = torch.empty((kr, n), dtype=torch.uint8, device=dev)
+    si = torch.empty(1, dtype=torch.float32, device=dev)
+    red = torch.empty(n, dtype=torch.float32, device=dev)
+    ms = time_kernel(lambda: fq.fp8_allreduce_sum(g, F.E5M2, amax, q, si, red), flush=flush)
+    out["allreduce"]["8x8192^2"] = bw(ms, kr * n * 2 + kr * n * 3 + 4 * n)
+    del g, q, red
+    torch.cuda.synchronize()
+    assert fq.fp8_get_device_status() == fq.Status.OK
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(fq, x, w, args, world):
@@ -325,7 +525,6 @@ def run_e2e(fq, x, w, args, world):
     (copy in, compute, copy out) with two sets of device buffers."""
     xh = x.cpu().pin_memory()
     wh = w.cpu().pin_memory()
-    dev = x.device
     paths = [Path(fq, torch.empty_like(x), torch.empty_like(w)) for _ in range(2)]
     yh = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
@@ -347,9 +546,7 @@ def run_e2e(fq, x, w, args, world):
             comp.wait_event(in_done[b])
             if i >= 2:
                 comp.wait_event(out_done[b])              # buffer b's previous result has left
-            p.cast_x()
-            p.cast_w()
-            p.gemm()
+            p.step()
             comp_done[b].record(comp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(comp_done[b])
@@ -376,151 +573,101 @@ def run_e2e(fq, x, w, args, world):
             "h2d_bytes_per_step": int(xh.numel() * 2 + wh.numel() * 2), "d2h_bytes_per_step": int(M * N * 2)}
 
 
-def _time_kernel(fn, reps=20, flush=None):
-    s = torch.cuda.current_stream()
-    es = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    for _ in range(3):
-        fn()
-    for a, b in es:
-        if flush is not None:
-            flush()
-        a.record(s)
-        fn()
-        b.record(s)
-    torch.cuda.synchronize()
-    return statistics.median(a.elapsed_time(b) for a, b in es)
-
-
-def run_sweep(fq, wl, dev):
-    """Per-recipe kernel numbers: cast-transpose GB/s at 8192^2 and 16384^2 for each
-    recipe, and GEMM TFLOP/s per recipe at 4096^3, the MX LLaMA-7B shapes and the per-tensor
-    GPT-175B linears (fprop, dgrad, wgrad)."""
-    R, F = fq.Recipe, fq.Format
-    pk = peaks()
-    flush = L2Flush(dev)
-    out = {"cast_transpose": {}, "gemm": {}}
-    for size in (8192, 16384):
-        x = wl.cfg5_sweep(size, dev)
-        scale = torch.ones(1, dtype=torch.float32, device=dev)
-        for rec in (R.TENSOR, R.BLOCK_1x128, R.BLOCK_128x128, R.MX_1x32):
-            qr, sr, qc, sc = fq.cast_transpose(x, rec, F.E4M3, scale if rec == R.TENSOR else None)
-            ms = _time_kernel(lambda: fq.fp8_cast_transpose(x, rec, F.E4M3, scale if rec == R.TENSOR else None,
-                                                            None, qr, sr, qc, sc), flush=flush)
-            extra = {R.TENSOR: 0, R.BLOCK_1x128: 2 * size * size // 128 * 4, R.BLOCK_128x128: 0,
-                     R.MX_1x32: 2 * size * size // 32}[rec]
-            gbs = (4 * size * size + extra) / (ms * 1e-3) / 1e9
-            out["cast_transpose"][f"{rec.name}_{size}"] = {"us": round(ms * 1e3, 1), "GB/s": round(gbs, 1),
-                                                          "frac_hbm": round(gbs / pk["hbm_gbs"], 4)}
-            del qr, sr, qc, sc
-        amax = torch.empty(1, dtype=torch.float32, device=dev)
-        ms = _time_kernel(lambda: fq.fp8_amax(x, amax), flush=flush)
-        gbs = 2 * size * size / (ms * 1e-3) / 1e9
-        out["cast_transpose"][f"amax_{size}"] = {"us": round(ms * 1e3, 1), "GB/s": round(gbs, 1),
-                                                 "frac_hbm": round(gbs / pk["hbm_gbs"], 4)}
-        del x
-    fp8_peak = 2.0 * pk["bf16_tflops"]
-    shapes = [("tensor_4096", R.TENSOR, R.TENSOR, (4096, 4096, 4096)),
-              ("blockwise_4096", R.BLOCK_1x128, R.BLOCK_128x128, (4096, 4096, 4096)),
-              ("mx_4096", R.MX_1x32_TILED, R.MX_1x32_TILED, (4096, 4096, 4096))]
-    shapes += [(f"mx_{k}", R.MX_1x32_TILED, R.MX_1x32_TILED, v) for k, v in wl.CFG3_SHAPES.items()]
-    shapes = [(name, ra, rb, mnk, F.E4M3, F.E4M3, fq.OutDtype.BF16) for name, ra, rb, mnk in shapes]
-    # GPT-175B linears (2048 tokens), per-tensor: fprop E4M3 x E4M3 -> bf16, dgrad E5M2 dY x E4M3 W -> bf16,
-    # wgrad E5M2 dY^T x E4M3 X^T -> fp32
-    for lin, (fin, fout) in wl.CFG4_LINEARS.items():
-        t = wl.CFG4_TOKENS
-        shapes += [(f"gpt175b_{lin}_fprop", R.TENSOR, R.TENSOR, (t, fout, fin), F.E4M3, F.E4M3, fq.OutDtype.BF16),
-                   (f"gpt175b_{lin}_dgrad", R.TENSOR, R.TENSOR, (t, fin, fout), F.E5M2, F.E4M3, fq.OutDtype.BF16),
-                   (f"gpt175b_{lin}_wgrad", R.TENSOR, R.TENSOR, (fout, fin, t), F.E5M2, F.E4M3, fq.OutDtype.FP32)]
-    # blockwise weight gradient: 1x128 x 1x128 (a scale per row of B), FP32 out
-    shapes += [("blockwise_wgrad_4096", R.BLOCK_1x128, R.BLOCK_1x128, (4096, 4096, 4096), F.E4M3, F.E4M3,
-                fq.OutDtype.FP32),
-               ("gpt175b_qkv_wgrad_blockwise", R.BLOCK_1x128, R.BLOCK_1x128,
-                (wl.CFG4_LINEARS["qkv"][1], wl.CFG4_LINEARS["qkv"][0], wl.CFG4_TOKENS), F.E5M2, F.E4M3, fq.OutDtype.FP32)]
-    for name, ra, rb, (m, n, k), fa, fb, od in shapes:
-        a = wl.normal_bf16((m, k), 1, 1.0, dev)
-        b = wl.normal_bf16((n, k), 2, 0.02, dev)
-        sc = torch.ones(1, dtype=torch.float32, device=dev)
-        qa, sa, _, _ = fq.cast_transpose(a, ra, fa, sc if ra == R.TENSOR else None, col=False)
-        qb, sb, _, _ = fq.cast_transpose(b, rb, fb, sc if rb == R.TENSOR else None, col=False)
-        c = torch.empty((m, n), dtype=torch.float32 if od == fq.OutDtype.FP32 else torch.bfloat16, device=dev)
-        ms = _time_kernel(lambda: fq.fp8_scaled_gemm(qa, fa, ra, sa, qb, fb, rb, sb, c, od), flush=flush)
-        tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
-        out["gemm"][name] = {"us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1), "frac_fp8": round(tf / fp8_peak, 4)}
-        del a, b, qa, qb, c
-    torch.cuda.synchronize()
-    return out
-
-
 # ------------------------------------------------------------------ oracle (CPU) legs
-def cpu_baseline(x, w):
-    """The oracle as it stands, on the host cores: one 128-row slab of the step
-    (quantize 128 rows of X and of W, row + column copies; GEMM of 128 rows of Y
-    against all of W), the step time extrapolated x32 (M / 128)."""
-    import oracle
-    xh = x.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-    wh = w.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-    qw_full = oracle.quantize_rowwise(wh, oracle.KIND_128x128, oracle.E4M3)
-    t, info = _oracle_slab_time(oracle, xh, wh, 128, qw_full)
-    return {"value": round(2.0 * M * N * K / t / 1e12, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": info}
+def _bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def _oracle_slab_time(oracle, xh, wh, rows, qw_full):
-    """Time one slab of the step: quantize rows [0, rows) of X and of W (row and
-    column copies), and the GEMM of rows [0, rows) of Y against the whole
-    quantized W (quantized once beforehand).  Returns the extrapolated time of a
-    full step (x M/rows) and a description."""
-    xs = np.ascontiguousarray(xh[:rows])
-    ws = np.ascontiguousarray(wh[:rows])
+def _oracle_quantize_rows(oracle, xh, kind, threads):
+    """Row-wise oracle quantization of xh by `threads` host threads, each on its own run
+    of 128-row slabs (the oracle's C functions release the interpreter lock while they
+    run; the slabs are independent for the 1x128 and 128x128 recipes, so the result is
+    the single call's, byte for byte)."""
+    rows = xh.shape[0]
+    per = -(-(rows // 128) // threads) * 128
+    bounds = [(r0, min(rows, r0 + per)) for r0 in range(0, rows, per)]
+    res = [None] * len(bounds)
+
+    def work(i):
+        r0, r1 = bounds[i]
+        res[i] = oracle.quantize_rowwise(np.ascontiguousarray(xh[r0:r1]), kind, oracle.E4M3)
+
+    ts = [threading.Thread(target=work, args=(i,)) for i in range(len(bounds))]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    return np.concatenate([r[0] for r in res]), np.concatenate([r[1] for r in res])
+
+
+def _oracle_step(oracle, xh, wh, threads, gemm=True):
+    """One step of the workload on the oracle: X 1x128 and W 128x128, row-wise and
+    column-wise copies (quantization on `threads` host threads), then the GEMM
+    C = deq(X) deq(W)^T in float64 (the library matmul on its own thread pool).
+    Returns (quantize seconds, GEMM seconds)."""
     t0 = time.perf_counter()
-    qx, sx = oracle.quantize_rowwise(xs, oracle.KIND_1x128, oracle.E4M3)
-    oracle.quantize_colwise(xs, oracle.KIND_1x128, oracle.E4M3)
-    oracle.quantize_rowwise(ws, oracle.KIND_128x128, oracle.E4M3)
-    oracle.quantize_colwise(ws, oracle.KIND_128x128, oracle.E4M3)
-    t_q = time.perf_counter() - t0
-    qw, sw = qw_full
+    qx, sx = _oracle_quantize_rows(oracle, xh, oracle.KIND_1x128, threads)
+    _oracle_quantize_rows(oracle, oracle.transpose_bf16(xh), oracle.KIND_1x128, threads)
+    qw, sw = _oracle_quantize_rows(oracle, wh, oracle.KIND_128x128, threads)
+    _oracle_quantize_rows(oracle, oracle.transpose_bf16(wh), oracle.KIND_128x128, threads)
     t1 = time.perf_counter()
-    oracle.scaled_gemm_rows(qx, 0, oracle.KIND_1x128, sx, qw, 0, oracle.KIND_128x128, sw, np.arange(rows))
-    t_g = time.perf_counter() - t1
-    scale = M / rows
-    info = (f"{rows}-row slab of X and W quantized (row+col) in {t_q:.3f} s, GEMM of {rows} rows of Y in "
-            f"{t_g:.3f} s; full step extrapolated x{scale:.0f}; C oracle single-threaded, float64 matmul on "
-            f"the BLAS threads")
-    return (t_q + t_g) * scale, info
+    if gemm:
+        oracle.scaled_gemm(qx, oracle.E4M3, oracle.KIND_1x128, sx, qw, oracle.E4M3, oracle.KIND_128x128, sw)
+    return t1 - t0, time.perf_counter() - t1
+
+
+def cpu_baseline(x, w):
+    """The oracle as it stands on the host cores, on the whole step: quantization on
+    one thread and on every core (threads over 128-row slabs), the float64 GEMM on the
+    matmul library's thread pool (all cores).  value = the step's flops / the
+    all-core step time."""
+    import oracle
+    oracle.build()
+    xh, wh = _bits(x), _bits(w)
+    cores = os.cpu_count()
+    tq1, _ = _oracle_step(oracle, xh, wh, 1, gemm=False)
+    tq, tg = _oracle_step(oracle, xh, wh, cores)
+    step_s = tq + tg
+    return {"value": round(2.0 * M * N * K / step_s / 1e12, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"the whole step on the oracle, measured once: quantization of X and W (row + column "
+                       f"copies) {tq1:.3f} s on 1 thread, {tq:.3f} s on {cores} threads; float64 GEMM of the full "
+                       f"4096^3 product {tg:.3f} s on the matmul library's threads; all-core step {step_s:.3f} s"),
+            "single_thread_quantize_s": round(tq1, 4), "all_core_quantize_s": round(tq, 4),
+            "gemm_s": round(tg, 4), "all_core_step_s": round(step_s, 4)}
 
 
 def run_reference(args, rank, world):
-    """The oracle as the reference arm: each step is one 128-row slab of the workload
-    (1/32 of the step's work), value = the step's flops / extrapolated step time."""
+    """The oracle as the reference arm: every step is the whole workload on the host
+    cores (see _oracle_step), measured, not extrapolated."""
     import oracle
     from scaled_quantize_gemm_amax_gb300 import workloads as wl
 
     if rank != 0:
         return None
     x, w = wl.cfg2_blockwise("cpu")
-    xh = x.contiguous().view(torch.int16).numpy().view(np.uint16)
-    wh = w.contiguous().view(torch.int16).numpy().view(np.uint16)
+    xh, wh = _bits(x), _bits(w)
     oracle.build()
-    rows = 128
-    qw_full = oracle.quantize_rowwise(wh, oracle.KIND_128x128, oracle.E4M3)
+    cores = os.cpu_count()
     for _ in range(args.warmup):
-        _oracle_slab_time(oracle, xh, wh, rows, qw_full)
+        _oracle_step(oracle, xh, wh, cores)
     times = []
-    info = ""
     t_start = time.perf_counter()
     for _ in range(args.steps):
-        t, info = _oracle_slab_time(oracle, xh, wh, rows, qw_full)
-        times.append(t)
+        tq, tg = _oracle_step(oracle, xh, wh, cores)
+        times.append((tq, tg))
     wall = time.perf_counter() - t_start
-    step_s = statistics.mean(times)
+    step_s = wall / args.steps
     value = 2.0 * M * N * K / step_s / 1e12
+    info = (f"each step the whole workload on the oracle: quantization of X and W (row + column copies) on "
+            f"{cores} threads (median {statistics.median(t for t, _ in times):.3f} s), float64 GEMM of the full "
+            f"4096^3 product on the matmul library's threads (median {statistics.median(g for _, g in times):.3f} s)")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 oracle (fp8 codes)",
             "data": "synthetic (seeded, CPU generator)",
             "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "recipe": "blockwise 1x128 x 128x128",
-                       "parallelism": "cpu"},
-            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                       "parallelism": f"cpu x{cores} threads"},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": info},
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": round(wall, 2)}
@@ -556,8 +703,8 @@ def run_case(args):
             scale = torch.ones(1, dtype=torch.float32, device=dev) if rec == R.TENSOR else None
             qr, sr, qc, sc = fq.cast_transpose(x, rec, F.E4M3, scale)
             fn = lambda: fq.fp8_cast_transpose(x, rec, F.E4M3, scale, None, qr, sr, qc, sc)
-            nbytes = 4 * s * s
-        ms = _time_kernel(fn, reps=args.steps, flush=flush)
+            nbytes = bytes_cast(rec.name, s, s)
+        ms = time_kernel(fn, reps=args.steps, flush=flush)
         res = {"case": args.case, "size": s, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
         res["frac_hbm"] = round(res["GB/s"] / pk["hbm_gbs"], 4)
     elif args.case.startswith("dequant"):
@@ -568,7 +715,7 @@ def run_case(args):
         scale = torch.ones(1, dtype=torch.float32, device=dev) if rec == R.TENSOR else None
         q, sq, _, _ = fq.cast_transpose(x, rec, F.E4M3, scale, col=False)
         y = torch.empty((s, s), dtype=torch.bfloat16, device=dev)
-        ms = _time_kernel(lambda: fq.fp8_dequantize(q, rec, F.E4M3, sq, y), reps=args.steps, flush=flush)
+        ms = time_kernel(lambda: fq.fp8_dequantize(q, rec, F.E4M3, sq, y), reps=args.steps, flush=flush)
         nbytes = 3 * s * s + sq.numel() * sq.element_size()
         res = {"case": args.case, "size": s, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
         res["frac_hbm"] = round(res["GB/s"] / pk["hbm_gbs"], 4)
@@ -582,7 +729,7 @@ def run_case(args):
         q = torch.empty((k, n), dtype=torch.uint8, device=dev)
         si = torch.empty(1, dtype=torch.float32, device=dev)
         out = torch.empty(n, dtype=torch.float32, device=dev)
-        ms = _time_kernel(lambda: fq.fp8_allreduce_sum(g, F.E5M2, amax, q, si, out), reps=args.steps, flush=flush)
+        ms = time_kernel(lambda: fq.fp8_allreduce_sum(g, F.E5M2, amax, q, si, out), reps=args.steps, flush=flush)
         nbytes = k * n * 2 + k * n * 3 + 4 * n
         res = {"case": args.case, "size": s, "ranks": k, "us": round(ms * 1e3, 2),
                "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
@@ -607,11 +754,11 @@ def run_case(args):
             fq.fp8_scaled_gemm(qa, F.E4M3, R.TENSOR, sa, qb, F.E4M3, R.TENSOR, sb, c)
             fq.fp8_quantize(c, R.TENSOR, F.E4M3, c_scale, c_amax, c_q, c_sinv)
 
-        ms = _time_kernel(fused, reps=args.steps, flush=flush)
-        ms_u = _time_kernel(unfused, reps=args.steps, flush=flush)
+        ms = time_kernel(fused, reps=args.steps, flush=flush)
+        ms_u = time_kernel(unfused, reps=args.steps, flush=flush)
         tf = 2.0 * s ** 3 / (ms * 1e-3) / 1e12
         res = {"case": args.case, "size": s, "us": round(ms * 1e3, 2), "TFLOP/s": round(tf, 1),
-               "frac_fp8": round(tf / (2 * pk["bf16_tflops"]), 4), "unfused_us": round(ms_u * 1e3, 2)}
+               "frac_fp8": round(tf / fp8_peak_of(pk), 4), "unfused_us": round(ms_u * 1e3, 2)}
     else:
         # gemm_block_wgrad: the weight-gradient pairing, 1x128 x 1x128 (a scale per row of B), FP32 out
         ra = {"gemm_tensor": R.TENSOR, "gemm_block": R.BLOCK_1x128, "gemm_mx": R.MX_1x32_TILED,
@@ -619,17 +766,18 @@ def run_case(args):
         rb = {"gemm_tensor": R.TENSOR, "gemm_block": R.BLOCK_128x128, "gemm_mx": R.MX_1x32_TILED,
               "gemm_block_wgrad": R.BLOCK_1x128}[args.case]
         od = fq.OutDtype.FP32 if args.case == "gemm_block_wgrad" else fq.OutDtype.BF16
-        a = wl.normal_bf16((s, s), 1, 1.0, dev)
-        b = wl.normal_bf16((s, s), 2, 0.02, dev)
+        m, n, k = (args.size, args.size, args.size) if args.mnk is None else args.mnk
+        a = wl.normal_bf16((m, k), 1, 1.0, dev)
+        b = wl.normal_bf16((n, k), 2, 0.02, dev)
         sc1 = torch.ones(1, dtype=torch.float32, device=dev)
         qa, sa, _, _ = fq.cast_transpose(a, ra, F.E4M3, sc1 if ra == R.TENSOR else None, col=False)
         qb, sb, _, _ = fq.cast_transpose(b, rb, F.E4M3, sc1 if rb == R.TENSOR else None, col=False)
-        c = torch.empty((s, s), dtype=torch.float32 if od == fq.OutDtype.FP32 else torch.bfloat16, device=dev)
-        ms = _time_kernel(lambda: fq.fp8_scaled_gemm(qa, F.E4M3, ra, sa, qb, F.E4M3, rb, sb, c, od), reps=args.steps,
-                          flush=flush)
-        tf = 2.0 * s ** 3 / (ms * 1e-3) / 1e12
-        res = {"case": args.case, "size": s, "us": round(ms * 1e3, 2), "TFLOP/s": round(tf, 1),
-               "frac_fp8": round(tf / (2 * pk["bf16_tflops"]), 4)}
+        c = torch.empty((m, n), dtype=torch.float32 if od == fq.OutDtype.FP32 else torch.bfloat16, device=dev)
+        ms = time_kernel(lambda: fq.fp8_scaled_gemm(qa, F.E4M3, ra, sa, qb, F.E4M3, rb, sb, c, od), reps=args.steps,
+                         flush=flush)
+        tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
+        res = {"case": args.case, "M": m, "N": n, "K": k, "us": round(ms * 1e3, 2), "TFLOP/s": round(tf, 1),
+               "frac_fp8": round(tf / fp8_peak_of(pk), 4)}
     assert fq.fp8_get_device_status() == fq.Status.OK
     print(json.dumps(res), flush=True)
 
@@ -638,14 +786,15 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", choices=CASES, default=None, help="time one kernel in a loop (profiling)")
     ap.add_argument("--size", type=int, default=4096)
+    ap.add_argument("--mnk", type=int, nargs=3, default=None, help="GEMM cases: M N K instead of size^3")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--no-per-recipe", action="store_true", help="skip the per-recipe kernel figures")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--clocks-csv", default=None, help="also write the raw clock samples of the timed region here")
+    ap.add_argument("--clocks-csv", default=None, help="also write the raw clock samples of the run here")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
