@@ -89,3 +89,43 @@ def _check_scales(recipe, got, ref, what):
         assert_bytes_equal(got, ref, what)
     else:
         assert_bytes_equal(f32bits(got), f32bits(ref), what)
+
+
+def tile_spread(t: torch.Tensor, bh: int, bw: int, seed: int, span: int) -> torch.Tensor:
+    """Multiply each bh x bw tile of t by its own power of two 2^e, e in [-span, span]
+    (exact in BF16), so that a scale read for the wrong tile (row block, column block
+    or k-block) is off by a factor of 2 or more instead of a few per cent."""
+    r, c = t.shape
+    i = torch.arange((r + bh - 1) // bh, device=t.device)[:, None]
+    j = torch.arange((c + bw - 1) // bw, device=t.device)[None, :]
+    e = (i * 3 + j * 5 + seed) % (2 * span + 1) - span
+    f = torch.exp2(e.float()).repeat_interleave(bh, 0)[:r].repeat_interleave(bw, 1)[:, :c]
+    return (t.float() * f).to(torch.bfloat16)
+
+
+SENTINEL = 0xA5
+
+
+class Guarded:
+    """An output buffer with guard regions before and after it, every byte (the
+    buffer's own included) filled with SENTINEL before the call: check() finds any
+    write outside the buffer, which a comparison of the buffer alone cannot see."""
+
+    def __init__(self, shape, dtype, guard_bytes: int = 4096, device="cuda"):
+        esz = torch.empty((), dtype=dtype).element_size()
+        self.n = 1
+        for d in shape:
+            self.n *= int(d)
+        self.g = guard_bytes // esz
+        self.esz = esz
+        self.buf = torch.empty(2 * self.g + self.n, dtype=dtype, device=device)
+        self.buf.view(torch.uint8).fill_(SENTINEL)
+        self.t = self.buf[self.g:self.g + self.n].view(tuple(shape))
+
+    def check(self, what: str):
+        b = host(self.buf.view(torch.uint8))
+        gb, nb = self.g * self.esz, self.n * self.esz
+        before = np.flatnonzero(b[:gb] != SENTINEL)
+        after = np.flatnonzero(b[gb + nb:] != SENTINEL)
+        assert before.size == 0, f"{what}: {before.size} bytes written before the buffer (first at -{gb - before[0]})"
+        assert after.size == 0, f"{what}: {after.size} bytes written past the end (first at +{after[0]})"

@@ -11,7 +11,7 @@ import torch
 import oracle
 import scaled_quantize_gemm_amax_gb300 as fq
 from scaled_quantize_gemm_amax_gb300 import workloads as wl
-from gpu_util import R, F, KIND, assert_bytes_equal, assert_status_ok, bits16, host, require_gpu
+from gpu_util import R, F, KIND, assert_bytes_equal, assert_status_ok, bits16, host, require_gpu, tile_spread
 
 pytestmark = pytest.mark.gpu
 
@@ -186,3 +186,34 @@ def test_gemm_blockwise_rows_b_many_tiles(m, n, k, out, spread):
     if spread:
         x, w = _block_spread(x, 1), _block_spread(w, 4)
     gemm_check(x, w, R.BLOCK_1x128, R.BLOCK_1x128, F.E4M3, F.E4M3, out=out)
+
+
+@pytest.mark.parametrize("m,n,k", [
+    (512, 512, 4096),      # CTA pairs, the bench's K: 32 k-blocks a tile
+    (2048, 1536, 512),     # CTA pairs, several tiles a pair
+    (384, 512, 1024),      # M % 256 != 0: single CTAs
+    (512, 768, 640),       # K / 128 odd: single CTAs, 128-deep stages
+])
+def test_gemm_blockwise_128x128_b_tile_spread(m, n, k):
+    # 1x128 x 128x128 with every 1x128 block of A and every 128x128 tile of B scaled by
+    # its own power of two: a B scale taken from the wrong column block or k-block (or an
+    # A scale from the wrong row or k-block) is off by 2x-64x and fails the bar, at the
+    # bench's K too.  FP32 output: with this range the exact product rounded to BF16 uses
+    # most of the max-abs bar by itself.
+    x = tile_spread(wl.normal_bf16((m, k), 70, 1.0), 1, 128, 1, 3)
+    w = tile_spread(wl.normal_bf16((n, k), 71, 0.02), 128, 128, 4, 3)
+    gemm_check(x, w, R.BLOCK_1x128, R.BLOCK_128x128, F.E4M3, F.E4M3, out=fq.OutDtype.FP32)
+
+
+@pytest.mark.parametrize("m,n,k", [
+    (512, 512, 4096),      # CTA pairs, 128 MX blocks along K
+    (1024, 768, 512),      # CTA pairs, N % 256 == 0 over several tiles
+    (384, 640, 640),       # M % 256 != 0: single CTAs, N tail
+])
+def test_gemm_mx_exponent_spread(m, n, k):
+    # MXFP8 with every 1x32 block of both operands scaled by 2^e, e in [-8, 8]: each
+    # block's E8M0 exponent differs from its neighbours', so an exponent applied to the
+    # wrong 32-deep block, row or column is off by 2^(1..16).
+    x = tile_spread(wl.normal_bf16((m, k), 72, 1.0), 1, 32, 2, 8)
+    w = tile_spread(wl.normal_bf16((n, k), 73, 0.02), 1, 32, 5, 8)
+    gemm_check(x, w, R.MX_1x32_TILED, R.MX_1x32_TILED, F.E4M3, F.E4M3, out=fq.OutDtype.FP32)

@@ -9,7 +9,7 @@ import oracle
 from scaled_quantize_gemm_amax_gb300 import Format
 from scaled_quantize_gemm_amax_gb300 import linear as L
 from scaled_quantize_gemm_amax_gb300 import workloads as wl
-from gpu_util import assert_status_ok, bits16, host, require_gpu
+from gpu_util import assert_status_ok, bits16, host, require_gpu, tile_spread
 import scaled_quantize_gemm_amax_gb300 as fq
 
 pytestmark = pytest.mark.gpu
@@ -99,3 +99,40 @@ def test_fp8_linear_delayed_scaling_steps():
         st["w"].step(oracle.amax(wh))
         st["dy"].step(oracle.amax(dyh))
 
+
+@pytest.mark.parametrize("name,recipe", [("current", L.Float8CurrentScaling()), ("block", L.Float8BlockScaling()),
+                                         ("mx", L.MXFP8BlockScaling())])
+def test_dgrad_reads_the_weight_column_copy(name, recipe):
+    # The dgrad GEMM of the layer's backward, dX = dY . W, reads W's column-wise copy
+    # (W^T [K, N], K-major along N) made by the layer's own quantization.  W's tiles (or,
+    # for MX, its 1x32 blocks along N in the column copy) and dY's blocks each carry their
+    # own power of two, so a column-copy scale read for the wrong tile is off by 2x or
+    # more.  FP32 output (the same GEMM the layer runs with BF16 output), because with
+    # this range the exact product rounded to BF16 uses most of the max-abs bar itself.
+    m, k_in, n_out = 512, 1024, 768
+    kx, kw = L._kinds(recipe)
+    fx, fdy = recipe.fwd_format, recipe.bwd_format
+    if name == "mx":
+        w16 = tile_spread(wl.normal_bf16((n_out, k_in), 95, 0.02), 32, 1, 3, 6)   # 32 x 1: blocks of W^T's rows
+        dy = tile_spread(wl.normal_bf16((m, n_out), 96, 1e-3), 1, 32, 1, 6)
+    else:
+        w16 = tile_spread(wl.normal_bf16((n_out, k_in), 95, 0.02), 128, 128, 3, 3)
+        dy = tile_spread(wl.normal_bf16((m, n_out), 96, 1e-3), 1, 128, 1, 3)
+    _, _, qwt, swt = L._quantize(w16, kw, fx, None)
+    qdy, sdy, _, _ = L._quantize(dy, kx, fdy, None)
+    dx = torch.empty((m, k_in), dtype=torch.float32, device="cuda")
+    fq.fp8_scaled_gemm(qdy, fdy, kx, sdy, qwt, fx, kw, swt, dx, fq.OutDtype.FP32)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    okx, okw = KINDS[name]
+    wh, dyh = bits16(w16), bits16(dy)
+    sw = sdy_s = None
+    if name == "current":
+        sw, _ = oracle.tensor_scale(oracle.amax(wh), int(fx))
+        sdy_s, _ = oracle.tensor_scale(oracle.amax(dyh), int(fdy))
+    _, w_c = oracle_copies(wh, okw, int(fx), sw)
+    dy_r, _ = oracle_copies(dyh, okx, int(fdy), sdy_s)
+    # the column copy's bytes are the oracle's, bit for bit
+    got_q = host(qwt)
+    assert np.array_equal(got_q, w_c[0]), "W column copy bytes"
+    check(dx, deq(dy_r, okx, int(fdy)), deq(w_c, okw, int(fx)), f"dgrad ({name})")
