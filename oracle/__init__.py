@@ -88,6 +88,11 @@ def _load():
             "orc_quantize_128x128": (None, [P, I64, I64, ctypes.c_int, P, P]),
             "orc_quantize_mx": (None, [P, I64, I64, ctypes.c_int, P, P]),
             "orc_transpose_bf16": (None, [P, I64, I64, P]),
+            "orc_quantize_tensor_f32": (None, [P, I64, I64, ctypes.c_int, F, P]),
+            "orc_quantize_1x128_f32": (None, [P, I64, I64, ctypes.c_int, P, P]),
+            "orc_quantize_128x128_f32": (None, [P, I64, I64, ctypes.c_int, P, P]),
+            "orc_quantize_mx_f32": (None, [P, I64, I64, ctypes.c_int, P, P]),
+            "orc_transpose_f32": (None, [P, I64, I64, P]),
             "orc_dequantize": (None, [P, I64, I64, ctypes.c_int, ctypes.c_int, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -222,6 +227,52 @@ def quantize_rowwise(x_bf16, kind: int, fmt: int, scale=None):
 def quantize_colwise(x_bf16, kind: int, fmt: int, scale=None):
     """Column-wise copy: the row-wise recipe applied to the transposed matrix."""
     return quantize_rowwise(transpose_bf16(x_bf16), kind, fmt, scale)
+
+
+def _f32(x) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.float32:
+        raise TypeError("binary32 inputs are passed as float32 arrays")
+    return x
+
+
+def transpose_f32(x_f32) -> np.ndarray:
+    x = _f32(x_f32)
+    R, C = x.shape
+    out = np.empty((C, R), np.float32)
+    _load().orc_transpose_f32(_ptr(x), R, C, _ptr(out))
+    return out
+
+
+def quantize_rowwise_f32(x_f32, kind: int, fmt: int, scale=None):
+    """Row-wise quantize of a [R, C] binary32 matrix (the FP32 master copy of a weight):
+    the same recipes and outputs as quantize_rowwise, element rule
+    encode_sat(x * scale) with x the binary32 value itself."""
+    x = _f32(x_f32)
+    R, C = x.shape
+    q = np.empty((R, C), np.uint8)
+    lib = _load()
+    if kind == KIND_TENSOR:
+        sc = np.float32(scale)
+        lib.orc_quantize_tensor_f32(_ptr(x), R, C, fmt, ctypes.c_float(float(sc)), _ptr(q))
+        s = np.array([np.float32(1.0) / sc], np.float32)
+    elif kind == KIND_1x128:
+        s = np.empty((R, C // 128), np.float32)
+        lib.orc_quantize_1x128_f32(_ptr(x), R, C, fmt, _ptr(q), _ptr(s))
+    elif kind == KIND_128x128:
+        s = np.empty((R // 128, C // 128), np.float32)
+        lib.orc_quantize_128x128_f32(_ptr(x), R, C, fmt, _ptr(q), _ptr(s))
+    elif kind == KIND_MX:
+        s = np.empty((R, C // 32), np.uint8)
+        lib.orc_quantize_mx_f32(_ptr(x), R, C, fmt, _ptr(q), _ptr(s))
+    else:
+        raise ValueError(kind)
+    return q, s
+
+
+def quantize_colwise_f32(x_f32, kind: int, fmt: int, scale=None):
+    """Column-wise copy of a binary32 matrix: the row-wise recipe on its transpose."""
+    return quantize_rowwise_f32(transpose_f32(x_f32), kind, fmt, scale)
 
 
 # ----------------------------------------------------------------- MX tiled layout

@@ -308,6 +308,81 @@ void orc_quantize_mx(const uint16_t* x, int64_t R, int64_t C, int fmt, uint8_t* 
     }
 }
 
+/*
+ * The same four quantizers for a binary32 input matrix -- the FP32 master copy of
+ * a weight quantized directly (search-result page, mixed-precision dataflow
+ * paragraph: weights are held in higher precision and quantized to FP8 from
+ * that copy).  Each element is one binary32 product x * scale followed by the
+ * saturating cast, exactly as for bf16 inputs, whose values are a subset of the
+ * binary32 ones; block amaxes are taken over the binary32 values (NaN ignored).
+ */
+static uint8_t quantize_one_f32(float x, float scale, int fmt)
+{
+    return orc_encode(x * scale, fmt, 1);
+}
+
+void orc_quantize_tensor_f32(const float* x, int64_t R, int64_t C, int fmt, float scale, uint8_t* q)
+{
+    for (int64_t i = 0; i < R * C; ++i) q[i] = quantize_one_f32(x[i], scale, fmt);
+}
+
+void orc_quantize_1x128_f32(const float* x, int64_t R, int64_t C, int fmt, uint8_t* q, float* s_inv)
+{
+    int64_t nb = C / 128;
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const float* blk = x + r * C + b * 128;
+            float scale, sinv;
+            orc_tensor_scale(orc_amax_f32(blk, 128), fmt, &scale, &sinv);
+            for (int64_t j = 0; j < 128; ++j) q[r * C + b * 128 + j] = quantize_one_f32(blk[j], scale, fmt);
+            s_inv[r * nb + b] = sinv;
+        }
+    }
+}
+
+void orc_quantize_128x128_f32(const float* x, int64_t R, int64_t C, int fmt, uint8_t* q, float* s_inv)
+{
+    int64_t nbr = R / 128, nbc = C / 128;
+    for (int64_t br = 0; br < nbr; ++br) {
+        for (int64_t bc = 0; bc < nbc; ++bc) {
+            float amax = 0.0f;
+            for (int64_t i = 0; i < 128; ++i) {
+                float a = orc_amax_f32(x + (br * 128 + i) * C + bc * 128, 128);
+                if (a > amax) amax = a;
+            }
+            float scale, sinv;
+            orc_tensor_scale(amax, fmt, &scale, &sinv);
+            for (int64_t i = 0; i < 128; ++i)
+                for (int64_t j = 0; j < 128; ++j) {
+                    int64_t idx = (br * 128 + i) * C + bc * 128 + j;
+                    q[idx] = quantize_one_f32(x[idx], scale, fmt);
+                }
+            s_inv[br * nbc + bc] = sinv;
+        }
+    }
+}
+
+void orc_quantize_mx_f32(const float* x, int64_t R, int64_t C, int fmt, uint8_t* q, uint8_t* s_e8m0)
+{
+    int64_t nb = C / 32;
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const float* blk = x + r * C + b * 32;
+            int e = orc_mx_exponent(orc_amax_f32(blk, 32), fmt);
+            float scale = pow2_neg(e);
+            for (int64_t j = 0; j < 32; ++j) q[r * C + b * 32 + j] = quantize_one_f32(blk[j], scale, fmt);
+            s_e8m0[r * nb + b] = (uint8_t)(e + 127);
+        }
+    }
+}
+
+/* Plain transpose of a row-major [R, C] binary32 matrix into [C, R]. */
+void orc_transpose_f32(const float* x, int64_t R, int64_t C, float* xt)
+{
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) xt[c * R + r] = x[r * C + c];
+}
+
 /* Plain transpose of a row-major [R, C] bf16 matrix into [C, R]. */
 void orc_transpose_bf16(const uint16_t* x, int64_t R, int64_t C, uint16_t* xt)
 {

@@ -28,9 +28,20 @@ MUTANTS = {
     "history_window_one_slot": ("for (int32_t i = 0; i < len; ++i)\n        if (hist[i] > m)",
                                 "for (int32_t i = 0; i < 1; ++i)\n        if (hist[i] > m)"),
     "mx_exponent_strict": ("if ((double)amax <= ldexp(fmax, e)) return e;", "if ((double)amax < ldexp(fmax, e)) return e;"),
-    "mx_scale_sign": ("float scale = pow2_neg(e);", "float scale = pow2_neg(-e);"),
-    "tile128_first_row_only": ("for (int64_t i = 0; i < 128; ++i) {\n                float a",
-                               "for (int64_t i = 0; i < 1; ++i) {\n                float a"),
+    "mx_scale_sign": ("orc_amax_bf16(blk, 32), fmt);\n            float scale = pow2_neg(e);",
+                      "orc_amax_bf16(blk, 32), fmt);\n            float scale = pow2_neg(-e);"),
+    "tile128_first_row_only": ("for (int64_t i = 0; i < 128; ++i) {\n                float a = orc_amax_bf16(",
+                               "for (int64_t i = 0; i < 1; ++i) {\n                float a = orc_amax_bf16("),
+    # binary32-input quantizers
+    "f32_read_through_bf16": ("return orc_encode(x * scale, fmt, 1);",
+                              "return orc_encode(bf16_to_float((uint16_t)(float_to_bits(x) >> 16)) * scale, fmt, 1);"),
+    "f32_tile128_first_row_only": ("for (int64_t i = 0; i < 128; ++i) {\n                float a = orc_amax_f32(",
+                                   "for (int64_t i = 0; i < 1; ++i) {\n                float a = orc_amax_f32("),
+    "f32_1x128_block_stride": ("const float* blk = x + r * C + b * 128;", "const float* blk = x + r * C + b * 127;"),
+    "f32_mx_scale_sign": ("orc_amax_f32(blk, 32), fmt);\n            float scale = pow2_neg(e);",
+                          "orc_amax_f32(blk, 32), fmt);\n            float scale = pow2_neg(-e);"),
+    "f32_transpose_index": ("for (int64_t c = 0; c < C; ++c) xt[c * R + r] = x[r * C + c];\n}\n\n/* Plain transpose of a row-major [R, C] bf16",
+                            "for (int64_t c = 0; c < C; ++c) xt[c * R + r] = x[c * R + r];\n}\n\n/* Plain transpose of a row-major [R, C] bf16"),
     "dequant_1x128_index": ("case 1: m = (double)sf[r * (C / 128) + c / 128]; break;",
                             "case 1: m = (double)sf[(r / 128) * (C / 128) + c / 128]; break;"),
     "dequant_mx_bias": ("m = e == 255 ? NAN : ldexp(1.0, e - 127);", "m = e == 255 ? NAN : ldexp(1.0, e - 128);"),
@@ -58,6 +69,7 @@ def test_pins_reject_mutant(name, tmp_path):
                           os.path.join(ROOT, "tests", "test_oracle_scaling.py"),
                           os.path.join(ROOT, "tests", "test_oracle_formats.py"),
                           os.path.join(ROOT, "tests", "test_oracle_dequant.py"),
-                          os.path.join(ROOT, "tests", "test_oracle_allreduce.py")],
+                          os.path.join(ROOT, "tests", "test_oracle_allreduce.py"),
+                          os.path.join(ROOT, "tests", "test_oracle_f32.py")],
                          capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
     assert out.returncode != 0, f"the pins did not catch mutant {name}"
