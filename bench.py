@@ -207,12 +207,13 @@ class Path:
         self.gemm()
 
 
-def bytes_cast(recipe_name, r, c):
-    """Algorithmic bytes of a row + column cast-transpose of an r x c bf16 matrix: 2 B read
-    and 1 B + 1 B written per element, plus the scale arrays of both copies."""
+def bytes_cast(recipe_name, r, c, in_bytes=2):
+    """Algorithmic bytes of a row + column cast-transpose of an r x c matrix: the input read
+    (2 B per element for bf16, 4 B for float32) and 1 B + 1 B written per element, plus the
+    scale arrays of both copies."""
     extra = {"TENSOR": 0, "BLOCK_1x128": 2 * (r * c // 128) * 4, "BLOCK_128x128": 2 * (r * c // 16384) * 4,
              "MX_1x32": 2 * (r * c // 32), "MX_1x32_TILED": 2 * (r * c // 32)}[recipe_name]
-    return 4 * r * c + extra
+    return (in_bytes + 2) * r * c + extra
 
 
 class L2Flush:
@@ -446,6 +447,17 @@ def run_per_recipe(fq, wl, dev, flush):
         del x
         torch.cuda.empty_cache()
 
+    # ---- the FP32 master copy of a weight quantized directly (binary32 input, 4 B read per element)
+    out["cast_transpose_f32"] = {}
+    w32 = wl.normal_bf16((8192, 8192), 7, 0.02, dev).float()
+    for rec in (R.TENSOR, R.BLOCK_128x128, R.MX_1x32_TILED):
+        sc = one if rec == R.TENSOR else None
+        qr, sr, qc, scol = fq.cast_transpose(w32, rec, F.E4M3, sc)
+        ms = time_kernel(lambda: fq.fp8_cast_transpose_f32(w32, rec, F.E4M3, sc, None, qr, sr, qc, scol), flush=flush)
+        out["cast_transpose_f32"][f"{rec.name}_8192"] = bw(ms, bytes_cast(rec.name, 8192, 8192, in_bytes=4))
+        del qr, sr, qc, scol
+    del w32
+
     # ---- GEMMs
     shapes = [("tensor_4096", R.TENSOR, R.TENSOR, (4096, 4096, 4096), F.E4M3, F.E4M3, O.BF16),
               ("tensor_8192", R.TENSOR, R.TENSOR, (8192, 8192, 8192), F.E4M3, F.E4M3, O.BF16),
@@ -673,7 +685,8 @@ def run_reference(args, rank, world):
             "wall_s": round(wall, 2)}
 
 
-CASES = ("cast_tensor", "cast_1x128", "cast_128x128", "cast_mx", "amax", "gemm_tensor", "gemm_block", "gemm_mx",
+CASES = ("cast_tensor", "cast_1x128", "cast_128x128", "cast_mx", "cast_f32_tensor", "cast_f32_1x128", "cast_f32_128x128",
+         "cast_f32_mx", "amax", "amax_f32", "gemm_tensor", "gemm_block", "gemm_mx",
          "gemm_block_wgrad", "gemm_amax", "dequant_tensor", "dequant_1x128", "dequant_128x128", "dequant_mx", "allreduce")
 
 
@@ -691,19 +704,25 @@ def run_case(args):
     s = args.size
     flush = L2Flush(dev)
     pk = peaks()
-    if args.case.startswith("cast") or args.case == "amax":
+    if args.case.startswith("cast") or args.case.startswith("amax"):
         x = wl.cfg5_sweep(s, dev) if s in wl.CFG5_SIZES else wl.normal_bf16((s, s), 5, 1.0, dev)
+        f32 = "f32" in args.case
+        if f32:
+            x = x.float()
         rec = {"cast_tensor": R.TENSOR, "cast_1x128": R.BLOCK_1x128, "cast_128x128": R.BLOCK_128x128,
-               "cast_mx": R.MX_1x32_TILED, "amax": None}[args.case]
+               "cast_mx": R.MX_1x32_TILED, "amax": None, "amax_f32": None, "cast_f32_tensor": R.TENSOR,
+               "cast_f32_1x128": R.BLOCK_1x128, "cast_f32_128x128": R.BLOCK_128x128,
+               "cast_f32_mx": R.MX_1x32_TILED}[args.case]
         if rec is None:
             amax = torch.empty(1, dtype=torch.float32, device=dev)
-            fn = lambda: fq.fp8_amax(x, amax)
-            nbytes = 2 * s * s
+            fn = (lambda: fq.fp8_amax_f32(x, amax)) if f32 else (lambda: fq.fp8_amax(x, amax))
+            nbytes = (4 if f32 else 2) * s * s
         else:
             scale = torch.ones(1, dtype=torch.float32, device=dev) if rec == R.TENSOR else None
             qr, sr, qc, sc = fq.cast_transpose(x, rec, F.E4M3, scale)
-            fn = lambda: fq.fp8_cast_transpose(x, rec, F.E4M3, scale, None, qr, sr, qc, sc)
-            nbytes = bytes_cast(rec.name, s, s)
+            cast = fq.fp8_cast_transpose_f32 if f32 else fq.fp8_cast_transpose
+            fn = lambda: cast(x, rec, F.E4M3, scale, None, qr, sr, qc, sc)
+            nbytes = bytes_cast(rec.name, s, s, in_bytes=4 if f32 else 2)
         ms = time_kernel(fn, reps=args.steps, flush=flush)
         res = {"case": args.case, "size": s, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
         res["frac_hbm"] = round(res["GB/s"] / pk["hbm_gbs"], 4)

@@ -81,6 +81,14 @@ typedef enum { FP8_OUT_BF16 = 0, FP8_OUT_FP32 = 1 } fp8_out_dtype;
 fp8_status fp8_amax(const void* x, int64_t rows, int64_t cols, float* amax, cudaStream_t stream);
 
 /*
+ * fp8_amax_f32 -- fp8_amax of a binary32 tensor (e.g. the FP32 master copy of a
+ * weight that is quantized with current scaling; search-result page, the
+ * mixed-precision dataflow paragraph: FP8 weights come from the higher-precision
+ * copy).  x is device, [rows, cols] float, 16-byte aligned; otherwise as fp8_amax.
+ */
+fp8_status fp8_amax_f32(const float* x, int64_t rows, int64_t cols, float* amax, cudaStream_t stream);
+
+/*
  * fp8_compute_scale -- per-tensor current-scaling scale.  Colossal-AI FP8
  * page, "current scaling"; guide, "instant scaling scheme".
  *   amax       device, 1 float (input)
@@ -150,6 +158,21 @@ fp8_status amax_history_update(float* hist, int32_t len, int32_t* pos, const flo
 fp8_status fp8_cast_transpose(const void* x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
                               const float* scale, float* amax_out, uint8_t* q_row, void* s_row, uint8_t* q_col,
                               void* s_col, cudaStream_t stream);
+
+/*
+ * fp8_cast_transpose_f32 -- fp8_cast_transpose of a binary32 matrix: the FP32
+ * master copy of a weight quantized directly, without a bf16 copy in between
+ * (search-result page, mixed-precision dataflow paragraph: the FP8 weights come
+ * from the higher-precision copy).  Every argument, output, layout, shape rule and
+ * error as fp8_cast_transpose, except
+ *   x  device, [rows, cols] float (binary32), 16-byte aligned
+ * Element rule: q = saturating round-to-nearest-even FP8 of (x * s), one binary32
+ * product of the binary32 input; block amaxes (and amax_out) are taken over the
+ * binary32 values, NaN ignored.
+ */
+fp8_status fp8_cast_transpose_f32(const float* x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
+                                  const float* scale, float* amax_out, uint8_t* q_row, void* s_row, uint8_t* q_col,
+                                  void* s_col, cudaStream_t stream);
 
 /*
  * fp8_cast_transpose_multi -- several fp8_cast_transpose calls in one launch (e.g.

@@ -7,8 +7,9 @@ output tensors with torch.  There is no fallback: every call raises when
 ``libfp8q.so`` has not been built (``scaled_quantize_gemm_amax_gb300/build.py``).
 
 Entry points with the C names take tensors (or None for NULL) and raise
-``FP8Error`` on a non-OK status: ``fp8_amax``, ``fp8_compute_scale``,
-``amax_history_update``, ``fp8_quantize``, ``fp8_cast_transpose``, ``fp8_cast_transpose_multi``,
+``FP8Error`` on a non-OK status: ``fp8_amax``, ``fp8_amax_f32``, ``fp8_compute_scale``,
+``amax_history_update``, ``fp8_quantize``, ``fp8_cast_transpose``, ``fp8_cast_transpose_f32``,
+``fp8_cast_transpose_multi``,
 ``fp8_dequantize``, ``fp8_allreduce_sum``, ``fp8_scaled_gemm``, ``fp8_scaled_gemm_amax``,
 ``fp8_get_device_status``, ``fp8_debug_wait_timeout``.  ``cast_transpose`` /
 ``dequantize`` / ``scaled_gemm`` / ``scaled_gemm_amax`` are allocation helpers
@@ -25,7 +26,8 @@ import torch
 
 __all__ = [
     "Status", "Format", "Recipe", "OutDtype", "FP8Error", "lib_path", "load_library",
-    "fp8_amax", "fp8_compute_scale", "amax_history_update", "fp8_quantize", "fp8_cast_transpose",
+    "fp8_amax", "fp8_amax_f32", "fp8_compute_scale", "amax_history_update", "fp8_quantize", "fp8_cast_transpose",
+    "fp8_cast_transpose_f32",
     "fp8_cast_transpose_multi", "CastJob",
     "fp8_dequantize", "fp8_allreduce_sum", "fp8_allreduce_sum_noalloc", "fp8_scaled_gemm", "fp8_scaled_gemm_amax", "fp8_get_device_status",
     "fp8_debug_wait_timeout", "fp8_status_string",
@@ -92,6 +94,8 @@ class CastJob(ctypes.Structure):
 
 _SIGNATURES = {
     "fp8_amax": [_P, _I64, _I64, _P, _P],
+    "fp8_amax_f32": [_P, _I64, _I64, _P, _P],
+    "fp8_cast_transpose_f32": [_P, _I64, _I64, _E, _E, _P, _P, _P, _P, _P, _P, _P],
     "fp8_compute_scale": [_P, _E, _P, _P, _P],
     "amax_history_update": [_P, _I32, _P, _P, _E, _P, _P, _P],
     "fp8_cast_transpose": [_P, _I64, _I64, _E, _E, _P, _P, _P, _P, _P, _P, _P],
@@ -158,6 +162,12 @@ def fp8_amax(x, amax, stream=None):
     _check("fp8_amax", load_library().fp8_amax(_ptr(x), rows, cols, _ptr(amax), _stream(stream)))
 
 
+def fp8_amax_f32(x, amax, stream=None):
+    """amax[0] = max |x| of a float32 tensor."""
+    rows, cols = (x.shape[0], x.numel() // max(x.shape[0], 1)) if x.dim() >= 1 else (1, 1)
+    _check("fp8_amax_f32", load_library().fp8_amax_f32(_ptr(x), rows, cols, _ptr(amax), _stream(stream)))
+
+
 def fp8_compute_scale(amax, fmt, scale, scale_inv, stream=None):
     _check("fp8_compute_scale",
            load_library().fp8_compute_scale(_ptr(amax), int(fmt), _ptr(scale), _ptr(scale_inv), _stream(stream)))
@@ -175,6 +185,14 @@ def fp8_cast_transpose(x, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_c
            load_library().fp8_cast_transpose(_ptr(x), rows, cols, int(recipe), int(fmt), _ptr(scale),
                                              _ptr(amax_out), _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col),
                                              _stream(stream)))
+
+
+def fp8_cast_transpose_f32(x, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_col, stream=None):
+    rows, cols = x.shape
+    _check("fp8_cast_transpose_f32",
+           load_library().fp8_cast_transpose_f32(_ptr(x), rows, cols, int(recipe), int(fmt), _ptr(scale),
+                                                 _ptr(amax_out), _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col),
+                                                 _stream(stream)))
 
 
 def fp8_cast_transpose_multi(jobs, stream=None):
@@ -278,7 +296,8 @@ def scale_shape(recipe, rows: int, cols: int):
 
 
 def cast_transpose(x, recipe, fmt, scale=None, amax_out=None, row=True, col=True, stream=None):
-    """Allocate outputs with torch and run fp8_cast_transpose.
+    """Allocate outputs with torch and run fp8_cast_transpose (bf16 x) or
+    fp8_cast_transpose_f32 (float32 x).
 
     Returns (q_row, s_row, q_col, s_col); the parts not requested are None.
     """
@@ -293,7 +312,12 @@ def cast_transpose(x, recipe, fmt, scale=None, amax_out=None, row=True, col=True
         q_col = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
         shp, dt = scale_shape(recipe, cols, rows)
         s_col = torch.empty(shp, dtype=dt, device=dev)
-    fp8_cast_transpose(x, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_col, stream)
+    if x.dtype == torch.float32:
+        fp8_cast_transpose_f32(x, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_col, stream)
+    elif x.dtype == torch.bfloat16:
+        fp8_cast_transpose(x, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_col, stream)
+    else:
+        raise TypeError(f"cast_transpose takes bfloat16 or float32 input, not {x.dtype}")
     return q_row, s_row, q_col, s_col
 
 

@@ -1,7 +1,7 @@
 // amax.cu -- per-tensor amax reduction, per-tensor scale, and the delayed-scaling
 // amax-history update.
 //
-// amax: the maximum of |x| over a BF16 tensor, NaN ignored (Colossal-AI FP8,
+// amax: the maximum of |x| over a BF16 (or binary32) tensor, NaN ignored (Colossal-AI FP8,
 // "current scaling": the scale comes from the current tensor's maximum).  The
 // reduction is order-free (a max), so any grid shape gives the same bits.
 // History: a ring of past amaxes; the next scale comes from the window maximum
@@ -62,6 +62,49 @@ __global__ void __launch_bounds__(kAmaxThreads) k_amax(const uint4* __restrict__
   __shared__ float red[kAmaxThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) red[warp] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = red[0];
+    for (int w = 1; w < kAmaxThreads / 32; ++w) b = fmaxf(b, red[w]);
+    if (b > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(amax), __float_as_uint(b));
+  }
+}
+
+// The same maximum over binary32 values (the FP32 master copy of a weight quantized
+// with current scaling): 16-byte chunks of four values, NaN ignored by fmaxf.
+__device__ __forceinline__ float fold4(float m, float4 v) {
+  return fmaxf(fmaxf(fmaxf(fmaxf(m, fabsf(v.x)), fabsf(v.y)), fabsf(v.z)), fabsf(v.w));
+}
+
+__global__ void __launch_bounds__(kAmaxThreads) k_amax_f32(const float4* __restrict__ x4, int64_t n4,
+                                                          const float* __restrict__ tail, int ntail,
+                                                          float* __restrict__ amax) {
+  pdl_wait();
+  pdl_launch_dependents();
+  float m = 0.0f;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + (kAmaxUnroll - 1) * stride < n4; i += kAmaxUnroll * stride) {
+    float4 v[kAmaxUnroll];
+#pragma unroll
+    for (int u = 0; u < kAmaxUnroll; ++u) v[u] = __ldg(x4 + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < kAmaxUnroll; ++u) m = fold4(m, v[u]);
+  }
+  if (i < n4) {
+    float4 v[kAmaxUnroll];
+#pragma unroll
+    for (int u = 0; u < kAmaxUnroll; ++u)
+      v[u] = i + u * stride < n4 ? __ldg(x4 + i + u * stride) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+    for (int u = 0; u < kAmaxUnroll; ++u) m = fold4(m, v[u]);
+  }
+  if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < ntail) m = fmaxf(m, fabsf(tail[threadIdx.x]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  __shared__ float red[kAmaxThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = m;
   __syncthreads();
   if (threadIdx.x == 0) {
     float b = red[0];
@@ -139,6 +182,16 @@ cudaError_t launch_amax(const void* x, int64_t n, float* amax, int num_sms, cuda
   int grid = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
   return launch_pdl(k_amax, dim3(grid), dim3(kAmaxThreads), 0, s, 1, static_cast<const uint4*>(x), n16,
                     static_cast<const uint16_t*>(x) + n16 * 8, ntail, amax);
+}
+
+cudaError_t launch_amax_f32(const float* x, int64_t n, float* amax, int num_sms, cudaStream_t s) {
+  const int64_t n4 = n / 4;
+  const int ntail = static_cast<int>(n - n4 * 4);
+  int64_t want = (n4 + static_cast<int64_t>(kAmaxThreads) * kAmaxUnroll - 1) / (kAmaxThreads * kAmaxUnroll);
+  int64_t cap = static_cast<int64_t>(num_sms) * 4;
+  int grid = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
+  return launch_pdl(k_amax_f32, dim3(grid), dim3(kAmaxThreads), 0, s, 1, reinterpret_cast<const float4*>(x), n4,
+                    x + n4 * 4, ntail, amax);
 }
 
 cudaError_t launch_compute_scale(const float* amax, bool e5m2, float* scale, float* scale_inv, cudaStream_t s) {

@@ -111,17 +111,24 @@ using namespace fp8q;
 
 namespace {
 
+fp8_status cast_transpose_impl(const void* x, bool f32, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
+                               const float* scale, float* amax_out, uint8_t* q_row, void* s_row, uint8_t* q_col,
+                               void* s_col, cudaStream_t stream);
+
 // Validation and launch parameters of one cast; no device work.  fp8_cast_transpose and
 // every job of fp8_cast_transpose_multi go through the same checks.
 struct CastPlan {
   bool empty = false;   // no elements: nothing to launch
   bool tiled = false;   // the TMA path (else the plain per-tensor path)
+  bool f32 = false;     // binary32 input (else bf16)
   CastParams p{};
   CUtensorMap tm_x, tm_qr, tm_qc;
 };
 
 fp8_status plan_cast(const void* x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt, const float* scale,
-                     float* amax_out, uint8_t* q_row, void* s_row, uint8_t* q_col, void* s_col, CastPlan* plan) {
+                     float* amax_out, uint8_t* q_row, void* s_row, uint8_t* q_col, void* s_col, CastPlan* plan,
+                     bool f32 = false) {
+  plan->f32 = f32;
   if (rows < 0 || cols < 0 || !valid_fmt(fmt) || recipe < FP8_TENSOR || recipe > FP8_MX_1x32_TILED)
     return FP8_ERR_INVALID_ARG;
   if (rows * cols == 0) {
@@ -181,7 +188,9 @@ fp8_status plan_cast(const void* x, int64_t rows, int64_t cols, fp8_recipe recip
   if (plan->tiled) {
     std::memset(&plan->tm_qr, 0, sizeof(plan->tm_qr));
     std::memset(&plan->tm_qc, 0, sizeof(plan->tm_qc));
-    if (!make_map(&plan->tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, cols, rows, 64, 128)) return FP8_ERR_CUDA;
+    const bool ok = f32 ? make_map(&plan->tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x, cols, rows, 32, 128)
+                        : make_map(&plan->tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, cols, rows, 64, 128);
+    if (!ok) return FP8_ERR_CUDA;
     if (do_row && !make_map(&plan->tm_qr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q_row, cols, rows, 128, 128))
       return FP8_ERR_CUDA;
     if (do_col && !make_map(&plan->tm_qc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q_col, rows, cols, 128, 128))
@@ -355,8 +364,38 @@ fp8_status fp8_cast_transpose(const void* x, int64_t rows, int64_t cols, fp8_rec
                               const float* scale, float* amax_out, uint8_t* q_row, void* s_row, uint8_t* q_col,
                               void* s_col, cudaStream_t stream) {
   ApiRange nvtx_range("fp8_cast_transpose");
+  return cast_transpose_impl(x, false, rows, cols, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_col, stream);
+}
+
+fp8_status fp8_cast_transpose_f32(const float* x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
+                                  const float* scale, float* amax_out, uint8_t* q_row, void* s_row, uint8_t* q_col,
+                                  void* s_col, cudaStream_t stream) {
+  ApiRange nvtx_range("fp8_cast_transpose_f32");
+  return cast_transpose_impl(x, true, rows, cols, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_col, stream);
+}
+
+fp8_status fp8_amax_f32(const float* x, int64_t rows, int64_t cols, float* amax, cudaStream_t stream) {
+  ApiRange nvtx_range("fp8_amax_f32");
+  if (rows < 0 || cols < 0 || amax == nullptr) return FP8_ERR_INVALID_ARG;
+  const int64_t n = rows * cols;
+  if (n > 0 && x == nullptr) return FP8_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(amax, 4)) return FP8_ERR_ALIGNMENT;
+  DeviceInfo* d;
+  if (fp8_status st = device_info(&d)) return st;
+  if (launch_zero_f32(amax, 1, stream) != cudaSuccess) return FP8_ERR_CUDA;
+  if (n == 0) return FP8_OK;
+  return cuda_status(launch_amax_f32(x, n, amax, d->num_sms, stream));
+}
+
+}  // extern "C"
+
+namespace {
+
+fp8_status cast_transpose_impl(const void* x, bool f32, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
+                               const float* scale, float* amax_out, uint8_t* q_row, void* s_row, uint8_t* q_col,
+                               void* s_col, cudaStream_t stream) {
   CastPlan plan;
-  if (fp8_status st = plan_cast(x, rows, cols, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_col, &plan))
+  if (fp8_status st = plan_cast(x, rows, cols, recipe, fmt, scale, amax_out, q_row, s_row, q_col, s_col, &plan, f32))
     return st;
   if (plan.empty) {
     // nothing to cast (outputs of an empty tensor may be NULL); amax of nothing is 0
@@ -368,9 +407,17 @@ fp8_status fp8_cast_transpose(const void* x, int64_t rows, int64_t cols, fp8_rec
   if (amax_out != nullptr && launch_zero_f32(amax_out, 1, stream) != cudaSuccess) return FP8_ERR_CUDA;
   plan.p.err = d->err;
   // only the per-tensor recipe can miss the tiled path (block recipes imply its alignment)
+  if (f32) {
+    if (!plan.tiled) return cuda_status(launch_cast_generic_f32(plan.p, x, stream));
+    return cuda_status(launch_cast_transpose_tiled_f32(plan.p, plan.tm_x, plan.tm_qr, plan.tm_qc, d->num_sms, stream));
+  }
   if (!plan.tiled) return cuda_status(launch_cast_generic(plan.p, x, stream));
   return cuda_status(launch_cast_transpose_tiled(plan.p, plan.tm_x, plan.tm_qr, plan.tm_qc, d->num_sms, stream));
 }
+
+}  // namespace
+
+extern "C" {
 
 fp8_status fp8_cast_transpose_multi(const fp8_cast_job* jobs, int32_t n_jobs, cudaStream_t stream) {
   ApiRange nvtx_range("fp8_cast_transpose_multi");

@@ -25,6 +25,7 @@
 // other roles see a shared abort flag, and the CTA drains and frees TMEM.
 #include <cuda_bf16.h>
 
+#include "gemm_util.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "recipes.cuh"
@@ -33,10 +34,11 @@ namespace fp8q {
 
 namespace {
 
+using namespace gemm_util;
+
 constexpr int kBM = 128;
 constexpr int kBK = 128;               // bytes (= FP8 elements) of K per stage
 constexpr int kUmmaK = 32;             // K of one MMA instruction for 8-bit inputs
-constexpr int kGroupM = 8;             // tile raster: groups of 8 M-tiles share B tiles in L2
 constexpr uint32_t kTmemCols = 512;
 
 // Blockwise with per-row B scales (1x128 x 1x128, the wgrad pairing): its own
@@ -137,55 +139,6 @@ struct Layout {
   static constexpr uint32_t TX_BYTES = PAIR ? 2 * (STAGE_BYTES + SF_BYTES) : STAGE_BYTES + SF_BYTES;
 };
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  uint32_t d;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
-  return d;
-}
-
-// Packed pairs of binary32 (Blackwell's f32x2 arithmetic: one instruction, two lanes).
-__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ uint64_t pack_f32x2(uint32_t lo, uint32_t hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-  return r;
-}
-__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-
-__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
-}
-
-__device__ __forceinline__ void sts32(uint32_t a, float v) {
-  asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
-}
-// volatile: stays after the barrier wait that precedes it
-__device__ __forceinline__ float4 lds128f(uint32_t a) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
-__device__ __forceinline__ void stg128(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
 // Store 32 consecutive FP32 values (already scaled) of one output row.
 __device__ __forceinline__ void store_row32(void* c, int64_t off, const float (&v)[32], bool fp32) {
   if (fp32) {
@@ -201,28 +154,6 @@ __device__ __forceinline__ void store_row32(void* c, int64_t off, const float (&
       stg128(p + 8 * i, pack_bf16(v[8 * i], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
              pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
   }
-}
-
-// a / b for a >= 0, b > 0.  Below 2^22 a binary32 estimate (relative error under 2^-23,
-// so within one of the quotient) corrected by one step either way: a few instructions
-// instead of an integer division, which the tile walker paid at every tile change
-// (1-2 % at 8192^3, measured).
-__device__ __forceinline__ int div_small(int a, int b) {
-  if (a >= (1 << 22)) return a / b;
-  int q = __float2int_rz(__fmul_rn(static_cast<float>(a), __frcp_rn(static_cast<float>(b))));
-  const int r = a - q * b;
-  q += (r >= b) - (r < 0);
-  return q;
-}
-
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
-  const int per_group = kGroupM * tiles_n;
-  const int group = div_small(t, per_group);
-  const int first_m = group * kGroupM;
-  const int gsize = min(tiles_m - first_m, kGroupM);
-  const int r = t - group * per_group;
-  tn = div_small(r, gsize);
-  tm = first_m + (r - tn * gsize);
 }
 
 // control warps (producer, MMA), EPI epilogue warps, then (CTRL = 2) the second MMA issuer if any

@@ -62,6 +62,7 @@ cudaError_t launch_reciprocal(const float* in, float* out, cudaStream_t s);
 // p[0 .. n) = 0 as a (programmatically launched) kernel, ahead of an atomicMax reduction
 cudaError_t launch_zero_f32(float* p, int n, cudaStream_t s);
 cudaError_t launch_amax(const void* x, int64_t n, float* amax, int num_sms, cudaStream_t s);
+cudaError_t launch_amax_f32(const float* x, int64_t n, float* amax, int num_sms, cudaStream_t s);
 cudaError_t launch_compute_scale(const float* amax, bool e5m2, float* scale, float* scale_inv, cudaStream_t s);
 cudaError_t launch_history_update(float* hist, int32_t len, int32_t* pos, const float* amax, bool e5m2, float* scale,
                                   float* scale_inv, uint32_t* err, cudaStream_t s);
@@ -87,6 +88,11 @@ cudaError_t launch_cast_transpose_tiled(const CastParams& p, const CUtensorMap& 
                                         const CUtensorMap& tm_qcol, int num_sms, cudaStream_t s);
 // Plain path for the per-tensor recipe at any shape.
 cudaError_t launch_cast_generic(const CastParams& p, const void* x, cudaStream_t s);
+// The same two paths for a binary32 input (quantize_f32.cu); the tiled path's tensor map
+// holds the input as 32-column boxes of 128 rows.
+cudaError_t launch_cast_transpose_tiled_f32(const CastParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_qrow,
+                                            const CUtensorMap& tm_qcol, int num_sms, cudaStream_t s);
+cudaError_t launch_cast_generic_f32(const CastParams& p, const void* x, cudaStream_t s);
 // Several tiled casts in one launch: job j owns tiles [tile_start[j], tile_start[j+1]).
 constexpr int kMaxCastJobs = 4;
 struct CastJobMaps {

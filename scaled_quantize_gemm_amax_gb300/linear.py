@@ -23,8 +23,12 @@ column-wise copies in one pass).  Recipes:
   Float8BlockScaling    X, dY 1x128 and W 128x128 FP32 scales (guide,
                         "block-level scaling")
   MXFP8BlockScaling     1x32 E8M0 scales everywhere (guide, "MXFP8 scaling")
-Every computation runs in the library's kernels; M, N and K must be multiples
-of 128 (the GEMM's tile), which the library checks.
+Every computation runs in the library's kernels -- torch only allocates: the
+FP32 master weight is quantized directly (fp8_cast_transpose_f32, with
+fp8_amax_f32 for current scaling), bf16 or float32 activations and gradients
+go to the cast of their own dtype, and each GEMM writes its output in the
+dtype autograd expects (Y and dX in the input's dtype, dW in FP32).  M, N and
+K must be multiples of 128 (the GEMM's tile), which the library checks.
 """
 from __future__ import annotations
 
@@ -35,7 +39,7 @@ import threading
 import torch
 
 from . import (DelayedScaling, Format, OutDtype, Recipe, amax_history_update, cast_transpose, fp8_amax,
-               fp8_compute_scale, fp8_scaled_gemm)
+               fp8_amax_f32, fp8_compute_scale, fp8_scaled_gemm)
 
 __all__ = ["Float8CurrentScaling", "Float8DelayedScaling", "Float8BlockScaling", "MXFP8BlockScaling", "fp8_autocast",
            "get_fp8_recipe", "FP8Linear", "fp8_linear"]
@@ -93,7 +97,9 @@ def fp8_autocast(enabled: bool = True, fp8_recipe=None):
 
 # ------------------------------------------------------------------ quantization of one operand
 def _quantize(x, recipe_kind, fmt, delayed: DelayedScaling | None):
-    """Row- and column-wise FP8 copies of a [R, C] bf16 matrix: (q_row, s_row, q_col, s_col)."""
+    """Row- and column-wise FP8 copies of a [R, C] bf16 or float32 matrix: (q_row, s_row, q_col, s_col)."""
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError(f"FP8 linear operands are bfloat16 or float32, not {x.dtype}")
     if recipe_kind == Recipe.TENSOR:
         if delayed is not None:
             out = cast_transpose(x, Recipe.TENSOR, fmt, delayed.scale, delayed.amax)
@@ -102,7 +108,7 @@ def _quantize(x, recipe_kind, fmt, delayed: DelayedScaling | None):
         amax = torch.empty(1, dtype=torch.float32, device=x.device)
         scale = torch.empty(1, dtype=torch.float32, device=x.device)
         scale_inv = torch.empty(1, dtype=torch.float32, device=x.device)
-        fp8_amax(x, amax)
+        (fp8_amax_f32 if x.dtype == torch.float32 else fp8_amax)(x, amax)
         fp8_compute_scale(amax, fmt, scale, scale_inv)
         return cast_transpose(x, Recipe.TENSOR, fmt, scale)
     return cast_transpose(x, recipe_kind, fmt)
@@ -124,39 +130,41 @@ class _FP8LinearFn(torch.autograd.Function):
     def forward(ctx, x2d, weight, recipe, states):
         kx, kw = _kinds(recipe)
         fx, fdy = recipe.fwd_format, recipe.bwd_format
-        # the BF16 copy of the (FP32) master weight is quantized; its gradient goes to the
-        # master weight in FP32, as the wgrad GEMM produces it
-        w16 = weight.detach().to(torch.bfloat16).contiguous()
+        # the master weight (FP32) is quantized as it is; its gradient goes to it in FP32,
+        # as the wgrad GEMM produces it
         qx, sx, qxt, sxt = _quantize(x2d, kx, fx, states.get("x"))
-        qw, sw, qwt, swt = _quantize(w16, kw, fx, states.get("w"))
-        y = torch.empty((x2d.shape[0], weight.shape[0]), dtype=torch.bfloat16, device=x2d.device)
-        fp8_scaled_gemm(qx, fx, kx, sx, qw, fx, kw, sw, y, OutDtype.BF16)
+        qw, sw, qwt, swt = _quantize(weight.detach().contiguous(), kw, fx, states.get("w"))
+        out = OutDtype.FP32 if x2d.dtype == torch.float32 else OutDtype.BF16
+        y = torch.empty((x2d.shape[0], weight.shape[0]), dtype=x2d.dtype, device=x2d.device)
+        fp8_scaled_gemm(qx, fx, kx, sx, qw, fx, kw, sw, y, out)
         ctx.save_for_backward(qxt, sxt, qwt, swt)
-        ctx.meta = (kx, kw, fx, fdy, states.get("dy"))
+        ctx.meta = (kx, kw, fx, fdy, states.get("dy"), x2d.dtype, weight.dtype)
         return y
 
     @staticmethod
     def backward(ctx, dy):
         qxt, sxt, qwt, swt = ctx.saved_tensors
-        kx, kw, fx, fdy, st_dy = ctx.meta
-        dy = dy.contiguous().to(torch.bfloat16)
-        qdy, sdy, qdyt, sdyt = _quantize(dy, kx, fdy, st_dy)
+        kx, kw, fx, fdy, st_dy, x_dtype, w_dtype = ctx.meta
+        qdy, sdy, qdyt, sdyt = _quantize(dy.contiguous(), kx, fdy, st_dy)
         M, N = dy.shape
         K = qxt.shape[0]
-        dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device)
+        dx = torch.empty((M, K), dtype=x_dtype, device=dy.device)
         # dgrad: dY [M, N] . (W^T [K, N])^T; the W copy along N is its column-wise copy
-        fp8_scaled_gemm(qdy, fdy, kx, sdy, qwt, fx, kw, swt, dx, OutDtype.BF16)
-        dw = torch.empty((N, K), dtype=torch.float32, device=dy.device)
-        # wgrad: dY^T [N, M] . (X^T [K, M])^T, both column-wise copies (blockwise: 1x128 with 1x128)
-        fp8_scaled_gemm(qdyt, fdy, kx, sdyt, qxt, fx, kx, sxt, dw, OutDtype.FP32)
+        fp8_scaled_gemm(qdy, fdy, kx, sdy, qwt, fx, kw, swt, dx,
+                        OutDtype.FP32 if x_dtype == torch.float32 else OutDtype.BF16)
+        dw = torch.empty((N, K), dtype=w_dtype, device=dy.device)
+        # wgrad: dY^T [N, M] . (X^T [K, M])^T, both column-wise copies (blockwise: 1x128 with 1x128);
+        # FP32 for the FP32 master weight
+        fp8_scaled_gemm(qdyt, fdy, kx, sdyt, qxt, fx, kx, sxt, dw,
+                        OutDtype.FP32 if w_dtype == torch.float32 else OutDtype.BF16)
         return dx, dw, None, None
 
 
 def fp8_linear(x, weight, recipe=None, states=None):
-    """Y = X W^T through the three FP8 GEMMs (x [..., K] bf16, weight [N, K])."""
+    """Y = X W^T through the three FP8 GEMMs (x [..., K] bf16 or float32, weight [N, K] float32)."""
     recipe = recipe if recipe is not None else get_fp8_recipe()
     lead = x.shape[:-1]
-    x2d = x.reshape(-1, x.shape[-1]).to(torch.bfloat16).contiguous()
+    x2d = x.reshape(-1, x.shape[-1]).contiguous()
     y = _FP8LinearFn.apply(x2d, weight, recipe, states or {})
     return y.reshape(*lead, weight.shape[0])
 
@@ -164,8 +172,8 @@ def fp8_linear(x, weight, recipe=None, states=None):
 class FP8Linear(torch.nn.Module):
     """Linear layer (no bias) whose GEMMs run in FP8 under the active recipe.
 
-    The FP32 master weight is cast to BF16 and quantized every step (the guide's
-    "weight dual copy": FP8 weights come from a higher-precision copy).  Under a
+    The FP32 master weight is quantized directly every step (the guide's "weight
+    dual copy": FP8 weights come from a higher-precision copy).  Under a
     Float8DelayedScaling recipe the layer keeps one delayed-scaling state per
     tensor role (X and W in E4M3, dY in the backward format)."""
 

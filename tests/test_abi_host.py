@@ -56,6 +56,20 @@ def test_amax_rejects(lib):
     assert lib.fp8_amax(FAKE + 2, 4, 4, FAKE, None) == ALIGN
 
 
+def test_f32_entry_points_reject(lib):
+    assert lib.fp8_amax_f32(None, 4, 4, FAKE, None) == INVALID       # null x with elements
+    assert lib.fp8_amax_f32(FAKE, 4, 4, None, None) == INVALID       # null amax
+    assert lib.fp8_amax_f32(FAKE + 4, 4, 4, FAKE, None) == ALIGN     # x not 16-byte aligned
+    ct = lib.fp8_cast_transpose_f32
+    T, B1, B128, MXT = 0, 1, 2, 4
+    assert ct(FAKE, 128, 128, T, 0, FAKE, None, None, None, None, None, None) == INVALID    # nothing requested
+    assert ct(FAKE, 128, 128, T, 0, None, None, FAKE, None, None, None, None) == INVALID    # per-tensor scale
+    assert ct(FAKE, 100, 256, B128, 0, None, None, FAKE, FAKE, None, None, None) == SHAPE   # rows % 128
+    assert ct(FAKE, 128, 96, MXT, 0, None, None, FAKE, FAKE, None, None, None) == SHAPE     # cols % 128
+    assert ct(FAKE + 8, 128, 128, B1, 0, None, None, FAKE, FAKE, None, None, None) == ALIGN
+    assert ct(FAKE, 0, 128, B1, 0, None, None, None, None, None, None, None) == OK          # empty: no-op
+
+
 def test_scale_and_history_reject(lib):
     assert lib.fp8_compute_scale(FAKE, 7, FAKE, FAKE, None) == INVALID    # bad format
     assert lib.fp8_compute_scale(None, 0, FAKE, FAKE, None) == INVALID
