@@ -31,6 +31,9 @@ import numpy as np
 
 E4M3, E5M2 = 0, 1
 KIND_TENSOR, KIND_1x128, KIND_128x128, KIND_MX = 0, 1, 2, 3
+# MXFP8 with the floor-rule exponent (the documented alternate); its E8M0 scales are
+# read like KIND_MX's everywhere else (dequantize, GEMM)
+KIND_MX_FLOOR = 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fp8_oracle.c")
@@ -83,6 +86,9 @@ def _load():
             "orc_tensor_scale": (None, [F, ctypes.c_int, P, P]),
             "orc_history_step": (None, [P, I32, P, F, ctypes.c_int, P, P]),
             "orc_mx_exponent": (ctypes.c_int, [F, ctypes.c_int]),
+            "orc_mx_exponent_floor": (ctypes.c_int, [F, ctypes.c_int]),
+            "orc_quantize_mx_floor": (None, [P, I64, I64, ctypes.c_int, P, P]),
+            "orc_quantize_mx_floor_f32": (None, [P, I64, I64, ctypes.c_int, P, P]),
             "orc_quantize_tensor": (None, [P, I64, I64, ctypes.c_int, F, P]),
             "orc_quantize_1x128": (None, [P, I64, I64, ctypes.c_int, P, P]),
             "orc_quantize_128x128": (None, [P, I64, I64, ctypes.c_int, P, P]),
@@ -185,6 +191,11 @@ def mx_exponent(amax_value, fmt: int) -> int:
     return int(_load().orc_mx_exponent(ctypes.c_float(float(np.float32(amax_value))), fmt))
 
 
+def mx_exponent_floor(amax_value, fmt: int) -> int:
+    """The floor-rule MX exponent (fp8_oracle.c: orc_mx_exponent_floor)."""
+    return int(_load().orc_mx_exponent_floor(ctypes.c_float(float(np.float32(amax_value))), fmt))
+
+
 # ----------------------------------------------------------------- quantize
 def transpose_bf16(x_bf16) -> np.ndarray:
     x = _bf16_bits(x_bf16)
@@ -219,6 +230,9 @@ def quantize_rowwise(x_bf16, kind: int, fmt: int, scale=None):
     elif kind == KIND_MX:
         s = np.empty((R, C // 32), np.uint8)
         lib.orc_quantize_mx(_ptr(x), R, C, fmt, _ptr(q), _ptr(s))
+    elif kind == KIND_MX_FLOOR:
+        s = np.empty((R, C // 32), np.uint8)
+        lib.orc_quantize_mx_floor(_ptr(x), R, C, fmt, _ptr(q), _ptr(s))
     else:
         raise ValueError(kind)
     return q, s
@@ -265,6 +279,9 @@ def quantize_rowwise_f32(x_f32, kind: int, fmt: int, scale=None):
     elif kind == KIND_MX:
         s = np.empty((R, C // 32), np.uint8)
         lib.orc_quantize_mx_f32(_ptr(x), R, C, fmt, _ptr(q), _ptr(s))
+    elif kind == KIND_MX_FLOOR:
+        s = np.empty((R, C // 32), np.uint8)
+        lib.orc_quantize_mx_floor_f32(_ptr(x), R, C, fmt, _ptr(q), _ptr(s))
     else:
         raise ValueError(kind)
     return q, s
@@ -304,7 +321,7 @@ def mx_from_tiled(tiled: np.ndarray, rows: int, cols: int) -> np.ndarray:
 def dequantize(q, kind: int, fmt: int, s) -> np.ndarray:
     q = np.ascontiguousarray(q, dtype=np.uint8)
     R, C = q.shape
-    s = np.ascontiguousarray(s, dtype=np.uint8 if kind == KIND_MX else np.float32)
+    s = np.ascontiguousarray(s, dtype=np.uint8 if kind in (KIND_MX, KIND_MX_FLOOR) else np.float32)
     out = np.empty((R, C), np.float64)
     _load().orc_dequantize(_ptr(q), R, C, fmt, kind, _ptr(s), _ptr(out))
     return out
@@ -321,7 +338,7 @@ def dequantize_bf16(q, kind: int, fmt: int, s) -> np.ndarray:
     """FP8 codes + multipliers -> bfloat16 bit patterns: the exact product rounded once."""
     q = np.ascontiguousarray(q, dtype=np.uint8)
     R, C = q.shape
-    s = np.ascontiguousarray(s, dtype=np.uint8 if kind == KIND_MX else np.float32)
+    s = np.ascontiguousarray(s, dtype=np.uint8 if kind in (KIND_MX, KIND_MX_FLOOR) else np.float32)
     out = np.empty((R, C), np.uint16)
     _load().orc_dequantize_bf16(_ptr(q), R, C, fmt, kind, _ptr(s), _ptr(out))
     return out
@@ -354,7 +371,7 @@ def scaled_gemm_rows(qa, fa, ka, sa, qb, fb, kb, sb, rows) -> np.ndarray:
     """
     rows = np.asarray(rows, dtype=np.int64)
     qa = np.ascontiguousarray(qa)[rows]
-    if ka == KIND_1x128 or ka == KIND_MX:
+    if ka in (KIND_1x128, KIND_MX, KIND_MX_FLOOR):
         sa = np.ascontiguousarray(sa)[rows]
     elif ka == KIND_128x128:
         raise ValueError("row sampling of a 128x128-scaled A is not supported")

@@ -228,6 +228,23 @@ int orc_mx_exponent(float amax, int fmt)
     return 127;
 }
 
+/*
+ * MX block exponent, floor convention -- the documented alternate (the ceil rule above
+ * is the default).  e = floor(log2 amax) - emax, with emax the exponent of the format's
+ * largest power of two (8 for E4M3: 256; 15 for E5M2: 32768), so the block maximum
+ * scales into [2^emax, 2^(emax + 1)) and the part of the block above FMAX saturates.
+ * Taken as the largest e in [-127, 127] with 2^(e + emax) <= amax, by direct search
+ * (each comparison exact in double); amax == 0 or non-finite gives e = 0.
+ */
+int orc_mx_exponent_floor(float amax, int fmt)
+{
+    if (!(amax > 0.0f) || isinf(amax)) return 0;
+    int emax = fmt == ORC_E4M3 ? 8 : 15;
+    for (int e = 127; e >= -127; --e)
+        if (ldexp(1.0, e + emax) <= (double)amax) return e;
+    return -127;
+}
+
 /* 2^-e as a binary32 (exact for e in [-127, 127]; 2^-127 is subnormal). */
 static float pow2_neg(int e) { return (float)ldexp(1.0, -e); }
 
@@ -369,6 +386,35 @@ void orc_quantize_mx_f32(const float* x, int64_t R, int64_t C, int fmt, uint8_t*
         for (int64_t b = 0; b < nb; ++b) {
             const float* blk = x + r * C + b * 32;
             int e = orc_mx_exponent(orc_amax_f32(blk, 32), fmt);
+            float scale = pow2_neg(e);
+            for (int64_t j = 0; j < 32; ++j) q[r * C + b * 32 + j] = quantize_one_f32(blk[j], scale, fmt);
+            s_e8m0[r * nb + b] = (uint8_t)(e + 127);
+        }
+    }
+}
+
+/* MXFP8 quantize with the floor-rule exponent (bf16 and binary32 inputs). */
+void orc_quantize_mx_floor(const uint16_t* x, int64_t R, int64_t C, int fmt, uint8_t* q, uint8_t* s_e8m0)
+{
+    int64_t nb = C / 32;
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint16_t* blk = x + r * C + b * 32;
+            int e = orc_mx_exponent_floor(orc_amax_bf16(blk, 32), fmt);
+            float scale = pow2_neg(e);
+            for (int64_t j = 0; j < 32; ++j) q[r * C + b * 32 + j] = quantize_one(blk[j], scale, fmt);
+            s_e8m0[r * nb + b] = (uint8_t)(e + 127);
+        }
+    }
+}
+
+void orc_quantize_mx_floor_f32(const float* x, int64_t R, int64_t C, int fmt, uint8_t* q, uint8_t* s_e8m0)
+{
+    int64_t nb = C / 32;
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const float* blk = x + r * C + b * 32;
+            int e = orc_mx_exponent_floor(orc_amax_f32(blk, 32), fmt);
             float scale = pow2_neg(e);
             for (int64_t j = 0; j < 32; ++j) q[r * C + b * 32 + j] = quantize_one_f32(blk[j], scale, fmt);
             s_e8m0[r * nb + b] = (uint8_t)(e + 127);

@@ -28,8 +28,8 @@ MUTANTS = {
     "history_window_one_slot": ("for (int32_t i = 0; i < len; ++i)\n        if (hist[i] > m)",
                                 "for (int32_t i = 0; i < 1; ++i)\n        if (hist[i] > m)"),
     "mx_exponent_strict": ("if ((double)amax <= ldexp(fmax, e)) return e;", "if ((double)amax < ldexp(fmax, e)) return e;"),
-    "mx_scale_sign": ("orc_amax_bf16(blk, 32), fmt);\n            float scale = pow2_neg(e);",
-                      "orc_amax_bf16(blk, 32), fmt);\n            float scale = pow2_neg(-e);"),
+    "mx_scale_sign": ("orc_mx_exponent(orc_amax_bf16(blk, 32), fmt);\n            float scale = pow2_neg(e);",
+                      "orc_mx_exponent(orc_amax_bf16(blk, 32), fmt);\n            float scale = pow2_neg(-e);"),
     "tile128_first_row_only": ("for (int64_t i = 0; i < 128; ++i) {\n                float a = orc_amax_bf16(",
                                "for (int64_t i = 0; i < 1; ++i) {\n                float a = orc_amax_bf16("),
     # binary32-input quantizers
@@ -38,8 +38,11 @@ MUTANTS = {
     "f32_tile128_first_row_only": ("for (int64_t i = 0; i < 128; ++i) {\n                float a = orc_amax_f32(",
                                    "for (int64_t i = 0; i < 1; ++i) {\n                float a = orc_amax_f32("),
     "f32_1x128_block_stride": ("const float* blk = x + r * C + b * 128;", "const float* blk = x + r * C + b * 127;"),
-    "f32_mx_scale_sign": ("orc_amax_f32(blk, 32), fmt);\n            float scale = pow2_neg(e);",
-                          "orc_amax_f32(blk, 32), fmt);\n            float scale = pow2_neg(-e);"),
+    "f32_mx_scale_sign": ("orc_mx_exponent(orc_amax_f32(blk, 32), fmt);\n            float scale = pow2_neg(e);",
+                          "orc_mx_exponent(orc_amax_f32(blk, 32), fmt);\n            float scale = pow2_neg(-e);"),
+    # floor-rule MX exponent
+    "mx_floor_strict": ("if (ldexp(1.0, e + emax) <= (double)amax) return e;", "if (ldexp(1.0, e + emax) < (double)amax) return e;"),
+    "mx_floor_emax": ("int emax = fmt == ORC_E4M3 ? 8 : 15;", "int emax = fmt == ORC_E4M3 ? 9 : 15;"),
     "f32_transpose_index": ("for (int64_t c = 0; c < C; ++c) xt[c * R + r] = x[r * C + c];\n}\n\n/* Plain transpose of a row-major [R, C] bf16",
                             "for (int64_t c = 0; c < C; ++c) xt[c * R + r] = x[c * R + r];\n}\n\n/* Plain transpose of a row-major [R, C] bf16"),
     "dequant_1x128_index": ("case 1: m = (double)sf[r * (C / 128) + c / 128]; break;",
@@ -70,6 +73,7 @@ def test_pins_reject_mutant(name, tmp_path):
                           os.path.join(ROOT, "tests", "test_oracle_formats.py"),
                           os.path.join(ROOT, "tests", "test_oracle_dequant.py"),
                           os.path.join(ROOT, "tests", "test_oracle_allreduce.py"),
-                          os.path.join(ROOT, "tests", "test_oracle_f32.py")],
+                          os.path.join(ROOT, "tests", "test_oracle_f32.py"),
+                          os.path.join(ROOT, "tests", "test_oracle_mx_floor.py")],
                          capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
     assert out.returncode != 0, f"the pins did not catch mutant {name}"
