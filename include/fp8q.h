@@ -66,7 +66,14 @@ typedef enum {
   FP8_BLOCK_1x128 = 1,   /* one FP32 scale per 128 consecutive elements of a row */
   FP8_BLOCK_128x128 = 2, /* one FP32 scale per 128x128 tile */
   FP8_MX_1x32 = 3,       /* one E8M0 byte per 32 consecutive elements of a row, row-major */
-  FP8_MX_1x32_TILED = 4  /* the same exponents in the GEMM-ready tiled layout (below) */
+  FP8_MX_1x32_TILED = 4, /* the same exponents in the GEMM-ready tiled layout (below) */
+  /* MXFP8 with the floor-rule exponent, the documented alternate of the default ceil
+   * rule: e = floor(log2 amax) - emax (emax 8 for E4M3, 15 for E5M2), so a block's
+   * largest elements may saturate to +-FMAX.  Same layouts as FP8_MX_1x32 and
+   * FP8_MX_1x32_TILED; everything that reads E8M0 scales (GEMM, dequantize) takes them
+   * like the default MX recipes. */
+  FP8_MX_1x32_FLOOR = 5,
+  FP8_MX_1x32_FLOOR_TILED = 6
 } fp8_recipe;
 
 typedef enum { FP8_OUT_BF16 = 0, FP8_OUT_FP32 = 1 } fp8_out_dtype;

@@ -58,6 +58,8 @@ class Recipe(enum.IntEnum):
     BLOCK_128x128 = 2
     MX_1x32 = 3
     MX_1x32_TILED = 4
+    MX_1x32_FLOOR = 5          # floor-rule exponent (the alternate); layouts as MX_1x32 / MX_1x32_TILED
+    MX_1x32_FLOOR_TILED = 6
 
 
 class OutDtype(enum.IntEnum):
@@ -290,7 +292,7 @@ def scale_shape(recipe, rows: int, cols: int):
         return (rows, cols // 128), torch.float32
     if recipe == Recipe.BLOCK_128x128:
         return (rows // 128, cols // 128), torch.float32
-    if recipe == Recipe.MX_1x32:
+    if recipe in (Recipe.MX_1x32, Recipe.MX_1x32_FLOOR):
         return (rows, cols // 32), torch.uint8
     return ((rows + 127) // 128, (cols + 127) // 128, 512), torch.uint8
 

@@ -75,6 +75,12 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t elem, const void*
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool valid_recipe(fp8_recipe r) { return r >= FP8_TENSOR && r <= FP8_MX_1x32_FLOOR_TILED; }
+bool is_mx(fp8_recipe r) {
+  return r == FP8_MX_1x32 || r == FP8_MX_1x32_TILED || r == FP8_MX_1x32_FLOOR || r == FP8_MX_1x32_FLOOR_TILED;
+}
+bool is_mx_tiled(fp8_recipe r) { return r == FP8_MX_1x32_TILED || r == FP8_MX_1x32_FLOOR_TILED; }
+bool is_mx_floor(fp8_recipe r) { return r == FP8_MX_1x32_FLOOR || r == FP8_MX_1x32_FLOOR_TILED; }
 bool valid_fmt(fp8_format f) { return f == FP8_E4M3 || f == FP8_E5M2; }
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;   // TMA coordinates are signed 32-bit
 
@@ -129,8 +135,7 @@ fp8_status plan_cast(const void* x, int64_t rows, int64_t cols, fp8_recipe recip
                      float* amax_out, uint8_t* q_row, void* s_row, uint8_t* q_col, void* s_col, CastPlan* plan,
                      bool f32 = false) {
   plan->f32 = f32;
-  if (rows < 0 || cols < 0 || !valid_fmt(fmt) || recipe < FP8_TENSOR || recipe > FP8_MX_1x32_TILED)
-    return FP8_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || !valid_fmt(fmt) || !valid_recipe(recipe)) return FP8_ERR_INVALID_ARG;
   if (rows * cols == 0) {
     if (!aligned(amax_out, 4)) return FP8_ERR_ALIGNMENT;
     plan->empty = true;
@@ -139,7 +144,7 @@ fp8_status plan_cast(const void* x, int64_t rows, int64_t cols, fp8_recipe recip
   const bool do_row = q_row != nullptr, do_col = q_col != nullptr;
   if (!do_row && !do_col) return FP8_ERR_INVALID_ARG;
   if (x == nullptr) return FP8_ERR_INVALID_ARG;
-  const bool mx = recipe == FP8_MX_1x32 || recipe == FP8_MX_1x32_TILED;
+  const bool mx = is_mx(recipe);
   if (recipe == FP8_TENSOR) {
     if (scale == nullptr) return FP8_ERR_INVALID_ARG;
   } else {
@@ -154,9 +159,11 @@ fp8_status plan_cast(const void* x, int64_t rows, int64_t cols, fp8_recipe recip
       if (rows % 128 || cols % 128) return FP8_ERR_SHAPE;
       break;
     case FP8_MX_1x32:
+    case FP8_MX_1x32_FLOOR:
       if ((do_row && cols % 32) || (do_col && rows % 32)) return FP8_ERR_SHAPE;
       break;
     case FP8_MX_1x32_TILED:
+    case FP8_MX_1x32_FLOOR_TILED:
       if (rows % 128 || cols % 128) return FP8_ERR_SHAPE;
       break;
     default:
@@ -165,7 +172,7 @@ fp8_status plan_cast(const void* x, int64_t rows, int64_t cols, fp8_recipe recip
   if (rows > kMaxDim || cols > kMaxDim) return FP8_ERR_SHAPE;
   if (!aligned(x, 16) || !aligned(q_row, 16) || !aligned(q_col, 16)) return FP8_ERR_ALIGNMENT;
   if (!mx && (!aligned(s_row, 4) || !aligned(s_col, 4))) return FP8_ERR_ALIGNMENT;
-  if (recipe == FP8_MX_1x32_TILED && (!aligned(s_row, 16) || !aligned(s_col, 16))) return FP8_ERR_ALIGNMENT;
+  if (is_mx_tiled(recipe) && (!aligned(s_row, 16) || !aligned(s_col, 16))) return FP8_ERR_ALIGNMENT;
   if (!aligned(scale, 4) || !aligned(amax_out, 4)) return FP8_ERR_ALIGNMENT;
 
   CastParams& p = plan->p;
@@ -173,7 +180,8 @@ fp8_status plan_cast(const void* x, int64_t rows, int64_t cols, fp8_recipe recip
   p.C = cols;
   p.recipe = mx ? kMx : static_cast<int>(recipe);
   p.e5m2 = fmt == FP8_E5M2;
-  p.mx_tiled = recipe == FP8_MX_1x32_TILED;
+  p.mx_tiled = is_mx_tiled(recipe);
+  p.mx_floor = is_mx_floor(recipe);
   p.do_row = do_row;
   p.do_col = do_col;
   p.scale = scale;
@@ -222,9 +230,9 @@ fp8_status scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const voi
   } else if (ra == FP8_BLOCK_1x128 && rb == FP8_BLOCK_1x128) {
     kind = kBlock1x128;
     b_1x128 = 1;
-  } else if (ra == FP8_MX_1x32_TILED && rb == FP8_MX_1x32_TILED) {
-    kind = kMx;
-  } else if ((ra >= FP8_TENSOR && ra <= FP8_MX_1x32_TILED) && (rb >= FP8_TENSOR && rb <= FP8_MX_1x32_TILED)) {
+  } else if (is_mx_tiled(ra) && is_mx_tiled(rb)) {
+    kind = kMx;   // either exponent rule: the tensor core reads E8M0 bytes either way
+  } else if (valid_recipe(ra) && valid_recipe(rb)) {
     return FP8_ERR_UNSUPPORTED;
   } else {
     return FP8_ERR_INVALID_ARG;
@@ -464,8 +472,7 @@ fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, fp8_recipe re
 fp8_status fp8_dequantize(const uint8_t* q, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_format fmt,
                           const void* s, void* y, cudaStream_t stream) {
   ApiRange nvtx_range("fp8_dequantize");
-  if (rows < 0 || cols < 0 || !valid_fmt(fmt) || recipe < FP8_TENSOR || recipe > FP8_MX_1x32_TILED)
-    return FP8_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || !valid_fmt(fmt) || !valid_recipe(recipe)) return FP8_ERR_INVALID_ARG;
   if (rows == 0 || cols == 0) return FP8_OK;
   if (q == nullptr || s == nullptr || y == nullptr) return FP8_ERR_INVALID_ARG;
   if (rows > kMaxDim || cols > kMaxDim) return FP8_ERR_SHAPE;
@@ -475,22 +482,24 @@ fp8_status fp8_dequantize(const uint8_t* q, int64_t rows, int64_t cols, fp8_reci
       break;
     case FP8_BLOCK_128x128:
     case FP8_MX_1x32_TILED:
+    case FP8_MX_1x32_FLOOR_TILED:
       if (rows % 128 || cols % 128) return FP8_ERR_SHAPE;
       break;
     case FP8_MX_1x32:
+    case FP8_MX_1x32_FLOOR:
       if (cols % 32) return FP8_ERR_SHAPE;
       break;
     default:
       break;
   }
   if (!aligned(q, 16) || !aligned(y, 16)) return FP8_ERR_ALIGNMENT;
-  const bool mx = recipe == FP8_MX_1x32 || recipe == FP8_MX_1x32_TILED;
+  const bool mx = is_mx(recipe);
   if (!mx && !aligned(s, 4)) return FP8_ERR_ALIGNMENT;
   DeviceInfo* d;
   if (fp8_status st = device_info(&d)) return st;
   const int kind = recipe == FP8_TENSOR ? kTensor : recipe == FP8_BLOCK_1x128 ? kBlock1x128
                    : recipe == FP8_BLOCK_128x128 ? kBlock128x128 : kMx;
-  return cuda_status(launch_dequantize(q, rows, cols, kind, recipe == FP8_MX_1x32_TILED, fmt == FP8_E5M2, s, y,
+  return cuda_status(launch_dequantize(q, rows, cols, kind, is_mx_tiled(recipe), fmt == FP8_E5M2, s, y,
                                        d->num_sms, stream));
 }
 

@@ -73,6 +73,7 @@ struct CastParams {
   int recipe;
   int e5m2;
   int mx_tiled;          // MX scales in the GEMM-ready tiled layout
+  int mx_floor;          // MX exponent by the floor rule (else the ceil rule)
   int do_row, do_col;
   const float* scale;    // per-tensor scale (device)
   float* amax_out;       // optional (device, pre-zeroed)

@@ -200,7 +200,7 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
     } else if (RECIPE == kMx) {
       // the 32-column block of lane j is lanes 4 (j/4) .. +3; row i = j % 4 ends up in lane 4 (j/4) + i
       const float m = reduce_scatter4(a, lane, 2, 1);
-      const int e = mx_exponent(m, fexp);
+      const int e = (p.mx_floor ? mx_exponent_floor(m, fexp) : mx_exponent(m, fexp));
       const float mine = pow2_neg(e);
       const int64_t grow = row0 + (j & 3) * 32 + warp * 2 + (lane >> 4);
       const int64_t b = tc * 4 + (j >> 2);
@@ -246,7 +246,7 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
       for (int t = 0; t < 4; ++t) at[t] = pair_abs_f32(xabs_max(xabs_max(d[t][0], d[t][1]), xabs_max(d[t][2], d[t][3])));
       // block t = lane % 4 of this column ends up in this lane
       const float m = reduce_scatter4(at, lane, 2, 1);
-      const int e = mx_exponent(m, fexp);
+      const int e = (p.mx_floor ? mx_exponent_floor(m, fexp) : mx_exponent(m, fexp));
       const float mine = pow2_neg(e);
       const int64_t b = static_cast<int64_t>(tr) * 4 + (lane & 3);
       if (gcol < p.C && b < nb32_r) {

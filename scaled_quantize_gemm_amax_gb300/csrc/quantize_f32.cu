@@ -142,7 +142,7 @@ __device__ __forceinline__ void cast_tile_f32(const CastParams& p, uint32_t xs, 
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-        const int e = mx_exponent(m, fexp);
+        const int e = (p.mx_floor ? mx_exponent_floor(m, fexp) : mx_exponent(m, fexp));
         s = pow2_neg(e);
         const int64_t b = static_cast<int64_t>(tc) * 4 + (lane >> 3);
         if ((lane & 7) == 0 && grow < p.R && b < nb32_c) {   // a tile hanging over C has blocks past the last one
@@ -173,7 +173,7 @@ __device__ __forceinline__ void cast_tile_f32(const CastParams& p, uint32_t xs, 
       s = scale_from_amax(m, fmax);
       if (rq == 0 && gcol < p.C) static_cast<float*>(p.s_col)[gcol * nb128_r + tr] = recip_rn(s);
     } else if (RECIPE == kMx) {
-      const int e = mx_exponent(am, fexp);
+      const int e = (p.mx_floor ? mx_exponent_floor(am, fexp) : mx_exponent(am, fexp));
       s = pow2_neg(e);
       const int64_t b = static_cast<int64_t>(tr) * 4 + rq;
       if (gcol < p.C && b < nb32_r) {

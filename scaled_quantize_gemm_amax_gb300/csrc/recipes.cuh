@@ -8,6 +8,7 @@
 // MXFP8 (guide, "MXFP8 scaling": 1x32 blocks, E8M0 power-of-two scale):
 //   e = smallest integer with amax <= FMAX * 2^e, clamped to [-127, 127],
 //   amax == 0 or non-finite -> 0; elements are multiplied by 2^-e; byte = e + 127.
+//   (Alternate, its own recipe: e = floor(log2 amax) - floor(log2 FMAX).)
 // The cast is round-to-nearest-even with saturation to +-FMAX.
 #pragma once
 #include <cfloat>
@@ -49,6 +50,19 @@ __device__ __forceinline__ int mx_exponent(float amax, int fmax_exp) {
     E = static_cast<int>(ef) - 127;
   }
   int e = E - fmax_exp + (m > 0xE00000u ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// The floor convention (the alternate behind FP8_MX_1x32_FLOOR*): e = floor(log2 amax)
+// - fmax_exp, the unbiased binary exponent of amax less the format's largest power-of-two
+// exponent, so the block maximum scales into [2^fmax_exp, 2^(fmax_exp + 1)) and what lies
+// above FMAX saturates; amax == 0 or non-finite -> 0; clamped to [-127, 127].
+__device__ __forceinline__ int mx_exponent_floor(float amax, int fmax_exp) {
+  const uint32_t b = __float_as_uint(amax) & 0x7FFFFFFFu;
+  const uint32_t ef = b >> 23, mf = b & 0x7FFFFFu;
+  if (b == 0 || ef == 0xFFu) return 0;
+  const int E = ef == 0 ? -126 - (__clz(mf) - 8) : static_cast<int>(ef) - 127;
+  const int e = E - fmax_exp;
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 

@@ -10,7 +10,10 @@ R = fq.Recipe
 F = fq.Format
 
 KIND = {R.TENSOR: oracle.KIND_TENSOR, R.BLOCK_1x128: oracle.KIND_1x128, R.BLOCK_128x128: oracle.KIND_128x128,
-        R.MX_1x32: oracle.KIND_MX, R.MX_1x32_TILED: oracle.KIND_MX}
+        R.MX_1x32: oracle.KIND_MX, R.MX_1x32_TILED: oracle.KIND_MX, R.MX_1x32_FLOOR: oracle.KIND_MX_FLOOR,
+        R.MX_1x32_FLOOR_TILED: oracle.KIND_MX_FLOOR}
+MX_RECIPES = (R.MX_1x32, R.MX_1x32_TILED, R.MX_1x32_FLOOR, R.MX_1x32_FLOOR_TILED)
+MX_TILED = (R.MX_1x32_TILED, R.MX_1x32_FLOOR_TILED)
 
 
 def require_gpu():
@@ -49,7 +52,7 @@ def assert_status_ok():
 
 def oracle_scales_like(recipe, s_ref, rows, cols):
     """Oracle multipliers in the layout the GPU writes (MX tiled: permuted)."""
-    if recipe == R.MX_1x32_TILED:
+    if recipe in MX_TILED:
         return oracle.mx_to_tiled(s_ref).reshape(((rows + 127) // 128, (cols + 127) // 128, 512))
     return s_ref
 
@@ -85,7 +88,7 @@ def check_cast(x: torch.Tensor, recipe, fmt, row=True, col=True, scale_np=None):
 
 
 def _check_scales(recipe, got, ref, what):
-    if recipe in (R.MX_1x32, R.MX_1x32_TILED):
+    if recipe in MX_RECIPES:
         assert_bytes_equal(got, ref, what)
     else:
         assert_bytes_equal(f32bits(got), f32bits(ref), what)

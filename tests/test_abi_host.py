@@ -70,6 +70,21 @@ def test_f32_entry_points_reject(lib):
     assert ct(FAKE, 0, 128, B1, 0, None, None, None, None, None, None, None) == OK          # empty: no-op
 
 
+def test_floor_rule_mx_recipes_are_checked_like_mx(lib):
+    ct = lib.fp8_cast_transpose
+    MXF, MXFT = 5, 6
+    assert ct(FAKE, 128, 96, MXF, 0, None, None, FAKE, FAKE, None, None, None) != SHAPE      # 96 % 32 == 0
+    assert ct(FAKE, 128, 100, MXF, 0, None, None, FAKE, FAKE, None, None, None) == SHAPE     # cols % 32
+    assert ct(FAKE, 128, 96, MXFT, 0, None, None, FAKE, FAKE, None, None, None) == SHAPE     # tiled: cols % 128
+    assert ct(FAKE, 128, 128, 7, 0, None, None, FAKE, FAKE, None, None, None) == INVALID     # no recipe 7
+    g = lib.fp8_scaled_gemm
+    # empty GEMMs return on the host: the pairing checks come first
+    assert g(FAKE, 0, 4, FAKE, FAKE, 0, MXFT, FAKE, 0, 0, 0, FAKE, 0, None) == OK             # MX x MX-floor
+    assert g(FAKE, 0, MXFT, FAKE, FAKE, 0, MXFT, FAKE, 0, 0, 0, FAKE, 0, None) == OK
+    assert g(FAKE, 0, MXF, FAKE, FAKE, 0, MXFT, FAKE, 0, 0, 0, FAKE, 0, None) == UNSUP       # row-major scales
+    assert lib.fp8_dequantize(FAKE, 128, 100, MXF, 0, FAKE, FAKE, None) == SHAPE
+
+
 def test_scale_and_history_reject(lib):
     assert lib.fp8_compute_scale(FAKE, 7, FAKE, FAKE, None) == INVALID    # bad format
     assert lib.fp8_compute_scale(None, 0, FAKE, FAKE, None) == INVALID

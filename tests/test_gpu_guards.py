@@ -11,7 +11,7 @@ import torch
 import oracle
 import scaled_quantize_gemm_amax_gb300 as fq
 from scaled_quantize_gemm_amax_gb300 import workloads as wl
-from gpu_util import (R, F, KIND, Guarded, assert_bytes_equal, assert_status_ok, bits16, f32bits, host,
+from gpu_util import (R, F, KIND, MX_RECIPES, Guarded, assert_bytes_equal, assert_status_ok, bits16, f32bits, host,
                       oracle_scales_like, require_gpu)
 
 pytestmark = pytest.mark.gpu
@@ -23,7 +23,7 @@ def _gpu():
 
 
 def _scales_check(recipe, got, ref, what):
-    if recipe in (R.MX_1x32, R.MX_1x32_TILED):
+    if recipe in MX_RECIPES:
         assert_bytes_equal(got, ref, what)
     else:
         assert_bytes_equal(f32bits(got), f32bits(ref), what)

@@ -9,8 +9,8 @@ import torch
 
 import oracle
 import scaled_quantize_gemm_amax_gb300 as fq
-from gpu_util import (R, F, KIND, Guarded, assert_bytes_equal, assert_status_ok, f32bits, host, oracle_scales_like,
-                      require_gpu)
+from gpu_util import (R, F, KIND, MX_RECIPES, Guarded, assert_bytes_equal, assert_status_ok, f32bits, host,
+                      oracle_scales_like, require_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +33,7 @@ def f32_input(shape, seed, sigma=1.0, outliers=True):
 
 
 def _check_scales(recipe, got, ref, what):
-    if recipe in (R.MX_1x32, R.MX_1x32_TILED):
+    if recipe in MX_RECIPES:
         assert_bytes_equal(got, ref, what)
     else:
         assert_bytes_equal(f32bits(got), f32bits(ref), what)
