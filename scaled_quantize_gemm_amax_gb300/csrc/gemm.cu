@@ -67,9 +67,10 @@ struct Cfg<kBlockK2> {
   static constexpr int BN = 128, STAGES = 3, ACC = 4, EPI = 8, KSUB = 2, CTRL = 4;
 };
 // The same with per-row B scales (1x128 x 1x128): each output column has its own factor
-// sB[n, kb].  The epilogue copies the tile's B scales into a shared table at each tile
-// start (per half of the tile's columns, [kb][64] floats, K / 128 <= kMaxTableKb) and
-// reads a k-block's 64 factors as broadcast 16-byte loads.
+// sB[n, kb].  The epilogue copies the tile's B scales into a shared table (per half of the
+// tile's columns, [kb][64] floats, K / 128 <= kMaxTableKb; two buffers, the next tile's
+// fetched a tile ahead, when K / 128 <= kMaxTableKb / 2) and reads a k-block's 64 factors
+// as broadcast 16-byte loads.
 constexpr int kBlockK2RowsB = 6;
 constexpr int kMaxTableKb = 64;
 template <>
@@ -134,7 +135,7 @@ struct Layout {
   static constexpr uint32_t OFF_TMEM = OFF_SFR + 8 * S, OFF_ABORT = OFF_TMEM + 4;
   // B-scale table barriers: tbl_full[2] (the half's table is filled), tbl_free[2] (read)
   static constexpr uint32_t OFF_TBAR = (OFF_ABORT + 4 + 7) & ~7u;
-  static constexpr uint32_t SMEM = OFF_TBAR + 32 + 64 + 1024;   // + alignment slack
+  static constexpr uint32_t SMEM = OFF_TBAR + 64 + 32 + 1024;   // + alignment slack
   // bytes one stage's full barrier expects (in a pair: the leader's barrier sees both CTAs' loads)
   static constexpr uint32_t TX_BYTES = PAIR ? 2 * (STAGE_BYTES + SF_BYTES) : STAGE_BYTES + SF_BYTES;
 };
@@ -228,9 +229,9 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     }
     mbar_init(base + L::OFF_FINAL, NISS);
     if (TABLE) {
-      for (int hh = 0; hh < 2; ++hh) {
-        mbar_init(base + L::OFF_TBAR + 8 * hh, 4 * 32);     // every lane of the half's four warps
-        mbar_init(base + L::OFF_TBAR + 16 + 8 * hh, 4);     // one arrive per warp
+      for (int hb = 0; hb < 4; ++hb) {   // (half, table buffer)
+        mbar_init(base + L::OFF_TBAR + 8 * hb, 4 * 32);     // filled: every lane's copies of the half's four warps
+        mbar_init(base + L::OFF_TBAR + 32 + 8 * hb, 4);     // read: one arrive per warp
       }
     }
     *abort_flag = 0;
@@ -636,9 +637,10 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         // per-row B scales: this half's table, and the factor of column j at k-block kb:
         // sA[m, kb] * sB[n0 + j, kb] rounded once, then the FMA (as the single-CTA kernel)
         const uint32_t tbl = base + L::OFF_TBL + static_cast<uint32_t>(h) * L::TBL_HALF;
+        uint32_t tbl_cur = tbl;   // the table buffer of this tile
         auto promote64t = [&](const uint32_t (&r)[2][32], float sa, int kb) {
           const uint64_t sa2 = pack_f32x2(sa, sa);
-          const uint32_t trow = tbl + static_cast<uint32_t>(kb) * 256u;
+          const uint32_t trow = tbl_cur + static_cast<uint32_t>(kb) * 256u;
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -652,18 +654,45 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
             }
         };
         if constexpr (TABLE) {
-          // The half's four warps fill its table with this tile's B scales (warp q: its 16
-          // columns, every k-block), once all four have finished reading the previous tile's.
-          const uint32_t tbar_full = base + L::OFF_TBAR + 8 * h, tbar_free = base + L::OFF_TBAR + 16 + 8 * h;
-          if (tile_it > 0 &&
-              !__all_sync(0xFFFFFFFFu, mbar_wait(tbar_free, (tile_it - 1) & 1u, p.err, kErrTimeoutMma, abort_flag)))
+          // The half's four warps fill its table with a tile's B scales (warp q: its 16
+          // columns, every k-block) by asynchronous copies that arrive on the buffer's
+          // "filled" barrier when they land.  With K / 128 <= 32 the table has two buffers and
+          // the next tile's scales are fetched at the start of this one, a whole tile ahead;
+          // otherwise this tile's fill is awaited at its start.  A buffer is refilled once the
+          // half's four warps have finished reading it (its "read" barrier).
+          const int nbuf = KB <= kMaxTableKb / 2 ? 2 : 1;
+          auto tbar_full = [&](uint32_t b) { return base + L::OFF_TBAR + 8 * (2 * h + b); };
+          auto tbar_free = [&](uint32_t b) { return base + L::OFF_TBAR + 32 + 8 * (2 * h + b); };
+          auto fill = [&](int tile, uint32_t b) {
+            int ftm, ftn;
+            tile_coords(tile, tiles_m, tiles_n, ftm, ftn);
+            const int cq = 16 * q + (lane & 15);
+            const float* src = static_cast<const float*>(p.sb) + (static_cast<int64_t>(ftn) * BN + h * COLS + cq) * KB;
+            const uint32_t dst = tbl + b * (L::TBL_HALF / 2);
+            for (int kb = lane >> 4; kb < KB; kb += 2) cp_async_4(dst + static_cast<uint32_t>(kb * 64 + cq) * 4u, src + kb);
+            cp_async_arrive_noinc(tbar_full(b));
+          };
+          bool tok = true;
+          if (nbuf == 2) {
+            if (tile_it == 0) fill(t, 0);
+            const int tnext = t + units;
+            if (tnext < ntiles) {
+              const uint32_t bn = (tile_it + 1) & 1u;
+              if (tile_it >= 1)   // the tile before this one read buffer bn
+                tok = __all_sync(0xFFFFFFFFu, mbar_wait(tbar_free(bn), ((tile_it - 1) >> 1) & 1u, p.err,
+                                                        kErrTimeoutMma, abort_flag));
+              if (tok) fill(tnext, bn);
+            }
+          } else {
+            if (tile_it > 0)
+              tok = __all_sync(0xFFFFFFFFu, mbar_wait(tbar_free(0), (tile_it - 1) & 1u, p.err, kErrTimeoutMma, abort_flag));
+            if (tok) fill(t, 0);
+          }
+          tbl_cur = tbl + (nbuf == 2 ? (tile_it & 1u) * (L::TBL_HALF / 2) : 0u);
+          if (!tok || !__all_sync(0xFFFFFFFFu, mbar_wait(tbar_full(nbuf == 2 ? (tile_it & 1u) : 0u),
+                                                         (nbuf == 2 ? (tile_it >> 1) : tile_it) & 1u, p.err,
+                                                         kErrTimeoutMma, abort_flag)))
             break;
-          const int cq = 16 * q + (lane & 15);
-          const float* src = static_cast<const float*>(p.sb) + (gcol0 + cq) * KB;
-#pragma unroll 4
-          for (int kb = lane >> 4; kb < KB; kb += 2) sts32(tbl + static_cast<uint32_t>(kb * 64 + cq) * 4u, __ldg(src + kb));
-          mbar_arrive(tbar_full);   // every lane: its own stores are released by its arrive
-          if (!__all_sync(0xFFFFFFFFu, mbar_wait(tbar_full, tile_it & 1u, p.err, kErrTimeoutMma, abort_flag))) break;
         }
         // scale factors of the group to promote next (loads in flight)
         float sa0 = sa_row[0], sa1 = sa_row[1];
@@ -715,7 +744,8 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         if (!ok) break;
         if constexpr (TABLE) {
           __syncwarp();   // every lane's table reads of this tile are done
-          if (lane == 0) mbar_arrive(base + L::OFF_TBAR + 16 + 8 * h);
+          const uint32_t b = KB <= kMaxTableKb / 2 ? (tile_it & 1u) : 0u;
+          if (lane == 0) mbar_arrive(base + L::OFF_TBAR + 32 + 8 * (2 * h + b));
           ++tile_it;
         }
         // C through TMA stores of this warp's staged box (as the other kinds)
@@ -862,6 +892,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
       }
     }
     if (L::TSTORE && lane == 0) bulk_wait_all<0>();   // this warp's TMA stores have finished
+    if (TABLE) cp_async_wait_all();                  // no table copy of this thread still in flight
     if (QOUT && want_amax) {
       // one atomic per warp, on the (non-negative) float bits, which order like the values
 #pragma unroll
