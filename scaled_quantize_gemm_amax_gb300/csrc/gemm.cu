@@ -638,21 +638,26 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         // sA[m, kb] * sB[n0 + j, kb] rounded once, then the FMA (as the single-CTA kernel)
         const uint32_t tbl = base + L::OFF_TBL + static_cast<uint32_t>(h) * L::TBL_HALF;
         uint32_t tbl_cur = tbl;   // the table buffer of this tile
-        auto promote64t = [&](const uint32_t (&r)[2][32], float sa, int kb) {
+        // factors of one partial: fpk[16 c + j] = sA * (sB[2 (16 c + j)], sB[2 (16 c + j) + 1]),
+        // each product rounded once (as the single-CTA kernel), from broadcast table loads
+        auto factors64 = [&](uint64_t (&f)[32], float sa, int kb) {
           const uint64_t sa2 = pack_f32x2(sa, sa);
           const uint32_t trow = tbl_cur + static_cast<uint32_t>(kb) * 256u;
 #pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const float4 fb = lds128f(trow + static_cast<uint32_t>(4 * jj) * 4u);
+            f[2 * jj] = mul_f32x2(sa2, pack_f32x2(fb.x, fb.y));
+            f[2 * jj + 1] = mul_f32x2(sa2, pack_f32x2(fb.z, fb.w));
+          }
+        };
+        auto fma64 = [&](const uint32_t (&r)[2][32], const uint64_t (&f)[32]) {
+#pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-              const float4 fb = lds128f(trow + static_cast<uint32_t>(32 * c + 4 * jj) * 4u);
-              const uint64_t f01 = mul_f32x2(sa2, pack_f32x2(fb.x, fb.y));
-              const uint64_t f23 = mul_f32x2(sa2, pack_f32x2(fb.z, fb.w));
-              acc[16 * c + 2 * jj] = fma_f32x2(f01, pack_f32x2(r[c][4 * jj], r[c][4 * jj + 1]), acc[16 * c + 2 * jj]);
-              acc[16 * c + 2 * jj + 1] =
-                  fma_f32x2(f23, pack_f32x2(r[c][4 * jj + 2], r[c][4 * jj + 3]), acc[16 * c + 2 * jj + 1]);
-            }
+            for (int j = 0; j < 16; ++j)
+              acc[16 * c + j] = fma_f32x2(f[16 * c + j], pack_f32x2(r[c][2 * j], r[c][2 * j + 1]), acc[16 * c + j]);
         };
+        uint64_t fpk[32];
         if constexpr (TABLE) {
           // The half's four warps fill its table with a tile's B scales (warp q: its 16
           // columns, every k-block) by asynchronous copies that arrive on the buffer's
@@ -703,6 +708,41 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         }
         bool ok = true;
         for (int kg = 0; kg < NG; ++kg) {
+          if constexpr (TABLE) {
+            // Per-row B scales: a partial's 64 columns each have their own factor
+            // sA[m, kb] * sB[n, kb].  The factors of a partial are formed into registers
+            // (table loads and packed multiplies) while its TMEM load is in flight, so the
+            // FMAs that follow have no load in their chain; the group's second partial is
+            // loaded into the registers of the first once its FMAs are done, and the group
+            // goes back to the MMA issuers when it has landed.  (Holding both partials, as
+            // below, left no registers for the factors: each FMA then waited on its table
+            // load and multiply.)
+            const float a0 = sa0, a1 = sa1;
+            if (kg + 1 < NG) {
+              sa0 = sa_row[2 * kg + 2];
+              sa1 = sa_row[2 * kg + 3];
+            }
+            factors64(fpk, a0, 2 * kg);   // before the wait: needs no MMA result
+            ok = wait_full();
+            if (!ok) break;
+            load64(0, pa);
+            tc_wait_ld(pa[0]);
+            tc_tie(pa[1]);
+            fma64(pa, fpk);
+            load64(1, pa);                // the second partial, into the same registers
+            factors64(fpk, a1, 2 * kg + 1);
+            tc_wait_ld(pa[0]);
+            tc_tie(pa[1]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              const uint32_t next = part_it + GROUPS;
+              if (next < total_groups) release(base + L::OFF_FULL + 8 * (next % S));
+            }
+            ++part_it;
+            fma64(pa, fpk);
+            continue;
+          }
           ok = wait_full();
           if (!ok) break;
           load64(0, pa);
@@ -721,15 +761,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           ++part_it;
           // the scale factors are used only after the release (a tile's first ones were
           // loaded at its start and may still be in flight)
-          if constexpr (TABLE) {
-            const float a0 = sa0, a1 = sa1;
-            if (kg + 1 < NG) {
-              sa0 = sa_row[2 * kg + 2];
-              sa1 = sa_row[2 * kg + 3];
-            }
-            promote64t(pa, a0, 2 * kg);   // the FMAs run while the MMAs refill the group
-            promote64t(pb, a1, 2 * kg + 1);
-          } else {
+          {
             const float f0 = sa0 * sb0, f1 = sa1 * sb1;
             if (kg + 1 < NG) {
               sa0 = sa_row[2 * kg + 2];
