@@ -41,7 +41,11 @@ constexpr uint32_t kOffOutR = kStages * kXBytes;     // 128 KB
 constexpr uint32_t kOffOutT = kOffOutR + 2 * kQBytes;
 constexpr uint32_t kOffBar = kOffOutT + 2 * kQBytes;  // 192 KB
 constexpr uint32_t kOffRed = kOffBar + 64;
-constexpr uint32_t kSmemBytes = kOffRed + 128 + 1024;  // + alignment slack
+// MX with the tiled layout: a tile's exponents of one copy are exactly one 512-byte atom of
+// the GEMM-ready layout; they are staged here ([tile parity][row, col][512 B]) and leave by
+// one bulk copy each instead of 512 scattered byte stores
+constexpr uint32_t kOffSf = kOffRed + 128;
+constexpr uint32_t kSmemBytes = kOffSf + 2 * 2 * 512 + 1024;  // + alignment slack
 
 // Address of 16-byte chunk `c16` (0..15) of row r in a bf16 tile held as two
 // 64-column halves, each [128 rows][128 B] with the 128-byte swizzle.
@@ -60,6 +64,9 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
 }
 __device__ __forceinline__ void sts64(uint32_t a, uint32_t x, uint32_t y) {
   asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void sts8(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u8 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 __device__ __forceinline__ void sts16(uint32_t a, uint32_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"(static_cast<uint16_t>(v)) : "memory");
@@ -142,22 +149,32 @@ __device__ __forceinline__ float block_max(float v, float* red, int warp, int la
   return r;
 }
 
-// Byte offset of the E8M0 exponent for (row r, 32-block b) in the GEMM-ready
-// tiled layout: 128-row x 4-block atoms of 512 B, atom (r/128, b/4) at
-// ((r/128) * atoms_per_row + b/4) * 512, inside it (r%32)*16 + ((r%128)/32)*4 + b%4.
-__device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t b, int64_t atoms_per_row) {
-  return ((r >> 7) * atoms_per_row + (b >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (b & 3);
-}
 
 // One 128x128 tile already in shared memory (stage buffer xs): both passes, scales
 // written to global memory, quantized bytes staged in outR (row-wise) and outT
 // (column-wise) for the TMA stores.  thr_amax accumulates this thread's |x| maximum.
 // `red` is this tile's block-maximum buffer (the caller alternates two), and every
 // thread of the CTA calls this (the 128x128 recipe synchronises inside).
+// The staged atoms of tile (tr, tc) to their places in the tiled scale arrays: the row
+// copy's atom (tr, tc) of [R, C], the column copy's atom (tc, tr) of [C, R].
+__device__ __forceinline__ void store_mx_atoms(const CastParams& p, uint32_t sf, int tr, int tc) {
+  if (p.do_row)
+    bulk_store(static_cast<uint8_t*>(p.s_row) + (static_cast<int64_t>(tr) * p.tiles_c + tc) * 512, sf, 512);
+  if (p.do_col)
+    bulk_store(static_cast<uint8_t*>(p.s_col) + (static_cast<int64_t>(tc) * p.tiles_r + tr) * 512, sf + 512, 512);
+}
+
+// The GEMM-ready tiled E8M0 layout: 128-row x 4-block atoms of 512 B, atom (r/128, b/4)
+// at ((r/128) * atoms_per_row + b/4) * 512; exponent (local row r, local block b) at
+// (r%32)*16 + (r/32)*4 + b inside it.
+__device__ __forceinline__ uint32_t mx_atom_offset(int r, int b) {
+  return static_cast<uint32_t>((r & 31) * 16 + (r >> 5) * 4 + b);
+}
+
 template <int RECIPE>
 __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs, uint32_t outR, uint32_t outT, int tr,
                                                int tc, int64_t row0, int64_t col0, float g_scale, float& thr_amax,
-                                               float* red, int tid, int warp, int lane) {
+                                               float* red, uint32_t sf, int tid, int warp, int lane) {
   const bool e5 = p.e5m2 != 0;
   const float fmax = fmax_of(e5);
   const int fexp = fmax_exp_of(e5);
@@ -202,11 +219,13 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
       const float m = reduce_scatter4(a, lane, 2, 1);
       const int e = (p.mx_floor ? mx_exponent_floor(m, fexp) : mx_exponent(m, fexp));
       const float mine = pow2_neg(e);
-      const int64_t grow = row0 + (j & 3) * 32 + warp * 2 + (lane >> 4);
+      const int lrow = (j & 3) * 32 + warp * 2 + (lane >> 4);
+      const int64_t grow = row0 + lrow;
       const int64_t b = tc * 4 + (j >> 2);
-      if (grow < p.R && b < nb32_c) {   // a tile hanging over C has blocks past the last one
-        const int64_t off = p.mx_tiled ? mx_tiled_offset(grow, b, (p.C + 127) / 128) : grow * nb32_c + b;
-        static_cast<uint8_t*>(p.s_row)[off] = static_cast<uint8_t>(e + 127);
+      if (p.mx_tiled) {
+        sts8(sf + mx_atom_offset(lrow, j >> 2), static_cast<uint32_t>(e + 127));   // the tile's atom (dims % 128 == 0)
+      } else if (grow < p.R && b < nb32_c) {   // a tile hanging over C has blocks past the last one
+        static_cast<uint8_t*>(p.s_row)[grow * nb32_c + b] = static_cast<uint8_t>(e + 127);
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, mine, (lane & ~3) | i);
@@ -249,9 +268,10 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
       const int e = (p.mx_floor ? mx_exponent_floor(m, fexp) : mx_exponent(m, fexp));
       const float mine = pow2_neg(e);
       const int64_t b = static_cast<int64_t>(tr) * 4 + (lane & 3);
-      if (gcol < p.C && b < nb32_r) {
-        const int64_t off = p.mx_tiled ? mx_tiled_offset(gcol, b, (p.R + 127) / 128) : gcol * nb32_r + b;
-        static_cast<uint8_t*>(p.s_col)[off] = static_cast<uint8_t>(e + 127);
+      if (p.mx_tiled) {
+        sts8(sf + 512 + mx_atom_offset(cc, lane & 3), static_cast<uint32_t>(e + 127));
+      } else if (gcol < p.C && b < nb32_r) {
+        static_cast<uint8_t*>(p.s_col)[gcol * nb32_r + b] = static_cast<uint8_t>(e + 127);
       }
 #pragma unroll
       for (int t = 0; t < 4; ++t) sc[t] = __shfl_sync(0xFFFFFFFFu, mine, (lane & ~3) | t);
@@ -335,7 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // reaches the same barriers; the barrier then ends the loop on every thread.
     const bool ok = mbar_wait(base + kOffBar + 8 * s, (it / kStages) & 1, p.err, kErrTimeoutTmaLoad, nullptr);
 
-    cast_tile_body<RECIPE>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red + (it & 1) * kWarps, tid,
+    const uint32_t sf = base + kOffSf + static_cast<uint32_t>(ob) * 1024u;
+    cast_tile_body<RECIPE>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red + (it & 1) * kWarps, sf, tid,
                            warp, lane);
 
     fence_proxy_async_smem();
@@ -347,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
       if (p.do_row) tma_store_2d(&tm_qrow, outR, static_cast<int>(col0), static_cast<int>(row0));
       if (p.do_col) tma_store_2d(&tm_qcol, outT, static_cast<int>(row0), static_cast<int>(col0));
+      if (RECIPE == kMx && p.mx_tiled) store_mx_atoms(p, sf, tr, tc);
       bulk_commit();
       const int next = tile + kStages * gridDim.x;
       if (next < ntiles) issue_load(it + kStages, next);
@@ -494,18 +516,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_cast_jobs(const __grid_constant
     // one barrier a tile, as in k_cast_transpose
     const bool ok = mbar_wait(base + kOffBar + 8 * s, (it / kStages) & 1, p.err, kErrTimeoutTmaLoad, nullptr);
     float* const red_t = red + (it & 1) * kWarps;
+    const uint32_t sf = base + kOffSf + static_cast<uint32_t>(ob) * 1024u;
     switch (p.recipe) {
       case kTensor:
-        cast_tile_body<kTensor>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red_t, tid, warp, lane);
+        cast_tile_body<kTensor>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red_t, sf, tid, warp, lane);
         break;
       case kBlock1x128:
-        cast_tile_body<kBlock1x128>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red_t, tid, warp, lane);
+        cast_tile_body<kBlock1x128>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red_t, sf, tid, warp,
+                                    lane);
         break;
       case kBlock128x128:
-        cast_tile_body<kBlock128x128>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red_t, tid, warp, lane);
+        cast_tile_body<kBlock128x128>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red_t, sf, tid, warp,
+                                      lane);
         break;
       default:
-        cast_tile_body<kMx>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red_t, tid, warp, lane);
+        cast_tile_body<kMx>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red_t, sf, tid, warp, lane);
         break;
     }
     fence_proxy_async_smem();
@@ -517,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_cast_jobs(const __grid_constant
     if (tid == 0) {
       if (p.do_row) tma_store_2d(&J.m[j].qrow, outR, static_cast<int>(col0), static_cast<int>(row0));
       if (p.do_col) tma_store_2d(&J.m[j].qcol, outT, static_cast<int>(row0), static_cast<int>(col0));
+      if (p.recipe == kMx && p.mx_tiled) store_mx_atoms(p, sf, tr, tc);
       bulk_commit();
       const int next = gt + kStages * gridDim.x;
       if (next < ntiles) issue_load(it + kStages, next);

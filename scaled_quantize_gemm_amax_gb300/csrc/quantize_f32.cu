@@ -35,7 +35,10 @@ constexpr uint32_t kOffOutT = kOffOutR + 2 * kQBytes;
 constexpr uint32_t kOffBar = kOffOutT + 2 * kQBytes;  // 192 KB
 constexpr uint32_t kOffRed = kOffBar + 64;            // [2][kWarps] block maxima
 constexpr uint32_t kOffCol = kOffRed + 2 * kWarps * 4;   // [4][128] column-quarter maxima
-constexpr uint32_t kSmemBytes = kOffCol + 4 * kTile * 4 + 1024;   // + alignment slack
+// MX with the tiled layout: [tile parity][row, col][512 B], one tile's exponents of a copy
+// (exactly one atom of the GEMM-ready layout), sent out by one bulk copy each
+constexpr uint32_t kOffSf = kOffCol + 4 * kTile * 4;
+constexpr uint32_t kSmemBytes = kOffSf + 2 * 2 * 512 + 1024;   // + alignment slack
 
 // Element (r, c) of a binary32 tile held as four 32-column boxes, each [128 rows][128 B]
 // with the 128-byte swizzle (16-byte chunk k of row r at chunk k ^ (r % 8)).
@@ -92,17 +95,20 @@ __device__ __forceinline__ float block_max_1(float v, float* red, int warp, int 
   return r;
 }
 
-// Byte offset of the E8M0 exponent for (row r, 32-block b) in the GEMM-ready tiled
-// layout: 128-row x 4-block atoms of 512 B, atom (r/128, b/4) at
-// ((r/128) * atoms_per_row + b/4) * 512, inside it (r%32)*16 + ((r%128)/32)*4 + b%4.
-__device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t b, int64_t atoms_per_row) {
-  return ((r >> 7) * atoms_per_row + (b >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (b & 3);
+// The GEMM-ready tiled E8M0 layout: 128-row x 4-block atoms of 512 B, atom (r/128, b/4)
+// at ((r/128) * atoms_per_row + b/4) * 512; exponent (local row r, local block b) at
+// (r%32)*16 + (r/32)*4 + b inside it.
+__device__ __forceinline__ uint32_t mx_atom_offset(int r, int b) {
+  return static_cast<uint32_t>((r & 31) * 16 + (r >> 5) * 4 + b);
+}
+__device__ __forceinline__ void sts8(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u8 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
 template <int RECIPE>
 __device__ __forceinline__ void cast_tile_f32(const CastParams& p, uint32_t xs, uint32_t outR, uint32_t outT, int tr,
                                               int tc, int64_t row0, int64_t col0, float g_scale, float& thr_amax,
-                                              float* red, float* colmax, int warp, int lane) {
+                                              float* red, float* colmax, uint32_t sf, int warp, int lane) {
   const bool e5 = p.e5m2 != 0;
   const float fmax = fmax_of(e5);
   const int fexp = fmax_exp_of(e5);
@@ -145,9 +151,11 @@ __device__ __forceinline__ void cast_tile_f32(const CastParams& p, uint32_t xs, 
         const int e = (p.mx_floor ? mx_exponent_floor(m, fexp) : mx_exponent(m, fexp));
         s = pow2_neg(e);
         const int64_t b = static_cast<int64_t>(tc) * 4 + (lane >> 3);
-        if ((lane & 7) == 0 && grow < p.R && b < nb32_c) {   // a tile hanging over C has blocks past the last one
-          const int64_t off = p.mx_tiled ? mx_tiled_offset(grow, b, (p.C + 127) / 128) : grow * nb32_c + b;
-          static_cast<uint8_t*>(p.s_row)[off] = static_cast<uint8_t>(e + 127);
+        if ((lane & 7) == 0) {
+          if (p.mx_tiled)   // the tile's atom (both dims are multiples of 128)
+            sts8(sf + mx_atom_offset(r, lane >> 3), static_cast<uint32_t>(e + 127));
+          else if (grow < p.R && b < nb32_c)   // a tile hanging over C has blocks past the last one
+            static_cast<uint8_t*>(p.s_row)[grow * nb32_c + b] = static_cast<uint8_t>(e + 127);
         }
       }
       sts32(q_addr(outR, r, 4 * lane), q4(v[i], s, e5));
@@ -176,10 +184,10 @@ __device__ __forceinline__ void cast_tile_f32(const CastParams& p, uint32_t xs, 
       const int e = (p.mx_floor ? mx_exponent_floor(am, fexp) : mx_exponent(am, fexp));
       s = pow2_neg(e);
       const int64_t b = static_cast<int64_t>(tr) * 4 + rq;
-      if (gcol < p.C && b < nb32_r) {
-        const int64_t off = p.mx_tiled ? mx_tiled_offset(gcol, b, (p.R + 127) / 128) : gcol * nb32_r + b;
-        static_cast<uint8_t*>(p.s_col)[off] = static_cast<uint8_t>(e + 127);
-      }
+      if (p.mx_tiled)
+        sts8(sf + 512 + mx_atom_offset(c, rq), static_cast<uint32_t>(e + 127));
+      else if (gcol < p.C && b < nb32_r)
+        static_cast<uint8_t*>(p.s_col)[gcol * nb32_r + b] = static_cast<uint8_t>(e + 127);
     }
     uint32_t qw[8];
 #pragma unroll
@@ -257,7 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // timed out still runs the body (its results are dropped) so that every thread reaches
     // the same barriers; the tile barrier then ends the loop on every thread.
     const bool ok = mbar_wait(base + kOffBar + 8 * s, (it / kStages) & 1, p.err, kErrTimeoutTmaLoad, nullptr);
-    cast_tile_f32<RECIPE>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red + (it & 1) * kWarps, colmax,
+    const uint32_t sf = base + kOffSf + static_cast<uint32_t>(ob) * 1024u;
+    cast_tile_f32<RECIPE>(p, xs, outR, outT, tr, tc, row0, col0, g_scale, thr_amax, red + (it & 1) * kWarps, colmax, sf,
                           warp, lane);
     fence_proxy_async_smem();
     if (tid == 0) bulk_wait_read<0>();  // the previous tile's stores have read their staging buffer
@@ -268,6 +277,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
       if (p.do_row) tma_store_2d(&tm_qrow, outR, static_cast<int>(col0), static_cast<int>(row0));
       if (p.do_col) tma_store_2d(&tm_qcol, outT, static_cast<int>(row0), static_cast<int>(col0));
+      if (RECIPE == kMx && p.mx_tiled) {   // the staged atoms: row copy's (tr, tc), column copy's (tc, tr)
+        if (p.do_row)
+          bulk_store(static_cast<uint8_t*>(p.s_row) + (static_cast<int64_t>(tr) * p.tiles_c + tc) * 512, sf, 512);
+        if (p.do_col)
+          bulk_store(static_cast<uint8_t*>(p.s_col) + (static_cast<int64_t>(tc) * p.tiles_r + tr) * 512, sf + 512,
+                     512);
+      }
       bulk_commit();
       const int next = tile + kStages * gridDim.x;
       if (next < ntiles) issue_load(it + kStages, next);
