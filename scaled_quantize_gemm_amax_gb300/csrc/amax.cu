@@ -32,10 +32,13 @@ __device__ __forceinline__ uint32_t fold16(uint32_t m, uint4 v) {
 // which leaves a max of magnitudes unchanged) so that no round has fewer loads in
 // flight; the n % 8 tail is folded in by block 0.  One atomicMax per block on the
 // (non-negative) float bit pattern, which orders like the value.
+//
+// Launched right after k_zero_f32 (programmatic launch): that kernel waits for every
+// earlier kernel in the stream before it lets this one start, so x is complete and may
+// be read at once; only the atomic on amax waits (griddepcontrol.wait) for the zeroing.
 __global__ void __launch_bounds__(kAmaxThreads) k_amax(const uint4* __restrict__ x16, int64_t n16,
                                                       const uint16_t* __restrict__ tail, int ntail,
                                                       float* __restrict__ amax) {
-  pdl_wait();
   pdl_launch_dependents();
   uint32_t m = 0;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -66,6 +69,7 @@ __global__ void __launch_bounds__(kAmaxThreads) k_amax(const uint4* __restrict__
   if (threadIdx.x == 0) {
     float b = red[0];
     for (int w = 1; w < kAmaxThreads / 32; ++w) b = fmaxf(b, red[w]);
+    pdl_wait();   // the zeroing of amax is done
     if (b > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(amax), __float_as_uint(b));
   }
 }
@@ -76,10 +80,10 @@ __device__ __forceinline__ float fold4(float m, float4 v) {
   return fmaxf(fmaxf(fmaxf(fmaxf(m, fabsf(v.x)), fabsf(v.y)), fabsf(v.z)), fabsf(v.w));
 }
 
+// Launched right after k_zero_f32, as k_amax.
 __global__ void __launch_bounds__(kAmaxThreads) k_amax_f32(const float4* __restrict__ x4, int64_t n4,
                                                           const float* __restrict__ tail, int ntail,
                                                           float* __restrict__ amax) {
-  pdl_wait();
   pdl_launch_dependents();
   float m = 0.0f;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -109,6 +113,7 @@ __global__ void __launch_bounds__(kAmaxThreads) k_amax_f32(const float4* __restr
   if (threadIdx.x == 0) {
     float b = red[0];
     for (int w = 1; w < kAmaxThreads / 32; ++w) b = fmaxf(b, red[w]);
+    pdl_wait();   // the zeroing of amax is done
     if (b > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(amax), __float_as_uint(b));
   }
 }

@@ -61,6 +61,10 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 cudaError_t launch_reciprocal(const float* in, float* out, cudaStream_t s);
 // p[0 .. n) = 0 as a (programmatically launched) kernel, ahead of an atomicMax reduction
 cudaError_t launch_zero_f32(float* p, int n, cudaStream_t s);
+// The amax kernels, and the casts when amax_out is set, must be launched right after
+// launch_zero_f32 of their amax: they read their inputs before griddepcontrol.wait (the
+// zeroing kernel waited for every earlier kernel before letting them start) and wait
+// only before the atomic.
 cudaError_t launch_amax(const void* x, int64_t n, float* amax, int num_sms, cudaStream_t s);
 cudaError_t launch_amax_f32(const float* x, int64_t n, float* amax, int num_sms, cudaStream_t s);
 cudaError_t launch_compute_scale(const float* amax, bool e5m2, float* scale, float* scale_inv, cudaStream_t s);
@@ -76,7 +80,7 @@ struct CastParams {
   int mx_floor;          // MX exponent by the floor rule (else the ceil rule)
   int do_row, do_col;
   const float* scale;    // per-tensor scale (device)
-  float* amax_out;       // optional (device, pre-zeroed)
+  float* amax_out;       // optional (device, zeroed by the kernel launched just before)
   uint8_t* q_row;        // [R, C] (generic path only; the tiled path stores through tensor maps)
   uint8_t* q_col;        // [C, R]
   void* s_row;

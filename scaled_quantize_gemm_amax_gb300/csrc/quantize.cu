@@ -306,7 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   __syncthreads();
-  pdl_wait();   // from here on: global memory
+  // With amax_out, the host launched the zeroing of amax_out just before this kernel; that
+  // kernel waited for every earlier one before letting this one start, so only the atomic
+  // on amax_out has to wait (griddepcontrol.wait) for it.  Otherwise wait here.
+  const bool zeroed = p.amax_out != nullptr;
+  if (!zeroed) pdl_wait();   // from here on: global memory
   pdl_launch_dependents();
 
   float g_scale = 1.0f;
@@ -385,9 +389,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 0) bulk_wait_all<0>();
 
-  if (p.amax_out != nullptr) {
+  if (zeroed) {
     const float am = block_max(thr_amax, red, warp, lane);
-    if (tid == 0 && am > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(am));
+    if (tid == 0) {
+      pdl_wait();   // the zeroing of amax_out is done
+      if (am > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(am));
+    }
   }
 }
 
@@ -396,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // bytes through a transposed shared tile.
 __global__ void __launch_bounds__(256) k_cast_generic(const uint16_t* __restrict__ x, CastParams p) {
   __shared__ float tile[32][33];
-  pdl_wait();
+  const bool zeroed = p.amax_out != nullptr;   // as the tiled kernel: only the atomic waits then
+  if (!zeroed) pdl_wait();
   pdl_launch_dependents();
   const bool e5 = p.e5m2 != 0;
   const float s = *p.scale;
@@ -426,10 +434,13 @@ __global__ void __launch_bounds__(256) k_cast_generic(const uint16_t* __restrict
     if (p.do_row && p.s_row) *static_cast<float*>(p.s_row) = si;
     if (p.do_col && p.s_col) *static_cast<float*>(p.s_col) = si;
   }
-  if (p.amax_out != nullptr) {
+  if (zeroed) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    if (tx == 0 && amax > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(amax));
+    if (tx == 0) {
+      pdl_wait();
+      if (amax > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(amax));
+    }
   }
 }
 
@@ -451,7 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_cast_jobs(const __grid_constant
     fence_mbar_init();
   }
   __syncthreads();
-  pdl_wait();   // from here on: global memory
+  // a zeroing kernel ran just before this one when any job has amax_out (as the single cast)
+  bool zeroed = false;
+  for (int j = 0; j < J.n; ++j) zeroed = zeroed || J.p[j].amax_out != nullptr;
+  if (!zeroed) pdl_wait();   // from here on: global memory
   pdl_launch_dependents();
 
   if (blockIdx.x == 0 && tid == 0) {
@@ -488,7 +502,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_cast_jobs(const __grid_constant
   auto flush_amax = [&](int j, float thr_amax) {
     if (J.p[j].amax_out == nullptr) return;
     const float am = block_max(thr_amax, red, warp, lane);
-    if (tid == 0 && am > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(J.p[j].amax_out), __float_as_uint(am));
+    if (tid == 0) {
+      pdl_wait();   // the zeroing of the amaxes is done
+      if (am > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(J.p[j].amax_out), __float_as_uint(am));
+    }
   };
 
   float thr_amax = 0.0f, g_scale = 1.0f;

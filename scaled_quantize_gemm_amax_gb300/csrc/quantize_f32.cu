@@ -219,7 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   __syncthreads();
-  pdl_wait();   // from here on: global memory
+  // with amax_out a zeroing kernel ran just before this one: only the atomic waits (as the
+  // BF16-input kernel)
+  const bool zeroed = p.amax_out != nullptr;
+  if (!zeroed) pdl_wait();   // from here on: global memory
   pdl_launch_dependents();
 
   float g_scale = 1.0f;
@@ -300,12 +303,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 0) bulk_wait_all<0>();
 
-  if (p.amax_out != nullptr) {
+  if (zeroed) {
     // the block maximum (the red buffer of the next tile index is free: every thread has
     // passed the last tile barrier)
     float* const r = red + (it & 1) * kWarps;
     const float am = block_max_1(thr_amax, r, warp, lane);
-    if (tid == 0 && am > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(am));
+    if (tid == 0) {
+      pdl_wait();   // the zeroing of amax_out is done
+      if (am > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(am));
+    }
   }
 }
 
@@ -314,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // bytes through a transposed shared tile.
 __global__ void __launch_bounds__(256) k_cast_generic_f32(const float* __restrict__ x, CastParams p) {
   __shared__ float tile[32][33];
-  pdl_wait();
+  const bool zeroed = p.amax_out != nullptr;   // as the tiled kernel: only the atomic waits then
+  if (!zeroed) pdl_wait();
   pdl_launch_dependents();
   const bool e5 = p.e5m2 != 0;
   const float s = *p.scale;
@@ -344,9 +351,12 @@ __global__ void __launch_bounds__(256) k_cast_generic_f32(const float* __restric
     if (p.do_row && p.s_row) *static_cast<float*>(p.s_row) = si;
     if (p.do_col && p.s_col) *static_cast<float*>(p.s_col) = si;
   }
-  if (p.amax_out != nullptr) {
+  if (zeroed) {
     amax = warp_max(amax);
-    if (tx == 0 && amax > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(amax));
+    if (tx == 0) {
+      pdl_wait();
+      if (amax > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(amax));
+    }
   }
 }
 
