@@ -90,9 +90,9 @@ struct Cfg<kMx> {
 
 // CTRL = 4: warps 0..3 (producer, the two MMA issuers, an idle warp) form a warpgroup
 // that gives registers to the two epilogue warpgroups (warps 4..11) with setmaxnreg, so
-// that the promotion can hold both 128-deep partials of a group (its 64 columns of
-// each) in registers at once and hand the group back before its FMAs.  The kernel must
-// be launched with kSplitLaunchRegs a thread (checked on the host before the first
+// that the promotion can hold a group's partials (the 1x128 x 128x128 kind: both, its 64
+// columns of each) in registers and hand the group back before its FMAs.  The kernel
+// must be launched with kSplitLaunchRegs a thread (checked on the host before the first
 // launch: an increase beyond the launch pool is never granted).
 constexpr int kSplitLaunchRegs = 168, kCtrlRegs = 72, kEpiRegs = 216;
 static_assert(128 * kCtrlRegs + 256 * kEpiRegs <= 384 * kSplitLaunchRegs, "register split exceeds the launch pool");
@@ -123,19 +123,21 @@ struct Layout {
   static constexpr bool TSTORE = !(KIND == kBlock1x128 || KIND == kBlockRowsB);
   static constexpr uint32_t STG_BYTES = TSTORE ? Cfg<KIND>::EPI * 4096 : 0;
   static constexpr uint32_t OFF_STG = (OFF_SF + S * SF_BYTES + 1023) & ~1023u;
-  // per-row B scales on CTA pairs: the tile's B-scale table, two halves of [kb][64] floats
-  static constexpr uint32_t TBL_HALF = KIND == kBlockK2RowsB ? kMaxTableKb * 64 * 4 : 0;
+  // per-row B scales on CTA pairs: the tile's B-scale table, one part of [kb][COLS] floats
+  // per epilogue warpgroup (its COLS columns)
+  static constexpr int NPART = Cfg<KIND>::EPI / 4, PCOLS = BN / NPART;
+  static constexpr uint32_t TBL_PART = KIND == kBlockK2RowsB ? kMaxTableKb * PCOLS * 4 : 0;
   static constexpr uint32_t OFF_TBL = OFF_STG + STG_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_TBL + 2 * TBL_HALF;
+  static constexpr uint32_t OFF_BAR = OFF_TBL + NPART * TBL_PART;
   // barriers: full[S], empty[S], tfull[4], tempty[4], final
   static constexpr uint32_t OFF_FULL = OFF_BAR, OFF_EMPTY = OFF_BAR + 8 * S;
   static constexpr uint32_t OFF_TFULL = OFF_EMPTY + 8 * S, OFF_TEMPTY = OFF_TFULL + 32;
   static constexpr uint32_t OFF_FINAL = OFF_TEMPTY + 32;
   static constexpr uint32_t OFF_SFR = OFF_FINAL + 8;   // MX: a stage's scale factors are in TMEM
   static constexpr uint32_t OFF_TMEM = OFF_SFR + 8 * S, OFF_ABORT = OFF_TMEM + 4;
-  // B-scale table barriers: tbl_full[2] (the half's table is filled), tbl_free[2] (read)
+  // B-scale table barriers per (part, buffer): filled, then (at 8 * 2 * NPART) read
   static constexpr uint32_t OFF_TBAR = (OFF_ABORT + 4 + 7) & ~7u;
-  static constexpr uint32_t SMEM = OFF_TBAR + 64 + 32 + 1024;   // + alignment slack
+  static constexpr uint32_t SMEM = OFF_TBAR + 32 * NPART + 1024;   // + alignment slack
   // bytes one stage's full barrier expects (in a pair: the leader's barrier sees both CTAs' loads)
   static constexpr uint32_t TX_BYTES = PAIR ? 2 * (STAGE_BYTES + SF_BYTES) : STAGE_BYTES + SF_BYTES;
 };
@@ -229,9 +231,9 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     }
     mbar_init(base + L::OFF_FINAL, NISS);
     if (TABLE) {
-      for (int hb = 0; hb < 4; ++hb) {   // (half, table buffer)
-        mbar_init(base + L::OFF_TBAR + 8 * hb, 4 * 32);     // filled: every lane's copies of the half's four warps
-        mbar_init(base + L::OFF_TBAR + 32 + 8 * hb, 4);     // read: one arrive per warp
+      for (int hb = 0; hb < 2 * L::NPART; ++hb) {   // (part, table buffer)
+        mbar_init(base + L::OFF_TBAR + 8 * hb, 4 * 32);                  // filled: every lane's copies of the part's four warps
+        mbar_init(base + L::OFF_TBAR + 16 * L::NPART + 8 * hb, 4);       // read: one arrive per warp
       }
     }
     *abort_flag = 0;
@@ -609,9 +611,9 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         // pa / pb hold the group's two partials.
         const float* sa_row = static_cast<const float*>(p.sa) + grow * KB;
         const float* sb_tile = static_cast<const float*>(p.sb) + (gcol0 / 128) * KB;
-        uint64_t acc[32];
+        uint64_t acc[COLS / 2];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] = 0;
+        for (int j = 0; j < COLS / 2; ++j) acc[j] = 0;
         uint32_t pa[2][32], pb[2][32];
         auto wait_full = [&]() -> bool {
           const uint32_t g = part_it % GROUPS;
@@ -634,47 +636,55 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[16 * c + j] = fma_f32x2(f2, pack_f32x2(r[c][2 * j], r[c][2 * j + 1]), acc[16 * c + j]);
         };
-        // per-row B scales: this half's table, and the factor of column j at k-block kb:
-        // sA[m, kb] * sB[n0 + j, kb] rounded once, then the FMA (as the single-CTA kernel)
-        const uint32_t tbl = base + L::OFF_TBL + static_cast<uint32_t>(h) * L::TBL_HALF;
+        // per-row B scales: this warpgroup's part of the table ([kb][COLS] floats), and the
+        // factor of column j at k-block kb: sA[m, kb] * sB[n0 + j, kb] rounded once, then
+        // the FMA (as the single-CTA kernel)
+        const uint32_t tbl = base + L::OFF_TBL + static_cast<uint32_t>(h) * L::TBL_PART;
         uint32_t tbl_cur = tbl;   // the table buffer of this tile
-        // factors of one partial: fpk[16 c + j] = sA * (sB[2 (16 c + j)], sB[2 (16 c + j) + 1]),
-        // each product rounded once (as the single-CTA kernel), from broadcast table loads
-        auto factors64 = [&](uint64_t (&f)[32], float sa, int kb) {
+        // One chunk q of the group: partial q / 2, columns CW (q % 2) .. +CW-1 of this
+        // thread's COLS; its factors fk[j] = sA * (sB[c0 + 2 j], sB[c0 + 2 j + 1]) (each
+        // product rounded once) from broadcast table loads, and its FMAs into
+        // acc[CW / 2 (q % 2) + j].
+        constexpr int CW = COLS / 2;
+        uint32_t ra[CW], rb[CW];
+        uint64_t fk[CW / 2];
+        auto ldc = [&](int q4, uint32_t (&r)[CW]) {
+          tc_ld_32x32b(lane_base + ((part_it % GROUPS) * KSUB + (q4 >> 1)) * BN + h * COLS + CW * (q4 & 1), r);
+        };
+        auto factors = [&](uint64_t (&f)[CW / 2], float sa, int kb, int half) {
           const uint64_t sa2 = pack_f32x2(sa, sa);
-          const uint32_t trow = tbl_cur + static_cast<uint32_t>(kb) * 256u;
+          const uint32_t trow = tbl_cur + static_cast<uint32_t>(kb * COLS + half * CW) * 4u;
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const float4 fb = lds128f(trow + static_cast<uint32_t>(4 * jj) * 4u);
+          for (int jj = 0; jj < CW / 4; ++jj) {
+            const float4 fb = lds128f(trow + static_cast<uint32_t>(jj) * 16u);
             f[2 * jj] = mul_f32x2(sa2, pack_f32x2(fb.x, fb.y));
             f[2 * jj + 1] = mul_f32x2(sa2, pack_f32x2(fb.z, fb.w));
           }
         };
-        auto fma64 = [&](const uint32_t (&r)[2][32], const uint64_t (&f)[32]) {
+        auto fmac = [&](const uint32_t (&r)[CW], const uint64_t (&f)[CW / 2], int half) {
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              acc[16 * c + j] = fma_f32x2(f[16 * c + j], pack_f32x2(r[c][2 * j], r[c][2 * j + 1]), acc[16 * c + j]);
+          for (int j = 0; j < CW / 2; ++j)
+            acc[CW / 2 * half + j] = fma_f32x2(f[j], pack_f32x2(r[2 * j], r[2 * j + 1]), acc[CW / 2 * half + j]);
         };
-        uint64_t fpk[32];
         if constexpr (TABLE) {
-          // The half's four warps fill its table with a tile's B scales (warp q: its 16
+          // The part's four warps fill its table with a tile's B scales (warp q: its COLS / 4
           // columns, every k-block) by asynchronous copies that arrive on the buffer's
           // "filled" barrier when they land.  With K / 128 <= 32 the table has two buffers and
           // the next tile's scales are fetched at the start of this one, a whole tile ahead;
           // otherwise this tile's fill is awaited at its start.  A buffer is refilled once the
-          // half's four warps have finished reading it (its "read" barrier).
+          // part's four warps have finished reading it (its "read" barrier).
           const int nbuf = KB <= kMaxTableKb / 2 ? 2 : 1;
           auto tbar_full = [&](uint32_t b) { return base + L::OFF_TBAR + 8 * (2 * h + b); };
-          auto tbar_free = [&](uint32_t b) { return base + L::OFF_TBAR + 32 + 8 * (2 * h + b); };
+          auto tbar_free = [&](uint32_t b) { return base + L::OFF_TBAR + 16 * L::NPART + 8 * (2 * h + b); };
           auto fill = [&](int tile, uint32_t b) {
+            constexpr int CPW = COLS / 4;   // columns a warp fills
             int ftm, ftn;
             tile_coords(tile, tiles_m, tiles_n, ftm, ftn);
-            const int cq = 16 * q + (lane & 15);
+            const int cq = CPW * q + (lane % CPW);
             const float* src = static_cast<const float*>(p.sb) + (static_cast<int64_t>(ftn) * BN + h * COLS + cq) * KB;
-            const uint32_t dst = tbl + b * (L::TBL_HALF / 2);
-            for (int kb = lane >> 4; kb < KB; kb += 2) cp_async_4(dst + static_cast<uint32_t>(kb * 64 + cq) * 4u, src + kb);
+            const uint32_t dst = tbl + b * (L::TBL_PART / 2);
+            for (int kb = lane / CPW; kb < KB; kb += 32 / CPW)
+              cp_async_4(dst + static_cast<uint32_t>(kb * COLS + cq) * 4u, src + kb);
             cp_async_arrive_noinc(tbar_full(b));
           };
           bool tok = true;
@@ -693,7 +703,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
               tok = __all_sync(0xFFFFFFFFu, mbar_wait(tbar_free(0), (tile_it - 1) & 1u, p.err, kErrTimeoutMma, abort_flag));
             if (tok) fill(t, 0);
           }
-          tbl_cur = tbl + (nbuf == 2 ? (tile_it & 1u) * (L::TBL_HALF / 2) : 0u);
+          tbl_cur = tbl + (nbuf == 2 ? (tile_it & 1u) * (L::TBL_PART / 2) : 0u);
           if (!tok || !__all_sync(0xFFFFFFFFu, mbar_wait(tbar_full(nbuf == 2 ? (tile_it & 1u) : 0u),
                                                          (nbuf == 2 ? (tile_it >> 1) : tile_it) & 1u, p.err,
                                                          kErrTimeoutMma, abort_flag)))
@@ -707,32 +717,45 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           sb1 = __ldg(sb_tile + 1);
         }
         bool ok = true;
-        for (int kg = 0; kg < NG; ++kg) {
-          if constexpr (TABLE) {
-            // Per-row B scales: a partial's 64 columns each have their own factor
-            // sA[m, kb] * sB[n, kb].  The factors of a partial are formed into registers
-            // (table loads and packed multiplies) while its TMEM load is in flight, so the
-            // FMAs that follow have no load in their chain; the group's second partial is
-            // loaded into the registers of the first once its FMAs are done, and the group
-            // goes back to the MMA issuers when it has landed.  (Holding both partials, as
-            // below, left no registers for the factors: each FMA then waited on its table
-            // load and multiply.)
+        if constexpr (TABLE) {
+          // Per-row B scales: every column n has its own factor sA[m, kb] * sB[n, kb], so
+          // the promotion does twice the FP32 work of the common pairing and, with the MMAs
+          // far ahead, its own instruction stream sets the pace.  The group is taken in four
+          // 32-column chunks (partial 0 columns 0-31, 32-63, then partial 1), software-
+          // pipelined over two register buffers: each chunk's TMEM load is in flight while
+          // the previous chunk's FMAs and the next chunk's factors (table loads, packed
+          // multiplies) run; the group goes back to the MMA issuers once the last chunk has
+          // landed.  The next group's barrier is tested right after that and its answer used
+          // after the last FMAs.  (Two loads in flight per warp over three buffers ran
+          // slower: the TMEM read rate, not the load latency, bounds the loop.)
+          bool ready_next = false;   // the next group's partials were seen complete early
+          for (int kg = 0; kg < NG; ++kg) {
             const float a0 = sa0, a1 = sa1;
             if (kg + 1 < NG) {
               sa0 = sa_row[2 * kg + 2];
               sa1 = sa_row[2 * kg + 3];
             }
-            factors64(fpk, a0, 2 * kg);   // before the wait: needs no MMA result
-            ok = wait_full();
-            if (!ok) break;
-            load64(0, pa);
-            tc_wait_ld(pa[0]);
-            tc_tie(pa[1]);
-            fma64(pa, fpk);
-            load64(1, pa);                // the second partial, into the same registers
-            factors64(fpk, a1, 2 * kg + 1);
-            tc_wait_ld(pa[0]);
-            tc_tie(pa[1]);
+            if (!__all_sync(0xFFFFFFFFu, ready_next)) {
+              ok = wait_full();
+              if (!ok) break;
+            } else {
+              tc_fence_after();
+            }
+            ldc(0, ra);
+            factors(fk, a0, 2 * kg, 0);
+            tc_wait_ld(ra);
+            ldc(1, rb);
+            fmac(ra, fk, 0);
+            factors(fk, a0, 2 * kg, 1);
+            tc_wait_ld(rb);
+            ldc(2, ra);
+            fmac(rb, fk, 1);
+            factors(fk, a1, 2 * kg + 1, 0);
+            tc_wait_ld(ra);
+            ldc(3, rb);
+            fmac(ra, fk, 0);
+            factors(fk, a1, 2 * kg + 1, 1);
+            tc_wait_ld(rb);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -740,9 +763,13 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
               if (next < total_groups) release(base + L::OFF_FULL + 8 * (next % S));
             }
             ++part_it;
-            fma64(pa, fpk);
-            continue;
+            ready_next = kg + 1 < NG &&
+                         mbar_test_wait(base + L::OFF_TFULL + 8 * (part_it % GROUPS), (part_it / GROUPS) & 1u);
+            fmac(rb, fk, 1);
           }
+        }
+        if constexpr (!TABLE)
+        for (int kg = 0; kg < NG; ++kg) {
           ok = wait_full();
           if (!ok) break;
           load64(0, pa);
@@ -777,13 +804,13 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         if constexpr (TABLE) {
           __syncwarp();   // every lane's table reads of this tile are done
           const uint32_t b = KB <= kMaxTableKb / 2 ? (tile_it & 1u) : 0u;
-          if (lane == 0) mbar_arrive(base + L::OFF_TBAR + 32 + 8 * (2 * h + b));
+          if (lane == 0) mbar_arrive(base + L::OFF_TBAR + 16 * L::NPART + 8 * (2 * h + b));
           ++tile_it;
         }
         // C through TMA stores of this warp's staged box (as the other kinds)
         const int box_row = static_cast<int>(static_cast<int64_t>(tm) * TM + row_off) + 32 * q;
 #pragma unroll
-        for (int c32 = 0; c32 < 2; ++c32) {
+        for (int c32 = 0; c32 < COLS / 32; ++c32) {
           float v[32];
 #pragma unroll
           for (int j = 0; j < 16; ++j) unpack_f32x2(acc[16 * c32 + j], v[2 * j], v[2 * j + 1]);
