@@ -291,6 +291,14 @@ fp8_status fp8_allreduce_sum_noalloc(const void* g, int32_t k, int64_t n, fp8_fo
  * (BLOCK_1x128, BLOCK_1x128); (MX_1x32_TILED, MX_1x32_TILED).  Others return
  * FP8_ERR_UNSUPPORTED.  M, N, K must be multiples of 128 (FP8_ERR_SHAPE);
  * M or N == 0 is a no-op, K == 0 writes zeros.
+ * Workspace: with (TENSOR, TENSOR) or (MX, MX) and M % 256 == 0, a GEMM whose last
+ * wave of 256-row tiles would leave at least half of the CTA pairs idle (one partial
+ * wave, or at least four full ones and a partial one) cuts that wave's tiles along K
+ * and sums the ranges in a fixed order; it uses a workspace the library allocates on
+ * the first such call on `stream` (SMs / 2 slots of 256 KB and their counters, kept
+ * for the process's lifetime; up to 16 streams a device).  A call on a stream that is
+ * being captured and has none yet runs unsplit.  Results are deterministic either way
+ * but differ in the last bits between the split and unsplit runs of one shape.
  */
 fp8_status fp8_scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const void* sA, const uint8_t* B,
                            fp8_format fb, fp8_recipe rb, const void* sB, int64_t M, int64_t N, int64_t K, void* C,

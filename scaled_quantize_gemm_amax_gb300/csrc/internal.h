@@ -143,6 +143,15 @@ struct GemmParams {
   float* c_scale_inv;    // float[1]
   int e5m2_c;
   uint32_t* err;
+  // Split of the last, partial wave (per-tensor and MX on CTA pairs): the tiles from
+  // tail0 on are cut into `split` K ranges computed by otherwise idle pairs; range c > 0
+  // leaves its raw FP32 accumulators in ws slot (c - 1) * (tiles - tail0) + j and counts
+  // its warps on ws_flags[slot]; the pair with range 0 adds the ranges in order and
+  // resets the count.  split = 1: off (tail0 = the tile count).
+  int split;
+  int tail0;
+  float* ws;             // [slots][256][256] fp32
+  int* ws_flags;         // [slots], 0 between launches
 };
 // Width (N) of one output tile of the GEMM variant these parameters select.
 int gemm_block_n(const GemmParams& p);

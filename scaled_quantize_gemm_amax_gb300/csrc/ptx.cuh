@@ -29,6 +29,28 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ------------------------------------------------------------------ counters in global memory
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Wait until *count >= target, another CTA's warps having released their writes (fence,
+// then the increment) before counting.  Gives up after kWaitTimeoutNs: ORs `code` into
+// the device error word and returns false.
+__device__ __forceinline__ bool wait_count(const int* count, int target, uint32_t* err, uint32_t code) {
+  if (ld_acquire_gpu(count) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_gpu(count) < target) {
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      atomicOr(err, code);
+      return false;
+    }
+    __nanosleep(128);
+  }
+  return true;
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

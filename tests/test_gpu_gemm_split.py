@@ -1,0 +1,90 @@
+"""The K-split last wave of the per-tensor and MX GEMMs on CTA pairs: a last wave that
+would leave at least half of the pairs idle has its tiles cut into K ranges on otherwise
+idle pairs, range 0 adding the others' FP32 values in order (a GEMM of one partial wave,
+or of at least four full waves and a partial one).  Parity with the oracle on shapes that
+split (one tile into 8 ranges, a ragged N, four full waves plus a split tail), bit-identical
+results from repeated launches (the per-slot counters are back at zero after every
+launch) and from two streams running at once (each stream has its own workspace).  The
+wave counts assume the 76 resident pairs of a 152-SM part; elsewhere the shapes still
+check parity."""
+import numpy as np
+import pytest
+import torch
+
+import scaled_quantize_gemm_amax_gb300 as fq
+from scaled_quantize_gemm_amax_gb300 import workloads as wl
+from gpu_util import R, F, assert_status_ok, host, require_gpu
+from test_gpu_gemm import _quant_gpu, _quant_oracle, gemm_check
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+SPLIT_PAIRS = [(R.TENSOR, R.TENSOR), (R.MX_1x32_TILED, R.MX_1x32_TILED)]
+
+
+@pytest.mark.parametrize("ra,rb", SPLIT_PAIRS)
+@pytest.mark.parametrize("m,n,k,out", [
+    (256, 256, 4096, fq.OutDtype.BF16),     # one tile, 32 k-blocks: 8 ranges of 4
+    (512, 384, 640, fq.OutDtype.FP32),      # 4 tiles (N ragged: half of the second column of tiles), 5 ranges
+    (4608, 4608, 512, fq.OutDtype.BF16),    # 324 tiles: four full waves, 20 tail tiles in 3 ranges
+    (4608, 4608, 256, fq.OutDtype.FP32),    # the same in 2 ranges (two k-blocks)
+    (2560, 2304, 1024, fq.OutDtype.BF16),   # 90 tiles: one full wave and 14 tail tiles, not split
+])
+def test_split_tail_parity(ra, rb, m, n, k, out):
+    # independent seeds for A and B (equal seeds would make B a multiple of A's rows, and
+    # C's diagonal a sum of squares, which the max-abs bar does not describe)
+    x = wl.normal_bf16((m, k), 700 + m % 97, 1.0)
+    w = wl.normal_bf16((n, k), 900 + n % 89, 0.02)
+    rows = None if m * n <= 2560 * 2304 else np.arange(0, m, 5)
+    gemm_check(x, w, ra, rb, F.E4M3, F.E4M3, out=out, rows=rows)
+
+
+def _operands(ra, rb, m, n, k, seed):
+    x = wl.normal_bf16((m, k), seed, 1.0)
+    w = wl.normal_bf16((n, k), seed + 1, 0.02)
+    _, _, sca = _quant_oracle(x.view(torch.int16).cpu().numpy().view(np.uint16), ra, F.E4M3)
+    _, _, scb = _quant_oracle(w.view(torch.int16).cpu().numpy().view(np.uint16), rb, F.E4M3)
+    qa, sa = _quant_gpu(x, ra, F.E4M3, sca)
+    qb, sb = _quant_gpu(w, rb, F.E4M3, scb)
+    return qa, sa, qb, sb
+
+
+@pytest.mark.parametrize("ra,rb", SPLIT_PAIRS)
+def test_split_repeated_launches_identical(ra, rb):
+    m, n, k = 4608, 4608, 512
+    qa, sa, qb, sb = _operands(ra, rb, m, n, k, 80)
+    cs = [torch.empty((m, n), dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    for c in cs:   # back to back on one stream: each launch finds the counters reset by the previous one
+        fq.fp8_scaled_gemm(qa, F.E4M3, ra, sa, qb, F.E4M3, rb, sb, c)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    ref = host(cs[0].view(torch.int16))
+    for i, c in enumerate(cs[1:], 1):
+        assert np.array_equal(host(c.view(torch.int16)), ref), f"launch {i} differs from launch 0"
+
+
+def test_split_two_streams_at_once():
+    m, n, k = 4608, 4608, 512
+    ops = [_operands(R.TENSOR, R.TENSOR, m, n, k, 90), _operands(R.MX_1x32_TILED, R.MX_1x32_TILED, m, n, k, 92)]
+    recs = [(R.TENSOR, R.TENSOR), (R.MX_1x32_TILED, R.MX_1x32_TILED)]
+    refs = []
+    for (qa, sa, qb, sb), (ra, rb) in zip(ops, recs):
+        c = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+        fq.fp8_scaled_gemm(qa, F.E4M3, ra, sa, qb, F.E4M3, rb, sb, c)
+        refs.append(c)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [[torch.empty((m, n), dtype=torch.bfloat16, device="cuda") for _ in range(3)] for _ in range(2)]
+    for it in range(3):
+        for s, (qa, sa, qb, sb), (ra, rb), o in zip(streams, ops, recs, outs):
+            fq.fp8_scaled_gemm(qa, F.E4M3, ra, sa, qb, F.E4M3, rb, sb, o[it], stream=s)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    for ref, o in zip(refs, outs):
+        for c in o:
+            assert np.array_equal(host(c.view(torch.int16)), host(ref.view(torch.int16)))
