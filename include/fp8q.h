@@ -293,7 +293,7 @@ fp8_status fp8_allreduce_sum_noalloc(const void* g, int32_t k, int64_t n, fp8_fo
  * M or N == 0 is a no-op, K == 0 writes zeros.
  * Workspace: with (TENSOR, TENSOR) or (MX, MX) and M % 256 == 0, a GEMM whose last
  * wave of 256-row tiles would leave at least half of the CTA pairs idle (one partial
- * wave, or at least four full ones and a partial one) cuts that wave's tiles along K
+ * wave, or full ones and a partial one when K >= 8192) cuts that wave's tiles along K
  * and sums the ranges in a fixed order; it uses a workspace the library allocates on
  * the first such call on `stream` (SMs / 2 slots of 256 KB and their counters, kept
  * for the process's lifetime; up to 16 streams a device).  A call on a stream that is

@@ -1226,11 +1226,12 @@ cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUte
   if constexpr (KIND == kTensor || KIND == kMx) {
     // A last wave that would leave at least half of the pairs idle is cut along K: its R
     // tiles into S ranges on R * S pairs (every pair resident, so the waits below end).
-    // Measured side by side: +2 % at 8192^3 (13 full waves), nothing gained at 4096^3 (3 full
-    // waves: the ranges' hand-over costs what the shorter wave saves), so the cut is made
-    // for a GEMM of one partial wave or of at least four full ones.
+    // The hand-over of the ranges costs a few microseconds whatever K is, the time saved
+    // grows with K: measured side by side, +1-2 % at 8192^3, +3 % at 2048 x 36864 x 12288,
+    // +9 % at 2048 x 12288 x 49152, but nothing at 4096^3 and -6 % at 49152 x 12288 x 2048.
+    // So the cut is made for K >= 8192, or when there is only the one partial wave.
     const int64_t full = ntiles / pairs, rest = ntiles % pairs, ng = p.K / kBK;
-    if (rest > 0 && 2 * rest <= pairs && ng >= 2 && (full == 0 || full >= 4)) {
+    if (rest > 0 && 2 * rest <= pairs && ng >= 2 && (full == 0 || ng >= 64)) {
       int64_t split = pairs / rest;
       if (split > ng) split = ng;
       if (split > kMaxSplit) split = kMaxSplit;

@@ -1,8 +1,8 @@
 """The K-split last wave of the per-tensor and MX GEMMs on CTA pairs: a last wave that
 would leave at least half of the pairs idle has its tiles cut into K ranges on otherwise
 idle pairs, range 0 adding the others' FP32 values in order (a GEMM of one partial wave,
-or of at least four full waves and a partial one).  Parity with the oracle on shapes that
-split (one tile into 8 ranges, a ragged N, four full waves plus a split tail), bit-identical
+or with K >= 8192 full waves and a partial one).  Parity with the oracle on shapes that
+split (one tile into 8 ranges, a ragged N, full waves plus a split tail), bit-identical
 results from repeated launches (the per-slot counters are back at zero after every
 launch) and from two streams running at once (each stream has its own workspace).  The
 wave counts assume the 76 resident pairs of a 152-SM part; elsewhere the shapes still
@@ -31,9 +31,8 @@ SPLIT_PAIRS = [(R.TENSOR, R.TENSOR), (R.MX_1x32_TILED, R.MX_1x32_TILED)]
 @pytest.mark.parametrize("m,n,k,out", [
     (256, 256, 4096, fq.OutDtype.BF16),     # one tile, 32 k-blocks: 8 ranges of 4
     (512, 384, 640, fq.OutDtype.FP32),      # 4 tiles (N ragged: half of the second column of tiles), 5 ranges
-    (4608, 4608, 512, fq.OutDtype.BF16),    # 324 tiles: four full waves, 20 tail tiles in 3 ranges
-    (4608, 4608, 256, fq.OutDtype.FP32),    # the same in 2 ranges (two k-blocks)
-    (2560, 2304, 1024, fq.OutDtype.BF16),   # 90 tiles: one full wave and 14 tail tiles, not split
+    (2560, 2304, 8192, fq.OutDtype.BF16),   # 90 tiles: one full wave, 14 tail tiles in 5 ranges
+    (4608, 4608, 512, fq.OutDtype.FP32),    # 324 tiles, K < 8192: not split
 ])
 def test_split_tail_parity(ra, rb, m, n, k, out):
     # independent seeds for A and B (equal seeds would make B a multiple of A's rows, and
@@ -56,7 +55,7 @@ def _operands(ra, rb, m, n, k, seed):
 
 @pytest.mark.parametrize("ra,rb", SPLIT_PAIRS)
 def test_split_repeated_launches_identical(ra, rb):
-    m, n, k = 4608, 4608, 512
+    m, n, k = 2560, 2304, 8192
     qa, sa, qb, sb = _operands(ra, rb, m, n, k, 80)
     cs = [torch.empty((m, n), dtype=torch.bfloat16, device="cuda") for _ in range(4)]
     for c in cs:   # back to back on one stream: each launch finds the counters reset by the previous one
@@ -69,7 +68,7 @@ def test_split_repeated_launches_identical(ra, rb):
 
 
 def test_split_two_streams_at_once():
-    m, n, k = 4608, 4608, 512
+    m, n, k = 2560, 2304, 8192
     ops = [_operands(R.TENSOR, R.TENSOR, m, n, k, 90), _operands(R.MX_1x32_TILED, R.MX_1x32_TILED, m, n, k, 92)]
     recs = [(R.TENSOR, R.TENSOR), (R.MX_1x32_TILED, R.MX_1x32_TILED)]
     refs = []
