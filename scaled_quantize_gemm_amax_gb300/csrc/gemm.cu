@@ -210,6 +210,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   constexpr int TM = PAIR ? 2 * kBM : kBM;                  // rows of one tile
+  constexpr int kRasterM = BN == 256 ? 16 : 8;              // M-tiles that walk N together
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;      // 0 = the pair's leader
   const bool leader = rank == 0;
   const int tiles_m = static_cast<int>(p.M / TM), tiles_n = static_cast<int>((p.N + BN - 1) / BN);
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     for (int wi = 0; wi < nwork && ok; ++wi) {
       const Work w = work_at(wi);
       int tm, tn;
-      tile_coords(w.t, tiles_m, tiles_n, tm, tn);
+      tile_coords<kRasterM>(w.t, tiles_m, tiles_n, tm, tn);
       for (int kg = w.kg0; kg < w.kg1; ++kg) {
         const int kb = kg * KSUB;   // first 128-deep K block of this stage
         const uint32_t full = base + L::OFF_FULL + 8 * stage;
@@ -623,7 +624,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     for (int wi = 0; wi < nwork; ++wi) {
       const Work w = work_at(wi);
       int tm, tn;
-      tile_coords(w.t, tiles_m, tiles_n, tm, tn);
+      tile_coords<kRasterM>(w.t, tiles_m, tiles_n, tm, tn);
       const int64_t grow = static_cast<int64_t>(tm) * TM + row_off + row;
       const int64_t gcol0 = static_cast<int64_t>(tn) * BN + h * COLS;
       if constexpr (WIDE) {
@@ -704,7 +705,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           auto fill = [&](int tile, uint32_t b) {
             constexpr int CPW = COLS / 4;   // columns a warp fills
             int ftm, ftn;
-            tile_coords(tile, tiles_m, tiles_n, ftm, ftn);
+            tile_coords<kRasterM>(tile, tiles_m, tiles_n, ftm, ftn);
             const int cq = CPW * q + (lane % CPW);
             const float* src = static_cast<const float*>(p.sb) + (static_cast<int64_t>(ftn) * BN + h * COLS + cq) * KB;
             const uint32_t dst = tbl + b * (L::TBL_PART / 2);

@@ -8,7 +8,9 @@
 namespace fp8q {
 namespace gemm_util {
 
-constexpr int kGroupM = 8;   // tile raster: groups of 8 M-tiles share B tiles in L2
+// Tile raster: groups of GM M-tiles walk N together, so they share B tiles in L2 (8 for
+// the blockwise kernels' 256 x 128 tiles, 16 for the 256 x 256 per-tensor and MX tiles:
+// both measured side by side, per-tensor and MX 8192^3 +2 % with 16, blockwise -1 %).
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t d;
@@ -71,11 +73,12 @@ __device__ __forceinline__ int div_small(int a, int b) {
   return q;
 }
 
+template <int GM>
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
-  const int per_group = kGroupM * tiles_n;
+  const int per_group = GM * tiles_n;
   const int group = div_small(t, per_group);
-  const int first_m = group * kGroupM;
-  const int gsize = min(tiles_m - first_m, kGroupM);
+  const int first_m = group * GM;
+  const int gsize = min(tiles_m - first_m, GM);
   const int r = t - group * per_group;
   tn = div_small(r, gsize);
   tm = first_m + (r - tn * gsize);
