@@ -10,8 +10,9 @@
 // A 2-stage ring of 64 KB tiles is filled by TMA (four 32-column boxes, 128-byte
 // swizzle).  For each tile:
 //   row pass  -- warp w owns rows 8w .. 8w+7, lane l columns 4l .. 4l+3 (16-byte shared
-//                loads, conflict-free); a row's 1x128 amax is a warp max, a 1x32 MX
-//                block's a max over 8 lanes;
+//                loads, conflict-free); the 8 rows' 1x128 (or 1x32 MX block) maxima are
+//                reduce-scattered over the warp (or the block's 8 lanes), so each lane
+//                computes one scale, and the scales return by shuffles;
 //   col pass  -- warp w owns columns 32 (w % 4) + lane over rows 32 (w / 4) .. +31 (one
 //                MX block along the rows; scalar shared loads, conflict-free); a column's
 //                1x128 amax combines the four row quarters through shared memory;
@@ -135,31 +136,50 @@ __device__ __forceinline__ void cast_tile_f32(const CastParams& p, uint32_t xs, 
     }
   }
   if (p.do_row) {
+    // the scale of each of this lane's 8 rows
+    float sc[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = 8 * warp + i;
-      const int64_t grow = row0 + r;
-      float s = tile_scale;
+    for (int i = 0; i < 8; ++i) sc[i] = tile_scale;
+    if (RECIPE == kBlock1x128 || RECIPE == kMx) {
+      // Reduce-scatter the 8 rows' maxima: each exchange halves the rows a lane keeps, so
+      // one scale computation per lane serves a whole row (1x128: lanes 4r .. 4r+3 end with
+      // row r's maximum over the warp) or a whole 1x32 block (MX: lane 8b + r ends with row
+      // r's maximum over block b's 8 lanes); the scales then go back by shuffles.
+      constexpr int X0 = RECIPE == kMx ? 4 : 16, X1 = X0 / 2, X2 = X0 / 4;
+      const bool k0 = lane & X0, k1 = lane & X1, k2 = lane & X2;
+      float b4[4], b2[2];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        b4[k] = fmaxf(k0 ? a[k + 4] : a[k], __shfl_xor_sync(0xFFFFFFFFu, k0 ? a[k] : a[k + 4], X0));
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        b2[k] = fmaxf(k1 ? b4[k + 2] : b4[k], __shfl_xor_sync(0xFFFFFFFFu, k1 ? b4[k] : b4[k + 2], X1));
+      float m = fmaxf(k2 ? b2[1] : b2[0], __shfl_xor_sync(0xFFFFFFFFu, k2 ? b2[0] : b2[1], X2));
+      // the row this lane now holds: 4 k0 + 2 k1 + k2
+      const int rr = (k0 ? 4 : 0) + (k1 ? 2 : 0) + (k2 ? 1 : 0);
+      const int64_t grow = row0 + 8 * warp + rr;
+      float s_mine;
       if (RECIPE == kBlock1x128) {
-        s = scale_from_amax(warp_max(a[i]), fmax);
-        if (lane == 0 && grow < p.R) static_cast<float*>(p.s_row)[grow * nb128_c + tc] = recip_rn(s);
-      } else if (RECIPE == kMx) {
-        float m = a[i];
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        s_mine = scale_from_amax(m, fmax);
+        if ((lane & 3) == 0 && grow < p.R) static_cast<float*>(p.s_row)[grow * nb128_c + tc] = recip_rn(s_mine);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, s_mine, 4 * i);
+      } else {
         const int e = (p.mx_floor ? mx_exponent_floor(m, fexp) : mx_exponent(m, fexp));
-        s = pow2_neg(e);
+        s_mine = pow2_neg(e);
         const int64_t b = static_cast<int64_t>(tc) * 4 + (lane >> 3);
-        if ((lane & 7) == 0) {
-          if (p.mx_tiled)   // the tile's atom (both dims are multiples of 128)
-            sts8(sf + mx_atom_offset(r, lane >> 3), static_cast<uint32_t>(e + 127));
-          else if (grow < p.R && b < nb32_c)   // a tile hanging over C has blocks past the last one
-            static_cast<uint8_t*>(p.s_row)[grow * nb32_c + b] = static_cast<uint8_t>(e + 127);
-        }
+        if (p.mx_tiled)   // the tile's atom (both dims are multiples of 128)
+          sts8(sf + mx_atom_offset(8 * warp + rr, lane >> 3), static_cast<uint32_t>(e + 127));
+        else if (grow < p.R && b < nb32_c)   // a tile hanging over C has blocks past the last one
+          static_cast<uint8_t*>(p.s_row)[grow * nb32_c + b] = static_cast<uint8_t>(e + 127);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, s_mine, (lane & ~7) | i);
       }
-      sts32(q_addr(outR, r, 4 * lane), q4(v[i], s, e5));
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sts32(q_addr(outR, 8 * warp + i, 4 * lane), q4(v[i], sc[i], e5));
   }
   // ---------------- col pass
   if (p.do_col) {
