@@ -450,7 +450,7 @@ def run_per_recipe(fq, wl, dev, flush):
     # ---- the FP32 master copy of a weight quantized directly (binary32 input, 4 B read per element)
     out["cast_transpose_f32"] = {}
     w32 = wl.normal_bf16((8192, 8192), 7, 0.02, dev).float()
-    for rec in (R.TENSOR, R.BLOCK_128x128, R.MX_1x32_TILED):
+    for rec in (R.TENSOR, R.BLOCK_1x128, R.BLOCK_128x128, R.MX_1x32_TILED):
         sc = one if rec == R.TENSOR else None
         qr, sr, qc, scol = fq.cast_transpose(w32, rec, F.E4M3, sc)
         ms = time_kernel(lambda: fq.fp8_cast_transpose_f32(w32, rec, F.E4M3, sc, None, qr, sr, qc, scol), flush=flush)
