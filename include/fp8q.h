@@ -291,10 +291,12 @@ fp8_status fp8_allreduce_sum_noalloc(const void* g, int32_t k, int64_t n, fp8_fo
  * (BLOCK_1x128, BLOCK_1x128); (MX_1x32_TILED, MX_1x32_TILED).  Others return
  * FP8_ERR_UNSUPPORTED.  M, N, K must be multiples of 128 (FP8_ERR_SHAPE);
  * M or N == 0 is a no-op, K == 0 writes zeros.
- * Workspace: with (TENSOR, TENSOR) or (MX, MX) and M % 256 == 0, a GEMM whose last
- * wave of 256-row tiles would leave at least half of the CTA pairs idle (one partial
- * wave, or full ones and a partial one when K >= 8192) cuts that wave's tiles along K
- * and sums the ranges in a fixed order; it uses a workspace the library allocates on
+ * Workspace: with (TENSOR, TENSOR) or (MX, MX) and M % 256 == 0, a GEMM whose tiles
+ * do not fill a whole number of waves of CTA pairs may cut tiles along K (one to three
+ * full waves: every pair takes an equal share of the last tiles' K blocks; otherwise,
+ * when the last wave leaves at least half of the pairs idle, with one wave or with
+ * K >= 8192, that wave's tiles are cut into K ranges) and sums the parts of a tile in a
+ * fixed order; it uses a workspace the library allocates on
  * the first such call on `stream` (SMs / 2 slots of 256 KB and their counters, kept
  * for the process's lifetime; up to 16 streams a device).  A call on a stream that is
  * being captured and has none yet runs unsplit.  Results are deterministic either way

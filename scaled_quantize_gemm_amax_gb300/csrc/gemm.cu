@@ -219,23 +219,45 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   const int NG = KB / KSUB;   // stages per tile (K / 128 is a multiple of KSUB)
   const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);   // tile-walker index
   const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-  // This unit's work: whole tiles unit0, unit0 + units, ... below tail0, then (when the
+  // This unit's work.  Whole tiles unit0, unit0 + units, ... below tail0, then (when the
   // last partial wave is split) K range c = unit0 / ntail of tail tile tail0 + unit0 % ntail.
+  // Or (stream-K) whole tiles unit0, unit0 + units, ... below tail0, then the share
+  // [W unit0 / units, W (unit0 + 1) / units) of the W = (ntiles - tail0) * NG K blocks of the
+  // tiles from tail0 on, in tile order: a part of a tile at each end of the share, whole
+  // tiles between (a share is at least one tile long, so a tile has at most two parts).
+  // Both keep the tiles in flight at one time neighbours, which the raster needs for L2.
   constexpr bool SPLITK = PAIR && (KIND == kTensor || KIND == kMx);
-  const int split = SPLITK && p.split > 1 ? p.split : 1;
-  const int tail0 = split > 1 ? p.tail0 : ntiles;
+  const bool streamk = SPLITK && p.streamk != 0;
+  const int split = SPLITK && !streamk && p.split > 1 ? p.split : 1;
+  const int tail0 = split > 1 || streamk ? p.tail0 : ntiles;
   const int ntail = ntiles - tail0;
-  const int nfull = split > 1 ? tail0 / units : 0;
-  const int nwork = split > 1 ? nfull + (unit0 < ntail * split ? 1 : 0)
-                              : (unit0 < ntiles ? (ntiles - unit0 + units - 1) / units : 0);
+  const int nfull = split > 1 || streamk ? tail0 / units : 0;
+  const int64_t sk_w = static_cast<int64_t>(ntail) * NG;
+  const int64_t sk_s = streamk ? sk_w * unit0 / units : 0, sk_e = streamk ? sk_w * (unit0 + 1) / units : 0;
+  const int nwork = streamk    ? nfull + (sk_e > sk_s ? static_cast<int>((sk_e - 1) / NG - sk_s / NG + 1) : 0)
+                    : split > 1 ? nfull + (unit0 < ntail * split ? 1 : 0)
+                                : (unit0 < ntiles ? (ntiles - unit0 + units - 1) / units : 0);
   struct Work {
     int t, kg0, kg1;
-    int part;   // -1: the whole tile; 0: range 0, which adds the others; c > 0: range c, left in the workspace
+    int part;     // -1: the whole tile; 0: adds the other parts' slots to its own; 1: leaves its part in `slot`
+    int slot;     // part 1: its slot; part 0: the first slot it adds
+    int nslot;    // part 0: how many slots it adds, `sstride` apart
+    int sstride;
   };
   auto work_at = [&](int i) -> Work {
-    if (split == 1 || i < nfull) return Work{unit0 + i * units, 0, NG, -1};
-    const int c = unit0 / ntail;
-    return Work{tail0 + unit0 % ntail, c * NG / split, (c + 1) * NG / split, c};
+    if (streamk && i >= nfull) {
+      i -= nfull;
+      const int t = tail0 + static_cast<int>(sk_s / NG) + i;
+      const int kg0 = i == 0 ? static_cast<int>(sk_s % NG) : 0;
+      const int kg1 = t == tail0 + static_cast<int>((sk_e - 1) / NG) ? static_cast<int>((sk_e - 1) % NG) + 1 : NG;
+      if (kg0 > 0) return Work{t, kg0, kg1, 1, unit0, 0, 0};            // the later part of a tile begun by unit0 - 1
+      if (kg1 < NG) return Work{t, kg0, kg1, 0, unit0 + 1, 1, 0};       // the earlier part: adds unit0 + 1's slot
+      return Work{t, 0, NG, -1, 0, 0, 0};
+    }
+    if ((split == 1 && !streamk) || i < nfull) return Work{unit0 + i * units, 0, NG, -1, 0, 0, 0};
+    const int c = unit0 / ntail, j = unit0 % ntail;
+    if (c > 0) return Work{tail0 + j, c * NG / split, (c + 1) * NG / split, 1, (c - 1) * ntail + j, 0, 0};
+    return Work{tail0 + j, 0, NG / split, 0, j, split - 1, ntail};
   };
   const int64_t row_off = static_cast<int64_t>(rank) * kBM;   // this CTA's rows within a tile
 
@@ -954,20 +976,19 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         constexpr int CH = COLS / 32;
         if (SPLITK && w.part >= 0) {
           const int box_row = static_cast<int>(static_cast<int64_t>(tm) * TM + row_off) + 32 * q;
-          // A split tail tile (this unit's last work): 32 columns at a time straight from TMEM,
-          // the accumulator released at the end.  Range c > 0 leaves its raw FP32 values in its
-          // slot and counts its warps there; range 0 waits for every other range's count, adds
-          // their values in order, then scales and stores as a whole tile would.  Both CTAs'
-          // epilogue warps of a pair count on (and, for range 0, read) each slot.  A slot holds
-          // 16-byte pieces [column slice][chunk][piece][row of the tile], so a warp's 16-byte
-          // stores and loads cover 512 consecutive bytes.
+          // A part of a tile cut along K: 32 columns at a time straight from TMEM, the
+          // accumulator released at the end.  A part 1 leaves its raw FP32 values in its slot
+          // and counts its warps there; a part 0 (the tile's first K blocks) waits for each of
+          // its slots' counts, adds their values in order, then scales and stores as a whole
+          // tile would.  Both CTAs' epilogue warps of a pair count on (and, for part 0, read)
+          // a slot.  A slot holds 16-byte pieces [column slice][chunk][piece][row of the tile],
+          // so a warp's 16-byte stores and loads cover 512 consecutive bytes.
           constexpr int kSlotWarps = 2 * EPI;
-          const int j = w.t - tail0;
           if (w.part == 0) {
             bool got = true;
             if (lane == 0)
-              for (int cp = 1; cp < split && got; ++cp)
-                got = wait_count(p.ws_flags + (cp - 1) * ntail + j, kSlotWarps, p.err, kErrTimeoutMma);
+              for (int k = 0; k < w.nslot && got; ++k)
+                got = wait_count(p.ws_flags + w.slot + k * w.sstride, kSlotWarps, p.err, kErrTimeoutMma);
             if (!__shfl_sync(0xFFFFFFFFu, got, 0)) break;   // timed out: the error word says so
           }
           // float offset of 16-byte piece i of chunk c of this thread's row in slot `sl`
@@ -975,8 +996,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
             return ((static_cast<int64_t>(sl) * (BN / 4) + (h * CH + c) * 8 + i) * TM + row_off + row) * 4;
           };
           if (w.part > 0) {
-            // range c > 0: the thread's whole row slice from TMEM at once, then its pieces
-            const int sl = (w.part - 1) * ntail + j;
+            // the thread's whole row slice from TMEM at once, then its pieces
             uint32_t r[CH][32];
 #pragma unroll
             for (int c = 0; c < CH; ++c) tc_ld_32x32b_x32(col_base + 32 * c, r[c]);
@@ -986,13 +1006,13 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
             for (int c = 0; c < CH; ++c)
 #pragma unroll
               for (int i = 0; i < 8; ++i)
-                stg128(p.ws + piece(sl, c, i), r[c][4 * i], r[c][4 * i + 1], r[c][4 * i + 2], r[c][4 * i + 3]);
+                stg128(p.ws + piece(w.slot, c, i), r[c][4 * i], r[c][4 * i + 1], r[c][4 * i + 2], r[c][4 * i + 3]);
           } else {
-            // range 0: range 1's pieces of the next chunk are in flight while this chunk is
-            // summed (ranges 2.. are loaded as they are added)
+            // the first slot's pieces of the next chunk are in flight while this chunk is
+            // summed (further slots are loaded as they are added)
             float4 o[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = __ldcg(reinterpret_cast<const float4*>(p.ws + piece(j, 0, i)));
+            for (int i = 0; i < 8; ++i) o[i] = __ldcg(reinterpret_cast<const float4*>(p.ws + piece(w.slot, 0, i)));
             for (int c = 0; c < CH; ++c) {
               uint32_t rc[32];
               tc_ld_32x32b_x32(col_base + 32 * c, rc);
@@ -1007,10 +1027,11 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
               }
               if (c + 1 < CH) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) o[i] = __ldcg(reinterpret_cast<const float4*>(p.ws + piece(j, c + 1, i)));
+                for (int i = 0; i < 8; ++i)
+                  o[i] = __ldcg(reinterpret_cast<const float4*>(p.ws + piece(w.slot, c + 1, i)));
               }
-              for (int cp = 2; cp < split; ++cp) {
-                const int sl = (cp - 1) * ntail + j;
+              for (int k = 1; k < w.nslot; ++k) {
+                const int sl = w.slot + k * w.sstride;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                   const float4 e = __ldcg(reinterpret_cast<const float4*>(p.ws + piece(sl, c, i)));
@@ -1034,11 +1055,11 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           if (w.part > 0) {
             __threadfence();   // this thread's slot values, before the warp is counted
             __syncwarp();
-            if (lane == 0) atomicAdd(p.ws_flags + (w.part - 1) * ntail + j, 1);
+            if (lane == 0) atomicAdd(p.ws_flags + w.slot, 1);
           } else if (lane == 0) {
             // the last of the two pairs' warps to count on a slot (all have read it) resets it
-            for (int cp = 1; cp < split; ++cp) {
-              int* f = p.ws_flags + (cp - 1) * ntail + j;
+            for (int k = 0; k < w.nslot; ++k) {
+              int* f = p.ws_flags + w.slot + k * w.sstride;
               if (atomicAdd(f, 1) == 2 * kSlotWarps - 1) atomicExch(f, 0);
             }
           }
@@ -1095,6 +1116,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
 // none yet (or a full table, or a failed allocation) runs the GEMM unsplit.  Launches on
 // one stream are ordered, so they never share a workspace concurrently.
 constexpr int kMaxSplit = 8;
+constexpr bool kStreamK = true;
 constexpr int kMaxSplitStreams = 16;
 constexpr size_t kSplitSlotBytes = size_t(2 * kBM) * 256 * sizeof(float);
 struct SplitWorkspace {
@@ -1221,10 +1243,28 @@ cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUte
   GemmParams q = p;
   q.split = 1;
   q.tail0 = static_cast<int>(ntiles);
+  q.streamk = 0;
   q.ws = nullptr;
   q.ws_flags = nullptr;
   int64_t launched = ntiles < pairs ? ntiles : pairs;
-  if constexpr (KIND == kTensor || KIND == kMx) {
+  if constexpr ((KIND == kTensor || KIND == kMx) && kStreamK) {
+    // One to three full waves and a partial one: all but the last full wave as whole tiles,
+    // then every pair an equal share of the remaining tiles' K blocks (each share over one
+    // tile long).  With more waves the partial one costs less than the hand-overs (measured:
+    // MX 8192 x 12288 x 4096, 20 waves, 4 % slower).
+    if (ntiles > pairs && ntiles % pairs != 0 && ntiles / pairs <= 3) {
+      float* ws = nullptr;
+      int* flags = nullptr;
+      if (split_workspace(s, static_cast<int>(num_sms / 2), &ws, &flags)) {
+        q.streamk = 1;
+        q.tail0 = static_cast<int>((ntiles / pairs - 1) * pairs);
+        q.ws = ws;
+        q.ws_flags = flags;
+        launched = pairs;
+      }
+    }
+  }
+  if constexpr (KIND == kTensor || KIND == kMx) if (q.streamk == 0) {
     // A last wave that would leave at least half of the pairs idle is cut along K: its R
     // tiles into S ranges on R * S pairs (every pair resident, so the waits below end).
     // The hand-over of the ranges costs a few microseconds whatever K is, the time saved

@@ -150,6 +150,11 @@ struct GemmParams {
   // resets the count.  split = 1: off (tail0 = the tile count).
   int split;
   int tail0;
+  // Balanced division instead (streamk = 1, same kernels and workspace): the tiles' K
+  // blocks in order, cut into one contiguous share per pair; a tile cut between pairs u
+  // and u + 1 has its later part left in slot u + 1 by pair u + 1 (its first work) and
+  // added by pair u (its last work).
+  int streamk;
   float* ws;             // [slots][256][256] fp32
   int* ws_flags;         // [slots], 0 between launches
 };
