@@ -289,6 +289,7 @@ fp8_status scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const voi
   p.c_scale_inv = x.c_scale_inv;
   p.e5m2_c = x.fc == FP8_E5M2;
   p.err = d->err;
+  p.wide160 = gemm_select_wide(p, d->num_sms) ? 1 : 0;
   CUtensorMap tm_a, tm_b;
   if (!make_map(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128)) return FP8_ERR_CUDA;
   if (!make_map(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, static_cast<uint32_t>(gemm_b_box_rows(p))))
@@ -304,12 +305,16 @@ fp8_status scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const voi
       return FP8_ERR_CUDA;
   }
   // C leaves through TMA stores of 32-row x 128-byte boxes (all kernels but the blockwise
-  // ones with 128-deep stages, which store directly)
+  // ones with 128-deep stages, which store directly; the 160-wide blockwise tiles use
+  // unswizzled 32-row x 16-column boxes)
   CUtensorMap tm_c;
   std::memset(&tm_c, 0, sizeof(tm_c));
   if (C != nullptr) {
+    const uint32_t box_cols = static_cast<uint32_t>(gemm_c_box_cols(p));
     const bool ok = out == FP8_OUT_FP32
                         ? make_map(&tm_c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, 32, 32)
+                    : box_cols != 0
+                        ? make_map(&tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, N, M, box_cols, 32, CU_TENSOR_MAP_SWIZZLE_NONE)
                         : make_map(&tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, N, M, 64, 32);
     if (!ok) return FP8_ERR_CUDA;
   }

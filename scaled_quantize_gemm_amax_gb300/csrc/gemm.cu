@@ -90,6 +90,21 @@ template <>
 struct Cfg<kMx> {
   static constexpr int BN = 256, STAGES = 3, ACC = 1, EPI = 8, KSUB = 1, CTRL = 2;
 };
+// Blockwise 1x128 x 128x128 on 256 x 160 pair tiles with 128-deep stages (BF16 out, no
+// fused output cast), for K / 128 odd, where the 256-deep stages above do not fit and the
+// alternative is one CTA per 128 x 128 tile (measured: 1.10-1.34x faster than that).
+// Three 160-column partial buffers fill 480 of TMEM's 512 columns; a single MMA issuer
+// (a 256 x 160 x 32 MMA runs longer than the ~74 cycles one thread needs to issue it);
+// the promotion holds a whole partial (80 columns a thread) next to its 80 accumulators,
+// with registers from the control warpgroup as below.  (A 256 x N x 32 pair MMA costs
+// about 88 + 0.34 N cycles inside these kernels, so 160 columns would do 1.14x the work a
+// cycle of 128, but with K / 128 even this kernel ran at 0.55 of the FP8 peak at 8192^3
+// against 0.68 for the 256-deep stages, measured.)
+constexpr int kBlock160 = 7;
+template <>
+struct Cfg<kBlock160> {
+  static constexpr int BN = 160, STAGES = 6, ACC = 3, EPI = 8, KSUB = 1, CTRL = 4;
+};
 
 // CTRL = 4: warps 0..3 (producer, the two MMA issuers, an idle warp) form a warpgroup
 // that gives registers to the two epilogue warpgroups (warps 4..11) with setmaxnreg, so
@@ -100,13 +115,19 @@ struct Cfg<kMx> {
 constexpr int kSplitLaunchRegs = 168, kCtrlRegs = 72, kEpiRegs = 216;
 static_assert(128 * kCtrlRegs + 256 * kEpiRegs <= 384 * kSplitLaunchRegs, "register split exceeds the launch pool");
 static_assert(kCtrlRegs + 2 * kEpiRegs <= 512, "register split exceeds a sub-partition");
+// The 160-wide blockwise kernel: its single MMA issuer's loop needs more than 72 (it
+// spilled), its promotion less than 216.
+constexpr int kCtrlRegs160 = 80, kEpiRegs160 = 208;
+static_assert(128 * kCtrlRegs160 + 256 * kEpiRegs160 <= 384 * kSplitLaunchRegs, "register split exceeds the launch pool");
+static_assert(kCtrlRegs160 + 2 * kEpiRegs160 <= 512, "register split exceeds a sub-partition");
 
 // Stages of the 2-CTA (pair) variant: each CTA holds 128 rows of A and half of B
 // (blockwise with 256-deep stages: 48 KB a stage; three ran 3 % faster than four at
 // 4096^3 and 8192^3, measured).
 template <int KIND>
 constexpr int pair_stages() {
-  return Cfg<KIND>::KSUB == 2 ? 3 : (KIND == kMx ? 5 : (Cfg<KIND>::BN == 256 ? 6 : 8));
+  return KIND == kBlock160 ? Cfg<kBlock160>::STAGES
+                           : (Cfg<KIND>::KSUB == 2 ? 3 : (KIND == kMx ? 5 : (Cfg<KIND>::BN == 256 ? 6 : 8)));
 }
 
 template <int KIND, bool PAIR>
@@ -122,9 +143,11 @@ struct Layout {
   static constexpr uint32_t OFF_SF = S * STAGE_BYTES;
   // per-tensor / MX / blockwise with 256-deep stages: one 4 KB staging box per epilogue
   // warp for the TMA stores of C
-  // (32 rows x 128 B, 128-byte swizzle; the box must start on 1024 bytes)
+  // (32 rows x 128 B, 128-byte swizzle; the box must start on 1024 bytes).  The 160-wide
+  // blockwise tiles: five unswizzled 1 KB boxes a warp (32 rows x 16 BF16 columns each).
   static constexpr bool TSTORE = !(KIND == kBlock1x128 || KIND == kBlockRowsB);
-  static constexpr uint32_t STG_BYTES = TSTORE ? Cfg<KIND>::EPI * 4096 : 0;
+  static constexpr uint32_t STG_WARP = KIND == kBlock160 ? 5 * 1024 : 4096;
+  static constexpr uint32_t STG_BYTES = TSTORE ? Cfg<KIND>::EPI * STG_WARP : 0;
   static constexpr uint32_t OFF_STG = (OFF_SF + S * SF_BYTES + 1023) & ~1023u;
   // per-row B scales on CTA pairs: the tile's B-scale table, one part of [kb][COLS] floats
   // per epilogue warpgroup (its COLS columns)
@@ -183,7 +206,8 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
            const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
   using L = Layout<KIND, PAIR>;
   constexpr int BN = L::BN, S = L::S, ACC = Cfg<KIND>::ACC, EPI = Cfg<KIND>::EPI;
-  constexpr bool BLOCK = (KIND == kBlock1x128 || KIND == kBlockRowsB || KIND == kBlockK2 || KIND == kBlockK2RowsB);   // promotion path
+  constexpr bool BLOCK = (KIND == kBlock1x128 || KIND == kBlockRowsB || KIND == kBlockK2 || KIND == kBlockK2RowsB ||
+                          KIND == kBlock160);   // promotion path
   constexpr int KSUB = L::KSUB;
   constexpr int GROUPS = ACC / KSUB;   // partial-buffer groups (blockwise)
   static_assert(KSUB == 1 || BLOCK, "multi-block stages: blockwise only");
@@ -201,7 +225,8 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   static_assert(NISS == 1 || NISS == KSUB || SFCP, "MMA issuers");
   constexpr int CTRL = Cfg<KIND>::CTRL;                 // warps before the epilogue warps
   constexpr int ISS1 = CTRL == 4 ? 2 : 2 + EPI;         // warp of the second MMA issuer
-  constexpr bool WIDE = CTRL == 4;                      // 64-column partial loads (see Cfg)
+  constexpr bool REGSPLIT = CTRL == 4;                  // registers move to the epilogue (see Cfg)
+  constexpr bool WIDE = REGSPLIT && KIND != kBlock160;  // 64-column partial loads of 256-deep stages
   static_assert(!WIDE || (BLOCK && KSUB == 2 && COLS == 64 && B_ROWS == TABLE), "wide promotion layout");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -300,7 +325,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base_ptr + L::OFF_TMEM);
 
   if (warp < CTRL || (CTRL == 2 && NISS > 1 && warp == ISS1)) {
-  if constexpr (WIDE) setmaxnreg_dec<kCtrlRegs>();
+  if constexpr (REGSPLIT) setmaxnreg_dec<KIND == kBlock160 ? kCtrlRegs160 : kCtrlRegs>();
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------ producer
     pdl_wait();   // operands may come from the previous kernel in the stream
@@ -555,7 +580,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   }
   } else if (warp >= CTRL && warp < CTRL + EPI) {
     // ------------------------------------------------ epilogue
-    if constexpr (WIDE) setmaxnreg_inc<kEpiRegs>();
+    if constexpr (REGSPLIT) setmaxnreg_inc<KIND == kBlock160 ? kEpiRegs160 : kEpiRegs>();
     pdl_wait();   // scales and C: ordered after the previous kernel in the stream
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
     const int h = (warp - CTRL) >> 2;       // which COLS-wide slice of the tile's columns
@@ -605,7 +630,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     // lines (a thread per row storing its own 16 bytes would not).  Chunk c holds columns
     // [gcol + 32 c, gcol + 32 c + 32) of this thread's row; bf16 chunks go out in pairs.
     auto store_chunk = [&](const float (&v)[32], int c, int64_t gcol, int box_row) {
-      const uint32_t stg = base + L::OFF_STG + static_cast<uint32_t>(warp - CTRL) * 4096u;
+      const uint32_t stg = base + L::OFF_STG + static_cast<uint32_t>(warp - CTRL) * L::STG_WARP;
       if (fp32 || (c & 1) == 0) {
         // the box is free once the previous store from it has read it
         if (lane == 0) bulk_wait_read<0>();
@@ -649,7 +674,91 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
       tile_coords<kRasterM>(w.t, tiles_m, tiles_n, tm, tn);
       const int64_t grow = static_cast<int64_t>(tm) * TM + row_off + row;
       const int64_t gcol0 = static_cast<int64_t>(tn) * BN + h * COLS;
-      if constexpr (WIDE) {
+      if constexpr (KIND == kBlock160) {
+        // Promotion, one 128-deep partial per TMEM wait: this thread's 80 columns as five
+        // 16-column loads, issued together; the buffer goes back to the MMA issuer once they
+        // land and the FMAs follow while the MMAs refill it.  Tiles and their column halves
+        // start on multiples of 16 and B's scale blocks on multiples of 128, so a chunk lies
+        // in one block: its factor is sA[m, kb] * sB[nb, kb] (rounded once, then the FMA, as
+        // the other blockwise kernels), and this thread's columns span at most two blocks.
+        constexpr int NCH = COLS / 16;
+        const float* sa_row = static_cast<const float*>(p.sa) + grow * KB;
+        const int64_t nlast = (p.N - 1) / 128;   // columns past N (a ragged last tile) are never stored
+        const int64_t nb_lo = min(gcol0 / 128, nlast), nb_hi = min((gcol0 + COLS - 1) / 128, nlast);
+        const float* sb_lo = static_cast<const float*>(p.sb) + nb_lo * KB;
+        const float* sb_hi = static_cast<const float*>(p.sb) + nb_hi * KB;
+        const int64_t lo_cols = (nb_lo + 1) * 128 - gcol0;   // chunks [0, nlo) take the low block
+        const int nlo = lo_cols <= 0 ? 0 : (lo_cols >= COLS ? NCH : static_cast<int>(lo_cols / 16));
+        uint64_t acc[COLS / 2];
+#pragma unroll
+        for (int j = 0; j < COLS / 2; ++j) acc[j] = 0;
+        uint32_t r[NCH][16];
+        float sa_n = sa_row[0], sl_n = __ldg(sb_lo), sh_n = __ldg(sb_hi);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          const float sa_v = sa_n, sl_v = sl_n, sh_v = sh_n;
+          if (kb + 1 < KB) {
+            sa_n = sa_row[kb + 1];
+            sl_n = __ldg(sb_lo + kb + 1);
+            sh_n = __ldg(sb_hi + kb + 1);
+          }
+          const uint32_t b = part_it % GROUPS;
+          // warp-uniform decision: the TMEM loads that follow are .sync.aligned
+          if (!__all_sync(0xFFFFFFFFu,
+                          mbar_wait(base + L::OFF_TFULL + 8 * b, (part_it / GROUPS) & 1u, p.err, kErrTimeoutMma, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t col = lane_base + b * BN + h * COLS;
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) tc_ld_32x32b_x16(col + 16 * c, r[c]);
+          tc_wait_ld(r[0]);
+#pragma unroll
+          for (int c = 1; c < NCH; ++c) tc_tie(r[c]);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            // the stage that writes this buffer next is GROUPS stages later
+            const uint32_t next = part_it + GROUPS;
+            if (next < total_groups) release(base + L::OFF_FULL + 8 * (next % S));
+          }
+          ++part_it;
+          const float fl = sa_v * sl_v, fh = sa_v * sh_v;
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            const float f1 = c < nlo ? fl : fh;
+            const uint64_t f = pack_f32x2(f1, f1);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[8 * c + j] = fma_f32x2(f, pack_f32x2(r[c][2 * j], r[c][2 * j + 1]), acc[8 * c + j]);
+          }
+        }
+        if (!ok) break;
+        // C: this warp's 32 rows x 80 columns staged as five 32-row x 16-column boxes
+        // (32-byte rows), each leaving by one TMA store unless it lies past N
+        const int box_row = static_cast<int>(static_cast<int64_t>(tm) * TM + row_off) + 32 * q;
+        const uint32_t stg = base + L::OFF_STG + static_cast<uint32_t>(warp - CTRL) * L::STG_WARP;
+        if (lane == 0) bulk_wait_read<0>();   // the previous tile's stores have read the boxes
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) unpack_f32x2(acc[8 * c + j], v[2 * j], v[2 * j + 1]);
+          const uint32_t rowb = stg + static_cast<uint32_t>(c) * 1024u + static_cast<uint32_t>(lane) * 32u;
+          sts128(rowb, pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+          sts128(rowb + 16u, pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]), pack_bf16(v[12], v[13]),
+                 pack_bf16(v[14], v[15]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int c = 0; c < NCH; ++c)
+            if (gcol0 + 16 * c < p.N) tma_store_2d(&tm_c, stg + static_cast<uint32_t>(c) * 1024u, static_cast<int>(gcol0 + 16 * c), box_row);
+          bulk_commit();
+        }
+      } else if constexpr (WIDE) {
         // Promotion, one partial group (two 128-deep partials; this thread's 64 columns
         // of each: four 32-column loads) per TMEM wait.  All four loads are issued
         // together and the group goes back to the MMA issuers as soon as they land;
@@ -1293,9 +1402,20 @@ cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUte
 
 }  // namespace
 
+bool gemm_select_wide(const GemmParams& p, int num_sms) {
+  if (p.kind != kBlock1x128 || p.b_1x128 || p.out_fp32 || p.c == nullptr || p.cq != nullptr || p.c_amax != nullptr)
+    return false;
+  if (p.M % (2 * kBM) != 0 || num_sms < 2) return false;
+  // The other pair kernel needs K / 128 even (else one CTA per 128 x 128 tile, slower).
+  return (p.K / kBK) % 2 != 0;
+}
+
 int gemm_block_n(const GemmParams& p) {
+  if (p.wide160) return Cfg<kBlock160>::BN;
   return p.kind == kBlock1x128 ? Cfg<kBlock1x128>::BN : (p.kind == kMx ? Cfg<kMx>::BN : Cfg<kTensor>::BN);
 }
+
+int gemm_c_box_cols(const GemmParams& p) { return p.wide160 ? 16 : 0; }
 
 // CTA pairs need M a multiple of 256.  Blockwise runs on pairs only with 256-deep
 // stages (K / 128 even) and 128x128 B scales: there each stage's two partials go to
@@ -1305,6 +1425,7 @@ int gemm_block_n(const GemmParams& p) {
 // made the blockwise pair 40 % slower (measured).
 bool gemm_uses_pair(const GemmParams& p) {
   if (p.M % (2 * kBM) != 0) return false;
+  if (p.wide160) return true;
   if (p.kind == kBlock1x128) return (p.K / kBK) % 2 == 0 && (!p.b_1x128 || p.K / kBK <= kMaxTableKb);
   return true;
 }
@@ -1322,6 +1443,8 @@ cudaError_t launch_gemm_q(const GemmParams& p, const CUtensorMap& tm_a, const CU
       if (p.b_1x128)
         return gemm_uses_pair(p) ? launch_pair<kBlockK2RowsB, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s)
                                  : launch_kind<kBlockRowsB, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);
+      if constexpr (!QOUT)
+        if (p.wide160) return launch_pair<kBlock160, false>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);
       if (gemm_uses_pair(p)) return launch_pair<kBlockK2, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);
       return (p.K / kBK) % 2 == 0 ? launch_kind<kBlockK2, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s)
                                   : launch_kind<kBlock1x128, QOUT>(p, tm_a, tm_b, tm_sfa, tm_sfb, tm_c, num_sms, s);

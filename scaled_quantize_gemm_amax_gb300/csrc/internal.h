@@ -157,13 +157,23 @@ struct GemmParams {
   int streamk;
   float* ws;             // [slots][256][256] fp32
   int* ws_flags;         // [slots], 0 between launches
+  // Blockwise 1x128 x 128x128 on 256 x 160 pair tiles (set by gemm_select_wide)
+  int wide160;
 };
+// Whether the blockwise 1x128 x 128x128 GEMM these parameters describe runs on 256 x 160
+// pair tiles with 128-deep stages (BF16 out, no fused output cast, M % 256 == 0, K / 128
+// odd); the caller stores the answer in p.wide160 before asking for the tile shape and
+// building the tensor maps.
+bool gemm_select_wide(const GemmParams& p, int num_sms);
 // Width (N) of one output tile of the GEMM variant these parameters select.
 int gemm_block_n(const GemmParams& p);
 // Whether the GEMM runs on 2-CTA pairs (256-row tiles) for these parameters.
 bool gemm_uses_pair(const GemmParams& p);
 // Rows of B one TMA box carries (the tile width, or half of it for a pair).
 int gemm_b_box_rows(const GemmParams& p);
+// Columns of C one TMA store box carries: 16 (BF16, unswizzled) for the 160-wide tiles,
+// else 0: the usual 128-byte box (64 BF16 or 32 FP32 columns, 128-byte swizzle).
+int gemm_c_box_cols(const GemmParams& p);
 // tm_sfa / tm_sfb: MX only (the tiled E8M0 buffers as [atoms * 2, 256] bytes, box 2 x 256).
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
                         const CUtensorMap& tm_sfb, const CUtensorMap& tm_c, int num_sms, cudaStream_t s);

@@ -256,6 +256,10 @@ __device__ __forceinline__ void tc_tie(uint32_t (&r)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
 }
+__device__ __forceinline__ void tc_tie(uint32_t (&r)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(r[i]));
+}
 __device__ __forceinline__ void tc_ld_32x32b(uint32_t taddr, uint32_t (&r)[32]) { tc_ld_32x32b_x32(taddr, r); }
 __device__ __forceinline__ void tc_ld_32x32b(uint32_t taddr, uint32_t (&r)[16]) { tc_ld_32x32b_x16(taddr, r); }
 

@@ -136,8 +136,8 @@ def test_gemm_k_zero_writes_zeros():
 @pytest.mark.parametrize("ra,rb", PAIRS)
 @pytest.mark.parametrize("m,n,k", [(256, 256, 128), (512, 640, 384), (768, 384, 256)])
 def test_gemm_cta_pair_tiles(ra, rb, m, n, k):
-    # M a multiple of 256: 2-CTA pairs (blockwise: pairs when K / 128 is even, single CTAs
-    # for K = 128 and 384)
+    # M a multiple of 256: 2-CTA pairs (blockwise with K = 128 and 384: 160-wide pair tiles
+    # with BF16 output, single CTAs with FP32 output)
     x = wl.normal_bf16((m, k), 40, 1.0)
     w = wl.normal_bf16((n, k), 41, 0.02)
     gemm_check(x, w, ra, rb, F.E4M3, F.E5M2 if k == 384 else F.E4M3,
@@ -148,12 +148,13 @@ def test_gemm_cta_pair_tiles(ra, rb, m, n, k):
     (2048, 1536, 512, fq.OutDtype.BF16),    # CTA pairs: 96 tiles of 256x128, more than pairs
     (2048, 1408, 512, fq.OutDtype.BF16),    # CTA pairs, N % 256 == 128
     (512, 256, 2048, fq.OutDtype.BF16),     # a long K that wraps the stage ring many times
-    (768, 1024, 640, fq.OutDtype.FP32),     # odd K blocks: single CTAs, FP32 output
-    (1536, 2304, 1152, fq.OutDtype.BF16),   # odd K blocks over 216 single-CTA tiles
+    (768, 1024, 640, fq.OutDtype.FP32),     # odd K blocks, FP32 output: single CTAs
+    (1536, 2304, 1152, fq.OutDtype.BF16),   # odd K blocks, BF16 output: 90 pair tiles 160 wide
 ])
 def test_gemm_blockwise_pairs_many_tiles(m, n, k, out):
-    # blockwise with M % 256 == 0: CTA pairs with 256-deep stages when K / 128 is even,
-    # single CTAs otherwise; each pair (CTA) walks several tiles
+    # blockwise with M % 256 == 0: CTA pairs with 256-deep stages when K / 128 is even;
+    # otherwise 160-wide pair tiles with 128-deep stages (BF16 output) or single CTAs
+    # (FP32 output); each pair (CTA) walks several tiles
     x = wl.normal_bf16((m, k), 50, 1.0)
     w = wl.normal_bf16((n, k), 51, 0.02)
     gemm_check(x, w, R.BLOCK_1x128, R.BLOCK_128x128, F.E4M3, F.E4M3, out=out)
@@ -203,6 +204,42 @@ def test_gemm_blockwise_128x128_b_tile_spread(m, n, k):
     x = tile_spread(wl.normal_bf16((m, k), 70, 1.0), 1, 128, 1, 3)
     w = tile_spread(wl.normal_bf16((n, k), 71, 0.02), 128, 128, 4, 3)
     gemm_check(x, w, R.BLOCK_1x128, R.BLOCK_128x128, F.E4M3, F.E4M3, out=fq.OutDtype.FP32)
+
+
+@pytest.mark.parametrize("m,n,k,spread", [
+    (2048, 4096, 640, False),    # 26 tiles of 160 columns a row of tiles, the last one 96 wide
+    (4096, 2176, 384, True),     # last tile 96 wide; thread slices spanning two 128-column blocks
+    (2048, 2560, 1152, True),    # N a multiple of 160: 128 tiles, two per pair
+    (1536, 2304, 1152, False),   # 15 tiles a row, the last one 64 wide
+    (512, 640, 384, False),      # a single wave
+])
+def test_gemm_blockwise_160_wide_tiles(m, n, k, spread):
+    # 1x128 x 128x128 with BF16 output, M % 256 == 0 and K / 128 odd: 256 x 160 pair tiles
+    # with 128-deep stages.  Spread: every 128x128 tile of B scaled by its own power of two
+    # (2^-2..2^2), so that a B scale from the wrong column block or k-block moves the
+    # relative Frobenius error far past 1e-2; the exact product rounded to BF16 alone uses
+    # 0.70 / 0.62 of the max-abs bar at these shapes (oracle).
+    x = wl.normal_bf16((m, k), 74, 1.0)
+    w = wl.normal_bf16((n, k), 75, 0.02)
+    if spread:
+        w = tile_spread(w, 128, 128, 4, 2)
+    gemm_check(x, w, R.BLOCK_1x128, R.BLOCK_128x128, F.E4M3, F.E4M3)
+
+
+@pytest.mark.parametrize("m,n,k", [(2048, 4096, 640), (4096, 1920, 1152)])
+def test_gemm_blockwise_160_matches_single_cta(m, n, k):
+    # K / 128 odd: the 160-wide pair tiles (BF16 output) and the single-CTA 128 x 128 tiles
+    # (FP32 output) add the same promoted partials in the same k-block order, so the BF16
+    # result is the FP32 one rounded to nearest even, bit for bit.
+    x = tile_spread(wl.normal_bf16((m, k), 76, 1.0), 1, 128, 2, 2)
+    w = tile_spread(wl.normal_bf16((n, k), 77, 0.02), 128, 128, 3, 2)
+    qa, sa, _, _ = fq.cast_transpose(x, R.BLOCK_1x128, F.E4M3, row=True, col=False)
+    qb, sb, _, _ = fq.cast_transpose(w, R.BLOCK_128x128, F.E4M3, row=True, col=False)
+    c16 = fq.scaled_gemm(qa, F.E4M3, R.BLOCK_1x128, sa, qb, F.E4M3, R.BLOCK_128x128, sb, out=fq.OutDtype.BF16)
+    c32 = fq.scaled_gemm(qa, F.E4M3, R.BLOCK_1x128, sa, qb, F.E4M3, R.BLOCK_128x128, sb, out=fq.OutDtype.FP32)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    assert torch.equal(c16.view(torch.int16), c32.to(torch.bfloat16).view(torch.int16))
 
 
 @pytest.mark.parametrize("m,n,k", [
