@@ -68,3 +68,32 @@ def test_cast_multi_equals_single_calls_on_the_blockwise_workload():
     assert_status_ok()
     for a, b in zip((mx_, ms_, mxt, mst, mw, mws, mwt, mwst), sx + sw):
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+@pytest.mark.parametrize("recipes,fmts,shapes", [
+    ((R.BLOCK_1x128, R.BLOCK_128x128), (F.E4M3, F.E5M2), ((384, 640), (256, 384))),
+    ((R.BLOCK_1x128, R.BLOCK_128x128), (F.E4M3, F.E4M3), ((2048, 1536), (1536, 2048))),
+    ((R.MX_1x32_TILED, R.MX_1x32_TILED), (F.E4M3, F.E5M2), ((256, 384), (384, 256))),
+    ((R.TENSOR, R.TENSOR), (F.E5M2, F.E4M3), ((128, 512), (384, 384))),
+])
+def test_cast_multi_two_job_pairings(recipes, fmts, shapes):
+    # Two jobs whose recipes form a common pairing run in a kernel compiled for that pair
+    # (each tile reads its job's parameters at fixed places); job 1's tiles follow job 0's
+    # on every CTA, so the per-job amax hand-over is exercised where a CTA holds both.
+    xs = [wl.normal_bf16(shapes[0], 84, 1.0), wl.normal_bf16(shapes[1], 85, 0.5)]
+    xs[1][:, 3] *= 50.0
+    scales, scale_nps = [], []
+    for x, r, f in zip(xs, recipes, fmts):
+        if r == R.TENSOR:
+            s_np = oracle.tensor_scale(oracle.amax(bits16(x)), int(f))[0]
+            scales.append(torch.tensor([s_np], dtype=torch.float32, device="cuda"))
+            scale_nps.append(s_np)
+        else:
+            scales.append(None)
+            scale_nps.append(None)
+    amaxes = [torch.full((1,), 7.0, device="cuda"), torch.full((1,), 7.0, device="cuda")]
+    outs = fq.cast_transpose_multi(list(zip(xs, recipes, fmts, scales, amaxes)))
+    torch.cuda.synchronize()
+    assert_status_ok()
+    for x, r, f, s_np, am, o in zip(xs, recipes, fmts, scale_nps, amaxes, outs):
+        check_job(x, r, f, s_np, o, am)
