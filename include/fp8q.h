@@ -292,8 +292,9 @@ fp8_status fp8_allreduce_sum_noalloc(const void* g, int32_t k, int64_t n, fp8_fo
  * FP8_ERR_UNSUPPORTED.  M, N, K must be multiples of 128 (FP8_ERR_SHAPE);
  * M or N == 0 is a no-op, K == 0 writes zeros.
  * Workspace: with (TENSOR, TENSOR) or (MX, MX) and M % 256 == 0, a GEMM whose tiles
- * do not fill a whole number of waves of CTA pairs may cut tiles along K (one to three
- * full waves: every pair takes an equal share of the last tiles' K blocks; otherwise,
+ * do not fill a whole number of waves of CTA pairs may cut tiles along K (two or three
+ * full waves, or one when K >= 8192: every pair takes an equal share of the last tiles'
+ * K blocks; otherwise,
  * when the last wave leaves at least half of the pairs idle, with one wave or with
  * K >= 8192, that wave's tiles are cut into K ranges) and sums the parts of a tile in a
  * fixed order; it uses a workspace the library allocates on

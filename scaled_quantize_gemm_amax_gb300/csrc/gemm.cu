@@ -1357,11 +1357,14 @@ cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUte
   q.ws_flags = nullptr;
   int64_t launched = ntiles < pairs ? ntiles : pairs;
   if constexpr ((KIND == kTensor || KIND == kMx) && kStreamK) {
-    // One to three full waves and a partial one: all but the last full wave as whole tiles,
+    // Two or three full waves and a partial one: all but the last full wave as whole tiles,
     // then every pair an equal share of the remaining tiles' K blocks (each share over one
     // tile long).  With more waves the partial one costs less than the hand-overs (measured:
-    // MX 8192 x 12288 x 4096, 20 waves, 4 % slower).
-    if (ntiles > pairs && ntiles % pairs != 0 && ntiles / pairs <= 3) {
+    // MX 8192 x 12288 x 4096, 20 waves, 4 % slower).  With one full wave every tile is
+    // shared: worth it for K >= 8192 (2560 x 2304 x 8192: 0.54 -> 0.61 against the K-range
+    // cut), not at K = 4096 (MX 2048 x 4096 x 4096: 0.55 -> 0.50 against whole tiles).
+    const int64_t waves = ntiles / pairs;
+    if (ntiles > pairs && ntiles % pairs != 0 && waves <= 3 && (waves >= 2 || p.K / kBK >= 64)) {
       float* ws = nullptr;
       int* flags = nullptr;
       if (split_workspace(s, static_cast<int>(num_sms / 2), &ws, &flags)) {

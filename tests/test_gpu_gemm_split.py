@@ -1,9 +1,10 @@
 """The partial last wave of the per-tensor and MX GEMMs on CTA pairs, cut along K on
-otherwise idle pairs: with one to three full waves, all but the last full wave run as
-whole tiles and every pair then takes an equal share of the remaining tiles' K blocks
-(stream-K: a tile cut between two pairs is finished by the first, which adds the second's
-FP32 values); with one partial wave only, or with K >= 8192 and more waves, the last
-wave's tiles are cut into K ranges that range 0 adds in order.  Parity with the oracle on
+otherwise idle pairs: with two or three full waves (or one, when K >= 8192), all but the
+last full wave run as whole tiles and every pair then takes an equal share of the
+remaining tiles' K blocks (stream-K: a tile cut between two pairs is finished by the
+first, which adds the second's FP32 values); with one partial wave only, or with
+K >= 8192 and more waves, the last wave's tiles are cut into K ranges that range 0 adds
+in order.  Parity with the oracle on
 shapes of each kind, bit-identical results from repeated launches (the per-slot counters
 are back at zero after every launch) and from two streams running at once (each stream
 has its own workspace).  The wave counts assume the 76 resident pairs of a 152-SM part;
@@ -33,6 +34,7 @@ SPLIT_PAIRS = [(R.TENSOR, R.TENSOR), (R.MX_1x32_TILED, R.MX_1x32_TILED)]
     (256, 256, 4096, fq.OutDtype.BF16),     # one tile, 32 k-blocks: 8 ranges of 4
     (512, 384, 640, fq.OutDtype.FP32),      # 4 tiles (N ragged: half of the second column of tiles), 5 ranges
     (2560, 2304, 8192, fq.OutDtype.BF16),   # 90 tiles, one full wave: stream-K shares of 7.6 tiles' K blocks
+    (2560, 2304, 4096, fq.OutDtype.BF16),   # the same with K = 4096: whole tiles
     (4096, 4096, 512, fq.OutDtype.FP32),    # 256 tiles, three full waves: two whole, then shares of 1.4 tiles
     (8192, 6144, 8192, fq.OutDtype.BF16),   # 768 tiles, ten full waves and 8 tail tiles in 8 ranges
     (4608, 4608, 512, fq.OutDtype.FP32),    # 324 tiles, four full waves, K < 8192: not cut
