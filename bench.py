@@ -48,7 +48,7 @@ KERNEL_REPS = 50          # event-timed launches per kernel figure (median repor
 SUSTAIN_S = 1.5           # back-to-back steps after the timed region, for the clock record
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one blockwise GEMM launch at
 # 4096^3 from an ncu capture of the current kernel version; None when not captured for it
-TRAFFIC_GEMM = 34_124_544 + 2_114_816
+TRAFFIC_GEMM = 34_121_472 + 2_049_536
 
 
 def peaks():
