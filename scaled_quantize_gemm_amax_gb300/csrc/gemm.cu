@@ -257,9 +257,21 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   const int tail0 = split > 1 || streamk ? p.tail0 : ntiles;
   const int ntail = ntiles - tail0;
   const int nfull = split > 1 || streamk ? tail0 / units : 0;
-  const int64_t sk_w = static_cast<int64_t>(ntail) * NG;
-  const int64_t sk_s = streamk ? sk_w * unit0 / units : 0, sk_e = streamk ? sk_w * (unit0 + 1) / units : 0;
-  const int nwork = streamk    ? nfull + (sk_e > sk_s ? static_cast<int>((sk_e - 1) / NG - sk_s / NG + 1) : 0)
+  // The share's first tile and K block and its last tile and end, divided out once here: the
+  // 64-bit divisions cost the single MMA-issuing thread 0.5-1.4 us at each work item of the
+  // share when done there (measured), with the tensor core idle.
+  int sk_t0 = 0, sk_kg0 = 0, sk_t1 = -1, sk_kg1 = 0;
+  if (streamk) {
+    const int64_t sk_w = static_cast<int64_t>(ntail) * NG;
+    const int64_t sk_s = sk_w * unit0 / units, sk_e = sk_w * (unit0 + 1) / units;
+    if (sk_e > sk_s) {
+      sk_t0 = tail0 + static_cast<int>(sk_s / NG);
+      sk_kg0 = static_cast<int>(sk_s % NG);
+      sk_t1 = tail0 + static_cast<int>((sk_e - 1) / NG);
+      sk_kg1 = static_cast<int>((sk_e - 1) % NG) + 1;
+    }
+  }
+  const int nwork = streamk    ? nfull + (sk_t1 >= sk_t0 ? sk_t1 - sk_t0 + 1 : 0)
                     : split > 1 ? nfull + (unit0 < ntail * split ? 1 : 0)
                                 : (unit0 < ntiles ? (ntiles - unit0 + units - 1) / units : 0);
   struct Work {
@@ -272,9 +284,9 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   auto work_at = [&](int i) -> Work {
     if (streamk && i >= nfull) {
       i -= nfull;
-      const int t = tail0 + static_cast<int>(sk_s / NG) + i;
-      const int kg0 = i == 0 ? static_cast<int>(sk_s % NG) : 0;
-      const int kg1 = t == tail0 + static_cast<int>((sk_e - 1) / NG) ? static_cast<int>((sk_e - 1) % NG) + 1 : NG;
+      const int t = sk_t0 + i;
+      const int kg0 = i == 0 ? sk_kg0 : 0;
+      const int kg1 = t == sk_t1 ? sk_kg1 : NG;
       if (kg0 > 0) return Work{t, kg0, kg1, 1, unit0, 0, 0};            // the later part of a tile begun by unit0 - 1
       if (kg1 < NG) return Work{t, kg0, kg1, 0, unit0 + 1, 1, 0};       // the earlier part: adds unit0 + 1's slot
       return Work{t, 0, NG, -1, 0, 0, 0};
@@ -1105,12 +1117,17 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
             return ((static_cast<int64_t>(sl) * (BN / 4) + (h * CH + c) * 8 + i) * TM + row_off + row) * 4;
           };
           if (w.part > 0) {
-            // the thread's whole row slice from TMEM at once, then its pieces
+            // the thread's whole row slice from TMEM at once; the accumulator goes back to the
+            // MMA issuer before the pieces are stored (with one accumulator, MX, its next work
+            // item waited ~2.6 us for these stores, measured)
             uint32_t r[CH][32];
 #pragma unroll
             for (int c = 0; c < CH; ++c) tc_ld_32x32b_x32(col_base + 32 * c, r[c]);
 #pragma unroll
             for (int c = 0; c < CH; ++c) tc_wait_ld(r[c]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) release(base + L::OFF_TEMPTY + 8 * a);
 #pragma unroll
             for (int c = 0; c < CH; ++c)
 #pragma unroll
@@ -1158,9 +1175,11 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
               if (p.c != nullptr) store_chunk(v, c, gcol0, box_row);
             }
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) release(base + L::OFF_TEMPTY + 8 * a);
+          if (w.part == 0) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) release(base + L::OFF_TEMPTY + 8 * a);
+          }
           if (w.part > 0) {
             __threadfence();   // this thread's slot values, before the warp is counted
             __syncwarp();
