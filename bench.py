@@ -463,6 +463,8 @@ def run_per_recipe(fq, wl, dev, flush):
               ("tensor_8192", R.TENSOR, R.TENSOR, (8192, 8192, 8192), F.E4M3, F.E4M3, O.BF16),
               ("blockwise_4096", R.BLOCK_1x128, R.BLOCK_128x128, (4096, 4096, 4096), F.E4M3, F.E4M3, O.BF16),
               ("blockwise_8192", R.BLOCK_1x128, R.BLOCK_128x128, (8192, 8192, 8192), F.E4M3, F.E4M3, O.BF16),
+              # K / 128 odd: the 256 x 160 pair tiles with 128-deep stages
+              ("blockwise_4096x4096x4224", R.BLOCK_1x128, R.BLOCK_128x128, (4096, 4096, 4224), F.E4M3, F.E4M3, O.BF16),
               ("blockwise_wgrad_4096", R.BLOCK_1x128, R.BLOCK_1x128, (4096, 4096, 4096), F.E4M3, F.E4M3, O.FP32),
               ("blockwise_wgrad_8192", R.BLOCK_1x128, R.BLOCK_1x128, (8192, 8192, 8192), F.E4M3, F.E4M3, O.FP32),
               ("mx_4096", R.MX_1x32_TILED, R.MX_1x32_TILED, (4096, 4096, 4096), F.E4M3, F.E4M3, O.BF16),
