@@ -347,6 +347,22 @@ fp8_status fp8_get_device_status(cudaStream_t stream);
  */
 fp8_status fp8_debug_wait_timeout(cudaStream_t stream);
 
+/*
+ * fp8_debug_gemm_plan -- how fp8_scaled_gemm (fused != 0: fp8_scaled_gemm_amax with an
+ * FP8 copy of C) would divide an M x N x K product with these recipes and output type on
+ * a device with `num_sms` SMs of which `resident_pairs` 2-CTA clusters fit at once (0: no
+ * limit): host logic only, no device call.  Writes plan[0..7] = {CTA pairs (0/1), kernel
+ * variant (0 per-tensor, 1 blockwise one CTA 128-deep stages, 3 MXFP8, 4 blockwise per-row
+ * B one CTA, 5 blockwise 256-deep stages, 6 blockwise per-row B pairs, 7 blockwise 256 x
+ * 160 pair tiles), tile width, tile count, stream-K (0/1), K ranges of the last wave (1:
+ * uncut), first tile shared or cut, CTAs or pairs launched}.  A stream-K or K-range plan
+ * also needs the per-stream workspace; a real call without one runs whole tiles.  Errors
+ * as fp8_scaled_gemm's argument checks; `plan` (8 int64, host memory) is the caller's.
+ * Exists to test the dispatch rules without a GPU.
+ */
+fp8_status fp8_debug_gemm_plan(fp8_recipe ra, fp8_recipe rb, fp8_out_dtype out, int64_t M, int64_t N, int64_t K,
+                               int32_t fused, int32_t num_sms, int32_t resident_pairs, int64_t* plan);
+
 /* Human-readable name of a status code (static storage). */
 const char* fp8_status_string(fp8_status status);
 

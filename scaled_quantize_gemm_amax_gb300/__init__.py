@@ -11,7 +11,7 @@ Entry points with the C names take tensors (or None for NULL) and raise
 ``amax_history_update``, ``fp8_quantize``, ``fp8_cast_transpose``, ``fp8_cast_transpose_f32``,
 ``fp8_cast_transpose_multi``,
 ``fp8_dequantize``, ``fp8_allreduce_sum``, ``fp8_scaled_gemm``, ``fp8_scaled_gemm_amax``,
-``fp8_get_device_status``, ``fp8_debug_wait_timeout``.  ``cast_transpose`` /
+``fp8_get_device_status``, ``fp8_debug_wait_timeout``, ``fp8_debug_gemm_plan``.  ``cast_transpose`` /
 ``dequantize`` / ``scaled_gemm`` / ``scaled_gemm_amax`` are allocation helpers
 over them; ``linear`` holds the FP8 linear layer and the autocast scope built
 on these calls.
@@ -30,7 +30,7 @@ __all__ = [
     "fp8_cast_transpose_f32",
     "fp8_cast_transpose_multi", "CastJob",
     "fp8_dequantize", "fp8_allreduce_sum", "fp8_allreduce_sum_noalloc", "fp8_scaled_gemm", "fp8_scaled_gemm_amax", "fp8_get_device_status",
-    "fp8_debug_wait_timeout", "fp8_status_string",
+    "fp8_debug_wait_timeout", "fp8_debug_gemm_plan", "fp8_status_string",
     "scale_shape", "cast_transpose", "cast_transpose_multi", "dequantize", "allreduce_sum", "scaled_gemm", "scaled_gemm_amax",
     "DelayedScaling",
 ]
@@ -110,6 +110,7 @@ _SIGNATURES = {
     "fp8_scaled_gemm_amax": [_P, _E, _E, _P, _P, _E, _E, _P, _I64, _I64, _I64, _P, _E, _P, _P, _E, _P, _P, _P],
     "fp8_get_device_status": [_P],
     "fp8_debug_wait_timeout": [_P],
+    "fp8_debug_gemm_plan": [_E, _E, _E, _I64, _I64, _I64, _I32, _I32, _I32, _P],
     "fp8_status_string": [_E],
 }
 
@@ -280,6 +281,21 @@ def fp8_get_device_status(stream=None) -> Status:
 
 def fp8_debug_wait_timeout(stream=None):
     _check("fp8_debug_wait_timeout", load_library().fp8_debug_wait_timeout(_stream(stream)))
+
+
+GEMM_VARIANTS = {0: "per-tensor", 1: "blockwise, one CTA, 128-deep stages", 3: "MXFP8",
+                 4: "blockwise per-row B, one CTA", 5: "blockwise, 256-deep stages",
+                 6: "blockwise per-row B, CTA pairs", 7: "blockwise, 256 x 160 pair tiles"}
+
+
+def fp8_debug_gemm_plan(ra, rb, out, m: int, n: int, k: int, fused: bool = False, num_sms: int = 152,
+                        resident_pairs: int = 0) -> dict:
+    """The division fp8_scaled_gemm would choose (host logic only, no device call)."""
+    plan = (ctypes.c_int64 * 8)()
+    _check("fp8_debug_gemm_plan", load_library().fp8_debug_gemm_plan(int(ra), int(rb), int(out), m, n, k, int(fused),
+                                                                      num_sms, resident_pairs, plan))
+    keys = ("pair", "variant", "block_n", "tiles", "streamk", "split", "tail0", "launched")
+    return dict(zip(keys, (int(v) for v in plan)))
 
 
 # ------------------------------------------------------------------ allocation helpers

@@ -216,6 +216,27 @@ struct GemmExtra {
   float* c_scale_inv = nullptr;
 };
 
+// The GEMM kind of a recipe pairing (the guide's pairings: per-tensor x per-tensor,
+// 1x128 x 128x128, 1x128 x 1x128 for the weight gradient, MXFP8 x MXFP8 in the tiled layout).
+fp8_status gemm_kind(fp8_recipe ra, fp8_recipe rb, int* kind, int* b_1x128) {
+  *b_1x128 = 0;
+  if (ra == FP8_TENSOR && rb == FP8_TENSOR) {
+    *kind = kTensor;
+  } else if (ra == FP8_BLOCK_1x128 && rb == FP8_BLOCK_128x128) {
+    *kind = kBlock1x128;
+  } else if (ra == FP8_BLOCK_1x128 && rb == FP8_BLOCK_1x128) {
+    *kind = kBlock1x128;
+    *b_1x128 = 1;
+  } else if (is_mx_tiled(ra) && is_mx_tiled(rb)) {
+    *kind = kMx;   // either exponent rule: the tensor core reads E8M0 bytes either way
+  } else if (valid_recipe(ra) && valid_recipe(rb)) {
+    return FP8_ERR_UNSUPPORTED;
+  } else {
+    return FP8_ERR_INVALID_ARG;
+  }
+  return FP8_OK;
+}
+
 fp8_status scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const void* sA, const uint8_t* B, fp8_format fb,
                        fp8_recipe rb, const void* sB, int64_t M, int64_t N, int64_t K, void* C, fp8_out_dtype out,
                        const GemmExtra& x, cudaStream_t stream) {
@@ -223,20 +244,7 @@ fp8_status scaled_gemm(const uint8_t* A, fp8_format fa, fp8_recipe ra, const voi
     return FP8_ERR_INVALID_ARG;
   int kind;
   int b_1x128 = 0;
-  if (ra == FP8_TENSOR && rb == FP8_TENSOR) {
-    kind = kTensor;
-  } else if (ra == FP8_BLOCK_1x128 && rb == FP8_BLOCK_128x128) {
-    kind = kBlock1x128;
-  } else if (ra == FP8_BLOCK_1x128 && rb == FP8_BLOCK_1x128) {
-    kind = kBlock1x128;
-    b_1x128 = 1;
-  } else if (is_mx_tiled(ra) && is_mx_tiled(rb)) {
-    kind = kMx;   // either exponent rule: the tensor core reads E8M0 bytes either way
-  } else if (valid_recipe(ra) && valid_recipe(rb)) {
-    return FP8_ERR_UNSUPPORTED;
-  } else {
-    return FP8_ERR_INVALID_ARG;
-  }
+  if (fp8_status st = gemm_kind(ra, rb, &kind, &b_1x128)) return st;
   const bool fused = x.c_amax != nullptr || x.cq != nullptr;
   const int64_t outsz = out == FP8_OUT_FP32 ? 4 : 2;
   if (fused) {
@@ -575,6 +583,38 @@ fp8_status fp8_get_device_status(cudaStream_t stream) {
   }
   if (word & (kErrTimeoutTmaLoad | kErrTimeoutMma | kErrTimeoutStage)) return FP8_ERR_TIMEOUT;
   if (word & kErrBadState) return FP8_ERR_DEVICE_STATE;
+  return FP8_OK;
+}
+
+fp8_status fp8_debug_gemm_plan(fp8_recipe ra, fp8_recipe rb, fp8_out_dtype out, int64_t M, int64_t N, int64_t K,
+                               int32_t fused, int32_t num_sms, int32_t resident_pairs, int64_t* plan) {
+  if (plan == nullptr || M <= 0 || N <= 0 || K <= 0 || num_sms < 2 || (out != FP8_OUT_BF16 && out != FP8_OUT_FP32))
+    return FP8_ERR_INVALID_ARG;
+  int kind, b_1x128;
+  if (fp8_status st = gemm_kind(ra, rb, &kind, &b_1x128)) return st;
+  if (M % 128 || N % 128 || K % 128) return FP8_ERR_SHAPE;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8_ERR_SHAPE;
+  // the parameters the dispatch reads; the pointers only say which outputs exist
+  static uint8_t present;
+  GemmParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.kind = kind;
+  p.b_1x128 = b_1x128;
+  p.out_fp32 = out == FP8_OUT_FP32;
+  p.c = &present;
+  if (fused) p.cq = &present;
+  p.wide160 = gemm_select_wide(p, num_sms) ? 1 : 0;
+  const GemmPlan g = gemm_plan(p, num_sms, resident_pairs);
+  plan[0] = g.pair;
+  plan[1] = g.variant;
+  plan[2] = g.block_n;
+  plan[3] = g.ntiles;
+  plan[4] = g.div.streamk;
+  plan[5] = g.div.split;
+  plan[6] = g.div.tail0;
+  plan[7] = g.div.launched;
   return FP8_OK;
 }
 

@@ -1326,6 +1326,43 @@ cudaError_t check_split_regs(K kern, bool split, std::atomic<bool> (&checked)[kM
   return cudaSuccess;
 }
 
+}  // namespace
+
+PairDivision pair_division(int kind, int64_t ntiles, int64_t pairs, int64_t k) {
+  PairDivision d{0, 1, static_cast<int>(ntiles), ntiles < pairs ? ntiles : pairs};
+  if (kind != kTensor && kind != kMx) return d;
+  const int64_t full = ntiles / pairs, rest = ntiles % pairs, ng = k / kBK;
+  // Two or three full waves and a partial one: all but the last full wave as whole tiles,
+  // then every pair an equal share of the remaining tiles' K blocks (each share over one
+  // tile long).  With more waves the partial one costs less than the hand-overs (measured:
+  // MX 8192 x 12288 x 4096, 20 waves, 4 % slower).  With one full wave every tile is
+  // shared: worth it for K >= 8192 (2560 x 2304 x 8192: 0.54 -> 0.61 against the K-range
+  // cut), not at K = 4096 (MX 2048 x 4096 x 4096: 0.55 -> 0.50 against whole tiles).
+  if (kStreamK && full >= 1 && rest > 0 && full <= 3 && (full >= 2 || ng >= 64)) {
+    d.streamk = 1;
+    d.tail0 = static_cast<int>((full - 1) * pairs);
+    d.launched = pairs;
+    return d;
+  }
+  // A last wave that would leave at least half of the pairs idle is cut along K: its R
+  // tiles into S ranges on R * S pairs (every pair resident, so the waits end).  The
+  // hand-over of the ranges costs a few microseconds whatever K is, the time saved grows
+  // with K: measured side by side, +1-2 % at 8192^3, +3 % at 2048 x 36864 x 12288, +9 % at
+  // 2048 x 12288 x 49152, but nothing at 4096^3 and -6 % at 49152 x 12288 x 2048.  So the
+  // cut is made for K >= 8192, or when there is only the one partial wave.
+  if (rest > 0 && 2 * rest <= pairs && ng >= 2 && (full == 0 || ng >= 64)) {
+    int64_t split = pairs / rest;
+    if (split > ng) split = ng;
+    if (split > kMaxSplit) split = kMaxSplit;
+    d.split = static_cast<int>(split);
+    d.tail0 = static_cast<int>(full * pairs);
+    d.launched = full > 0 ? pairs : rest * split;
+  }
+  return d;
+}
+
+namespace {
+
 template <int KIND, bool QOUT>
 cudaError_t launch_kind(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
                         const CUtensorMap& tm_sfb, const CUtensorMap& tm_c, int num_sms, cudaStream_t s) {
@@ -1387,48 +1424,20 @@ cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUte
   q.streamk = 0;
   q.ws = nullptr;
   q.ws_flags = nullptr;
+  const PairDivision d = pair_division(KIND, ntiles, pairs, p.K);
   int64_t launched = ntiles < pairs ? ntiles : pairs;
-  if constexpr ((KIND == kTensor || KIND == kMx) && kStreamK) {
-    // Two or three full waves and a partial one: all but the last full wave as whole tiles,
-    // then every pair an equal share of the remaining tiles' K blocks (each share over one
-    // tile long).  With more waves the partial one costs less than the hand-overs (measured:
-    // MX 8192 x 12288 x 4096, 20 waves, 4 % slower).  With one full wave every tile is
-    // shared: worth it for K >= 8192 (2560 x 2304 x 8192: 0.54 -> 0.61 against the K-range
-    // cut), not at K = 4096 (MX 2048 x 4096 x 4096: 0.55 -> 0.50 against whole tiles).
-    const int64_t waves = ntiles / pairs;
-    if (ntiles > pairs && ntiles % pairs != 0 && waves <= 3 && (waves >= 2 || p.K / kBK >= 64)) {
-      float* ws = nullptr;
-      int* flags = nullptr;
-      if (split_workspace(s, static_cast<int>(num_sms / 2), &ws, &flags)) {
-        q.streamk = 1;
-        q.tail0 = static_cast<int>((ntiles / pairs - 1) * pairs);
-        q.ws = ws;
-        q.ws_flags = flags;
-        launched = pairs;
-      }
-    }
-  }
-  if constexpr (KIND == kTensor || KIND == kMx) if (q.streamk == 0) {
-    // A last wave that would leave at least half of the pairs idle is cut along K: its R
-    // tiles into S ranges on R * S pairs (every pair resident, so the waits below end).
-    // The hand-over of the ranges costs a few microseconds whatever K is, the time saved
-    // grows with K: measured side by side, +1-2 % at 8192^3, +3 % at 2048 x 36864 x 12288,
-    // +9 % at 2048 x 12288 x 49152, but nothing at 4096^3 and -6 % at 49152 x 12288 x 2048.
-    // So the cut is made for K >= 8192, or when there is only the one partial wave.
-    const int64_t full = ntiles / pairs, rest = ntiles % pairs, ng = p.K / kBK;
-    if (rest > 0 && 2 * rest <= pairs && ng >= 2 && (full == 0 || ng >= 64)) {
-      int64_t split = pairs / rest;
-      if (split > ng) split = ng;
-      if (split > kMaxSplit) split = kMaxSplit;
-      float* ws = nullptr;
-      int* flags = nullptr;
-      if (split_workspace(s, static_cast<int>(num_sms / 2), &ws, &flags)) {
-        q.split = static_cast<int>(split);
-        q.tail0 = static_cast<int>(full * pairs);
-        q.ws = ws;
-        q.ws_flags = flags;
-        launched = full > 0 ? pairs : rest * split;
-      }
+  if (d.streamk || d.split > 1) {
+    // both need the stream's workspace; without one (a capture that has none yet, a full
+    // table, a failed allocation) the tiles run whole
+    float* ws = nullptr;
+    int* flags = nullptr;
+    if (split_workspace(s, static_cast<int>(num_sms / 2), &ws, &flags)) {
+      q.streamk = d.streamk;
+      q.split = d.split;
+      q.tail0 = d.tail0;
+      q.ws = ws;
+      q.ws_flags = flags;
+      launched = d.launched;
     }
   }
   cfg.gridDim = dim3(static_cast<unsigned>(2 * launched));
@@ -1466,6 +1475,29 @@ bool gemm_uses_pair(const GemmParams& p) {
 }
 
 int gemm_b_box_rows(const GemmParams& p) { return gemm_uses_pair(p) ? gemm_block_n(p) / 2 : gemm_block_n(p); }
+
+GemmPlan gemm_plan(const GemmParams& p, int num_sms, int resident_pairs) {
+  GemmPlan g{};
+  g.pair = gemm_uses_pair(p) ? 1 : 0;
+  g.block_n = gemm_block_n(p);
+  if (p.kind == kBlock1x128) {
+    if (p.b_1x128) g.variant = g.pair ? kBlockK2RowsB : kBlockRowsB;
+    else if (p.wide160) g.variant = kBlock160;
+    else g.variant = (g.pair || (p.K / kBK) % 2 == 0) ? kBlockK2 : kBlock1x128;
+  } else {
+    g.variant = p.kind;
+  }
+  const int64_t rows = g.pair ? 2 * kBM : kBM;
+  g.ntiles = (p.M / rows) * ((p.N + g.block_n - 1) / g.block_n);
+  if (g.pair) {
+    int64_t pairs = num_sms / 2;
+    if (resident_pairs > 0 && resident_pairs < pairs) pairs = resident_pairs;
+    g.div = pair_division(g.variant, g.ntiles, pairs, p.K);
+  } else {
+    g.div = PairDivision{0, 1, static_cast<int>(g.ntiles), g.ntiles < num_sms ? g.ntiles : num_sms};
+  }
+  return g;
+}
 
 template <bool QOUT>
 cudaError_t launch_gemm_q(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,

@@ -174,6 +174,29 @@ int gemm_b_box_rows(const GemmParams& p);
 // Columns of C one TMA store box carries: 16 (BF16, unswizzled) for the 160-wide tiles,
 // else 0: the usual 128-byte box (64 BF16 or 32 FP32 columns, 128-byte swizzle).
 int gemm_c_box_cols(const GemmParams& p);
+// The division of a CTA-pair launch's tiles (host logic only): whole tiles, stream-K
+// shares of the tiles from tail0 on (streamk = 1), or the last wave cut into `split` K
+// ranges; `launched` pairs.  Per-tensor and MX only (other kinds: whole tiles).  Both cuts
+// also need the stream's workspace; without it a launch runs whole tiles.
+struct PairDivision {
+  int streamk;
+  int split;
+  int tail0;
+  int64_t launched;
+};
+PairDivision pair_division(int kind, int64_t ntiles, int64_t pairs, int64_t k);
+// What a GEMM with these parameters launches (host logic only, p.wide160 already chosen):
+// kernel variant (kTensor, kBlock1x128, kMx, or the blockwise variants 4 = per-row B on
+// one CTA, 5 = 256-deep stages, 6 = per-row B on pairs, 7 = 256 x 160 pair tiles), CTA
+// pairs or not, tile width, tile count, and the division above.
+struct GemmPlan {
+  int pair;
+  int variant;
+  int block_n;
+  int64_t ntiles;
+  PairDivision div;
+};
+GemmPlan gemm_plan(const GemmParams& p, int num_sms, int resident_pairs);
 // tm_sfa / tm_sfb: MX only (the tiled E8M0 buffers as [atoms * 2, 256] bytes, box 2 x 256).
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
                         const CUtensorMap& tm_sfb, const CUtensorMap& tm_c, int num_sms, cudaStream_t s);
