@@ -92,3 +92,56 @@ def test_split_two_streams_at_once():
     for ref, o in zip(refs, outs):
         for c in o:
             assert np.array_equal(host(c.view(torch.int16)), host(ref.view(torch.int16)))
+
+
+def test_split_inside_cuda_graphs():
+    # Stream-K shape (256 tiles, three full waves).  A stream that has no workspace yet when
+    # a GEMM is captured gets whole tiles in its graph (no allocation inside a capture; the
+    # stream may come from a pool that already gave it one, then it is used); once the
+    # stream has one (after an eager call), a captured GEMM uses it.  Replays are
+    # deterministic, the second graph gives the eager result bit for bit, and both stay
+    # within the bar.
+    m, n, k = 4096, 4096, 512
+    x = wl.normal_bf16((m, k), 730, 1.0)
+    w = wl.normal_bf16((n, k), 731, 0.02)
+    qa, sa, qb, sb = _operands(R.TENSOR, R.TENSOR, m, n, k, 730)
+    s = torch.cuda.Stream()
+    c_whole = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    c_sk = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    run = lambda c: fq.fp8_scaled_gemm(qa, F.E4M3, R.TENSOR, sa, qb, F.E4M3, R.TENSOR, sb, c, fq.OutDtype.FP32,
+                                       stream=s)
+    g_whole = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_whole, stream=s):
+        run(c_whole)                       # the stream has no workspace: whole tiles
+    eager = torch.empty_like(c_sk)
+    with torch.cuda.stream(s):
+        run(eager)                         # allocates the stream's workspace: stream-K
+    torch.cuda.synchronize()
+    g_sk = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_sk, stream=s):
+        run(c_sk)
+    outs_whole, outs_sk = [], []
+    for _ in range(3):
+        g_whole.replay()
+        g_sk.replay()
+        torch.cuda.synchronize()
+        outs_whole.append(host(c_whole).copy())
+        outs_sk.append(host(c_sk).copy())
+    assert_status_ok()
+    for o in outs_sk:
+        assert np.array_equal(o.view(np.uint32), host(eager).view(np.uint32))
+    for o in outs_whole[1:]:
+        assert np.array_equal(o.view(np.uint32), outs_whole[0].view(np.uint32))
+    # both divisions against the oracle on sampled rows
+    from test_gpu_gemm import _quant_oracle
+    import oracle
+    from gpu_util import bits16
+    qa_ref, sa_ref, sca = _quant_oracle(bits16(x), R.TENSOR, F.E4M3)
+    qb_ref, sb_ref, scb = _quant_oracle(bits16(w), R.TENSOR, F.E4M3)
+    rows = np.arange(0, m, 9)
+    deq_a = oracle.dequantize(qa_ref[rows], oracle.KIND_TENSOR, int(F.E4M3), sa_ref)
+    deq_b = oracle.dequantize(qb_ref, oracle.KIND_TENSOR, int(F.E4M3), sb_ref)
+    c_ref = deq_a @ deq_b.T
+    for c in (outs_whole[0], outs_sk[0]):
+        rel, worst = oracle.gemm_tolerance_check(c[rows].astype(np.float64), c_ref, deq_a, deq_b)
+        assert rel <= 1e-2 and worst <= 1.0, (rel, worst)
