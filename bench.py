@@ -355,6 +355,7 @@ def run_ours(args, rank, world):
     result["clocks"] = ck
     if not args.no_per_recipe:
         result["per_recipe"]["clocks"] = clocks.summary([(t_pr0, t_pr1)])
+    result["quality_vs_bf16"] = quality_vs_bf16(fq, x, w)
     if not args.no_e2e:
         result["e2e"] = run_e2e(fq, x, w, args, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -397,6 +398,31 @@ def run_sustained(fq, wl, dev, x, w, path):
     return {"steps": n, "seconds": round(e0.elapsed_time(e1) * 1e-3, 3), "ms_per_step": round(ms, 5),
             "TFLOP/s": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1),
             "inputs": "four input sets in turn (512 MiB of bf16 with their FP8 copies), no flush", "t0": t0, "t1": t1}
+
+
+def quality_vs_bf16(fq, x, w):
+    """Informative only (no parity claim): ||Y_fp8 - Y_bf16||_F / ||Y_bf16||_F on the bench's
+    X, W for each recipe pairing, Y_bf16 being the BF16 product with FP32 accumulation that the
+    FP8 path replaces (computed by torch's matmul, outside the path)."""
+    R, F = fq.Recipe, fq.Format
+    y_ref = (x @ w.t()).double()
+    nref = torch.linalg.norm(y_ref)
+    out = {}
+    for name, ra, rb in (("per_tensor_current", R.TENSOR, R.TENSOR), ("blockwise", R.BLOCK_1x128, R.BLOCK_128x128),
+                         ("mxfp8", R.MX_1x32_TILED, R.MX_1x32_TILED)):
+        sa_t = sb_t = None
+        if ra == R.TENSOR:
+            sa_t, sb_t = torch.empty(1, device=x.device), torch.empty(1, device=x.device)
+            for t, sc in ((x, sa_t), (w, sb_t)):
+                am = torch.empty(1, device=x.device)
+                fq.fp8_amax(t, am)
+                fq.fp8_compute_scale(am, F.E4M3, sc, torch.empty(1, device=x.device))
+        qa, sa, _, _ = fq.cast_transpose(x, ra, F.E4M3, sa_t, col=False)
+        qb, sb, _, _ = fq.cast_transpose(w, rb, F.E4M3, sb_t, col=False)
+        y = fq.scaled_gemm(qa, F.E4M3, ra, sa, qb, F.E4M3, rb, sb)
+        out[name] = round(float(torch.linalg.norm(y.double() - y_ref) / nref), 6)
+    out["note"] = "relative Frobenius difference from the BF16 product (X with 1 % of columns x100), E4M3"
+    return out
 
 
 def run_per_recipe(fq, wl, dev, flush):
