@@ -35,8 +35,9 @@
  *     a rejected call enqueues nothing and returns FP8_ERR_INVALID_ARG,
  *     FP8_ERR_SHAPE, FP8_ERR_ALIGNMENT or FP8_ERR_UNSUPPORTED.  A CUDA launch
  *     error returns FP8_ERR_CUDA.  Kernels never trap: a device-side failure
- *     (a wait that ran out of time, a state argument out of range) sets a
- *     device error word, read and cleared by fp8_get_device_status.
+ *     (a wait that ran out of time, a state argument out of range, and in the
+ *     debug library an access outside its buffer) sets a device error word,
+ *     read and cleared by fp8_get_device_status.
  */
 #ifndef FP8Q_H
 #define FP8Q_H
@@ -56,7 +57,8 @@ typedef enum {
   FP8_ERR_UNSUPPORTED = 4, /* an operand / recipe pairing not provided */
   FP8_ERR_CUDA = 5,        /* a CUDA runtime error */
   FP8_ERR_TIMEOUT = 6,     /* a device wait ran out of time (see fp8_get_device_status) */
-  FP8_ERR_DEVICE_STATE = 7 /* a device-resident state argument was out of range */
+  FP8_ERR_DEVICE_STATE = 7, /* a device-resident state argument was out of range */
+  FP8_ERR_INDEX = 8         /* (debug library only) a kernel access fell outside its buffer and was skipped */
 } fp8_status;
 
 typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format;
@@ -346,6 +348,15 @@ fp8_status fp8_get_device_status(cudaStream_t stream);
  * fp8_get_device_status.  Exists to test the failure path without a fault.
  */
 fp8_status fp8_debug_wait_timeout(cudaStream_t stream);
+
+/*
+ * fp8_debug_index_check -- enqueue a one-thread kernel that checks `index` against
+ * `extent` as the kernels check their plain global accesses, touching no memory.  The
+ * debug library (built with FP8Q_DEBUG_INDEX) reports an index outside [0, extent) as
+ * FP8_ERR_INDEX through fp8_get_device_status; the release library checks nothing.
+ * Exists to test that reporting path without a fault.
+ */
+fp8_status fp8_debug_index_check(int64_t index, int64_t extent, cudaStream_t stream);
 
 /*
  * fp8_debug_gemm_plan -- how fp8_scaled_gemm (fused != 0: fp8_scaled_gemm_amax with an

@@ -11,7 +11,8 @@ Entry points with the C names take tensors (or None for NULL) and raise
 ``amax_history_update``, ``fp8_quantize``, ``fp8_cast_transpose``, ``fp8_cast_transpose_f32``,
 ``fp8_cast_transpose_multi``,
 ``fp8_dequantize``, ``fp8_allreduce_sum``, ``fp8_scaled_gemm``, ``fp8_scaled_gemm_amax``,
-``fp8_get_device_status``, ``fp8_debug_wait_timeout``, ``fp8_debug_gemm_plan``.  ``cast_transpose`` /
+``fp8_get_device_status``, ``fp8_debug_wait_timeout``, ``fp8_debug_gemm_plan``,
+``fp8_debug_index_check``.  ``cast_transpose`` /
 ``dequantize`` / ``scaled_gemm`` / ``scaled_gemm_amax`` are allocation helpers
 over them; ``linear`` holds the FP8 linear layer and the autocast scope built
 on these calls.
@@ -30,7 +31,7 @@ __all__ = [
     "fp8_cast_transpose_f32",
     "fp8_cast_transpose_multi", "CastJob",
     "fp8_dequantize", "fp8_allreduce_sum", "fp8_allreduce_sum_noalloc", "fp8_scaled_gemm", "fp8_scaled_gemm_amax", "fp8_get_device_status",
-    "fp8_debug_wait_timeout", "fp8_debug_gemm_plan", "fp8_status_string",
+    "fp8_debug_wait_timeout", "fp8_debug_gemm_plan", "fp8_debug_index_check", "fp8_status_string",
     "scale_shape", "cast_transpose", "cast_transpose_multi", "dequantize", "allreduce_sum", "scaled_gemm", "scaled_gemm_amax",
     "DelayedScaling",
 ]
@@ -45,6 +46,7 @@ class Status(enum.IntEnum):
     ERR_CUDA = 5
     ERR_TIMEOUT = 6
     ERR_DEVICE_STATE = 7
+    ERR_INDEX = 8
 
 
 class Format(enum.IntEnum):
@@ -111,6 +113,7 @@ _SIGNATURES = {
     "fp8_get_device_status": [_P],
     "fp8_debug_wait_timeout": [_P],
     "fp8_debug_gemm_plan": [_E, _E, _E, _I64, _I64, _I64, _I32, _I32, _I32, _P],
+    "fp8_debug_index_check": [_I64, _I64, _P],
     "fp8_status_string": [_E],
 }
 
@@ -281,6 +284,10 @@ def fp8_get_device_status(stream=None) -> Status:
 
 def fp8_debug_wait_timeout(stream=None):
     _check("fp8_debug_wait_timeout", load_library().fp8_debug_wait_timeout(_stream(stream)))
+
+
+def fp8_debug_index_check(index: int, extent: int, stream=None):
+    _check("fp8_debug_index_check", load_library().fp8_debug_index_check(index, extent, _stream(stream)))
 
 
 GEMM_VARIANTS = {0: "per-tensor", 1: "blockwise, one CTA, 128-deep stages", 3: "MXFP8",

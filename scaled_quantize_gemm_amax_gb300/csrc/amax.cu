@@ -233,4 +233,13 @@ cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// The index check the kernels apply to their plain global accesses, on one value and
+// touching no memory (it reports only in debug builds).
+__global__ void k_index_selftest(int64_t index, int64_t extent, uint32_t* err) { (void)in_range(index, extent, err); }
+
+cudaError_t launch_index_selftest(int64_t index, int64_t extent, uint32_t* err, cudaStream_t s) {
+  k_index_selftest<<<1, 1, 0, s>>>(index, extent, err);
+  return cudaGetLastError();
+}
+
 }  // namespace fp8q

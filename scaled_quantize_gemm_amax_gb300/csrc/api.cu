@@ -343,6 +343,7 @@ const char* fp8_status_string(fp8_status s) {
     case FP8_ERR_CUDA: return "FP8_ERR_CUDA";
     case FP8_ERR_TIMEOUT: return "FP8_ERR_TIMEOUT";
     case FP8_ERR_DEVICE_STATE: return "FP8_ERR_DEVICE_STATE";
+    case FP8_ERR_INDEX: return "FP8_ERR_INDEX";
   }
   return "FP8_ERR_UNKNOWN";
 }
@@ -583,6 +584,7 @@ fp8_status fp8_get_device_status(cudaStream_t stream) {
   }
   if (word & (kErrTimeoutTmaLoad | kErrTimeoutMma | kErrTimeoutStage)) return FP8_ERR_TIMEOUT;
   if (word & kErrBadState) return FP8_ERR_DEVICE_STATE;
+  if (word & kErrIndex) return FP8_ERR_INDEX;
   return FP8_OK;
 }
 
@@ -616,6 +618,13 @@ fp8_status fp8_debug_gemm_plan(fp8_recipe ra, fp8_recipe rb, fp8_out_dtype out, 
   plan[6] = g.div.tail0;
   plan[7] = g.div.launched;
   return FP8_OK;
+}
+
+fp8_status fp8_debug_index_check(int64_t index, int64_t extent, cudaStream_t stream) {
+  ApiRange nvtx_range("fp8_debug_index_check");
+  DeviceInfo* d;
+  if (fp8_status st = device_info(&d)) return st;
+  return cuda_status(launch_index_selftest(index, extent, d->err, stream));
 }
 
 fp8_status fp8_debug_wait_timeout(cudaStream_t stream) {

@@ -624,9 +624,10 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     if (want_q && p.c_scale_inv != nullptr && blockIdx.x == 0 && warp == CTRL && lane == 0)
       *p.c_scale_inv = recip_rn(c_scale);
     // 32 consecutive output values of one row, starting at column gcol
+    const int64_t mn = p.M * p.N;   // elements of C (and of its FP8 copy)
     auto emit = [&](const float (&v)[32], int64_t grow_, int64_t gcol, bool store_c = true) {
       const int64_t off = grow_ * p.N + gcol;
-      if (store_c && p.c != nullptr) store_row32(p.c, off, v, fp32);
+      if (store_c && p.c != nullptr) FP8Q_GUARD(off, 32, mn, p.err) { store_row32(p.c, off, v, fp32); }
       if (QOUT && (want_q || want_amax)) {
         float y[32];
 #pragma unroll
@@ -640,8 +641,10 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           for (int i = 0; i < 8; ++i)
             w[i] = cvt_pair(__fmul_rn(y[4 * i], c_scale), __fmul_rn(y[4 * i + 1], c_scale), e5_c) |
                    (cvt_pair(__fmul_rn(y[4 * i + 2], c_scale), __fmul_rn(y[4 * i + 3], c_scale), e5_c) << 16);
-          stg128(p.cq + off, w[0], w[1], w[2], w[3]);
-          stg128(p.cq + off + 16, w[4], w[5], w[6], w[7]);
+          FP8Q_GUARD(off, 32, mn, p.err) {
+            stg128(p.cq + off, w[0], w[1], w[2], w[3]);
+            stg128(p.cq + off + 16, w[4], w[5], w[6], w[7]);
+          }
         }
       }
     };
@@ -687,6 +690,8 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
     };
     uint32_t acc_it = 0, part_it = 0;
     uint32_t tile_it = 0;   // tiles this CTA has finished (B-scale table phases)
+    // blockwise scale arrays: sA [M, K/128]; sB [N/128, K/128], or [N, K/128] per row
+    const int64_t sa_len = p.M * KB, sb_len = (B_ROWS ? p.N : (p.N + 127) / 128) * KB;
     // stages (partial groups) this CTA runs in all; gated: the first GROUPS stages find
     // their partial groups free
     const uint32_t total_groups = static_cast<uint32_t>(nwork) * static_cast<uint32_t>(NG);   // blockwise: never split
@@ -718,14 +723,17 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
 #pragma unroll
         for (int j = 0; j < COLS / 2; ++j) acc[j] = 0;
         uint32_t r[NCH][16];
-        float sa_n = sa_row[0], sl_n = __ldg(sb_lo), sh_n = __ldg(sb_hi);
+        float sa_n = 0.0f, sl_n = 0.0f, sh_n = 0.0f;
+        FP8Q_GUARD(grow * KB, 1, sa_len, p.err) { sa_n = sa_row[0]; }
+        FP8Q_GUARD(nb_lo * KB, 1, sb_len, p.err) { sl_n = __ldg(sb_lo); }
+        FP8Q_GUARD(nb_hi * KB, 1, sb_len, p.err) { sh_n = __ldg(sb_hi); }
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
           const float sa_v = sa_n, sl_v = sl_n, sh_v = sh_n;
           if (kb + 1 < KB) {
-            sa_n = sa_row[kb + 1];
-            sl_n = __ldg(sb_lo + kb + 1);
-            sh_n = __ldg(sb_hi + kb + 1);
+            FP8Q_GUARD(grow * KB + kb + 1, 1, sa_len, p.err) { sa_n = sa_row[kb + 1]; }
+            FP8Q_GUARD(nb_lo * KB + kb + 1, 1, sb_len, p.err) { sl_n = __ldg(sb_lo + kb + 1); }
+            FP8Q_GUARD(nb_hi * KB + kb + 1, 1, sb_len, p.err) { sh_n = __ldg(sb_hi + kb + 1); }
           }
           const uint32_t b = part_it % GROUPS;
           // warp-uniform decision: the TMEM loads that follow are .sync.aligned
@@ -865,8 +873,9 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
             const int cq = CPW * q + (lane % CPW);
             const float* src = static_cast<const float*>(p.sb) + (static_cast<int64_t>(ftn) * BN + h * COLS + cq) * KB;
             const uint32_t dst = tbl + b * (L::TBL_PART / 2);
+            const int64_t src_i = (static_cast<int64_t>(ftn) * BN + h * COLS + cq) * KB;
             for (int kb = lane / CPW; kb < KB; kb += 32 / CPW)
-              cp_async_4(dst + static_cast<uint32_t>(kb * COLS + cq) * 4u, src + kb);
+              FP8Q_GUARD(src_i + kb, 1, sb_len, p.err) { cp_async_4(dst + static_cast<uint32_t>(kb * COLS + cq) * 4u, src + kb); }
             cp_async_arrive_noinc(tbar_full(b));
           };
           bool tok = true;
@@ -892,11 +901,17 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
             break;
         }
         // scale factors of the group to promote next (loads in flight)
-        float sa0 = sa_row[0], sa1 = sa_row[1];
+        float sa0 = 0.0f, sa1 = 0.0f;
+        FP8Q_GUARD(grow * KB, 2, sa_len, p.err) {
+          sa0 = sa_row[0];
+          sa1 = sa_row[1];
+        }
         float sb0 = 0.0f, sb1 = 0.0f;
         if constexpr (!TABLE) {
-          sb0 = __ldg(sb_tile);
-          sb1 = __ldg(sb_tile + 1);
+          FP8Q_GUARD((gcol0 / 128) * KB, 2, sb_len, p.err) {
+            sb0 = __ldg(sb_tile);
+            sb1 = __ldg(sb_tile + 1);
+          }
         }
         bool ok = true;
         if constexpr (TABLE) {
@@ -914,8 +929,10 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           for (int kg = 0; kg < NG; ++kg) {
             const float a0 = sa0, a1 = sa1;
             if (kg + 1 < NG) {
-              sa0 = sa_row[2 * kg + 2];
-              sa1 = sa_row[2 * kg + 3];
+              FP8Q_GUARD(grow * KB + 2 * kg + 2, 2, sa_len, p.err) {
+                sa0 = sa_row[2 * kg + 2];
+                sa1 = sa_row[2 * kg + 3];
+              }
             }
             if (!__all_sync(0xFFFFFFFFu, ready_next)) {
               ok = wait_full();
@@ -973,10 +990,14 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           {
             const float f0 = sa0 * sb0, f1 = sa1 * sb1;
             if (kg + 1 < NG) {
-              sa0 = sa_row[2 * kg + 2];
-              sa1 = sa_row[2 * kg + 3];
-              sb0 = __ldg(sb_tile + 2 * kg + 2);
-              sb1 = __ldg(sb_tile + 2 * kg + 3);
+              FP8Q_GUARD(grow * KB + 2 * kg + 2, 2, sa_len, p.err) {
+                sa0 = sa_row[2 * kg + 2];
+                sa1 = sa_row[2 * kg + 3];
+              }
+              FP8Q_GUARD((gcol0 / 128) * KB + 2 * kg + 2, 2, sb_len, p.err) {
+                sb0 = __ldg(sb_tile + 2 * kg + 2);
+                sb1 = __ldg(sb_tile + 2 * kg + 3);
+              }
             }
             promote64(pa, f0);          // the FMAs run while the MMAs refill the group
             promote64(pb, f1);
@@ -1014,8 +1035,15 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
 #pragma unroll
         for (int j = 0; j < COLS / 2; ++j) acc[j] = 0;
         // scale factors are fetched two k-blocks ahead, off the promotion's critical path
-        float sa0 = sa_row[0], sa1 = KB > 1 ? sa_row[1] : 0.0f;
-        float sb0 = B_ROWS ? 0.0f : __ldg(sb_tile), sb1 = (!B_ROWS && KB > 1) ? __ldg(sb_tile + 1) : 0.0f;
+        float sa0 = 0.0f, sa1 = 0.0f, sb0 = 0.0f, sb1 = 0.0f;
+        FP8Q_GUARD(grow * KB, KB > 1 ? 2 : 1, sa_len, p.err) {
+          sa0 = sa_row[0];
+          sa1 = KB > 1 ? sa_row[1] : 0.0f;
+        }
+        if (!B_ROWS) FP8Q_GUARD((gcol0 / 128) * KB, KB > 1 ? 2 : 1, sb_len, p.err) {
+          sb0 = __ldg(sb_tile);
+          sb1 = KB > 1 ? __ldg(sb_tile + 1) : 0.0f;
+        }
         auto wait_full = [&]() -> bool {
           const uint32_t pb = part_it % GROUPS;
           // warp-uniform decision: the TMEM loads that follow are .sync.aligned
@@ -1029,6 +1057,9 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           if (B_ROWS) {
             // per-column B scales: sB[n, kb]
             const float* sbc = sb_blk + (gcol0 + CW * c) * KB + kb;
+            if constexpr (kDebugIndex) {   // every column's scale of this k-block
+              for (int j = 0; j < CW; ++j) in_range((gcol0 + CW * c + j) * KB + kb, sb_len, p.err);
+            }
 #pragma unroll
             for (int j = 0; j < CW / 2; ++j) {
               const uint64_t f = pack_f32x2(sa_v * __ldg(sbc + (2 * j) * KB), sa_v * __ldg(sbc + (2 * j + 1) * KB));
@@ -1059,8 +1090,8 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
             sa0 = sa1;
             sb0 = sb1;
             if (kb + 2 < KB) {
-              sa1 = sa_row[kb + 2];
-              if (!B_ROWS) sb1 = __ldg(sb_tile + kb + 2);
+              FP8Q_GUARD(grow * KB + kb + 2, 1, sa_len, p.err) { sa1 = sa_row[kb + 2]; }
+              if (!B_ROWS) FP8Q_GUARD((gcol0 / 128) * KB + kb + 2, 1, sb_len, p.err) { sb1 = __ldg(sb_tile + kb + 2); }
             }
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
@@ -1122,7 +1153,9 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
             bool got = true;
             if (lane == 0)
               for (int k = 0; k < w.nslot && got; ++k)
-                got = wait_count(p.ws_flags + w.slot + k * w.sstride, kSlotWarps, p.err, kErrTimeoutMma);
+                FP8Q_GUARD(w.slot + k * w.sstride, 1, p.ws_nflags, p.err) {
+                  got = wait_count(p.ws_flags + w.slot + k * w.sstride, kSlotWarps, p.err, kErrTimeoutMma);
+                }
             if (!__shfl_sync(0xFFFFFFFFu, got, 0)) break;   // timed out: the error word says so
           }
           // float offset of 16-byte piece i of chunk c of this thread's row in slot `sl`
@@ -1145,13 +1178,20 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
             for (int c = 0; c < CH; ++c)
 #pragma unroll
               for (int i = 0; i < 8; ++i)
-                stg128(p.ws + piece(w.slot, c, i), r[c][4 * i], r[c][4 * i + 1], r[c][4 * i + 2], r[c][4 * i + 3]);
+                FP8Q_GUARD(piece(w.slot, c, i), 4, p.ws_len, p.err) {
+                  stg128(p.ws + piece(w.slot, c, i), r[c][4 * i], r[c][4 * i + 1], r[c][4 * i + 2], r[c][4 * i + 3]);
+                }
           } else {
             // the first slot's pieces of the next chunk are in flight while this chunk is
             // summed (further slots are loaded as they are added)
             float4 o[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = __ldcg(reinterpret_cast<const float4*>(p.ws + piece(w.slot, 0, i)));
+            for (int i = 0; i < 8; ++i) {
+              o[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+              FP8Q_GUARD(piece(w.slot, 0, i), 4, p.ws_len, p.err) {
+                o[i] = __ldcg(reinterpret_cast<const float4*>(p.ws + piece(w.slot, 0, i)));
+              }
+            }
             for (int c = 0; c < CH; ++c) {
               uint32_t rc[32];
               tc_ld_32x32b_x32(col_base + 32 * c, rc);
@@ -1167,13 +1207,18 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
               if (c + 1 < CH) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                  o[i] = __ldcg(reinterpret_cast<const float4*>(p.ws + piece(w.slot, c + 1, i)));
+                  FP8Q_GUARD(piece(w.slot, c + 1, i), 4, p.ws_len, p.err) {
+                    o[i] = __ldcg(reinterpret_cast<const float4*>(p.ws + piece(w.slot, c + 1, i)));
+                  }
               }
               for (int k = 1; k < w.nslot; ++k) {
                 const int sl = w.slot + k * w.sstride;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                  const float4 e = __ldcg(reinterpret_cast<const float4*>(p.ws + piece(sl, c, i)));
+                  float4 e = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                  FP8Q_GUARD(piece(sl, c, i), 4, p.ws_len, p.err) {
+                    e = __ldcg(reinterpret_cast<const float4*>(p.ws + piece(sl, c, i)));
+                  }
                   v[4 * i] += e.x;
                   v[4 * i + 1] += e.y;
                   v[4 * i + 2] += e.z;
@@ -1196,12 +1241,14 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
           if (w.part > 0) {
             __threadfence();   // this thread's slot values, before the warp is counted
             __syncwarp();
-            if (lane == 0) atomicAdd(p.ws_flags + w.slot, 1);
+            if (lane == 0) FP8Q_GUARD(w.slot, 1, p.ws_nflags, p.err) { atomicAdd(p.ws_flags + w.slot, 1); }
           } else if (lane == 0) {
             // the last of the two pairs' warps to count on a slot (all have read it) resets it
             for (int k = 0; k < w.nslot; ++k) {
               int* f = p.ws_flags + w.slot + k * w.sstride;
-              if (atomicAdd(f, 1) == 2 * kSlotWarps - 1) atomicExch(f, 0);
+              FP8Q_GUARD(w.slot + k * w.sstride, 1, p.ws_nflags, p.err) {
+                if (atomicAdd(f, 1) == 2 * kSlotWarps - 1) atomicExch(f, 0);
+              }
             }
           }
           ++acc_it;
@@ -1437,6 +1484,8 @@ cudaError_t launch_pair(const GemmParams& p, const CUtensorMap& tm_a, const CUte
       q.tail0 = d.tail0;
       q.ws = ws;
       q.ws_flags = flags;
+      q.ws_len = static_cast<int64_t>(num_sms / 2) * static_cast<int64_t>(kSplitSlotBytes / sizeof(float));
+      q.ws_nflags = num_sms / 2;
       launched = d.launched;
     }
   }

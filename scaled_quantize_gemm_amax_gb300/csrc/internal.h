@@ -157,6 +157,8 @@ struct GemmParams {
   int streamk;
   float* ws;             // [slots][256][256] fp32
   int* ws_flags;         // [slots], 0 between launches
+  int64_t ws_len;        // floats in ws, and
+  int ws_nflags;         // counters in ws_flags (index checks of debug builds)
   // Blockwise 1x128 x 128x128 on 256 x 160 pair tiles (set by gemm_select_wide)
   int wide160;
 };
@@ -203,5 +205,8 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tm_a, const CUte
 
 // Bounded-wait self test: one CTA waits on an mbarrier nothing arrives on.
 cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t s);
+// Index-check self test: one thread checks `index` against `extent` the way the kernels
+// check their accesses (no memory is touched); only debug builds report.
+cudaError_t launch_index_selftest(int64_t index, int64_t extent, uint32_t* err, cudaStream_t s);
 
 }  // namespace fp8q

@@ -14,7 +14,36 @@ enum : uint32_t {
   kErrTimeoutMma     = 1u << 1,   // a wait for an MMA result or a free accumulator ran out of time
   kErrTimeoutStage   = 1u << 2,   // a producer wait for a free pipeline stage ran out of time
   kErrBadState       = 1u << 3,   // a state argument (e.g. a history position) was out of range
+  kErrIndex          = 1u << 4,   // (debug builds) a plain global access fell outside its buffer
 };
+
+// Debug builds (compiled with -DFP8Q_DEBUG_INDEX) check the element index of the kernels'
+// plain global accesses (scale arrays, workspace, element stores) against the buffer's
+// extent: an access outside [0, n) is skipped and kErrIndex is OR-ed into the device error
+// word, which the host reads back as FP8_ERR_INDEX -- a stand-in for a memory checker that
+// never traps.  Release builds compile the check away.
+#ifdef FP8Q_DEBUG_INDEX
+constexpr bool kDebugIndex = true;
+#else
+constexpr bool kDebugIndex = false;
+#endif
+__device__ __forceinline__ bool in_range(int64_t i, int64_t n, uint32_t* err) {
+  if constexpr (kDebugIndex) {
+    if (i < 0 || i >= n) {
+      atomicOr(err, kErrIndex);
+      return false;
+    }
+  }
+  return true;
+}
+// [i, i + len) inside [0, n)
+__device__ __forceinline__ bool in_range(int64_t i, int64_t len, int64_t n, uint32_t* err) {
+  return in_range(i, n, err) && in_range(i + len - 1, n, err);
+}
+// Guard the statement that follows (always write it in braces): in debug builds it runs
+// only when elements [i, i + len) of an n-element buffer are in range; in release builds
+// the guard is compiled away and the statement is unchanged.
+#define FP8Q_GUARD(i, len, n, err) if (kDebugIndex && !in_range((i), (len), (n), (err))) {} else
 
 // A spin-wait gives up after this long and reports a timeout.
 constexpr uint64_t kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;   // 1 s

@@ -160,10 +160,10 @@ __device__ __forceinline__ float block_max(float v, float* red, int warp, int la
 // The staged atoms of tile (tr, tc) to their places in the tiled scale arrays: the row
 // copy's atom (tr, tc) of [R, C], the column copy's atom (tc, tr) of [C, R].
 __device__ __forceinline__ void store_mx_atoms(const CastParams& p, uint32_t sf, int tr, int tc) {
-  if (p.do_row)
-    bulk_store(static_cast<uint8_t*>(p.s_row) + (static_cast<int64_t>(tr) * p.tiles_c + tc) * 512, sf, 512);
-  if (p.do_col)
-    bulk_store(static_cast<uint8_t*>(p.s_col) + (static_cast<int64_t>(tc) * p.tiles_r + tr) * 512, sf + 512, 512);
+  const int64_t atoms = static_cast<int64_t>(p.tiles_r) * p.tiles_c * 512;   // bytes of either tiled array
+  const int64_t orow = (static_cast<int64_t>(tr) * p.tiles_c + tc) * 512, ocol = (static_cast<int64_t>(tc) * p.tiles_r + tr) * 512;
+  if (p.do_row) FP8Q_GUARD(orow, 512, atoms, p.err) { bulk_store(static_cast<uint8_t*>(p.s_row) + orow, sf, 512); }
+  if (p.do_col) FP8Q_GUARD(ocol, 512, atoms, p.err) { bulk_store(static_cast<uint8_t*>(p.s_col) + ocol, sf + 512, 512); }
 }
 
 // The GEMM-ready tiled E8M0 layout: 128-row x 4-block atoms of 512 B, atom (r/128, b/4)
@@ -197,8 +197,13 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
     tile_scale = scale_from_amax(tmax, fmax);
     if (tid == 0) {
       const float si = recip_rn(tile_scale);
-      if (p.do_row && p.s_row) static_cast<float*>(p.s_row)[tr * nb128_c + tc] = si;
-      if (p.do_col && p.s_col) static_cast<float*>(p.s_col)[tc * nb128_r + tr] = si;
+      const int64_t nblk = static_cast<int64_t>(nb128_r) * nb128_c;
+      if (p.do_row && p.s_row) FP8Q_GUARD(static_cast<int64_t>(tr) * nb128_c + tc, 1, nblk, p.err) {
+        static_cast<float*>(p.s_row)[tr * nb128_c + tc] = si;
+      }
+      if (p.do_col && p.s_col) FP8Q_GUARD(static_cast<int64_t>(tc) * nb128_r + tr, 1, nblk, p.err) {
+        static_cast<float*>(p.s_col)[tc * nb128_r + tr] = si;
+      }
     }
   } else {
     thr_amax = fmaxf(thr_amax, fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])));
@@ -213,7 +218,9 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
       m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
       const float mine = scale_from_amax(m, fmax);
       const int64_t grow = row0 + (j >> 2) * 32 + warp * 2 + (lane >> 4);
-      if ((j & 3) == 0 && grow < p.R) static_cast<float*>(p.s_row)[grow * nb128_c + tc] = recip_rn(mine);
+      if ((j & 3) == 0 && grow < p.R) FP8Q_GUARD(grow * nb128_c + tc, 1, p.R * nb128_c, p.err) {
+        static_cast<float*>(p.s_row)[grow * nb128_c + tc] = recip_rn(mine);
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, mine, (lane & 16) | (i << 2));
     } else if (RECIPE == kMx) {
@@ -227,7 +234,9 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
       if (p.mx_tiled) {
         sts8(sf + mx_atom_offset(lrow, j >> 2), static_cast<uint32_t>(e + 127));   // the tile's atom (dims % 128 == 0)
       } else if (grow < p.R && b < nb32_c) {   // a tile hanging over C has blocks past the last one
-        static_cast<uint8_t*>(p.s_row)[grow * nb32_c + b] = static_cast<uint8_t>(e + 127);
+        FP8Q_GUARD(grow * nb32_c + b, 1, p.R * nb32_c, p.err) {
+          static_cast<uint8_t*>(p.s_row)[grow * nb32_c + b] = static_cast<uint8_t>(e + 127);
+        }
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, mine, (lane & ~3) | i);
@@ -260,7 +269,9 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
       am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
       const float s1 = scale_from_amax(am, fmax);
       sc[0] = sc[1] = sc[2] = sc[3] = s1;
-      if ((lane & 3) == 0 && gcol < p.C) static_cast<float*>(p.s_col)[gcol * nb128_r + tr] = recip_rn(s1);
+      if ((lane & 3) == 0 && gcol < p.C) FP8Q_GUARD(gcol * nb128_r + tr, 1, p.C * nb128_r, p.err) {
+        static_cast<float*>(p.s_col)[gcol * nb128_r + tr] = recip_rn(s1);
+      }
     } else if (RECIPE == kMx) {
       float at[4];
 #pragma unroll
@@ -273,7 +284,9 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
       if (p.mx_tiled) {
         sts8(sf + 512 + mx_atom_offset(cc, lane & 3), static_cast<uint32_t>(e + 127));
       } else if (gcol < p.C && b < nb32_r) {
-        static_cast<uint8_t*>(p.s_col)[gcol * nb32_r + b] = static_cast<uint8_t>(e + 127);
+        FP8Q_GUARD(gcol * nb32_r + b, 1, p.C * nb32_r, p.err) {
+          static_cast<uint8_t*>(p.s_col)[gcol * nb32_r + b] = static_cast<uint8_t>(e + 127);
+        }
       }
 #pragma unroll
       for (int t = 0; t < 4; ++t) sc[t] = __shfl_sync(0xFFFFFFFFu, mine, (lane & ~3) | t);
@@ -419,7 +432,9 @@ __global__ void __launch_bounds__(256) k_cast_generic(const uint16_t* __restrict
     if (r < p.R && c < p.C) {
       v = __uint_as_float(static_cast<uint32_t>(x[r * p.C + c]) << 16);
       amax = fmaxf(amax, fabsf(v));
-      if (p.do_row) p.q_row[r * p.C + c] = static_cast<uint8_t>(cvt_pair(__fmul_rn(v, s), 0.0f, e5) & 0xFF);
+      if (p.do_row) FP8Q_GUARD(r * p.C + c, 1, p.R * p.C, p.err) {
+        p.q_row[r * p.C + c] = static_cast<uint8_t>(cvt_pair(__fmul_rn(v, s), 0.0f, e5) & 0xFF);
+      }
     }
     tile[k][tx] = v;
   }
@@ -427,8 +442,9 @@ __global__ void __launch_bounds__(256) k_cast_generic(const uint16_t* __restrict
   if (p.do_col) {
     for (int k = ty; k < 32; k += 8) {
       const int64_t c = c0 + k, r = r0 + tx;
-      if (r < p.R && c < p.C)
+      if (r < p.R && c < p.C) FP8Q_GUARD(c * p.R + r, 1, p.R * p.C, p.err) {
         p.q_col[c * p.R + r] = static_cast<uint8_t>(cvt_pair(__fmul_rn(tile[tx][k], s), 0.0f, e5) & 0xFF);
+      }
     }
   }
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {

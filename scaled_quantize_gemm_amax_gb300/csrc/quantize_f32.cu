@@ -131,8 +131,13 @@ __device__ __forceinline__ void cast_tile_f32(const CastParams& p, uint32_t xs, 
     tile_scale = scale_from_amax(tmax, fmax);
     if (warp == 0 && lane == 0) {
       const float si = recip_rn(tile_scale);
-      if (p.do_row && p.s_row) static_cast<float*>(p.s_row)[tr * nb128_c + tc] = si;
-      if (p.do_col && p.s_col) static_cast<float*>(p.s_col)[tc * nb128_r + tr] = si;
+      const int64_t nblk = nb128_r * nb128_c;
+      if (p.do_row && p.s_row) FP8Q_GUARD(tr * nb128_c + tc, 1, nblk, p.err) {
+        static_cast<float*>(p.s_row)[tr * nb128_c + tc] = si;
+      }
+      if (p.do_col && p.s_col) FP8Q_GUARD(tc * nb128_r + tr, 1, nblk, p.err) {
+        static_cast<float*>(p.s_col)[tc * nb128_r + tr] = si;
+      }
     }
   }
   if (p.do_row) {
@@ -163,7 +168,9 @@ __device__ __forceinline__ void cast_tile_f32(const CastParams& p, uint32_t xs, 
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
         s_mine = scale_from_amax(m, fmax);
-        if ((lane & 3) == 0 && grow < p.R) static_cast<float*>(p.s_row)[grow * nb128_c + tc] = recip_rn(s_mine);
+        if ((lane & 3) == 0 && grow < p.R) FP8Q_GUARD(grow * nb128_c + tc, 1, p.R * nb128_c, p.err) {
+          static_cast<float*>(p.s_row)[grow * nb128_c + tc] = recip_rn(s_mine);
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, s_mine, 4 * i);
       } else {
@@ -173,7 +180,9 @@ __device__ __forceinline__ void cast_tile_f32(const CastParams& p, uint32_t xs, 
         if (p.mx_tiled)   // the tile's atom (both dims are multiples of 128)
           sts8(sf + mx_atom_offset(8 * warp + rr, lane >> 3), static_cast<uint32_t>(e + 127));
         else if (grow < p.R && b < nb32_c)   // a tile hanging over C has blocks past the last one
-          static_cast<uint8_t*>(p.s_row)[grow * nb32_c + b] = static_cast<uint8_t>(e + 127);
+          FP8Q_GUARD(grow * nb32_c + b, 1, p.R * nb32_c, p.err) {
+            static_cast<uint8_t*>(p.s_row)[grow * nb32_c + b] = static_cast<uint8_t>(e + 127);
+          }
 #pragma unroll
         for (int i = 0; i < 8; ++i) sc[i] = __shfl_sync(0xFFFFFFFFu, s_mine, (lane & ~7) | i);
       }
@@ -199,7 +208,9 @@ __device__ __forceinline__ void cast_tile_f32(const CastParams& p, uint32_t xs, 
       __syncthreads();
       const float m = fmaxf(fmaxf(colmax[c], colmax[kTile + c]), fmaxf(colmax[2 * kTile + c], colmax[3 * kTile + c]));
       s = scale_from_amax(m, fmax);
-      if (rq == 0 && gcol < p.C) static_cast<float*>(p.s_col)[gcol * nb128_r + tr] = recip_rn(s);
+      if (rq == 0 && gcol < p.C) FP8Q_GUARD(gcol * nb128_r + tr, 1, p.C * nb128_r, p.err) {
+        static_cast<float*>(p.s_col)[gcol * nb128_r + tr] = recip_rn(s);
+      }
     } else if (RECIPE == kMx) {
       const int e = (p.mx_floor ? mx_exponent_floor(am, fexp) : mx_exponent(am, fexp));
       s = pow2_neg(e);
@@ -207,7 +218,9 @@ __device__ __forceinline__ void cast_tile_f32(const CastParams& p, uint32_t xs, 
       if (p.mx_tiled)
         sts8(sf + 512 + mx_atom_offset(c, rq), static_cast<uint32_t>(e + 127));
       else if (gcol < p.C && b < nb32_r)
-        static_cast<uint8_t*>(p.s_col)[gcol * nb32_r + b] = static_cast<uint8_t>(e + 127);
+        FP8Q_GUARD(gcol * nb32_r + b, 1, p.C * nb32_r, p.err) {
+          static_cast<uint8_t*>(p.s_col)[gcol * nb32_r + b] = static_cast<uint8_t>(e + 127);
+        }
     }
     uint32_t qw[8];
 #pragma unroll
@@ -301,11 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.do_row) tma_store_2d(&tm_qrow, outR, static_cast<int>(col0), static_cast<int>(row0));
       if (p.do_col) tma_store_2d(&tm_qcol, outT, static_cast<int>(row0), static_cast<int>(col0));
       if (RECIPE == kMx && p.mx_tiled) {   // the staged atoms: row copy's (tr, tc), column copy's (tc, tr)
-        if (p.do_row)
-          bulk_store(static_cast<uint8_t*>(p.s_row) + (static_cast<int64_t>(tr) * p.tiles_c + tc) * 512, sf, 512);
-        if (p.do_col)
-          bulk_store(static_cast<uint8_t*>(p.s_col) + (static_cast<int64_t>(tc) * p.tiles_r + tr) * 512, sf + 512,
-                     512);
+        const int64_t atoms = static_cast<int64_t>(p.tiles_r) * p.tiles_c * 512;
+        const int64_t orow = (static_cast<int64_t>(tr) * p.tiles_c + tc) * 512;
+        const int64_t ocol = (static_cast<int64_t>(tc) * p.tiles_r + tr) * 512;
+        if (p.do_row) FP8Q_GUARD(orow, 512, atoms, p.err) { bulk_store(static_cast<uint8_t*>(p.s_row) + orow, sf, 512); }
+        if (p.do_col) FP8Q_GUARD(ocol, 512, atoms, p.err) { bulk_store(static_cast<uint8_t*>(p.s_col) + ocol, sf + 512, 512); }
       }
       bulk_commit();
       const int next = tile + kStages * gridDim.x;
@@ -354,7 +367,9 @@ __global__ void __launch_bounds__(256) k_cast_generic_f32(const float* __restric
     if (r < p.R && c < p.C) {
       v = x[r * p.C + c];
       amax = fmaxf(amax, fabsf(v));
-      if (p.do_row) p.q_row[r * p.C + c] = static_cast<uint8_t>(cvt_pair(__fmul_rn(v, s), 0.0f, e5) & 0xFF);
+      if (p.do_row) FP8Q_GUARD(r * p.C + c, 1, p.R * p.C, p.err) {
+        p.q_row[r * p.C + c] = static_cast<uint8_t>(cvt_pair(__fmul_rn(v, s), 0.0f, e5) & 0xFF);
+      }
     }
     tile[k][tx] = v;
   }
@@ -362,8 +377,9 @@ __global__ void __launch_bounds__(256) k_cast_generic_f32(const float* __restric
   if (p.do_col) {
     for (int k = ty; k < 32; k += 8) {
       const int64_t c = c0 + k, r = r0 + tx;
-      if (r < p.R && c < p.C)
+      if (r < p.R && c < p.C) FP8Q_GUARD(c * p.R + r, 1, p.R * p.C, p.err) {
         p.q_col[c * p.R + r] = static_cast<uint8_t>(cvt_pair(__fmul_rn(tile[tx][k], s), 0.0f, e5) & 0xFF);
+      }
     }
   }
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
