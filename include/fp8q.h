@@ -337,7 +337,8 @@ fp8_status fp8_scaled_gemm_amax(const uint8_t* A, fp8_format fa, fp8_recipe ra, 
 /*
  * fp8_get_device_status -- synchronize `stream`, then read and clear the
  * device error word of the current device.  Returns FP8_OK, FP8_ERR_TIMEOUT
- * (some kernel gave up a wait), FP8_ERR_DEVICE_STATE, or FP8_ERR_CUDA.
+ * (some kernel gave up a wait), FP8_ERR_DEVICE_STATE, FP8_ERR_INDEX (debug
+ * library: a kernel skipped an access outside its buffer), or FP8_ERR_CUDA.
  */
 fp8_status fp8_get_device_status(cudaStream_t stream);
 
