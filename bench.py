@@ -187,7 +187,7 @@ class Path:
         self.qwt = torch.empty((K, N), dtype=torch.uint8, device=dev)
         self.swt = torch.empty((K // 128, N // 128), dtype=torch.float32, device=dev)
         self.y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        self.launches_per_step = 3
+        self.launches_per_step = 2
 
     def cast_x(self):
         self.fq.fp8_cast_transpose(self.x, self.R.BLOCK_1x128, self.F.E4M3, None, None, self.qx, self.sx, self.qxt,
@@ -197,13 +197,19 @@ class Path:
         self.fq.fp8_cast_transpose(self.w, self.R.BLOCK_128x128, self.F.E4M3, None, None, self.qw, self.sw, self.qwt,
                                    self.swt)
 
+    def casts(self):
+        # both casts in one launch (fp8_cast_transpose_multi; a kernel compiled for this pairing):
+        # one grid start and one tail instead of two (the step 94.2-94.7 against 94.7-96.0 us)
+        R, F = self.R, self.F
+        self.fq.fp8_cast_transpose_multi([(self.x, R.BLOCK_1x128, F.E4M3, None, None, self.qx, self.sx, self.qxt, self.sxt),
+                                          (self.w, R.BLOCK_128x128, F.E4M3, None, None, self.qw, self.sw, self.qwt, self.swt)])
+
     def gemm(self):
         self.fq.fp8_scaled_gemm(self.qx, self.F.E4M3, self.R.BLOCK_1x128, self.sx, self.qw, self.F.E4M3,
                                 self.R.BLOCK_128x128, self.sw, self.y)
 
     def step(self):
-        self.cast_x()
-        self.cast_w()
+        self.casts()
         self.gemm()
 
 
@@ -280,7 +286,7 @@ def run_ours(args, rank, world):
     clocks = ClockSampler(torch.cuda.current_device(), args.clocks_csv)
     clocks.start()
 
-    # the timed step is one CUDA graph of the three launches (no host launch cost inside it)
+    # the timed step is one CUDA graph of the two launches (no host launch cost inside it)
     g_step = _capture(path.step)
     for _ in range(args.warmup):
         g_step.replay()
@@ -307,7 +313,9 @@ def run_ours(args, rank, world):
     step_ms = max_over_ranks(statistics.mean(step_times), world)
     sustained = run_sustained(fq, wl, dev, x, w, path)
 
-    # per-kernel breakdown of the step: each launch alone, L2 flushed before it
+    # per-kernel breakdown of the step: each launch alone, L2 flushed before it (the two casts
+    # also one at a time, for their own rates)
+    t_cc = time_kernel(path.casts, flush=flush)
     t_cx = time_kernel(path.cast_x, flush=flush)
     t_cw = time_kernel(path.cast_w, flush=flush)
     g_ms = time_kernel(path.gemm, flush=flush)
@@ -318,6 +326,7 @@ def run_ours(args, rank, world):
     gemm_tflops = flops / (g_ms * 1e-3) / 1e12
     cx_gbs = bytes_cast("BLOCK_1x128", M, K) / (t_cx * 1e-3) / 1e9
     cw_gbs = bytes_cast("BLOCK_128x128", N, K) / (t_cw * 1e-3) / 1e9
+    cc_gbs = (bytes_cast("BLOCK_1x128", M, K) + bytes_cast("BLOCK_128x128", N, K)) / (t_cc * 1e-3) / 1e9
     value = world * flops / (step_ms * 1e-3) / 1e12
 
     result = {
@@ -331,6 +340,8 @@ def run_ours(args, rank, world):
         "step_ms_median": round(statistics.median(step_times), 5),
         "kernels": {
             "stat": f"median of {KERNEL_REPS} launches, L2 flushed before each",
+            "cast_transpose_x_and_w (the step's one two-job launch)": {
+                "us": round(t_cc * 1e3, 2), "GB/s": round(cc_gbs, 1), "frac_hbm": round(cc_gbs / pk["hbm_gbs"], 4)},
             "cast_transpose_x_1x128": {"us": round(t_cx * 1e3, 2), "GB/s": round(cx_gbs, 1),
                                        "frac_hbm": round(cx_gbs / pk["hbm_gbs"], 4)},
             "cast_transpose_w_128x128": {"us": round(t_cw * 1e3, 2), "GB/s": round(cw_gbs, 1),
