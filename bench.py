@@ -19,7 +19,8 @@ median of >= 50 event-timed launches with L2 flushed before each), a sustained
 window of back-to-back steps for the clock record, the same step end to end
 through the C ABI with host buffers (`e2e`), and the CPU oracle timed on the
 host cores (`cpu_baseline`).  --impl reference times the CPU oracle on the
-whole step instead.
+whole step instead; --cpu-baseline-sweep [SIZE ...] times the oracle's casts of
+every recipe on one thread and on every core (no GPU).
 """
 from __future__ import annotations
 
@@ -253,7 +254,7 @@ def _capture(fn):
     return g
 
 
-def time_kernel(fn, reps=KERNEL_REPS, flush=None, warm=3):
+def time_kernel(fn, reps=KERNEL_REPS, flush=None, warm=10):
     """Median of `reps` launches, each alone between two events on the launching stream,
     L2 flushed before each (the flush is enqueued ahead of the first event, so the host
     enqueues the launch while the flush runs and the events see the kernel alone)."""
@@ -687,6 +688,69 @@ def cpu_baseline(x, w):
             "gemm_s": round(tg, 4), "all_core_step_s": round(step_s, 4)}
 
 
+def _oracle_cast_both(oracle, xh, kind, threads, scale=None):
+    """Row + column copies of xh on the oracle, `threads` host threads: each thread takes
+    a run of 128-row slabs for the row-wise copy and a run of 128-column slabs (its slab
+    transposed, then the row-wise recipe: the column-wise copy's definition) for the
+    column-wise one.  Returns the (q, s) pieces of each copy in order (slabs of the
+    row-wise copy's rows, then of the column-wise copy's rows), not joined."""
+    rows, cols = xh.shape
+
+    def runs(n):
+        per = -(-(n // 128) // threads) * 128
+        return [(a, min(n, a + per)) for a in range(0, n, per)]
+
+    jobs = ([(lambda r0=r0, r1=r1: np.ascontiguousarray(xh[r0:r1])) for r0, r1 in runs(rows)] +
+            [(lambda c0=c0, c1=c1: oracle.transpose_bf16(np.ascontiguousarray(xh[:, c0:c1]))) for c0, c1 in runs(cols)])
+    out = [None] * len(jobs)
+
+    def work(i):
+        out[i] = oracle.quantize_rowwise(jobs[i](), kind, oracle.E4M3, scale)
+
+    ts = [threading.Thread(target=work, args=(i,)) for i in range(len(jobs))]
+    for i in range(0, len(ts), threads):
+        for t in ts[i:i + threads]:
+            t.start()
+        for t in ts[i:i + threads]:
+            t.join()
+    n_row = len(runs(rows))
+    return out[:n_row], out[n_row:]
+
+
+def cpu_baseline_sweep(sizes):
+    """The oracle's casts (row + column copies, E4M3) for every recipe on s x s inputs of
+    the bandwidth-sweep recipe (N(0, 1), 0.1 % of elements x1000, generated on the host):
+    one thread and every core for s <= 16384, every core only above (one run each).
+    Per-tensor current scaling includes its amax and scale.  GB/s counts the same
+    algorithmic bytes as the GPU casts.  Needs no GPU."""
+    import oracle
+    from scaled_quantize_gemm_amax_gb300 import workloads as wl
+    oracle.build()
+    cores = os.cpu_count()
+    recipes = (("TENSOR", oracle.KIND_TENSOR), ("BLOCK_1x128", oracle.KIND_1x128),
+               ("BLOCK_128x128", oracle.KIND_128x128), ("MX_1x32", oracle.KIND_MX))
+    rows = []
+    for s in sizes:
+        xh = _bits(wl.cfg5_sweep(s, "cpu"))
+        for name, kind in recipes:
+            for threads in ((1, cores) if s <= 16384 else (cores,)):
+                t0 = time.perf_counter()
+                scale = None
+                if kind == oracle.KIND_TENSOR:
+                    scale = oracle.tensor_scale(oracle.amax(xh), oracle.E4M3)[0]
+                _oracle_cast_both(oracle, xh, kind, threads, scale)
+                sec = time.perf_counter() - t0
+                gbs = bytes_cast(name, s, s) / sec / 1e9
+                rows.append({"size": s, "recipe": name, "threads": threads, "s": round(sec, 4),
+                             "GB/s": round(gbs, 4)})
+                print(f"# oracle cast {name} {s}^2 on {threads} thread(s): {sec:.3f} s, {gbs:.3f} GB/s",
+                      file=sys.stderr, flush=True)
+        del xh
+    return {"kind": "oracle", "what": "row + column casts, E4M3, every recipe", "cores": cores,
+            "host": os.uname().machine, "inputs": "s x s ~ N(0, 1), 0.1 % of elements x1000, host generator",
+            "runs": rows}
+
+
 def run_reference(args, rank, world):
     """The oracle as the reference arm: every step is the whole workload on the host
     cores (see _oracle_step), measured, not extrapolated."""
@@ -853,7 +917,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-csv", default=None, help="also write the raw clock samples of the run here")
+    ap.add_argument("--cpu-baseline-sweep", type=int, nargs="*", default=None, metavar="SIZE",
+                    help="time the oracle's casts on the host cores at these sizes (default: the bandwidth "
+                         "sweep's sizes) and print them as one JSON line; no GPU")
     args = ap.parse_args()
+    if args.cpu_baseline_sweep is not None:
+        from scaled_quantize_gemm_amax_gb300 import workloads as wl
+        print(json.dumps(cpu_baseline_sweep(args.cpu_baseline_sweep or wl.CFG5_SIZES)), flush=True)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.case is not None:
