@@ -194,7 +194,11 @@ fp8_status fp8_cast_transpose_f32(const float* x, int64_t rows, int64_t cols, fp
  *           same name of fp8_cast_transpose
  *   n_jobs  0..4 (FP8_ERR_INVALID_ARG beyond)
  * Every job is checked (as fp8_cast_transpose checks its arguments) before any
- * device work; the first failing job's status is returned.
+ * device work; the first failing job's status is returned.  Two jobs whose
+ * recipes are (BLOCK_1x128, BLOCK_128x128), two MX_1x32 recipes (any layout or
+ * exponent rule) or (TENSOR, TENSOR), in that order, run in a kernel compiled for
+ * that pairing; any other mix in the general one.  The results do not depend on
+ * which.
  */
 typedef struct fp8_cast_job {
   const void* x;
