@@ -790,7 +790,8 @@ def run_reference(args, rank, world):
 
 CASES = ("cast_tensor", "cast_1x128", "cast_128x128", "cast_mx", "cast_f32_tensor", "cast_f32_1x128", "cast_f32_128x128",
          "cast_f32_mx", "amax", "amax_f32", "gemm_tensor", "gemm_block", "gemm_mx",
-         "gemm_block_wgrad", "gemm_amax", "dequant_tensor", "dequant_1x128", "dequant_128x128", "dequant_mx", "allreduce")
+         "gemm_block_wgrad", "gemm_amax", "dequant_tensor", "dequant_1x128", "dequant_128x128", "dequant_mx", "allreduce",
+         "cast_step")
 
 
 def run_case(args):
@@ -807,7 +808,15 @@ def run_case(args):
     s = args.size
     flush = L2Flush(dev)
     pk = peaks()
-    if args.case.startswith("cast") or args.case.startswith("amax"):
+    if args.case == "cast_step":
+        # the step's one launch of both casts (X 1x128, W 128x128, row + col) on its 4096^2 inputs
+        x, w = wl.cfg2_blockwise(dev)
+        path = Path(fq, x, w)
+        ms = time_kernel(path.casts, reps=args.steps, flush=flush)
+        nbytes = bytes_cast("BLOCK_1x128", M, K) + bytes_cast("BLOCK_128x128", N, K)
+        res = {"case": args.case, "size": M, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+        res["frac_hbm"] = round(res["GB/s"] / pk["hbm_gbs"], 4)
+    elif args.case.startswith("cast") or args.case.startswith("amax"):
         x = wl.cfg5_sweep(s, dev) if s in wl.CFG5_SIZES else wl.normal_bf16((s, s), 5, 1.0, dev)
         f32 = "f32" in args.case
         if f32:

@@ -182,10 +182,16 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
   const int fexp = fmax_exp_of(e5);
   const int64_t nb128_c = p.C / 128, nb128_r = p.R / 128, nb32_c = p.C / 32, nb32_r = p.R / 32;
   const int j = lane & 15;
+  // Recipes whose two copies share one scale per tile (per-tensor, 128x128): the column
+  // copy is the byte transpose of the row copy.  There each warp quantizes 8 consecutive
+  // rows, so that its column pass transposes the bytes it staged itself; otherwise rows
+  // i*32 + 2w and +1 (the row scales' reduce-scatter depends on that order).
+  constexpr bool kOneScale = RECIPE == kTensor || RECIPE == kBlock128x128;
+  auto row_of = [&](int i) { return kOneScale ? 8 * warp + 2 * i + (lane >> 4) : i * 32 + warp * 2 + (lane >> 4); };
   // ---------------- row pass
   uint4 v[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = lds128(x_addr(xs, i * 32 + warp * 2 + (lane >> 4), j));
+  for (int i = 0; i < 4; ++i) v[i] = lds128(x_addr(xs, row_of(i), j));
   float a[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) a[i] = absmax_chunk(v[i]);
@@ -243,14 +249,40 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int r = i * 32 + warp * 2 + (lane >> 4);
+      const int r = row_of(i);
       const uint2 q = q_chunk(v[i], sc[i], e5);
       sts64(outR + (r << 7) + ((((j >> 1) ^ (r & 7))) << 4) + ((j & 1) << 3), q.x, q.y);
     }
   }
 
   // ---------------- col pass
-  if (p.do_col) {
+  if (kOneScale && p.do_col && p.do_row) {
+    // This warp's rows 8w..8w+7 of the staged row copy, loaded transposed as 2-byte
+    // elements: thread T gets, for each 16-byte column chunk m, rows ra = 8w + 2(T%4) and
+    // ra + 1 at byte columns c = 16m + 2(T/4) and c + 1; column c's two bytes and column
+    // c+1's go to the column copy's rows c and c+1 at byte ra.  The upper half-warp stores
+    // column c+1 first, so that each store instruction meets eight different 16-byte
+    // chunks of the swizzled tile (no bank conflict).
+    __syncwarp();
+    uint32_t d[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = 8 * warp + (lane & 7), m = 4 * h + (lane >> 3);
+      ldsm_x4_trans(outR + (r << 7) + ((m ^ (r & 7)) << 4), d[h]);
+    }
+    const int ra = 8 * warp + 2 * (lane & 3), up = lane >> 4;
+    const int c_first = 2 * (lane >> 2) + up, c_second = 2 * (lane >> 2) + 1 - up;
+    const uint32_t sel_first = up ? 0x31u : 0x20u, sel_second = up ? 0x20u : 0x31u;
+    const uint32_t a_first = q_addr(outT, c_first, ra), a_second = q_addr(outT, c_second, ra);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t m = static_cast<uint32_t>(4 * h + q);   // column chunk: rows c + 16m of the column copy
+        sts16(a_first + (m << 11), __byte_perm(d[h][q], 0u, sel_first));
+        sts16(a_second + (m << 11), __byte_perm(d[h][q], 0u, sel_second));
+      }
+  } else if (p.do_col) {
     const int g = warp;
     uint32_t d[4][4];
 #pragma unroll
