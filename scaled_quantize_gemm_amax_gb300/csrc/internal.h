@@ -87,6 +87,7 @@ struct CastParams {
   void* s_col;
   uint32_t* err;
   int tiles_r, tiles_c;
+  int col_from_row;      // set by the launcher: the column copy as the byte transpose of the row copy
 };
 // Tiled TMA path; requires C % 16 == 0 and (when do_col) R % 16 == 0.
 cudaError_t launch_cast_transpose_tiled(const CastParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_qrow,

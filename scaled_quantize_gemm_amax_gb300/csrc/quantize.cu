@@ -183,11 +183,13 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
   const int64_t nb128_c = p.C / 128, nb128_r = p.R / 128, nb32_c = p.C / 32, nb32_r = p.R / 32;
   const int j = lane & 15;
   // Recipes whose two copies share one scale per tile (per-tensor, 128x128): the column
-  // copy is the byte transpose of the row copy.  There each warp quantizes 8 consecutive
-  // rows, so that its column pass transposes the bytes it staged itself; otherwise rows
-  // i*32 + 2w and +1 (the row scales' reduce-scatter depends on that order).
+  // copy is the byte transpose of the row copy.  When the launcher chose that (col_from_row),
+  // each warp quantizes 8 consecutive rows, so that its column pass transposes the bytes it
+  // staged itself; otherwise rows i*32 + 2w and +1 (the row scales' reduce-scatter depends
+  // on that order).
   constexpr bool kOneScale = RECIPE == kTensor || RECIPE == kBlock128x128;
-  auto row_of = [&](int i) { return kOneScale ? 8 * warp + 2 * i + (lane >> 4) : i * 32 + warp * 2 + (lane >> 4); };
+  const bool contig = kOneScale && p.col_from_row != 0;
+  auto row_of = [&](int i) { return contig ? 8 * warp + 2 * i + (lane >> 4) : i * 32 + warp * 2 + (lane >> 4); };
   // ---------------- row pass
   uint4 v[4];
 #pragma unroll
@@ -256,7 +258,7 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
   }
 
   // ---------------- col pass
-  if (kOneScale && p.do_col && p.do_row) {
+  if (contig && p.do_col && p.do_row) {
     // This warp's rows 8w..8w+7 of the staged row copy, loaded transposed as 2-byte
     // elements: thread T gets, for each 16-byte column chunk m, rows ra = 8w + 2(T%4) and
     // ra + 1 at byte columns c = 16m + 2(T/4) and c + 1; column c's two bytes and column
@@ -758,6 +760,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_cast_two(const __grid_constant_
   if (!failed) flush_amax(in_job1 ? J.p[1].amax_out : J.p[0].amax_out, thr_amax);
 }
 
+// Whether a one-scale cast takes its column copy from the staged row copy: always for
+// per-tensor (measured side by side: equal or faster at every size, 0.68 against 0.60 of
+// HBM at 4096^2); for 128x128 up to 64 tiles a CTA (0.56 / 0.92 at 4096^2 / 8192^2 against
+// 0.53 / 0.84 quantizing the column copy again, but 0.92 / 0.89 at 16384^2 / 32768^2
+// against 0.97 / 1.00).
+int col_from_row(const CastParams& p, int num_sms) {
+  if (p.recipe == kTensor) return 1;
+  if (p.recipe != kBlock128x128) return 0;
+  return static_cast<int64_t>(p.tiles_r) * p.tiles_c <= 64LL * num_sms ? 1 : 0;
+}
+
 template <int RECIPE>
 cudaError_t launch_tiled(const CastParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_qrow,
                          const CUtensorMap& tm_qcol, int num_sms, cudaStream_t s) {
@@ -766,7 +779,9 @@ cudaError_t launch_tiled(const CastParams& p, const CUtensorMap& tm_x, const CUt
   if (e != cudaSuccess) return e;
   const int ntiles = p.tiles_r * p.tiles_c;
   const int grid = ntiles < num_sms ? ntiles : num_sms;
-  return launch_pdl(k_cast_transpose<RECIPE>, dim3(grid), dim3(kThreads), kSmemBytes, s, 1, tm_x, tm_qrow, tm_qcol, p);
+  CastParams q = p;
+  q.col_from_row = col_from_row(p, num_sms);
+  return launch_pdl(k_cast_transpose<RECIPE>, dim3(grid), dim3(kThreads), kSmemBytes, s, 1, tm_x, tm_qrow, tm_qcol, q);
 }
 
 }  // namespace
@@ -791,7 +806,9 @@ cudaError_t launch_two(const CastJobs& jobs, int grid, cudaStream_t s) {
 }
 }  // namespace
 
-cudaError_t launch_cast_jobs(const CastJobs& jobs, int num_sms, cudaStream_t s) {
+cudaError_t launch_cast_jobs(const CastJobs& jobs_in, int num_sms, cudaStream_t s) {
+  CastJobs jobs = jobs_in;
+  for (int j = 0; j < jobs.n; ++j) jobs.p[j].col_from_row = col_from_row(jobs.p[j], num_sms);
   const int ntiles = jobs.tile_start[jobs.n];
   const int grid = ntiles < num_sms ? ntiles : num_sms;
   if (jobs.n == 2) {
