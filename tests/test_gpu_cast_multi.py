@@ -97,3 +97,34 @@ def test_cast_multi_two_job_pairings(recipes, fmts, shapes):
     assert_status_ok()
     for x, r, f, s_np, am, o in zip(xs, recipes, fmts, scale_nps, amaxes, outs):
         check_job(x, r, f, s_np, o, am)
+
+
+def test_cast_two_with_a_weight_above_the_byte_transpose_limit():
+    # A 128x128 job of 16384 x 10240 (10240 tiles, more than 64 a CTA on 152 SMs) quantizes
+    # its column copy from the BF16 tile; a small one transposes its row copy's bytes.  Both
+    # beside a 1x128 job in the pairing kernel; sampled 128x128 tiles of the large job (each
+    # tile's bytes and scale depend on that tile alone) and the whole small jobs against the
+    # oracle.
+    x = wl.normal_bf16((512, 384), 86, 1.0)
+    big = wl.normal_bf16((16384, 10240), 87, 0.02)
+    big[5000:5003, 7000] = 30.0
+    for w in (big, wl.normal_bf16((256, 640), 88, 0.5)):
+        (qx, sx, qxt, sxt), (qw, sw, qwt, swt) = fq.cast_transpose_multi(
+            [(x, R.BLOCK_1x128, F.E4M3, None, None), (w, R.BLOCK_128x128, F.E4M3, None, None)])
+        torch.cuda.synchronize()
+        assert_status_ok()
+        check_job(x, R.BLOCK_1x128, F.E4M3, None, (qx, sx, qxt, sxt), None)
+        if w.shape[0] * w.shape[1] < (1 << 20):
+            check_job(w, R.BLOCK_128x128, F.E4M3, None, (qw, sw, qwt, swt), None)
+            continue
+        rng = np.random.default_rng(89)
+        tiles = [(0, 0), (127, 79), (5000 // 128, 7000 // 128)] + [tuple(t) for t in rng.integers(0, (128, 80), (5, 2))]
+        for ti, tj in tiles:
+            rs, cs = slice(ti * 128, ti * 128 + 128), slice(tj * 128, tj * 128 + 128)
+            xt = bits16(w[rs, cs])
+            q_ref, s_ref = oracle.quantize_rowwise(xt, KIND[R.BLOCK_128x128], int(F.E4M3))
+            assert_bytes_equal(host(qw[rs, cs]), q_ref, f"q_row tile {ti},{tj}")
+            assert f32bits(host(sw[ti, tj])) == f32bits(s_ref[0, 0])
+            qc_ref, sc_ref = oracle.quantize_colwise(xt, KIND[R.BLOCK_128x128], int(F.E4M3))
+            assert_bytes_equal(host(qwt[cs, rs]), qc_ref, f"q_col tile {ti},{tj}")
+            assert f32bits(host(swt[tj, ti])) == f32bits(sc_ref[0, 0])
