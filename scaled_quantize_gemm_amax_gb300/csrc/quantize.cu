@@ -73,6 +73,18 @@ __device__ __forceinline__ void sts8(uint32_t a, uint32_t v) {
 __device__ __forceinline__ void sts16(uint32_t a, uint32_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"(static_cast<uint16_t>(v)) : "memory");
 }
+// A 1x128 column-scale store with the L2 evict-last policy: a 32-byte sector of the
+// column-scale array ([C, R/128] floats) is written by 8 tile-rows, one tile-row at a time,
+// and should stay in L2 until it is complete rather than leave partly written (a row-scale
+// sector is completed by 8 neighbouring tiles of one tile-row, within one round).
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void st_f32_l2_last(float* a, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(a), "f"(v), "l"(pol) : "memory");
+}
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t a, uint32_t (&d)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
@@ -304,7 +316,7 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
       const float s1 = scale_from_amax(am, fmax);
       sc[0] = sc[1] = sc[2] = sc[3] = s1;
       if ((lane & 3) == 0 && gcol < p.C) FP8Q_GUARD(gcol * nb128_r + tr, 1, p.C * nb128_r, p.err) {
-        static_cast<float*>(p.s_col)[gcol * nb128_r + tr] = recip_rn(s1);
+        st_f32_l2_last(static_cast<float*>(p.s_col) + gcol * nb128_r + tr, recip_rn(s1), l2_evict_last_policy());
       }
     } else if (RECIPE == kMx) {
       float at[4];
