@@ -88,6 +88,7 @@ struct CastParams {
   uint32_t* err;
   int tiles_r, tiles_c;
   int col_from_row;      // set by the launcher: the column copy as the byte transpose of the row copy
+  int keep_col_scales;   // set by the launcher: 1x128 column scales stored with the L2 evict-last policy
 };
 // Tiled TMA path; requires C % 16 == 0 and (when do_col) R % 16 == 0.
 cudaError_t launch_cast_transpose_tiled(const CastParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_qrow,
