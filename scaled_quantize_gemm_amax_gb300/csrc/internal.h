@@ -89,6 +89,7 @@ struct CastParams {
   int tiles_r, tiles_c;
   int col_from_row;      // set by the launcher: the column copy as the byte transpose of the row copy
   int keep_col_scales;   // set by the launcher: 1x128 column scales stored with the L2 evict-last policy
+  int one_division;      // set by the launcher: a 1x128 tile's row and column scales from one division a lane
 };
 // Tiled TMA path; requires C % 16 == 0 and (when do_col) R % 16 == 0.
 cudaError_t launch_cast_transpose_tiled(const CastParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_qrow,

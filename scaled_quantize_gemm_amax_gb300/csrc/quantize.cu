@@ -185,6 +185,69 @@ __device__ __forceinline__ uint32_t mx_atom_offset(int r, int b) {
   return static_cast<uint32_t>((r & 31) * 16 + (r >> 5) * 4 + b);
 }
 
+// A 1x128 tile with both copies.  The row maxima (each row's 128 columns of the tile) and
+// the column maxima (each column's 128 rows) are both found before any scale is formed, so
+// that one correctly rounded division and one reciprocal a lane serve both copies: in each
+// group of four lanes, lanes 0-1 form their row's scale and lanes 2-3 their column's.  Same
+// bytes and scales as the two passes of cast_tile_body.
+__device__ __forceinline__ void cast_tile_1x128_both(const CastParams& p, uint32_t xs, uint32_t outR, uint32_t outT,
+                                                     int tr, int tc, int64_t row0, int64_t col0, float& thr_amax,
+                                                     int warp, int lane) {
+  const bool e5 = p.e5m2 != 0;
+  const float fmax = fmax_of(e5);
+  const int64_t nb128_c = p.C / 128, nb128_r = p.R / 128;
+  const int j = lane & 15;
+  // rows i*32 + 2w + (lane / 16), 16-byte chunk j
+  uint4 v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = lds128(x_addr(xs, i * 32 + warp * 2 + (lane >> 4), j));
+  float a[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) a[i] = absmax_chunk(v[i]);
+  thr_amax = fmaxf(thr_amax, fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])));
+  // row i = j / 4 ends up in lanes j = 4i..4i+3 of each half-warp
+  float mr = reduce_scatter4(a, lane, 8, 4);
+  mr = fmaxf(mr, __shfl_xor_sync(0xFFFFFFFFu, mr, 2));
+  mr = fmaxf(mr, __shfl_xor_sync(0xFFFFFFFFu, mr, 1));
+  // column cc = 8w + lane / 4, transposed: lanes 4k..4k+3 hold its 128 rows between them
+  uint32_t d[4][4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) ldsm_x4_trans(x_addr(xs, 32 * t + 8 * (lane >> 3) + (lane & 7), warp), d[t]);
+  uint32_t mb = 0;
+#pragma unroll
+  for (int t = 0; t < 4; ++t)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) mb = xabs_max(mb, d[t][q]);
+  float mc = pair_abs_f32(mb);
+  mc = fmaxf(mc, __shfl_xor_sync(0xFFFFFFFFu, mc, 1));
+  mc = fmaxf(mc, __shfl_xor_sync(0xFFFFFFFFu, mc, 2));
+  const float y = scale_from_amax((lane & 2) ? mc : mr, fmax);
+  const float yi = recip_rn(y);
+  const int64_t grow = row0 + (j >> 2) * 32 + warp * 2 + (lane >> 4);
+  if ((j & 3) == 0 && grow < p.R) FP8Q_GUARD(grow * nb128_c + tc, 1, p.R * nb128_c, p.err) {
+    static_cast<float*>(p.s_row)[grow * nb128_c + tc] = yi;
+  }
+  const int cc = 8 * warp + (lane >> 2);
+  const int64_t gcol = col0 + cc;
+  if ((lane & 3) == 2 && gcol < p.C) FP8Q_GUARD(gcol * nb128_r + tr, 1, p.C * nb128_r, p.err) {
+    float* const dst = static_cast<float*>(p.s_col) + gcol * nb128_r + tr;
+    if (p.keep_col_scales) st_f32_l2_last(dst, yi, l2_evict_last_policy());
+    else *dst = yi;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float sr = __shfl_sync(0xFFFFFFFFu, y, (lane & 16) | (i << 2));
+    const int r = i * 32 + warp * 2 + (lane >> 4);
+    const uint2 q = q_chunk(v[i], sr, e5);
+    sts64(outR + (r << 7) + ((((j >> 1) ^ (r & 7))) << 4) + ((j & 1) << 3), q.x, q.y);
+  }
+  const float s1 = __shfl_sync(0xFFFFFFFFu, y, (lane & ~3) | 2);
+#pragma unroll
+  for (int t = 0; t < 4; ++t)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) sts16(q_addr(outT, cc, 32 * t + 8 * q + 2 * (lane & 3)), q_pair(d[t][q], s1, e5));
+}
+
 template <int RECIPE>
 __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs, uint32_t outR, uint32_t outT, int tr,
                                                int tc, int64_t row0, int64_t col0, float g_scale, float& thr_amax,
@@ -194,6 +257,10 @@ __device__ __forceinline__ void cast_tile_body(const CastParams& p, uint32_t xs,
   const int fexp = fmax_exp_of(e5);
   const int64_t nb128_c = p.C / 128, nb128_r = p.R / 128, nb32_c = p.C / 32, nb32_r = p.R / 32;
   const int j = lane & 15;
+  if (RECIPE == kBlock1x128 && p.do_row && p.do_col && p.one_division) {
+    cast_tile_1x128_both(p, xs, outR, outT, tr, tc, row0, col0, thr_amax, warp, lane);
+    return;
+  }
   // Recipes whose two copies share one scale per tile (per-tensor, 128x128): the column
   // copy is the byte transpose of the row copy.  When the launcher chose that (col_from_row),
   // each warp quantizes 8 consecutive rows, so that its column pass transposes the bytes it
@@ -792,6 +859,14 @@ int col_from_row(const CastParams& p, int num_sms) {
 // three quarters of L2 (C >= 24576) on.
 int keep_col_scales(const CastParams& p) { return p.recipe == kBlock1x128 && p.C >= 24576 ? 1 : 0; }
 
+// Whether a 1x128 tile with both copies forms its row and column scales with one division a
+// lane (cast_tile_1x128_both): up to 64 tiles a CTA, where the cast is bound by its
+// instructions (measured side by side, both orders: the step's two-job launch 30.8 against
+// 31.2 us, 1x128 casts +2 % at 4096^2 and 8192^2; at 16384^2, bound by HBM, 2.5 % slower).
+int one_division(const CastParams& p, int num_sms) {
+  return p.recipe == kBlock1x128 && static_cast<int64_t>(p.tiles_r) * p.tiles_c <= 64LL * num_sms ? 1 : 0;
+}
+
 template <int RECIPE>
 cudaError_t launch_tiled(const CastParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_qrow,
                          const CUtensorMap& tm_qcol, int num_sms, cudaStream_t s) {
@@ -803,6 +878,7 @@ cudaError_t launch_tiled(const CastParams& p, const CUtensorMap& tm_x, const CUt
   CastParams q = p;
   q.col_from_row = col_from_row(p, num_sms);
   q.keep_col_scales = keep_col_scales(p);
+  q.one_division = one_division(p, num_sms);
   return launch_pdl(k_cast_transpose<RECIPE>, dim3(grid), dim3(kThreads), kSmemBytes, s, 1, tm_x, tm_qrow, tm_qcol, q);
 }
 
@@ -833,6 +909,7 @@ cudaError_t launch_cast_jobs(const CastJobs& jobs_in, int num_sms, cudaStream_t 
   for (int j = 0; j < jobs.n; ++j) {
     jobs.p[j].col_from_row = col_from_row(jobs.p[j], num_sms);
     jobs.p[j].keep_col_scales = keep_col_scales(jobs.p[j]);
+    jobs.p[j].one_division = one_division(jobs.p[j], num_sms);
   }
   const int ntiles = jobs.tile_start[jobs.n];
   const int grid = ntiles < num_sms ? ntiles : num_sms;
